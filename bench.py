@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark: FP8 paged decode attention step — achieved HBM GB/s and µs/step vs bf16.
+
+One step = one decode step of every layer of the workload: for each layer the new
+token's K/V are written into the paged cache (kv_quant_cache, e4m3 with per-KV-head
+scales) and fp8_decode_attn reads the whole cached context (split-K + FP32 merge).
+Inputs are seeded synthetic tensors shaped like the pages' Llama-3.1-8B decode under
+load (32 layers, 32/8 heads, head_dim 128, batch 8, contexts U[16384, 24576]); the
+cache (10.5 GB per step) is far larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a bounded
+sample of the same workload instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 paged decode attn: achieved HBM GB/s (% of peak) and µs/step vs bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _env_rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _traffic_record(kernel_file: str, summary: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (same sha256); else None."""
+    path = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "fp8_kv_cache_quant_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    rec = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip()
+    if rec.get("source_sha256_16") != sha:
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed regions run."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def decode_bytes(w, ctx, layer_is_bf16):
+    """Algorithmic HBM bytes of one step: every cached key/value of every layer read once,
+    Q read, O written, block-table entries read, the new token's bf16 K/V read and its
+    cache bytes written.  Split-K partials are overhead and excluded."""
+    import numpy as np
+    B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    per_layer = []
+    for l in range(w.num_layers):
+        S = 2 if layer_is_bf16[l] else 1
+        win = w.layer_window(l)
+        teff = [min(int(t), win) if win else int(t) for t in ctx]
+        kv = sum(2 * Hkv * D * S * t for t in teff)
+        table = sum(4 * ((t + 15) // 16 + 1) for t in teff)
+        qo = 2 * B * Hq * D * 2
+        write = B * Hkv * D * (2 * 2 + 2 * S)
+        per_layer.append({"kv": kv, "decode": kv + table + qo, "write": write})
+    return per_layer
+
+
+class DecodeState:
+    def __init__(self, f, w, device, all_bf16=False):
+        import numpy as np
+        import torch
+        import synth
+        self.w = w
+        self.f = f
+        self.ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+        self.table, self.nb = synth.block_table(self.ctx, seed=w.seed)
+        self.mask = np.ones(w.num_layers, np.uint8) if all_bf16 else w.skip_mask()
+        self.bf16 = [bool(x) for x in self.mask]
+        self.gran = f.SCALE_PER_HEAD if w.scale_mode == "amax" else f.SCALE_PER_TENSOR
+        self.table_d = torch.from_numpy(self.table).to(device)
+        self.ctx_d = torch.from_numpy(self.ctx).to(device)
+        cu = np.concatenate([[0], np.cumsum(self.ctx)])
+        last = cu[1:] - 1
+        self.slots_new = torch.from_numpy(synth.slot_mapping(self.table, self.ctx, positions=[[int(t) - 1] for t in self.ctx])).to(device)
+        slots_all = torch.from_numpy(synth.slot_mapping(self.table, self.ctx)).to(device)
+        self.layers = []
+        max_ws = 0
+        for l in range(w.num_layers):
+            data = synth.decode_layer(w, l, self.ctx, device=device)
+            cache = f.LayerCache.empty(self.nb, w.num_kv_heads, w.head_dim, bf16=self.bf16[l], device=device)
+            f.kv_quant_cache(data.k, data.v, slots_all, cache, data.k_scale, data.v_scale, self.gran, layer=l,
+                             skip_layer_mask=self.mask)
+            idx = torch.from_numpy(last).to(device)
+            lay = dict(cache=cache, q=data.q.contiguous(), k_new=data.k[idx].contiguous(), v_new=data.v[idx].contiguous(),
+                       qs=data.q_scale, ks=data.k_scale, vs=data.v_scale, window=w.layer_window(l),
+                       out=torch.empty_like(data.q))
+            self.layers.append(lay)
+            max_ws = max(max_ws, f.fp8_decode_attn_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads,
+                                                                  w.head_dim, self.table.shape[1], lay["window"]))
+            del data
+        torch.cuda.synchronize()
+        self.ws = torch.empty(max_ws, dtype=torch.uint8, device=device)
+        self.bytes = decode_bytes(w, self.ctx, self.bf16)
+
+    def step(self, decode_only=False):
+        f = self.f
+        for l, lay in enumerate(self.layers):
+            if not decode_only:
+                f.kv_quant_cache(lay["k_new"], lay["v_new"], self.slots_new, lay["cache"], lay["ks"], lay["vs"],
+                                 self.gran, layer=l, skip_layer_mask=self.mask)
+            f.fp8_decode_attn(lay["q"], lay["cache"], self.table_d, self.ctx_d, lay["qs"], lay["ks"], lay["vs"],
+                              self.gran, window=lay["window"], layer=l, skip_layer_mask=self.mask, out=lay["out"],
+                              workspace=self.ws)
+
+    def launches_per_step(self):
+        return 3 * len(self.layers)
+
+    def step_bytes(self):
+        return sum(x["decode"] + x["write"] for x in self.bytes)
+
+
+def _graph(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # eager warm-up on the capture stream (sets kernel attributes)
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def _time_graph(g, stream, steps, warmup, barrier):
+    import torch
+    for _ in range(warmup):
+        g.replay()
+    stream.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    return e0.elapsed_time(e1) / steps
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(workload_id: int, keys: int, heads: int):
+    """Time the oracle on one sequence of layer 0: its cache write (quantise K/V) and its
+    decode attention for ``heads`` query heads over ``keys`` cached keys.  Returns
+    (seconds, algorithmic bytes of that sample)."""
+    import numpy as np
+    import synth
+    from oracle import attention, e4m3
+    w = synth.WORKLOADS[workload_id]
+    G = w.group
+    nkv = max(1, heads // G)
+    q = synth.bf16_to_f64(synth.randn_bf16((heads, w.head_dim), w.seed, 0, "q"))
+    k = synth.bf16_to_f64(synth.randn_bf16((keys, nkv, w.head_dim), w.seed, 0, "k"))
+    v = synth.bf16_to_f64(synth.randn_bf16((keys, nkv, w.head_dim), w.seed, 0, "v"))
+    s = np.ones(1, np.float32) * np.float32(0.01)
+    t0 = time.perf_counter()
+    attention.decode_attention_contiguous(q, k, v, s, s, s, fp8=True)
+    dt = time.perf_counter() - t0
+    return dt, 2 * nkv * w.head_dim * keys
+
+
+def _cpu_baseline_subprocess(workload_id: int, keys: int, heads: int):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    code = (f"import bench, json; dt, b = bench.oracle_sample({workload_id}, {keys}, {heads}); "
+            f"print(json.dumps({{'s': dt, 'bytes': b}}))")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        return None
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["s"], d["bytes"]
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, one bounded sample per step."""
+    import synth
+    rank, world, _ = _env_rank()
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[args.workload]
+    heads = w.group
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    probe_keys = 2048
+    dt, _ = oracle_sample(args.workload, probe_keys, heads)
+    keys = int(max(512, min(w.ctx_hi, budget / max(dt, 1e-6) * probe_keys)))
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, keys, heads)
+    tot_s, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        s, b = oracle_sample(args.workload, keys, heads)
+        tot_s += s
+        tot_b += b
+    value = tot_b / tot_s / 1e9
+    sample = f"1 sequence x {keys} keys x {heads} query heads (one KV head) of layer 0, per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import fp8_kv_cache_quant_gb300 as f
+    import synth
+
+    rank, world, local = _env_rank()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    f.load_library()
+    w = synth.WORKLOADS[args.workload]
+    stream = torch.cuda.Stream(device)
+
+    fp8 = DecodeState(f, w, device)
+    g_fp8 = _graph(fp8.step, stream)
+    g_dec = _graph(lambda: fp8.step(decode_only=True), stream)
+
+    # end to end: pinned host inputs -> device, the step, outputs -> pinned host
+    host_in = [(torch.empty_like(l["q"], device="cpu").pin_memory(), torch.empty_like(l["k_new"], device="cpu").pin_memory(),
+                torch.empty_like(l["v_new"], device="cpu").pin_memory()) for l in fp8.layers]
+    for (hq, hk, hv), l in zip(host_in, fp8.layers):
+        hq.copy_(l["q"]); hk.copy_(l["k_new"]); hv.copy_(l["v_new"])
+    host_out = [torch.empty_like(l["out"], device="cpu").pin_memory() for l in fp8.layers]
+    h2d = sum(a.numel() * a.element_size() for t in host_in for a in t)
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
+
+    def e2e_step():
+        for (hq, hk, hv), l in zip(host_in, fp8.layers):
+            l["q"].copy_(hq, non_blocking=True)
+            l["k_new"].copy_(hk, non_blocking=True)
+            l["v_new"].copy_(hv, non_blocking=True)
+        fp8.step()
+        for o, l in zip(host_out, fp8.layers):
+            o.copy_(l["out"], non_blocking=True)
+
+    g_e2e = _graph(e2e_step, stream)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms_fp8 = max_over_ranks(_time_graph(g_fp8, stream, args.steps, args.warmup, barrier))
+    ms_dec = max_over_ranks(_time_graph(g_dec, stream, args.steps, args.warmup, barrier))
+    ms_e2e = max_over_ranks(_time_graph(g_e2e, stream, args.steps, args.warmup, barrier))
+    clocks.stop()
+
+    step_bytes = fp8.step_bytes()
+    value = world * step_bytes / (ms_fp8 * 1e-3) / 1e9
+    e2e_value = world * step_bytes / (ms_e2e * 1e-3) / 1e9
+    dec_bytes = sum(x["decode"] for x in fp8.bytes) / w.num_layers
+    dec_launch_ms = ms_dec / w.num_layers
+    peak, peak_kind = _peaks()
+    achieved = dec_bytes / (dec_launch_ms * 1e-3) / 1e9
+    traffic = _traffic_record("decode_attn.cu", "decode_attn_llama8b_decode.txt")
+
+    # the same step with a bf16 cache (all layers), for the FP8-vs-BF16 per-token cost
+    bf16_info = None
+    if not args.no_bf16:
+        del g_fp8, g_dec, g_e2e
+        bf = DecodeState(f, w, device, all_bf16=True)
+        g_bf = _graph(bf.step, stream)
+        ms_bf = max_over_ranks(_time_graph(g_bf, stream, args.steps, args.warmup, barrier))
+        bf_bytes = bf.step_bytes()
+        kv_fp8 = sum(x["kv"] for x in fp8.bytes)
+        kv_bf = sum(x["kv"] for x in bf.bytes)
+        bf16_info = {"ms_per_step": ms_bf, "GBps": bf_bytes / (ms_bf * 1e-3) / 1e9,
+                     "fp8_over_bf16_step_time": ms_fp8 / ms_bf,
+                     "kv_bytes_fp8": kv_fp8, "kv_bytes_bf16": kv_bf}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        ctx0 = int(fp8.ctx[0])
+        r = _cpu_baseline_subprocess(args.workload, ctx0, w.num_q_heads)
+        if r is not None:
+            s, b = r
+            cpu = {"value": b / s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": f"layer 0, sequence 0 ({ctx0} keys), all {w.num_q_heads} query heads: cache "
+                             f"quantisation + decode attention, {s:.1f} s single-threaded NumPy"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_fp8, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.num_layers, "batch": w.batch, "q_heads": w.num_q_heads,
+                       "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                       "context": [int(x) for x in fp8.ctx], "block_size": 16, "kv_cache_dtype": "e4m3",
+                       "scales": "per-KV-head amax/448" if w.scale_mode == "amax" else "per-tensor 1.0",
+                       "l2": f"no flush: each step reads {step_bytes / 1e9:.2f} GB (> 129 MB L2)",
+                       "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
+            "us_per_step": ms_fp8 * 1e3,
+            "pct_of_hbm_peak": value / peak,
+            "roofline": {"bound": "hbm", "kernel": "fp8_decode_attn (decode_split_kernel + decode_merge_kernel)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
+                         "algorithmic_bytes_per_launch": dec_bytes, "launch_ms": dec_launch_ms},
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": ms_e2e},
+            "gpu_launches": fp8.launches_per_step() * args.steps,
+            "clocks": clocks.summary(),
+            "bf16": bf16_info,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,214 @@
+// The C ABI of libfp8kv.so: argument validation, launch planning and dispatch.
+// Nothing here allocates memory or keeps state between calls.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using fkv::DecodeParams;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int current_num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // no device: plan for a full GB300
+    n = 152;
+  }
+  return n;
+}
+
+bool layer_is_bf16(int32_t layer, const uint8_t* mask, int32_t num_layers, fkv_status* st) {
+  if (mask == nullptr) return false;
+  if (layer < 0 || layer >= num_layers) {
+    *st = FKV_INVALID_ARG;
+    return false;
+  }
+  return mask[layer] != 0;
+}
+
+bool supported_head_dim(int32_t d) { return d == 64 || d == 128 || d == 256; }
+
+bool supported_group(int32_t G, int32_t D) {
+  if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16)) return false;
+  return G * D <= 2048;
+}
+
+struct DecodePlan {
+  int bps = 0;
+  int max_splits = 0;
+  size_t o_bytes = 0, lse_bytes = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Split-K plan.  Blocks per split (bps) are chosen so that the whole grid holds about
+// 16 CTAs per SM when num_splits is 0, within [8, 128] blocks; a requested num_splits
+// sets bps = ceil(blocks / num_splits).  At most 1024 splits per sequence.
+bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_blocks, int32_t window,
+                 int32_t num_splits, DecodePlan* plan) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks <= 0 || window < 0 || num_splits < 0) return false;
+  long long nblk_max = max_blocks;
+  if (window > 0) nblk_max = std::min<long long>(max_blocks, (window + 15) / 16 + 1);
+  long long bps;
+  if (num_splits > 0) {
+    bps = (nblk_max + num_splits - 1) / num_splits;
+  } else {
+    const long long units = static_cast<long long>(std::max(B, 1)) * Hkv;
+    const long long target = static_cast<long long>(current_num_sms()) * 16;
+    bps = (units * nblk_max + target - 1) / target;
+    bps = std::max<long long>(bps, 8);
+  }
+  bps = std::min<long long>(bps, 128);
+  bps = std::max<long long>(bps, (nblk_max + 1023) / 1024);
+  bps = std::max<long long>(bps, 1);
+  if (bps > 128) return false;  // context too long for 1024 splits of 128 blocks
+  plan->bps = static_cast<int>(bps);
+  plan->max_splits = static_cast<int>((nblk_max + bps - 1) / bps);
+  const size_t rows = static_cast<size_t>(B) * Hq * plan->max_splits;
+  plan->o_bytes = align256(rows * D * sizeof(float));
+  plan->lse_bytes = align256(rows * sizeof(float));
+  return true;
+}
+
+fkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FKV_OK : FKV_CUDA_ERROR; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fkv_status_string(fkv_status status) {
+  switch (status) {
+    case FKV_OK: return "ok";
+    case FKV_INVALID_ARG: return "invalid argument";
+    case FKV_UNSUPPORTED: return "unsupported";
+    case FKV_CUDA_ERROR: return "cuda error";
+  }
+  return "unknown status";
+}
+
+int32_t fkv_version(void) { return 100; }
+
+fkv_status kv_quant_cache(const void* k, const void* v, const int64_t* slot_mapping, int32_t n_tokens,
+                          fkv_layer_cache cache, const float* k_scale, const float* v_scale,
+                          fkv_scale_gran gran, int32_t layer, const uint8_t* skip_layer_mask,
+                          int32_t num_layers, int32_t* fault, fkv_stream_t stream) {
+  if (n_tokens < 0) return FKV_INVALID_ARG;
+  if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
+  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0) return FKV_INVALID_ARG;
+  if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
+  if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
+  fkv_status st = FKV_OK;
+  const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
+  if (st != FKV_OK) return st;
+  if (n_tokens == 0) return FKV_OK;
+  if (!k || !v || !slot_mapping || !cache.k_cache || !cache.v_cache) return FKV_INVALID_ARG;
+  if (!bf16 && (!k_scale || !v_scale)) return FKV_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache.k_cache, 16) || !aligned(cache.v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return FKV_INVALID_ARG;
+  return from_cuda(fkv::launch_kv_quant_cache(k, v, slot_mapping, n_tokens, cache, k_scale, v_scale,
+                                              gran == FKV_SCALE_PER_HEAD, bf16, fault,
+                                              reinterpret_cast<cudaStream_t>(stream), current_num_sms()));
+}
+
+size_t fp8_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t max_blocks, int32_t window,
+                                      int32_t num_splits) {
+  DecodePlan plan;
+  if (!supported_head_dim(head_dim)) return 0;
+  if (!plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks, window, num_splits, &plan)) return 0;
+  return plan.o_bytes + plan.lse_bytes;
+}
+
+int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t max_blocks, int32_t window,
+                                   int32_t num_splits) {
+  DecodePlan plan;
+  if (!plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks, window, num_splits, &plan)) return 0;
+  return plan.max_splits;
+}
+
+fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads, fkv_layer_cache cache,
+                           const int32_t* block_table, int32_t max_blocks, const int32_t* context_lens,
+                           const float* q_scale, const float* k_scale, const float* v_scale,
+                           fkv_scale_gran gran, float softmax_scale, int32_t window, int32_t layer,
+                           const uint8_t* skip_layer_mask, int32_t num_layers, void* out, void* workspace,
+                           size_t workspace_bytes, int32_t num_splits, int32_t* fault,
+                           fkv_stream_t stream) {
+  if (batch < 0 || num_q_heads <= 0 || max_blocks <= 0 || window < 0 || num_splits < 0)
+    return FKV_INVALID_ARG;
+  if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
+  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0) return FKV_INVALID_ARG;
+  if (num_q_heads % cache.num_kv_heads != 0) return FKV_INVALID_ARG;
+  if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
+  const int G = num_q_heads / cache.num_kv_heads;
+  if (!supported_group(G, cache.head_dim)) return FKV_UNSUPPORTED;
+  if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
+  if (!(softmax_scale >= 0.f) || std::isinf(softmax_scale)) return FKV_INVALID_ARG;
+  if (batch > 65535 || cache.num_kv_heads > 65535) return FKV_UNSUPPORTED;
+  fkv_status st = FKV_OK;
+  const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
+  if (st != FKV_OK) return st;
+  if (batch == 0) return FKV_OK;
+  if (!q || !out || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || !workspace)
+    return FKV_INVALID_ARG;
+  if (!bf16 && (!q_scale || !k_scale || !v_scale)) return FKV_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(cache.k_cache, 16) || !aligned(cache.v_cache, 16) ||
+      !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+    return FKV_INVALID_ARG;
+  DecodePlan plan;
+  if (!plan_decode(batch, num_q_heads, cache.num_kv_heads, cache.head_dim, max_blocks, window, num_splits, &plan))
+    return FKV_UNSUPPORTED;
+  if (workspace_bytes < plan.o_bytes + plan.lse_bytes) return FKV_INVALID_ARG;
+
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_cache = static_cast<const uint8_t*>(cache.k_cache);
+  p.v_cache = static_cast<const uint8_t*>(cache.v_cache);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.per_head = gran == FKV_SCALE_PER_HEAD;
+  p.B = batch;
+  p.Hq = num_q_heads;
+  p.Hkv = cache.num_kv_heads;
+  p.num_blocks = cache.num_blocks;
+  p.max_blocks = max_blocks;
+  const float tau = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache.head_dim));
+  p.sm_scale_log2 = tau * 1.4426950408889634f;
+  p.window = window;
+  p.bps = plan.bps;
+  p.max_splits = plan.max_splits;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.o_bytes);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.fault = fault;
+  return from_cuda(fkv::launch_decode(p, cache.head_dim, bf16, G, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t fkv_prefill_block_n(int32_t head_dim) { return supported_head_dim(head_dim) ? 128 : 0; }
+
+fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t batch, int32_t num_q_heads,
+                            int32_t max_q_len, fkv_layer_cache cache, const int32_t* block_table,
+                            int32_t max_blocks, const int32_t* context_lens, const float* q_scale,
+                            const float* k_scale, const float* v_scale, fkv_scale_gran gran,
+                            float softmax_scale, int32_t causal, int32_t window, int32_t promote_every,
+                            int32_t layer, const uint8_t* skip_layer_mask, int32_t num_layers, void* out,
+                            int32_t* fault, fkv_stream_t stream) {
+  (void)q; (void)cu_seqlens_q; (void)batch; (void)num_q_heads; (void)max_q_len; (void)cache;
+  (void)block_table; (void)max_blocks; (void)context_lens; (void)q_scale; (void)k_scale; (void)v_scale;
+  (void)gran; (void)softmax_scale; (void)causal; (void)window; (void)promote_every; (void)layer;
+  (void)skip_layer_mask; (void)num_layers; (void)out; (void)fault; (void)stream;
+  return FKV_UNSUPPORTED;
+}
+
+}  // extern "C"

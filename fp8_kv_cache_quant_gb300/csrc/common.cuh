@@ -1,0 +1,144 @@
+// Device helpers shared by the kernels: e4m3 conversions, mbarriers, bulk/TMA copies,
+// bounded waits.  sm_103a only.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fp8kv.h"
+
+#define FKV_DEV __device__ __forceinline__
+
+namespace fkv {
+
+// ---------------------------------------------------------------- fault word
+
+FKV_DEV void raise_fault(int32_t* fault, int32_t bits) {
+  if (fault) atomicOr(fault, bits);
+}
+
+// ---------------------------------------------------------------- e4m3
+
+// Two float32 values -> two e4m3 codes, round-to-nearest-even, saturating to +-448
+// (PTX cvt.rn.satfinite.e4m3x2.f32).  Returns (code(hi) << 8) | code(lo).
+FKV_DEV uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two e4m3 codes (low byte first) -> half2 (exact: every e4m3 value is an f16 value).
+FKV_DEV __half2 e4m3x2_to_h2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return *reinterpret_cast<__half2*>(&r);
+}
+
+// Four e4m3 codes packed little-endian in a word -> four floats (exact).
+FKV_DEV void e4m3x4_to_f32(uint32_t w, float& a, float& b, float& c, float& d) {
+  float2 lo = __half22float2(e4m3x2_to_h2(static_cast<uint16_t>(w & 0xFFFFu)));
+  float2 hi = __half22float2(e4m3x2_to_h2(static_cast<uint16_t>(w >> 16)));
+  a = lo.x; b = lo.y; c = hi.x; d = hi.y;
+}
+
+FKV_DEV void e4m3x4_to_f2(uint32_t w, float2& lo, float2& hi) {
+  lo = __half22float2(e4m3x2_to_h2(static_cast<uint16_t>(w & 0xFFFFu)));
+  hi = __half22float2(e4m3x2_to_h2(static_cast<uint16_t>(w >> 16)));
+}
+
+// Two bf16 packed in a word -> float2 (exact).
+FKV_DEV float2 bf16x2_to_f2(uint32_t w) {
+  float2 r;
+  r.x = __uint_as_float(w << 16);
+  r.y = __uint_as_float(w & 0xFFFF0000u);
+  return r;
+}
+
+// ---------------------------------------------------------------- shared memory / mbarrier
+
+FKV_DEV uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+FKV_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+FKV_DEV void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+FKV_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+FKV_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+FKV_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+FKV_DEV uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete, for at most ~timeout_ns of
+// wall time.  Returns false on timeout (the caller records a fault and unwinds).
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
+
+FKV_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
+// One-dimensional bulk copy global -> shared, completion counted on an mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+FKV_DEV void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+FKV_DEV void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+FKV_DEV float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+FKV_DEV float lg2(float x) {
+  float y;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace fkv

@@ -1,0 +1,503 @@
+// Paged GQA decode attention over an e4m3 (or bf16) KV pool, split-K over the context,
+// FP32 softmax state and P.V sums, then an FP32 log-sum-exp merge of the splits.
+//
+// The vLLM blog "FP8 KV-Cache and Attention quantization in vLLM": the decode step must
+// read every cached token, so its cost is the cache bytes (section "性能 Benchmark");
+// the blog tunes dedicated decode configurations (section "Kernel 与 vLLM 改进", "优化
+// FA3 FP8 tile size") and promotes partial sums into true FP32 registers ("Two-level
+// accumulation").  Here each split's partial output lives in FP32 registers and the
+// splits are merged in FP32, so a 128k-key contraction never accumulates in a reduced
+// precision register.
+//
+// CTA = (split, KV head g, sequence b); it serves all G query heads of g, so each K/V
+// byte is read from HBM once.  Warp NCW (the producer) copies each 16-token block's
+// contiguous K chunk and V chunk ([block][g][16][D] in the pool) into a shared-memory
+// ring with cp.async.bulk, completion counted on an mbarrier per stage.  Consumer warp
+// w takes blocks w, w+NCW, ...; per block:
+//   QK : lanes split (key, d-slice); FP32 FMAs on exact e4m3->f32 values; a transposing
+//        shuffle reduction leaves each lane with whole scores;
+//   softmax: running max m and sum l per head (base-2 domain), rescale factor per block;
+//   PV : lanes split (key sub-group, d-slice); acc[h][d] += p[h][key] * v[key][d].
+// The warps' states are merged in shared memory and written as (o / l, log2-sum-exp).
+// Every wait is bounded in time; on a timeout the CTA records FKV_FAULT_TIMEOUT, lets
+// its in-flight copies land and returns.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fkv {
+
+// Per-sequence key range in blocks; shared by the split and the merge kernels.
+struct SeqRange {
+  int T, lo, blk_begin, blk_end, nsplit;
+};
+
+FKV_DEV SeqRange seq_range(const DecodeParams& p, int b, bool report) {
+  SeqRange r;
+  int T = p.context_lens[b];
+  const int cap = p.max_blocks * 16;
+  if (T < 0 || T > cap) {
+    if (report) raise_fault(p.fault, FKV_FAULT_CONTEXT);
+    T = T < 0 ? 0 : cap;
+  }
+  r.T = T;
+  r.lo = p.window > 0 ? max(0, T - p.window) : 0;
+  r.blk_begin = r.lo >> 4;
+  r.blk_end = (T + 15) >> 4;
+  const int nb = r.blk_end - r.blk_begin;
+  r.nsplit = nb > 0 ? (nb + p.bps - 1) / p.bps : 0;
+  return r;
+}
+
+constexpr int kNCW = 4;           // consumer warps
+constexpr int kMaxBps = 128;      // blocks per split, upper bound (table ids staged in smem)
+
+template <int D, int ELT, int G>
+struct DecodeCfg {
+  static constexpr int CHUNK = 16 * D * ELT;                  // bytes of one (block, head) chunk
+  // QK mapping: EPL elements (EPL*ELT bytes) of one key per lane
+  static constexpr int EPL = ELT == 1 ? (G <= 4 ? 16 : (G == 8 ? 8 : 4)) : (G <= 8 ? 8 : 4);
+  static constexpr int LPK = D / EPL;                         // lanes per key
+  static constexpr int KPR = 32 / LPK;                        // keys per round
+  static constexpr int ROUNDS = 16 / KPR;
+  static constexpr int NVF = G > LPK ? G / LPK : 1;           // scores per lane per round
+  // PV mapping: VPL elements of one value row per lane
+  static constexpr int VPL0 = ELT == 1 ? (G <= 4 ? 8 : (G == 8 ? 4 : 2)) : (G <= 4 ? 4 : 2);
+  static constexpr int VPL = VPL0 > D / 32 ? VPL0 : D / 32;
+  static constexpr int LPV = D / VPL;                         // lanes per value row
+  static constexpr int KPV = 32 / LPV;                        // keys in parallel
+  static constexpr int STAGES = (2 * CHUNK <= 8192) ? 8 : 4;
+  static constexpr int RING = STAGES * 2 * CHUNK;
+  static_assert(LPK >= 2 && LPK <= 32, "lanes per key");
+  static_assert(LPV >= 1 && LPV <= 32, "lanes per value row");
+  static_assert(G * VPL <= 64 && G * EPL <= 64, "register budget");
+  static_assert(STAGES % kNCW == 0, "stage ownership");
+  static_assert(kNCW * G * D * 4 <= RING, "the warps' accumulators are merged inside the ring");
+};
+
+template <int N>
+FKV_DEV void load_bytes(const uint8_t* p, uint32_t (&w)[N / 4 > 0 ? N / 4 : 1]) {
+  if constexpr (N == 16) {
+    const uint4 x = *reinterpret_cast<const uint4*>(p);
+    w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+  } else if constexpr (N == 8) {
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    w[0] = x.x; w[1] = x.y;
+  } else if constexpr (N == 4) {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  } else {
+    w[0] = *reinterpret_cast<const uint16_t*>(p);
+  }
+}
+
+// Convert N elements (e4m3 or bf16) held in words to float2 pairs.
+template <int ELT, int N>
+FKV_DEV void to_f2(const uint32_t* w, float2* out) {
+  if constexpr (ELT == 1) {
+    if constexpr (N >= 4) {
+#pragma unroll
+      for (int i = 0; i < N / 4; ++i) e4m3x4_to_f2(w[i], out[2 * i], out[2 * i + 1]);
+    } else {
+      out[0] = __half22float2(e4m3x2_to_h2(static_cast<uint16_t>(w[0] & 0xFFFFu)));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) out[i] = bf16x2_to_f2(w[i]);
+  }
+}
+
+template <int D, int ELT, int G>
+__global__ void __launch_bounds__((kNCW + 1) * 32) decode_split_kernel(const DecodeParams p) {
+  using C = DecodeCfg<D, ELT, G>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING);
+  uint64_t* empty = full + C::STAGES;
+  float* p_s = reinterpret_cast<float*>(empty + C::STAGES);  // [NCW][16][G]
+  float* alpha_s = p_s + kNCW * 16 * G;                        // [NCW][G]
+  float* ml_s = alpha_s + kNCW * G;                            // [NCW][2][G]
+  int* ids_s = reinterpret_cast<int*>(ml_s + kNCW * 2 * G);    // [kMaxBps]
+  volatile int* abort_s = ids_s + kMaxBps;
+
+  const int sigma = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqRange r = seq_range(p, b, sigma == 0 && g == 0 && threadIdx.x == 0);
+  if (sigma >= r.nsplit) return;  // uniform over the CTA
+  const int blk_first = r.blk_begin + sigma * p.bps;
+  const int nblk = min(p.bps, r.blk_end - blk_first);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    *abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == kNCW) {
+    const int* row = p.block_table + static_cast<size_t>(b) * p.max_blocks + blk_first;
+    for (int i = lane; i < nblk; i += 32) {
+      int id = row[i];
+      if (id < 0 || id >= p.num_blocks) {
+        raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
+        id = 0;
+      }
+      ids_s[i] = id;
+    }
+  }
+  __syncthreads();
+
+  // consumer state lives at function scope so that it survives the CTA barriers below
+  const int kq = lane / C::LPK;  // key within a QK round
+  const int dq = (lane % C::LPK) * C::EPL;
+  const int vg = lane / C::LPV, dv = (lane % C::LPV) * C::VPL;
+  float2 acc[G][C::VPL / 2 > 0 ? C::VPL / 2 : 1];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
+
+  if (warp == kNCW) {
+    // ------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nblk; ++i) {
+        const int st = i % C::STAGES, use = i / C::STAGES;
+        if (use > 0 && !mbar_wait_bounded(&empty[st], (use - 1) & 1)) {
+          raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+          *abort_s = 1;
+          break;
+        }
+        if (*abort_s) break;
+        const size_t off = (static_cast<size_t>(ids_s[i]) * p.Hkv + g) * C::CHUNK;
+        mbar_arrive_expect_tx(&full[st], 2 * C::CHUNK);
+        bulk_g2s(ring + st * 2 * C::CHUNK, p.k_cache + off, C::CHUNK, &full[st]);
+        bulk_g2s(ring + st * 2 * C::CHUNK + C::CHUNK, p.v_cache + off, C::CHUNK, &full[st]);
+        issued = i + 1;
+      }
+      // let every issued copy land before the CTA may exit
+      for (int i = max(0, issued - C::STAGES); i < issued; ++i) {
+        if (!mbar_wait_bounded(&full[i % C::STAGES], (i / C::STAGES) & 1)) {
+          raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ consumers
+    const int h0 = g * G;
+    // softmax constant per head: softmax_scale * log2(e) * q_s * k_s
+    float cst[G];
+    const float ks = ELT == 1 ? p.k_scale[p.per_head ? g : 0] : 1.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      cst[h] = p.sm_scale_log2 * (ELT == 1 ? p.q_scale[p.per_head ? h0 + h : 0] * ks : 1.f);
+
+    // query slice for the QK mapping: lane's d-range [dq, dq + EPL)
+    float2 qf[G][C::EPL / 2];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const __nv_bfloat16* qp = p.q + (static_cast<size_t>(b) * p.Hq + h0 + h) * D + dq;
+      const float iq = ELT == 1 ? __frcp_rn(p.q_scale[p.per_head ? h0 + h : 0]) : 1.f;
+#pragma unroll
+      for (int e = 0; e < C::EPL / 2; ++e) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(qp + 2 * e);
+        float2 x = bf16x2_to_f2(w);
+        if constexpr (ELT == 1) {
+          const uint16_t c = f32x2_to_e4m3x2(__fmul_rn(x.x, iq), __fmul_rn(x.y, iq));
+          x = __half22float2(e4m3x2_to_h2(c));
+        }
+        qf[h][e] = x;
+      }
+    }
+
+    // head base of this lane after the transposing reduction
+    int hb = 0;
+    {
+      int nv = G;
+#pragma unroll
+      for (int off = C::LPK / 2; off >= 1; off >>= 1) {
+        if (nv > 1) {
+          if (lane & off) hb += nv / 2;
+          nv >>= 1;
+        }
+      }
+    }
+    const bool dup0 = (C::LPK <= G) ? true : ((lane % C::LPK) % (C::LPK / G) == 0);
+
+    // this lane's heads are hb .. hb+NVF-1: pick their constants without dynamic indexing
+    float cl[C::NVF];
+#pragma unroll
+    for (int j = 0; j < C::NVF; ++j) {
+      cl[j] = cst[0];
+#pragma unroll
+      for (int h = 1; h < G; ++h)
+        if (h == hb + j) cl[j] = cst[h];
+    }
+
+    float m_run[C::NVF], l_run[C::NVF];
+#pragma unroll
+    for (int i = 0; i < C::NVF; ++i) { m_run[i] = -INFINITY; l_run[i] = 0.f; }
+
+    float* pw = p_s + warp * 16 * G;
+    float* aw = alpha_s + warp * G;
+
+    for (int i = warp; i < nblk; i += kNCW) {
+      const int st = i % C::STAGES, use = i / C::STAGES;
+      if (!mbar_wait_bounded(&full[st], use & 1)) {
+        raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+        *abort_s = 1;
+        break;
+      }
+      const uint8_t* kb = ring + st * 2 * C::CHUNK;
+      const uint8_t* vb = kb + C::CHUNK;
+      const int key0 = (blk_first + i) * 16;  // absolute position of the block's first key
+
+      // ---------------- QK
+      float sc[C::ROUNDS][C::NVF];
+#pragma unroll
+      for (int rr = 0; rr < C::ROUNDS; ++rr) {
+        const int key = rr * C::KPR + kq;
+        uint32_t w[C::EPL * ELT / 4 > 0 ? C::EPL * ELT / 4 : 1];
+        load_bytes<C::EPL * ELT>(kb + key * D * ELT + dq * ELT, w);
+        float2 kf[C::EPL / 2];
+        to_f2<ELT, C::EPL>(w, kf);
+        float v[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < C::EPL / 2; ++e) a = __ffma2_rn(qf[h][e], kf[e], a);
+          v[h] = a.x + a.y;
+        }
+        // transposing reduction across the LPK lanes of this key
+        int nv = G;
+#pragma unroll
+        for (int off = C::LPK / 2; off >= 1; off >>= 1) {
+          if (nv > 1) {
+            const bool up = lane & off;
+#pragma unroll
+            for (int j = 0; j < nv / 2; ++j) {
+              const float send = up ? v[j] : v[j + nv / 2];
+              const float keep = up ? v[j + nv / 2] : v[j];
+              v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+            nv >>= 1;
+          } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+          }
+        }
+        const int kabs = key0 + key;
+        const bool valid = kabs >= r.lo && kabs < r.T;
+#pragma unroll
+        for (int j = 0; j < C::NVF; ++j) sc[rr][j] = valid ? v[j] * cl[j] : -INFINITY;
+      }
+
+      // ---------------- softmax (base 2)
+      float bmax[C::NVF], bsum[C::NVF], alpha[C::NVF];
+#pragma unroll
+      for (int j = 0; j < C::NVF; ++j) {
+        float mx = sc[0][j];
+#pragma unroll
+        for (int rr = 1; rr < C::ROUNDS; ++rr) mx = fmaxf(mx, sc[rr][j]);
+#pragma unroll
+        for (int off = C::LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        bmax[j] = mx;
+      }
+#pragma unroll
+      for (int j = 0; j < C::NVF; ++j) {
+        const float mn = fmaxf(m_run[j], bmax[j]);
+        alpha[j] = (m_run[j] == -INFINITY) ? 0.f : ex2(m_run[j] - mn);
+        m_run[j] = mn;
+        float s = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < C::ROUNDS; ++rr) {
+          const float pv = ex2(sc[rr][j] - mn);
+          s += pv;
+          if (dup0) pw[(rr * C::KPR + kq) * G + hb + j] = pv;
+        }
+#pragma unroll
+        for (int off = C::LPK; off < 32; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        bsum[j] = s;
+        l_run[j] = l_run[j] * alpha[j] + s;
+        if (dup0 && kq == 0) aw[hb + j] = alpha[j];
+      }
+      __syncwarp();
+
+      // ---------------- PV
+      bool rescale = false;
+#pragma unroll
+      for (int h = 0; h < G; ++h) rescale |= (aw[h] != 1.f);
+      if (rescale) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float a = aw[h];
+          const float2 a2 = make_float2(a, a);
+#pragma unroll
+          for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < 16 / C::KPV; ++kk) {
+        const int key = kk * C::KPV + vg;
+        uint32_t w[C::VPL * ELT / 4 > 0 ? C::VPL * ELT / 4 : 1];
+        load_bytes<C::VPL * ELT>(vb + key * D * ELT + dv * ELT, w);
+        float2 vf[C::VPL / 2];
+        to_f2<ELT, C::VPL>(w, vf);
+        const float* pk = pw + key * G;
+        float pv[G];
+        if constexpr (G % 4 == 0) {
+#pragma unroll
+          for (int h = 0; h < G; h += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(pk + h);
+            pv[h] = x.x; pv[h + 1] = x.y; pv[h + 2] = x.z; pv[h + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < G; ++h) pv[h] = pk[h];
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float pp = pv[h];
+          const float2 p2 = make_float2(pp, pp);
+#pragma unroll
+          for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      (void)bsum;
+    }
+
+    // reduce the key sub-groups of the PV mapping
+#pragma unroll
+    for (int off = C::LPV; off < 32; off <<= 1) {
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < C::VPL / 2; ++e) {
+          acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, off);
+          acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, off);
+        }
+    }
+    // publish m, l of this warp
+    if (dup0 && kq == 0) {
+#pragma unroll
+      for (int j = 0; j < C::NVF; ++j) {
+        ml_s[(warp * 2 + 0) * G + hb + j] = m_run[j];
+        ml_s[(warp * 2 + 1) * G + hb + j] = l_run[j];
+      }
+    }
+  }
+  __syncthreads();  // every copy has landed (producer drained) and every consumer is done
+  // stage the accumulators in the ring
+  float* acc_w = reinterpret_cast<float*>(ring);  // [NCW][G][D]
+  if (warp < kNCW && vg == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < C::VPL / 2; ++e)
+        *reinterpret_cast<float2*>(acc_w + (warp * G + h) * D + dv + 2 * e) = acc[h][e];
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------- merge the warps, write the split
+  const float* acc_s = reinterpret_cast<const float*>(ring);
+  for (int t = threadIdx.x; t < G * D; t += blockDim.x) {
+    const int h = t / D, d = t % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kNCW; ++w) M = fmaxf(M, ml_s[(w * 2) * G + h]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kNCW; ++w) {
+        const float mw = ml_s[(w * 2) * G + h];
+        if (mw == -INFINITY) continue;
+        const float f = ex2(mw - M);
+        L += ml_s[(w * 2 + 1) * G + h] * f;
+        O += acc_s[(w * G + h) * D + d] * f;
+      }
+    }
+    const size_t row = (static_cast<size_t>(b) * p.Hq + g * G + h) * p.max_splits + sigma;
+    p.o_part[row * D + d] = L > 0.f ? O / L : 0.f;
+    if (d == 0) p.lse_part[row] = L > 0.f ? M + lg2(L) : -INFINITY;
+  }
+}
+
+// Merge the splits of one (sequence, query head): o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
+// times the V scale, to bf16.  FP32 throughout.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p, int G, int apply_vscale) {
+  const int bh = blockIdx.x;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const SeqRange r = seq_range(p, b, false);
+  const size_t row0 = static_cast<size_t>(bh) * p.max_splits;
+  __shared__ float w_s[1024];
+  __shared__ float red_s[2];
+  const int ns = min(r.nsplit, 1024);
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, p.lse_part[row0 + s]);
+  float W = 0.f;
+  for (int s = threadIdx.x; s < ns; s += blockDim.x) {
+    const float l = p.lse_part[row0 + s];
+    w_s[s] = (l == -INFINITY) ? 0.f : ex2(l - M);
+  }
+  __syncthreads();
+  for (int s = 0; s < ns; ++s) W += w_s[s];
+  const float vs = apply_vscale ? p.v_scale[p.per_head ? h / G : 0] : 1.f;
+  const float inv = (W > 0.f) ? vs / W : 0.f;
+  for (int d = threadIdx.x * 2; d < D; d += blockDim.x * 2) {
+    float2 o = make_float2(0.f, 0.f);
+    for (int s = 0; s < ns; ++s) {
+      const float2 x = *reinterpret_cast<const float2*>(p.o_part + (row0 + s) * D + d);
+      o.x += w_s[s] * x.x;
+      o.y += w_s[s] * x.y;
+    }
+    __nv_bfloat162 y = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+    *reinterpret_cast<__nv_bfloat162*>(p.out + static_cast<size_t>(bh) * D + d) = y;
+  }
+  (void)red_s;
+}
+
+template <int D, int ELT, int G>
+size_t decode_smem_bytes() {
+  using C = DecodeCfg<D, ELT, G>;
+  return C::RING + 2 * C::STAGES * sizeof(uint64_t) + (kNCW * 16 * G + kNCW * G + kNCW * 2 * G) * sizeof(float) +
+         (kMaxBps + 4) * sizeof(int);
+}
+
+template <int D, int ELT, int G>
+cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
+  const size_t smem = decode_smem_bytes<D, ELT, G>();
+  auto kern = decode_split_kernel<D, ELT, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.max_splits, p.Hkv, p.B);
+  kern<<<grid, (kNCW + 1) * 32, smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<D><<<p.B * p.Hq, 128, 0, s>>>(p, G, ELT == 1 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+template <int D, int ELT>
+cudaError_t launch_decode_g(const DecodeParams& p, int G, cudaStream_t s) {
+  switch (G) {
+    case 1: return launch_decode_t<D, ELT, 1>(p, s);
+    case 2: return launch_decode_t<D, ELT, 2>(p, s);
+    case 4: return launch_decode_t<D, ELT, 4>(p, s);
+    case 8: return launch_decode_t<D, ELT, 8>(p, s);
+    case 16:
+      if constexpr (D <= 128) return launch_decode_t<D, ELT, 16>(p, s);
+      else return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16_layer, int G, cudaStream_t s) {
+  if (D == 64) return bf16_layer ? launch_decode_g<64, 2>(p, G, s) : launch_decode_g<64, 1>(p, G, s);
+  if (D == 128) return bf16_layer ? launch_decode_g<128, 2>(p, G, s) : launch_decode_g<128, 1>(p, G, s);
+  if (D == 256) return bf16_layer ? launch_decode_g<256, 2>(p, G, s) : launch_decode_g<256, 1>(p, G, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fkv

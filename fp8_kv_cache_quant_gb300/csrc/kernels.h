@@ -1,0 +1,39 @@
+// Internal launcher interfaces between the C ABI (abi.cu) and the kernel files.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/fp8kv.h"
+
+namespace fkv {
+
+struct DecodeParams {
+  const __nv_bfloat16* q;      // [B][Hq][D]
+  const uint8_t* k_cache;      // pool bytes
+  const uint8_t* v_cache;
+  const int32_t* block_table;  // [B][max_blocks]
+  const int32_t* context_lens; // [B]
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  int per_head;
+  int B, Hq, Hkv, num_blocks, max_blocks;
+  float sm_scale_log2;  // softmax_scale * log2(e)
+  int window;
+  int bps;              // blocks per split
+  int max_splits;
+  float* o_part;        // [B][Hq][max_splits][D]
+  float* lse_part;      // [B][Hq][max_splits], base 2
+  __nv_bfloat16* out;   // [B][Hq][D]
+  int32_t* fault;
+};
+
+cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* slots, int n_tokens,
+                                  const fkv_layer_cache& cache, const float* ks, const float* vs,
+                                  int per_head, bool bf16_layer, int32_t* fault, cudaStream_t s,
+                                  int num_sms);
+
+cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16_layer, int G, cudaStream_t s);
+
+}  // namespace fkv

@@ -1,0 +1,203 @@
+/*
+ * fp8kv — FP8 (e4m3) KV-cache quantisation and FP8 attention for GB300 (sm_103a).
+ *
+ * C ABI of libfp8kv.so.  Every tensor argument is a plain device pointer owned by the
+ * caller; the library allocates nothing, keeps no global state, and enqueues its
+ * kernels on the given stream without synchronising.  Host pointers are marked "host".
+ *
+ * The operations restate the vLLM blog "FP8 KV-Cache and Attention quantization in
+ * vLLM" (2026-04-22):
+ *   - 引言: `--kv-cache-dtype fp8` stores K/V in e4m3 and runs the whole attention in
+ *     FP8, the QK and Score*V matrix products included;
+ *   - "Kernel 与 vLLM 改进": two-level accumulation (partial sums promoted into a true
+ *     FP32 register), skip layers (`--kv-cache-dtype-skip-layers sliding_window` keeps
+ *     sliding-window layers in BF16), per-head scales (one scale per KV head, also for
+ *     the cache write `reshape_and_cache_flash`), query quantisation, decode-tuned
+ *     configurations;
+ *   - "大 Head Dimension 的限制": promoting every N steps or never (prefill).
+ *
+ * Formats and layouts (fixed by this library; the pages are silent on them):
+ *   e4m3      FP8 E4M3 "fn": 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no
+ *             infinities, S.1111.111 = NaN, largest finite +-448.  Quantisation of x
+ *             with scale s is e4m3(fl32(x * fl32(1/s))), round-to-nearest-even,
+ *             saturating; dequantisation is code * s.
+ *   K/V pool  per layer, [num_blocks][num_kv_heads][block_size][head_dim], one byte per
+ *             element (e4m3) or two (bf16, skip layers); block_size must be 16.
+ *   positions token position p of sequence b lives in slot
+ *             block_table[b][p / 16] * 16 + p % 16.
+ *   scales    float32 device arrays.  FKV_SCALE_PER_TENSOR: q/k/v scale arrays hold one
+ *             value.  FKV_SCALE_PER_HEAD: k/v scales hold num_kv_heads values and the
+ *             query scale num_q_heads values.
+ *   GQA       query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Errors.  Argument checks run on the host before anything is enqueued and return
+ * FKV_INVALID_ARG or FKV_UNSUPPORTED; a failed launch returns FKV_CUDA_ERROR.  Data
+ * errors that only the GPU can see (a block id outside [0, num_blocks), a slot outside
+ * the pool, a context longer than the block table, a prefill chunk longer than its
+ * context, a pipeline wait that ran out of time) never trap: the kernel skips or
+ * clamps the access and ORs an FKV_FAULT_* bit into *fault (a caller-owned device
+ * int32, may be NULL).  Kernels never spin without a time bound.
+ */
+#ifndef FP8KV_H
+#define FP8KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* fkv_stream_t;
+
+typedef enum {
+  FKV_OK = 0,
+  FKV_INVALID_ARG = 1,  /* NULL pointer, negative size, misaligned pointer, ...      */
+  FKV_UNSUPPORTED = 2,  /* valid but not implemented (head_dim, group size, ...)    */
+  FKV_CUDA_ERROR = 3    /* a CUDA call or kernel launch failed                      */
+} fkv_status;
+
+typedef enum {
+  FKV_SCALE_PER_TENSOR = 0, /* one scale for Q, one for K, one for V                 */
+  FKV_SCALE_PER_HEAD = 1    /* K/V: one per KV head; Q: one per query head           */
+} fkv_scale_gran;
+
+/* Bits ORed into the caller's device fault word. */
+#define FKV_FAULT_BLOCK_ID 1 /* block table entry outside [0, num_blocks): block 0 read instead */
+#define FKV_FAULT_SLOT 2     /* cache-write slot >= num_blocks * block_size: token skipped      */
+#define FKV_FAULT_CONTEXT 4  /* context length < 0 or > max_blocks * block_size: clamped      */
+#define FKV_FAULT_TIMEOUT 8  /* an in-kernel pipeline wait exceeded 1 s: work abandoned        */
+#define FKV_FAULT_QLEN 16    /* prefill: query length > context length: sequence skipped     */
+
+/* One layer of the paged cache.  k_cache / v_cache: device pools, 16-byte aligned,
+ * [num_blocks][num_kv_heads][block_size][head_dim] of e4m3 (1 byte) or bf16 (2 bytes),
+ * the element type being chosen per layer by the skip-layer mask. */
+typedef struct {
+  void* k_cache;
+  void* v_cache;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+} fkv_layer_cache;
+
+/* Human-readable name of a status code (static string). */
+const char* fkv_status_string(fkv_status status);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t fkv_version(void);
+
+/*
+ * kv_quant_cache — write new tokens' K and V into one layer of the paged cache.
+ *
+ * The blog's cache write (`reshape_and_cache_flash`, section "Kernel 与 vLLM 改进",
+ * paragraph "Per-Head Scales") extended to a per-KV-head scale array; skip layers
+ * ("跳过 Layer") are stored as an exact bf16 copy.
+ *
+ *   k, v          device bf16 [n_tokens][num_kv_heads][head_dim], contiguous, 16-byte aligned
+ *   slot_mapping  device int64 [n_tokens]; slot = block * 16 + offset; a negative slot
+ *                 skips the token (padding); a slot beyond the pool raises FKV_FAULT_SLOT
+ *   cache         the layer's pools (see fkv_layer_cache)
+ *   k_scale, v_scale  device float32 [1] or [num_kv_heads] (per gran); unused for
+ *                 skip layers (may be NULL there)
+ *   layer, skip_layer_mask (host uint8 [num_layers], may be NULL = no skipped layer),
+ *   num_layers    skip_layer_mask[layer] != 0 selects the bf16 pool format
+ *   fault         device int32 or NULL
+ * Each element is e4m3(fl32(x * fl32(1/scale))) (round-to-nearest-even, saturating);
+ * every other byte of the pools keeps its value.
+ */
+fkv_status kv_quant_cache(const void* k, const void* v, const int64_t* slot_mapping,
+                          int32_t n_tokens, fkv_layer_cache cache, const float* k_scale,
+                          const float* v_scale, fkv_scale_gran gran, int32_t layer,
+                          const uint8_t* skip_layer_mask, int32_t num_layers,
+                          int32_t* fault, fkv_stream_t stream);
+
+/*
+ * Workspace bytes fp8_decode_attn needs for these sizes (same argument meaning as
+ * there).  Returns 0 for invalid sizes.
+ */
+size_t fp8_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t max_blocks, int32_t window,
+                                      int32_t num_splits);
+
+/* Number of context splits per sequence fp8_decode_attn uses for these sizes. */
+int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t max_blocks, int32_t window,
+                                   int32_t num_splits);
+
+/*
+ * fp8_decode_attn — one decode step of paged GQA attention for one layer.
+ *
+ * For every sequence b and query head h (KV head g = h / G): keys j in
+ * [lo, T_b) with T_b = context_lens[b] (the current token included, already written
+ * by kv_quant_cache) and lo = max(0, T_b - window) (window 0 = all keys);
+ *   s_j = (e4m3(q*1/q_s) * q_s) . (k8_j * k_s[g]) * softmax_scale,
+ *   out = sum_j softmax(s)_j * (v8_j * v_s[g])     (bf16 [batch][num_q_heads][head_dim]).
+ * The context is split across CTAs (split-K, the blog's decode-tuned configurations);
+ * each split keeps its softmax state and P.V sum in FP32 registers and a second kernel
+ * merges the splits through their log-sum-exp in FP32 — the two-level accumulation of
+ * the blog's "Two-level accumulation" paragraph, so a 100k+ key contraction is summed
+ * in true FP32.  Skip layers read a bf16 pool and quantise nothing.
+ *
+ *   q             device bf16 [batch][num_q_heads][head_dim]
+ *   block_table   device int32 [batch][max_blocks]
+ *   context_lens  device int32 [batch]
+ *   q_scale, k_scale, v_scale  device float32 (see gran); unused on skip layers
+ *   softmax_scale 0 selects 1/sqrt(head_dim)
+ *   window        0 = full attention, else the number of most recent keys attended
+ *   out           device bf16 [batch][num_q_heads][head_dim]
+ *   workspace     device, >= fp8_decode_attn_workspace_size(...) bytes, 256-byte aligned;
+ *                 scratch only (no state is kept across calls)
+ *   num_splits    0 = automatic, else the requested number of context splits
+ * head_dim in {64, 128, 256}; G = num_q_heads / num_kv_heads in {1, 2, 4, 8, 16} with
+ * G * head_dim <= 2048.  A sequence with no key gets a zero row.
+ */
+fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads,
+                           fkv_layer_cache cache, const int32_t* block_table, int32_t max_blocks,
+                           const int32_t* context_lens, const float* q_scale, const float* k_scale,
+                           const float* v_scale, fkv_scale_gran gran, float softmax_scale,
+                           int32_t window, int32_t layer, const uint8_t* skip_layer_mask,
+                           int32_t num_layers, void* out, void* workspace, size_t workspace_bytes,
+                           int32_t num_splits, int32_t* fault, fkv_stream_t stream);
+
+/* Keys per tile of fp8_prefill_attn (its online-softmax and P-rounding granularity). */
+int32_t fkv_prefill_block_n(int32_t head_dim);
+
+/*
+ * fp8_prefill_attn — FP8 prefill (chunked) attention on tcgen05 tensor cores.
+ *
+ * Query row i of sequence b (rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1) sits at absolute
+ * position p = context_lens[b] - Lq_b + i (the chunk is the tail of the context, its own
+ * K/V already written by kv_quant_cache).  With causal != 0 it attends keys [0, p], else
+ * all context_lens[b] keys.  Q is quantised to e4m3 in the kernel prologue; S = Q8.K8^T
+ * and O_tile = P8.V8 run on the tensor cores with FP32 accumulation in tensor memory;
+ * per tile of fkv_prefill_block_n(head_dim) keys the online softmax takes the running
+ * max m, P8 = e4m3(exp(s - m) * 448), the denominator sums the unrounded p, and the
+ * tile's O partial is promoted into an FP32 accumulator (two-level accumulation).
+ * The result is O * v_s / (448 * l) as bf16.
+ *
+ *   q             device bf16 [total_q][num_q_heads][head_dim] (total_q = cu_seqlens_q[batch])
+ *   cu_seqlens_q  device int32 [batch + 1], non-decreasing, starting at 0
+ *   max_q_len     host upper bound of every Lq_b (sizes the grid)
+ *   causal        non-zero for causal masking
+ *   window        must be 0 (sliding-window prefill is not implemented: FKV_UNSUPPORTED)
+ *   promote_every must be 1 (two-level accumulation every tile); other values are
+ *                 FKV_UNSUPPORTED
+ *   out           device bf16 [total_q][num_q_heads][head_dim]
+ * head_dim in {64, 128, 256}; skip (bf16) layers are FKV_UNSUPPORTED.
+ */
+fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t batch,
+                            int32_t num_q_heads, int32_t max_q_len, fkv_layer_cache cache,
+                            const int32_t* block_table, int32_t max_blocks,
+                            const int32_t* context_lens, const float* q_scale,
+                            const float* k_scale, const float* v_scale, fkv_scale_gran gran,
+                            float softmax_scale, int32_t causal, int32_t window,
+                            int32_t promote_every, int32_t layer, const uint8_t* skip_layer_mask,
+                            int32_t num_layers, void* out, int32_t* fault, fkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8KV_H */

@@ -1,0 +1,113 @@
+"""The C ABI on the host (no GPU needed): the library loads, exports every entry point
+include/fp8kv.h declares, plans split-K sizes, and rejects invalid arguments before
+anything is enqueued."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+f = pytest.importorskip("fp8_kv_cache_quant_gb300")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "fp8kv.h")).read()
+    return set(re.findall(r"^(?:const char\*|fkv_status|size_t|int32_t)\s+(\w+)\(", text, re.M))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(f.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return f.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert names == set(f.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert lib.fkv_status_string(0) == b"ok"
+    assert lib.fkv_status_string(1) == b"invalid argument"
+    assert lib.fkv_status_string(2) == b"unsupported"
+    assert lib.fkv_status_string(3) == b"cuda error"
+    assert lib.fkv_version() >= 100
+
+
+def test_split_planning(lib):
+    # the Llama-shaped decode workload: 8 sequences of up to 1536 blocks
+    n = f.fp8_decode_attn_num_splits(8, 32, 8, 128, 1536)
+    assert 1 <= n <= 1024
+    ws = f.fp8_decode_attn_workspace_size(8, 32, 8, 128, 1536)
+    assert ws >= 8 * 32 * n * (128 + 1) * 4
+    # a requested split count is honoured when blocks allow it
+    assert f.fp8_decode_attn_num_splits(1, 32, 8, 128, 256, 0, 4) == 4
+    assert f.fp8_decode_attn_num_splits(1, 32, 8, 128, 256, 0, 1) == 2   # at most 128 blocks per split
+    # a window bounds the splits by the window's blocks
+    assert f.fp8_decode_attn_num_splits(8, 64, 8, 64, 2048, 128, 0) <= 9
+    # 128k keys fit in 1024 splits
+    assert 1 <= f.fp8_decode_attn_num_splits(1, 64, 8, 128, 8192) <= 1024
+    assert f.fp8_decode_attn_workspace_size(1, 8, 2, 96, 10) == 0      # unsupported head_dim
+
+
+def _cache(D=128, bs=16, nb=4, H=2, k=1 << 20, v=1 << 21):
+    return f._LayerCache(k, v, nb, bs, H, D)
+
+
+def test_kv_quant_cache_validation(lib):
+    st = lib.kv_quant_cache
+    one = 1 << 12
+    assert st(one, one, one, -1, _cache(), one, one, 0, 0, None, 0, None, None) == f.INVALID_ARG
+    assert st(one, one, one, 4, _cache(bs=8), one, one, 0, 0, None, 0, None, None) == f.UNSUPPORTED
+    assert st(one, one, one, 4, _cache(D=96), one, one, 0, 0, None, 0, None, None) == f.UNSUPPORTED
+    assert st(one, one, one, 4, _cache(), one, one, 7, 0, None, 0, None, None) == f.INVALID_ARG
+    assert st(None, one, one, 4, _cache(), one, one, 0, 0, None, 0, None, None) == f.INVALID_ARG
+    assert st(one, one, one, 4, _cache(), None, one, 0, 0, None, 0, None, None) == f.INVALID_ARG
+    assert st(one + 2, one, one, 4, _cache(), one, one, 0, 0, None, 0, None, None) == f.INVALID_ARG
+    mask = (ctypes.c_uint8 * 2)(0, 1)
+    assert st(one, one, one, 4, _cache(), one, one, 0, 5, mask, 2, None, None) == f.INVALID_ARG
+    assert st(one, one, one, 0, _cache(), one, one, 0, 0, None, 0, None, None) == f.OK   # nothing to do
+
+
+def test_decode_validation(lib):
+    d = lib.fp8_decode_attn
+    p = 1 << 12
+
+    def call(**kw):
+        a = dict(q=p, batch=2, hq=8, cache=_cache(), table=p, max_blocks=4, ctx=p, qs=p, ks=p, vs=p, gran=0,
+                 sm=0.0, window=0, layer=0, mask=None, nl=0, out=p, ws=p, wsb=1 << 30, splits=0, fault=None,
+                 stream=None)
+        a.update(kw)
+        return d(a["q"], a["batch"], a["hq"], a["cache"], a["table"], a["max_blocks"], a["ctx"], a["qs"], a["ks"],
+                 a["vs"], a["gran"], a["sm"], a["window"], a["layer"], a["mask"], a["nl"], a["out"], a["ws"],
+                 a["wsb"], a["splits"], a["fault"], a["stream"])
+
+    assert call(hq=7) == f.INVALID_ARG                       # Hq not a multiple of Hkv
+    assert call(hq=64) == f.UNSUPPORTED                      # G = 32
+    assert call(hq=32, cache=_cache(D=256)) == f.UNSUPPORTED  # G*D > 2048
+    assert call(cache=_cache(D=80)) == f.UNSUPPORTED
+    assert call(cache=_cache(bs=32)) == f.UNSUPPORTED
+    assert call(batch=-1) == f.INVALID_ARG
+    assert call(window=-3) == f.INVALID_ARG
+    assert call(sm=float("nan")) == f.INVALID_ARG
+    assert call(q=None) == f.INVALID_ARG
+    assert call(ws=p + 64) == f.INVALID_ARG                  # workspace must be 256-byte aligned
+    assert call(wsb=16) == f.INVALID_ARG                     # workspace too small
+    assert call(qs=None) == f.INVALID_ARG                    # fp8 layer needs scales
+    assert call(batch=0) == f.OK
+
+
+def test_prefill_validation(lib):
+    pre = lib.fp8_prefill_attn
+    p = 1 << 12
+    mask = (ctypes.c_uint8 * 1)(1)
+    # a bf16 (skip) layer has no FP8 prefill
+    assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 0, 1, 0, mask, 1, p, None, None) == f.UNSUPPORTED
+    assert f.fkv_prefill_block_n(128) == 128 and f.fkv_prefill_block_n(100) == 0

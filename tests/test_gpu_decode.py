@@ -1,0 +1,188 @@
+"""fp8_decode_attn (split-K paged decode + FP32 merge) on the GPU against the oracle.
+
+Tolerance: max-abs 2e-2 and relative L2 1e-2 of the oracle's float64 FP8-emulated
+result.  Small cases cover every head_dim, several GQA group sizes, both scale
+granularities, the bf16 skip-layer path, windows, ragged and empty contexts and forced
+split counts; the full-size workloads are checked on sampled sequences and heads in the
+launch configuration the benchmark times.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from helpers import assert_close, build_layer, oracle_pools, to_dev
+from oracle import attention, e4m3, kvcache
+
+f = pytest.importorskip("fp8_kv_cache_quant_gb300")
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(rng, ctx, Hq, Hkv, D, scale_k=3.0):
+    n = int(np.sum(ctx))
+    q = torch.from_numpy(rng.standard_normal((len(ctx), Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy((rng.standard_normal((n, Hkv, D)) * scale_k).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((n, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    return q, k, v
+
+
+CASES = [
+    # D, G, bf16 layer, gran, window, num_splits
+    (128, 4, False, 0, 0, 0),
+    (128, 4, False, 1, 0, 3),
+    (64, 8, False, 1, 0, 0),
+    (64, 8, True, 0, 128, 0),
+    (128, 8, False, 0, 0, 1),
+    (256, 1, False, 1, 0, 0),
+    (256, 8, True, 0, 0, 2),
+    (128, 16, False, 1, 50, 0),
+    (64, 2, False, 0, 0, 5),
+    (128, 1, True, 0, 0, 0),
+    (64, 16, True, 1, 0, 0),
+    (256, 4, False, 0, 33, 1),
+]
+
+
+@pytest.mark.parametrize("D,G,bf16_layer,gran,window,splits", CASES)
+def test_decode_small_parity(D, G, bf16_layer, gran, window, splits):
+    rng = np.random.default_rng(D * 7 + G * 3 + window + splits)
+    Hkv = 2
+    Hq = Hkv * G
+    ctx = np.array([1, 15, 16, 17, 300, 1000, 0, 129], np.int32)
+    table, nb = synth.block_table(ctx, seed=11, extra_blocks=2)
+    q, k, v = _inputs(rng, ctx, Hq, Hkv, D)
+    if gran:
+        qs, ks, vs = synth.amax_scales(q, 1), synth.amax_scales(k, 1), synth.amax_scales(v, 1)
+    else:
+        qs = torch.tensor([0.5]); ks = torch.tensor([1.0]); vs = torch.tensor([0.25])
+    cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran, bf16_layer)
+    mask = [1] if bf16_layer else None
+    out = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(qs), to_dev(ks), to_dev(vs),
+                            gran, window=window, skip_layer_mask=mask, num_splits=splits)
+    kp, vp = oracle_pools(kvcache, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), bf16_layer)
+    ref = attention.decode_attention(synth.bf16_to_f64(q), kp, vp, table, ctx, qs.numpy(), ks.numpy(), vs.numpy(),
+                                     fp8=not bf16_layer, window=window)
+    got = out.float().cpu().numpy()
+    assert np.all(got[6] == 0), "empty context must give a zero row"
+    assert_close(got, ref, what=f"D={D} G={G} bf16={bf16_layer} gran={gran} W={window} splits={splits}")
+
+
+def test_split_count_invariance_and_permutation():
+    rng = np.random.default_rng(3)
+    Hq, Hkv, D = 32, 8, 128
+    ctx = np.array([2000, 777, 4096], np.int32)
+    table, nb = synth.block_table(ctx, seed=5)
+    q, k, v = _inputs(rng, ctx, Hq, Hkv, D)
+    one = np.ones(1, np.float32)
+    cache = build_layer(f, ctx, table, nb, k, v, one, one, 0, False)
+    outs = {}
+    for s in (1, 2, 7, 0):
+        outs[s] = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(one), to_dev(one),
+                                    to_dev(one), 0, num_splits=s).float().cpu().numpy()
+    for s in (2, 7, 0):
+        np.testing.assert_allclose(outs[s], outs[1], rtol=2.0 ** -7, atol=1e-6)
+    # the same data under another physical block permutation: bit-identical output
+    table2, nb2 = synth.block_table(ctx, seed=99, extra_blocks=3)
+    cache2 = build_layer(f, ctx, table2, nb2, k, v, one, one, 0, False)
+    o2 = f.fp8_decode_attn(q.cuda(), cache2, to_dev(table2), to_dev(ctx), to_dev(one), to_dev(one), to_dev(one), 0,
+                           num_splits=7).float().cpu().numpy()
+    assert np.array_equal(o2, outs[7])
+
+
+def _decode_layer_check(w, layer, ctx, table, nb, seqs, heads, num_splits=0):
+    """Build one full-size layer through the C ABI and compare sampled (b, h) with the
+    oracle computed from the contiguous bf16 inputs."""
+    data = synth.decode_layer(w, layer, ctx, device="cuda")
+    bf16_layer = bool(w.skip_mask()[layer])
+    gran = f.SCALE_PER_HEAD if w.scale_mode == "amax" else f.SCALE_PER_TENSOR
+    cache = build_layer(f, ctx, table, nb, data.k, data.v, data.k_scale.cpu().numpy(), data.v_scale.cpu().numpy(),
+                        gran, bf16_layer)
+    window = w.layer_window(layer)
+    out = f.fp8_decode_attn(data.q, cache, to_dev(table), to_dev(ctx), data.q_scale, data.k_scale, data.v_scale,
+                            gran, window=window, layer=layer, skip_layer_mask=w.skip_mask(),
+                            num_splits=num_splits).float().cpu().numpy()
+    cu = np.concatenate([[0], np.cumsum(ctx)])
+    qs, ks, vs = (x.cpu().numpy() for x in (data.q_scale, data.k_scale, data.v_scale))
+    got, ref = [], []
+    G = w.group
+    for b in seqs:
+        T = int(ctx[b])
+        lo = max(0, T - window) if window else 0
+        for g in sorted(set(h // G for h in heads)):
+            hs = [h for h in heads if h // G == g]
+            kb = synth.bf16_to_f64(data.k[cu[b] + lo:cu[b] + T, g:g + 1])
+            vb = synth.bf16_to_f64(data.v[cu[b] + lo:cu[b] + T, g:g + 1])
+            qb = synth.bf16_to_f64(data.q[b, g * G:(g + 1) * G])
+            sel = lambda a, idx: a if a.size == 1 else a[idx]
+            res = attention.decode_attention_contiguous(
+                qb, kb, vb, sel(qs, slice(g * G, (g + 1) * G)), sel(ks, slice(g, g + 1)), sel(vs, slice(g, g + 1)),
+                fp8=not bf16_layer, heads=[h - g * G for h in hs])
+            for h in hs:
+                got.append(out[b, h])
+                ref.append(res[h - g * G])
+    return np.array(got), np.array(ref), data, out
+
+
+def test_workload1_full():
+    w = synth.WORKLOADS[1]
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    got, ref, _, _ = _decode_layer_check(w, 0, ctx, table, nb, range(w.batch), range(w.num_q_heads))
+    assert_close(got, ref, what="workload 1")
+
+
+@pytest.mark.parametrize("layer", [0, 31])
+def test_workload2_sampled(layer):
+    w = synth.WORKLOADS[2]
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    got, ref, _, _ = _decode_layer_check(w, layer, ctx, table, nb, range(w.batch), [0, 5, 13, 22, 31])
+    assert_close(got, ref, what=f"workload 2 layer {layer}")
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_workload3_sampled(layer):
+    w = synth.WORKLOADS[3]
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    got, ref, _, _ = _decode_layer_check(w, layer, ctx, table, nb, range(w.batch), [0, 9, 33, 63])
+    assert_close(got, ref, what=f"workload 3 layer {layer}")
+
+
+def test_workload4_needle_decode():
+    """128k-key contraction: parity on every head, and each KV group's defining head
+    returns the needle's (dequantised) value row."""
+    w = synth.WORKLOADS[4]
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    got, ref, data, out = _decode_layer_check(w, 0, ctx, table, nb, [0], list(range(w.num_q_heads)))
+    assert_close(got, ref, what="workload 4 decode")
+    vs = float(data.v_scale.cpu()[0])
+    for g in range(w.num_kv_heads):
+        vrow = e4m3.decode(e4m3.quantize(synth.bf16_to_f64(data.v[data.needle_pos, g]), vs)) * vs
+        r = np.linalg.norm(out[0, g * w.group] - vrow) / np.linalg.norm(vrow)
+        assert r <= 1e-2, f"needle head {g * w.group}: rel_l2 {r:.3e}"
+
+
+def test_fault_bits_block_id_and_context():
+    rng = np.random.default_rng(9)
+    ctx = np.array([40, 20], np.int32)
+    table, nb = synth.block_table(ctx, seed=1)
+    q, k, v = _inputs(rng, ctx, 8, 2, 64)
+    one = np.ones(1, np.float32)
+    cache = build_layer(f, ctx, table, nb, k, v, one, one, 0, False)
+    bad = table.copy()
+    bad[0, 1] = nb + 100
+    fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+    f.fp8_decode_attn(q.cuda(), cache, to_dev(bad), to_dev(ctx), to_dev(one), to_dev(one), to_dev(one), 0,
+                      fault=fault)
+    assert int(fault.item()) & f.FAULT_BLOCK_ID
+    fault.zero_()
+    long_ctx = np.array([40, 10_000], np.int32)
+    o = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(long_ctx), to_dev(one), to_dev(one), to_dev(one),
+                          0, fault=fault)
+    torch.cuda.synchronize()
+    assert int(fault.item()) & f.FAULT_CONTEXT
+    assert torch.isfinite(o.float()).all()
