@@ -161,18 +161,28 @@ class DecodeState:
         slots_all = torch.from_numpy(synth.slot_mapping(self.table, self.ctx)).to(device)
         self.layers = []
         max_ws = 0
-        for l in range(w.num_layers):
+        L, B, Hq, Hkv, D = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+        # one contiguous buffer per kind for all layers: a step's inputs and outputs move
+        # between host and device in one copy each
+        self.q_all = torch.empty((L, B, Hq, D), dtype=torch.bfloat16, device=device)
+        self.k_all = torch.empty((L, B, Hkv, D), dtype=torch.bfloat16, device=device)
+        self.v_all = torch.empty((L, B, Hkv, D), dtype=torch.bfloat16, device=device)
+        self.out_all = torch.empty((L, B, Hq, D), dtype=torch.bfloat16, device=device)
+        idx = torch.from_numpy(last).to(device)
+        for l in range(L):
             data = synth.decode_layer(w, l, self.ctx, device=device)
-            cache = f.LayerCache.empty(self.nb, w.num_kv_heads, w.head_dim, bf16=self.bf16[l], device=device)
+            cache = f.LayerCache.empty(self.nb, Hkv, D, bf16=self.bf16[l], device=device)
             f.kv_quant_cache(data.k, data.v, slots_all, cache, data.k_scale, data.v_scale, self.gran, layer=l,
                              skip_layer_mask=self.mask)
-            idx = torch.from_numpy(last).to(device)
-            lay = dict(cache=cache, q=data.q.contiguous(), k_new=data.k[idx].contiguous(), v_new=data.v[idx].contiguous(),
+            self.q_all[l].copy_(data.q)
+            self.k_all[l].copy_(data.k[idx])
+            self.v_all[l].copy_(data.v[idx])
+            lay = dict(cache=cache, q=self.q_all[l], k_new=self.k_all[l], v_new=self.v_all[l],
                        qs=data.q_scale, ks=data.k_scale, vs=data.v_scale, window=w.layer_window(l),
-                       out=torch.empty_like(data.q))
+                       out=self.out_all[l])
             self.layers.append(lay)
-            max_ws = max(max_ws, f.fp8_decode_attn_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads,
-                                                                  w.head_dim, self.table.shape[1], lay["window"]))
+            max_ws = max(max_ws, f.fp8_decode_attn_workspace_size(B, Hq, Hkv, D, self.table.shape[1],
+                                                                  lay["window"]))
             del data
         torch.cuda.synchronize()
         self.ws = torch.empty(max_ws, dtype=torch.uint8, device=device)
@@ -208,16 +218,18 @@ def _graph(fn, stream):
 
 def _time_graph(g, stream, steps, warmup, barrier):
     import torch
-    for _ in range(warmup):
-        g.replay()
+    with torch.cuda.stream(stream):      # CUDAGraph.replay launches on the current stream
+        for _ in range(warmup):
+            g.replay()
     stream.synchronize()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        g.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
     e1.synchronize()
     torch.cuda.synchronize()
     barrier()
@@ -325,22 +337,16 @@ def run_ours(args):
     g_dec = _graph(lambda: fp8.step(decode_only=True), stream)
 
     # end to end: pinned host inputs -> device, the step, outputs -> pinned host
-    host_in = [(torch.empty_like(l["q"], device="cpu").pin_memory(), torch.empty_like(l["k_new"], device="cpu").pin_memory(),
-                torch.empty_like(l["v_new"], device="cpu").pin_memory()) for l in fp8.layers]
-    for (hq, hk, hv), l in zip(host_in, fp8.layers):
-        hq.copy_(l["q"]); hk.copy_(l["k_new"]); hv.copy_(l["v_new"])
-    host_out = [torch.empty_like(l["out"], device="cpu").pin_memory() for l in fp8.layers]
-    h2d = sum(a.numel() * a.element_size() for t in host_in for a in t)
-    d2h = sum(o.numel() * o.element_size() for o in host_out)
+    host_in = [t.to("cpu").pin_memory() for t in (fp8.q_all, fp8.k_all, fp8.v_all)]
+    host_out = torch.empty_like(fp8.out_all, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
-        for (hq, hk, hv), l in zip(host_in, fp8.layers):
-            l["q"].copy_(hq, non_blocking=True)
-            l["k_new"].copy_(hk, non_blocking=True)
-            l["v_new"].copy_(hv, non_blocking=True)
+        for h, d in zip(host_in, (fp8.q_all, fp8.k_all, fp8.v_all)):
+            d.copy_(h, non_blocking=True)
         fp8.step()
-        for o, l in zip(host_out, fp8.layers):
-            o.copy_(l["out"], non_blocking=True)
+        host_out.copy_(fp8.out_all, non_blocking=True)
 
     g_e2e = _graph(e2e_step, stream)
 
@@ -376,13 +382,14 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        ctx0 = int(fp8.ctx[0])
-        r = _cpu_baseline_subprocess(args.workload, ctx0, w.num_q_heads)
+        keys = int(sum(int(t) for t in fp8.ctx))
+        r = _cpu_baseline_subprocess(args.workload, keys, w.num_q_heads)
         if r is not None:
             s, b = r
             cpu = {"value": b / s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                   "sample": f"layer 0, sequence 0 ({ctx0} keys), all {w.num_q_heads} query heads: cache "
-                             f"quantisation + decode attention, {s:.1f} s single-threaded NumPy"}
+                   "sample": f"layer 0 of {w.num_layers}, {keys} cached keys (the batch's total context) x all "
+                             f"{w.num_q_heads} query heads: cache quantisation + decode attention, {s:.1f} s "
+                             f"single-threaded NumPy"}
 
     if rank == 0:
         line = {

@@ -335,9 +335,10 @@ __global__ void __launch_bounds__((kNCW + 1) * 32) decode_split_kernel(const Dec
           for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
         }
       }
-#pragma unroll
-      for (int kk = 0; kk < 16 / C::KPV; ++kk) {
-        const int key = kk * C::KPV + vg;
+      // keys of this block inside [lo, T); the bytes of the other keys may be stale (even
+      // NaN codes), so they are skipped rather than weighted by p = 0.
+      const int kv_lo = max(r.lo - key0, 0), kv_hi = min(r.T - key0, 16);
+      auto pv_key = [&](int key) {
         uint32_t w[C::VPL * ELT / 4 > 0 ? C::VPL * ELT / 4 : 1];
         load_bytes<C::VPL * ELT>(vb + key * D * ELT + dv * ELT, w);
         float2 vf[C::VPL / 2];
@@ -356,10 +357,19 @@ __global__ void __launch_bounds__((kNCW + 1) * 32) decode_split_kernel(const Dec
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float pp = pv[h];
-          const float2 p2 = make_float2(pp, pp);
+          const float2 p2 = make_float2(pv[h], pv[h]);
 #pragma unroll
           for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+        }
+      };
+      if (kv_lo == 0 && kv_hi == 16) {
+#pragma unroll
+        for (int kk = 0; kk < 16 / C::KPV; ++kk) pv_key(kk * C::KPV + vg);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 16 / C::KPV; ++kk) {
+          const int key = kk * C::KPV + vg;
+          if (key >= kv_lo && key < kv_hi) pv_key(key);
         }
       }
       __syncwarp();

@@ -1,0 +1,58 @@
+"""Run one workload layer's kernels a few times, eagerly, for ncu captures.
+
+    python -m fp8_kv_cache_quant_gb300.profile_case --workload 2 --layer 0 --iters 3 [--bf16]
+
+Builds one layer of a decode workload (seeded synthetic inputs, pool filled by
+kv_quant_cache) and launches fp8_decode_attn ``iters`` times.  The layer's cache is
+larger than L2 for the Llama-shaped workload (335 MB), so DRAM counters are meaningful,
+and the device holds about 1 GB.  It prints nothing but a final line; it is not a
+benchmark.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+
+def main():
+    import numpy as np
+    import torch
+
+    import fp8_kv_cache_quant_gb300 as f
+    import synth
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--layer", type=int, default=0)
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--bf16", action="store_true", help="bf16 pool (the skip-layer path) instead of e4m3")
+    ap.add_argument("--splits", type=int, default=0)
+    a = ap.parse_args()
+    w = synth.WORKLOADS[a.workload]
+    dev = torch.device("cuda:0")
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    data = synth.decode_layer(w, a.layer, ctx, device=dev)
+    mask = np.array([1 if a.bf16 else 0], np.uint8)
+    gran = f.SCALE_PER_HEAD if w.scale_mode == "amax" else f.SCALE_PER_TENSOR
+    cache = f.LayerCache.empty(nb, w.num_kv_heads, w.head_dim, bf16=a.bf16, device=dev)
+    slots = torch.from_numpy(synth.slot_mapping(table, ctx)).to(dev)
+    f.kv_quant_cache(data.k, data.v, slots, cache, data.k_scale, data.v_scale, gran, layer=0, skip_layer_mask=mask)
+    del data.k, data.v
+    table_d = torch.from_numpy(table).to(dev)
+    ctx_d = torch.from_numpy(ctx).to(dev)
+    out = torch.empty_like(data.q)
+    ws = f.decode_workspace(w.batch, w.num_q_heads, cache, table.shape[1], w.layer_window(a.layer), a.splits, dev)
+    for _ in range(a.iters):
+        f.fp8_decode_attn(data.q, cache, table_d, ctx_d, data.q_scale, data.k_scale, data.v_scale, gran,
+                          window=w.layer_window(a.layer), layer=0, skip_layer_mask=mask, out=out, workspace=ws,
+                          num_splits=a.splits)
+    torch.cuda.synchronize()
+    print("profile_case done", w.name, "layer", a.layer, "bf16" if a.bf16 else "e4m3")
+
+
+if __name__ == "__main__":
+    main()

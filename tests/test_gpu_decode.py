@@ -57,7 +57,8 @@ def test_decode_small_parity(D, G, bf16_layer, gran, window, splits):
         qs, ks, vs = synth.amax_scales(q, 1), synth.amax_scales(k, 1), synth.amax_scales(v, 1)
     else:
         qs = torch.tensor([0.5]); ks = torch.tensor([1.0]); vs = torch.tensor([0.25])
-    cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran, bf16_layer)
+    # stale bytes of partly filled blocks are NaN codes (0xFF): they must not leak into the result
+    cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran, bf16_layer, sentinel=0xFF)
     mask = [1] if bf16_layer else None
     out = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(qs), to_dev(ks), to_dev(vs),
                             gran, window=window, skip_layer_mask=mask, num_splits=splits)
@@ -76,16 +77,17 @@ def test_split_count_invariance_and_permutation():
     table, nb = synth.block_table(ctx, seed=5)
     q, k, v = _inputs(rng, ctx, Hq, Hkv, D)
     one = np.ones(1, np.float32)
-    cache = build_layer(f, ctx, table, nb, k, v, one, one, 0, False)
+    cache = build_layer(f, ctx, table, nb, k, v, one, one, 0, False, sentinel=0xFF)
     outs = {}
     for s in (1, 2, 7, 0):
         outs[s] = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(one), to_dev(one),
                                     to_dev(one), 0, num_splits=s).float().cpu().numpy()
+    assert np.all(np.isfinite(outs[1]))
     for s in (2, 7, 0):
         np.testing.assert_allclose(outs[s], outs[1], rtol=2.0 ** -7, atol=1e-6)
     # the same data under another physical block permutation: bit-identical output
     table2, nb2 = synth.block_table(ctx, seed=99, extra_blocks=3)
-    cache2 = build_layer(f, ctx, table2, nb2, k, v, one, one, 0, False)
+    cache2 = build_layer(f, ctx, table2, nb2, k, v, one, one, 0, False, sentinel=0x7F)
     o2 = f.fp8_decode_attn(q.cuda(), cache2, to_dev(table2), to_dev(ctx), to_dev(one), to_dev(one), to_dev(one), 0,
                            num_splits=7).float().cpu().numpy()
     assert np.array_equal(o2, outs[7])
