@@ -48,30 +48,32 @@ FKV_DEV SeqRange seq_range(const DecodeParams& p, int b, bool report) {
   return r;
 }
 
-constexpr int kNCW = 4;           // consumer warps
-constexpr int kMaxBps = 128;      // blocks per split, upper bound (table ids staged in smem)
+constexpr int kNW = 4;           // warps per CTA; every warp prefetches and consumes its own tiles
+constexpr int kNBUF = 2;         // tile buffers per warp (one in use, one in flight)
+constexpr int kMaxBps = 128;     // blocks per split, upper bound (table ids staged in smem)
 
 template <int D, int ELT, int G>
 struct DecodeCfg {
   static constexpr int CHUNK = 16 * D * ELT;                  // bytes of one (block, head) chunk
+  static constexpr int TB = CHUNK <= 2048 ? 2 : 1;            // 16-key blocks per tile
+  static constexpr int TILE_BYTES = TB * 2 * CHUNK;           // K and V of a tile
+  static constexpr int RING = kNW * kNBUF * TILE_BYTES;
   // QK mapping: EPL elements (EPL*ELT bytes) of one key per lane
   static constexpr int EPL = ELT == 1 ? (G <= 4 ? 16 : (G == 8 ? 8 : 4)) : (G <= 8 ? 8 : 4);
   static constexpr int LPK = D / EPL;                         // lanes per key
   static constexpr int KPR = 32 / LPK;                        // keys per round
-  static constexpr int ROUNDS = 16 / KPR;
+  static constexpr int ROUNDS = 16 / KPR;                     // rounds per block
   static constexpr int NVF = G > LPK ? G / LPK : 1;           // scores per lane per round
   // PV mapping: VPL elements of one value row per lane
   static constexpr int VPL0 = ELT == 1 ? (G <= 4 ? 8 : (G == 8 ? 4 : 2)) : (G <= 4 ? 4 : 2);
   static constexpr int VPL = VPL0 > D / 32 ? VPL0 : D / 32;
   static constexpr int LPV = D / VPL;                         // lanes per value row
   static constexpr int KPV = 32 / LPV;                        // keys in parallel
-  static constexpr int STAGES = (2 * CHUNK <= 8192) ? 8 : 4;
-  static constexpr int RING = STAGES * 2 * CHUNK;
+  static constexpr int MIN_CTAS = (G * D <= 512 && RING <= 65536) ? 3 : 2;
   static_assert(LPK >= 2 && LPK <= 32, "lanes per key");
   static_assert(LPV >= 1 && LPV <= 32, "lanes per value row");
   static_assert(G * VPL <= 64 && G * EPL <= 64, "register budget");
-  static_assert(STAGES % kNCW == 0, "stage ownership");
-  static_assert(kNCW * G * D * 4 <= RING, "the warps' accumulators are merged inside the ring");
+  static_assert(kNW * G * D * 4 <= RING, "the warps' accumulators are merged inside the ring");
 };
 
 template <int N>
@@ -106,17 +108,16 @@ FKV_DEV void to_f2(const uint32_t* w, float2* out) {
 }
 
 template <int D, int ELT, int G>
-__global__ void __launch_bounds__((kNCW + 1) * 32) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
+    decode_split_kernel(const DecodeParams p) {
   using C = DecodeCfg<D, ELT, G>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING);
-  uint64_t* empty = full + C::STAGES;
-  float* p_s = reinterpret_cast<float*>(empty + C::STAGES);  // [NCW][16][G]
-  float* alpha_s = p_s + kNCW * 16 * G;                        // [NCW][G]
-  float* ml_s = alpha_s + kNCW * G;                            // [NCW][2][G]
-  int* ids_s = reinterpret_cast<int*>(ml_s + kNCW * 2 * G);    // [kMaxBps]
-  volatile int* abort_s = ids_s + kMaxBps;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING);             // [NW][NBUF]
+  float* p_s = reinterpret_cast<float*>(full + kNW * kNBUF);                // [NW][16*TB][G]
+  float* alpha_s = p_s + kNW * 16 * C::TB * G;                              // [NW][G]
+  float* ml_s = alpha_s + kNW * G;                                          // [NW][2][G]
+  int* ids_s = reinterpret_cast<int*>(ml_s + kNW * 2 * G);                  // [kMaxBps]
 
   const int sigma = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,18 +125,15 @@ __global__ void __launch_bounds__((kNCW + 1) * 32) decode_split_kernel(const Dec
   if (sigma >= r.nsplit) return;  // uniform over the CTA
   const int blk_first = r.blk_begin + sigma * p.bps;
   const int nblk = min(p.bps, r.blk_end - blk_first);
+  const int ntiles = (nblk + C::TB - 1) / C::TB;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    *abort_s = 0;
+    for (int s = 0; s < kNW * kNBUF; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
   }
-  if (warp == kNCW) {
+  {
     const int* row = p.block_table + static_cast<size_t>(b) * p.max_blocks + blk_first;
-    for (int i = lane; i < nblk; i += 32) {
+    for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
       int id = row[i];
       if (id < 0 || id >= p.num_blocks) {
         raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
@@ -146,113 +144,113 @@ __global__ void __launch_bounds__((kNCW + 1) * 32) decode_split_kernel(const Dec
   }
   __syncthreads();
 
-  // consumer state lives at function scope so that it survives the CTA barriers below
-  const int kq = lane / C::LPK;  // key within a QK round
-  const int dq = (lane % C::LPK) * C::EPL;
-  const int vg = lane / C::LPV, dv = (lane % C::LPV) * C::VPL;
+  // ---------------------------------------------------------------- per-warp pipeline
+  uint64_t* wfull = full + warp * kNBUF;
+  uint8_t* wring = ring + warp * kNBUF * C::TILE_BYTES;
+  // the k-th tile of this warp is tile warp + k*NW, in buffer k % NBUF
+  auto issue = [&](int k) {
+    const int t = warp + k * kNW;
+    if (t >= ntiles) return;
+    const int b0 = t * C::TB;
+    const int nb = min(C::TB, nblk - b0);
+    uint64_t* bar = &wfull[k % kNBUF];
+    uint8_t* dst = wring + (k % kNBUF) * C::TILE_BYTES;
+    mbar_arrive_expect_tx(bar, nb * 2 * C::CHUNK);
+    for (int j = 0; j < nb; ++j) {
+      const size_t off = (static_cast<size_t>(ids_s[b0 + j]) * p.Hkv + g) * C::CHUNK;
+      bulk_g2s(dst + j * 2 * C::CHUNK, p.k_cache + off, C::CHUNK, bar);
+      bulk_g2s(dst + j * 2 * C::CHUNK + C::CHUNK, p.v_cache + off, C::CHUNK, bar);
+    }
+  };
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < kNBUF; ++k) issue(k);
+  }
+
+  const int h0 = g * G;
+  const int kq = lane / C::LPK;                 // key within a QK round
+  const int dq = (lane % C::LPK) * C::EPL;      // first element of the lane's QK slice
+  const int vg = lane / C::LPV;                 // key sub-group of the PV mapping
+  const int dv = (lane % C::LPV) * C::VPL;      // first element of the lane's PV slice
+
+  // softmax constant per head: softmax_scale * log2(e) * q_s * k_s
+  float cst[G];
+  {
+    const float ks = ELT == 1 ? p.k_scale[p.per_head ? g : 0] : 1.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      cst[h] = p.sm_scale_log2 * (ELT == 1 ? p.q_scale[p.per_head ? h0 + h : 0] * ks : 1.f);
+  }
+  // query slice, quantised to e4m3 (exact float values of the codes) for FP8 layers
+  float2 qf[G][C::EPL / 2];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const __nv_bfloat16* qp = p.q + (static_cast<size_t>(b) * p.Hq + h0 + h) * D + dq;
+    const float iq = ELT == 1 ? __frcp_rn(p.q_scale[p.per_head ? h0 + h : 0]) : 1.f;
+#pragma unroll
+    for (int e = 0; e < C::EPL / 2; ++e) {
+      float2 x = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(qp + 2 * e));
+      if constexpr (ELT == 1) {
+        const uint16_t c = f32x2_to_e4m3x2(__fmul_rn(x.x, iq), __fmul_rn(x.y, iq));
+        x = __half22float2(e4m3x2_to_h2(c));
+      }
+      qf[h][e] = x;
+    }
+  }
+  // heads of this lane after the transposing reduction: hb .. hb+NVF-1
+  int hb = 0;
+  {
+    int nv = G;
+#pragma unroll
+    for (int off = C::LPK / 2; off >= 1; off >>= 1) {
+      if (nv > 1) {
+        if (lane & off) hb += nv / 2;
+        nv >>= 1;
+      }
+    }
+  }
+  const bool dup0 = (C::LPK <= G) ? true : ((lane % C::LPK) % (C::LPK / G) == 0);
+  float cl[C::NVF];
+#pragma unroll
+  for (int j = 0; j < C::NVF; ++j) {
+    cl[j] = cst[0];
+#pragma unroll
+    for (int h = 1; h < G; ++h)
+      if (h == hb + j) cl[j] = cst[h];
+  }
+
+  float m_run[C::NVF], l_run[C::NVF];
+#pragma unroll
+  for (int i = 0; i < C::NVF; ++i) { m_run[i] = -INFINITY; l_run[i] = 0.f; }
   float2 acc[G][C::VPL / 2 > 0 ? C::VPL / 2 : 1];
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
 
-  if (warp == kNCW) {
-    // ------------------------------------------------ producer
-    if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < nblk; ++i) {
-        const int st = i % C::STAGES, use = i / C::STAGES;
-        if (use > 0 && !mbar_wait_bounded(&empty[st], (use - 1) & 1)) {
-          raise_fault(p.fault, FKV_FAULT_TIMEOUT);
-          *abort_s = 1;
-          break;
-        }
-        if (*abort_s) break;
-        const size_t off = (static_cast<size_t>(ids_s[i]) * p.Hkv + g) * C::CHUNK;
-        mbar_arrive_expect_tx(&full[st], 2 * C::CHUNK);
-        bulk_g2s(ring + st * 2 * C::CHUNK, p.k_cache + off, C::CHUNK, &full[st]);
-        bulk_g2s(ring + st * 2 * C::CHUNK + C::CHUNK, p.v_cache + off, C::CHUNK, &full[st]);
-        issued = i + 1;
-      }
-      // let every issued copy land before the CTA may exit
-      for (int i = max(0, issued - C::STAGES); i < issued; ++i) {
-        if (!mbar_wait_bounded(&full[i % C::STAGES], (i / C::STAGES) & 1)) {
-          raise_fault(p.fault, FKV_FAULT_TIMEOUT);
-        }
-      }
+  float* pw = p_s + warp * 16 * C::TB * G;
+  float* aw = alpha_s + warp * G;
+  int issued = min(kNBUF, max(0, (ntiles - warp + kNW - 1) / kNW));
+  int k = 0;
+  bool timed_out = false;
+  for (;; ++k) {
+    const int t = warp + k * kNW;
+    if (t >= ntiles) break;
+    const int buf = k % kNBUF;
+    if (!mbar_wait_bounded(&wfull[buf], (k / kNBUF) & 1)) {
+      raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+      timed_out = true;
+      break;
     }
-  } else {
-    // ------------------------------------------------ consumers
-    const int h0 = g * G;
-    // softmax constant per head: softmax_scale * log2(e) * q_s * k_s
-    float cst[G];
-    const float ks = ELT == 1 ? p.k_scale[p.per_head ? g : 0] : 1.f;
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-      cst[h] = p.sm_scale_log2 * (ELT == 1 ? p.q_scale[p.per_head ? h0 + h : 0] * ks : 1.f);
+    const uint8_t* tile = wring + buf * C::TILE_BYTES;
+    const int nb = min(C::TB, nblk - t * C::TB);
+    const int key0 = (blk_first + t * C::TB) * 16;  // absolute position of the tile's first key
 
-    // query slice for the QK mapping: lane's d-range [dq, dq + EPL)
-    float2 qf[G][C::EPL / 2];
+    // ---------------- QK
+    float sc[C::TB][C::ROUNDS][C::NVF];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const __nv_bfloat16* qp = p.q + (static_cast<size_t>(b) * p.Hq + h0 + h) * D + dq;
-      const float iq = ELT == 1 ? __frcp_rn(p.q_scale[p.per_head ? h0 + h : 0]) : 1.f;
-#pragma unroll
-      for (int e = 0; e < C::EPL / 2; ++e) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(qp + 2 * e);
-        float2 x = bf16x2_to_f2(w);
-        if constexpr (ELT == 1) {
-          const uint16_t c = f32x2_to_e4m3x2(__fmul_rn(x.x, iq), __fmul_rn(x.y, iq));
-          x = __half22float2(e4m3x2_to_h2(c));
-        }
-        qf[h][e] = x;
-      }
-    }
-
-    // head base of this lane after the transposing reduction
-    int hb = 0;
-    {
-      int nv = G;
-#pragma unroll
-      for (int off = C::LPK / 2; off >= 1; off >>= 1) {
-        if (nv > 1) {
-          if (lane & off) hb += nv / 2;
-          nv >>= 1;
-        }
-      }
-    }
-    const bool dup0 = (C::LPK <= G) ? true : ((lane % C::LPK) % (C::LPK / G) == 0);
-
-    // this lane's heads are hb .. hb+NVF-1: pick their constants without dynamic indexing
-    float cl[C::NVF];
-#pragma unroll
-    for (int j = 0; j < C::NVF; ++j) {
-      cl[j] = cst[0];
-#pragma unroll
-      for (int h = 1; h < G; ++h)
-        if (h == hb + j) cl[j] = cst[h];
-    }
-
-    float m_run[C::NVF], l_run[C::NVF];
-#pragma unroll
-    for (int i = 0; i < C::NVF; ++i) { m_run[i] = -INFINITY; l_run[i] = 0.f; }
-
-    float* pw = p_s + warp * 16 * G;
-    float* aw = alpha_s + warp * G;
-
-    for (int i = warp; i < nblk; i += kNCW) {
-      const int st = i % C::STAGES, use = i / C::STAGES;
-      if (!mbar_wait_bounded(&full[st], use & 1)) {
-        raise_fault(p.fault, FKV_FAULT_TIMEOUT);
-        *abort_s = 1;
-        break;
-      }
-      const uint8_t* kb = ring + st * 2 * C::CHUNK;
-      const uint8_t* vb = kb + C::CHUNK;
-      const int key0 = (blk_first + i) * 16;  // absolute position of the block's first key
-
-      // ---------------- QK
-      float sc[C::ROUNDS][C::NVF];
+    for (int j = 0; j < C::TB; ++j) {
+      const uint8_t* kb = tile + j * 2 * C::CHUNK;
 #pragma unroll
       for (int rr = 0; rr < C::ROUNDS; ++rr) {
         const int key = rr * C::KPR + kq;
@@ -275,75 +273,81 @@ __global__ void __launch_bounds__((kNCW + 1) * 32) decode_split_kernel(const Dec
           if (nv > 1) {
             const bool up = lane & off;
 #pragma unroll
-            for (int j = 0; j < nv / 2; ++j) {
-              const float send = up ? v[j] : v[j + nv / 2];
-              const float keep = up ? v[j + nv / 2] : v[j];
-              v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            for (int q2 = 0; q2 < nv / 2; ++q2) {
+              const float send = up ? v[q2] : v[q2 + nv / 2];
+              const float keep = up ? v[q2 + nv / 2] : v[q2];
+              v[q2] = keep + __shfl_xor_sync(0xffffffffu, send, off);
             }
             nv >>= 1;
           } else {
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
           }
         }
-        const int kabs = key0 + key;
-        const bool valid = kabs >= r.lo && kabs < r.T;
+        const int kabs = key0 + j * 16 + key;
+        const bool valid = j < nb && kabs >= r.lo && kabs < r.T;
 #pragma unroll
-        for (int j = 0; j < C::NVF; ++j) sc[rr][j] = valid ? v[j] * cl[j] : -INFINITY;
+        for (int jv = 0; jv < C::NVF; ++jv) sc[j][rr][jv] = valid ? v[jv] * cl[jv] : -INFINITY;
       }
+    }
 
-      // ---------------- softmax (base 2)
-      float bmax[C::NVF], bsum[C::NVF], alpha[C::NVF];
+    // ---------------- softmax (base 2) over the tile's keys
 #pragma unroll
-      for (int j = 0; j < C::NVF; ++j) {
-        float mx = sc[0][j];
+    for (int jv = 0; jv < C::NVF; ++jv) {
+      float mx = -INFINITY;
 #pragma unroll
-        for (int rr = 1; rr < C::ROUNDS; ++rr) mx = fmaxf(mx, sc[rr][j]);
+      for (int j = 0; j < C::TB; ++j)
 #pragma unroll
-        for (int off = C::LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        bmax[j] = mx;
-      }
+        for (int rr = 0; rr < C::ROUNDS; ++rr) mx = fmaxf(mx, sc[j][rr][jv]);
 #pragma unroll
-      for (int j = 0; j < C::NVF; ++j) {
-        const float mn = fmaxf(m_run[j], bmax[j]);
-        alpha[j] = (m_run[j] == -INFINITY) ? 0.f : ex2(m_run[j] - mn);
-        m_run[j] = mn;
-        float s = 0.f;
+      for (int off = C::LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m_run[jv], mx);
+      const float alpha = (m_run[jv] == -INFINITY) ? 0.f : ex2(m_run[jv] - mn);
+      m_run[jv] = mn;
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < C::TB; ++j)
 #pragma unroll
         for (int rr = 0; rr < C::ROUNDS; ++rr) {
-          const float pv = ex2(sc[rr][j] - mn);
-          s += pv;
-          if (dup0) pw[(rr * C::KPR + kq) * G + hb + j] = pv;
+          const float pv = ex2(sc[j][rr][jv] - mn);
+          sum += pv;
+          if (dup0) pw[(j * 16 + rr * C::KPR + kq) * G + hb + jv] = pv;
         }
 #pragma unroll
-        for (int off = C::LPK; off < 32; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        bsum[j] = s;
-        l_run[j] = l_run[j] * alpha[j] + s;
-        if (dup0 && kq == 0) aw[hb + j] = alpha[j];
-      }
-      __syncwarp();
+      for (int off = C::LPK; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      l_run[jv] = l_run[jv] * alpha + sum;
+      if (dup0 && kq == 0) aw[hb + jv] = alpha;
+    }
+    __syncwarp();
 
-      // ---------------- PV
+    // ---------------- PV
+    {
       bool rescale = false;
 #pragma unroll
       for (int h = 0; h < G; ++h) rescale |= (aw[h] != 1.f);
       if (rescale) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float a = aw[h];
-          const float2 a2 = make_float2(a, a);
+          const float2 a2 = make_float2(aw[h], aw[h]);
 #pragma unroll
           for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
         }
       }
+    }
+#pragma unroll
+    for (int j = 0; j < C::TB; ++j) {
+      if (j >= nb) break;
+      const uint8_t* vb = tile + j * 2 * C::CHUNK + C::CHUNK;
+      const float* pj = pw + j * 16 * G;
       // keys of this block inside [lo, T); the bytes of the other keys may be stale (even
       // NaN codes), so they are skipped rather than weighted by p = 0.
-      const int kv_lo = max(r.lo - key0, 0), kv_hi = min(r.T - key0, 16);
+      const int kb0 = key0 + j * 16;
+      const int kv_lo = max(r.lo - kb0, 0), kv_hi = min(r.T - kb0, 16);
       auto pv_key = [&](int key) {
         uint32_t w[C::VPL * ELT / 4 > 0 ? C::VPL * ELT / 4 : 1];
         load_bytes<C::VPL * ELT>(vb + key * D * ELT + dv * ELT, w);
         float2 vf[C::VPL / 2];
         to_f2<ELT, C::VPL>(w, vf);
-        const float* pk = pw + key * G;
+        const float* pk = pj + key * G;
         float pv[G];
         if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -372,35 +376,41 @@ __global__ void __launch_bounds__((kNCW + 1) * 32) decode_split_kernel(const Dec
           if (key >= kv_lo && key < kv_hi) pv_key(key);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-      (void)bsum;
     }
+    __syncwarp();
+    // the buffer is free again: refill it with this warp's tile k + NBUF
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      issue(k + kNBUF);
+    }
+    if (warp + (k + kNBUF) * kNW < ntiles) ++issued;
+  }
+  if (timed_out && lane == 0) {
+    // let the copies still in flight land before the CTA can exit
+    for (int kk = k; kk < issued; ++kk) mbar_wait_bounded(&wfull[kk % kNBUF], (kk / kNBUF) & 1);
+  }
 
-    // reduce the key sub-groups of the PV mapping
+  // reduce the key sub-groups of the PV mapping
 #pragma unroll
-    for (int off = C::LPV; off < 32; off <<= 1) {
+  for (int off = C::LPV; off < 32; off <<= 1) {
 #pragma unroll
-      for (int h = 0; h < G; ++h)
+    for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int e = 0; e < C::VPL / 2; ++e) {
-          acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, off);
-          acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, off);
-        }
-    }
-    // publish m, l of this warp
-    if (dup0 && kq == 0) {
-#pragma unroll
-      for (int j = 0; j < C::NVF; ++j) {
-        ml_s[(warp * 2 + 0) * G + hb + j] = m_run[j];
-        ml_s[(warp * 2 + 1) * G + hb + j] = l_run[j];
+      for (int e = 0; e < C::VPL / 2; ++e) {
+        acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, off);
+        acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, off);
       }
+  }
+  if (dup0 && kq == 0) {
+#pragma unroll
+    for (int jv = 0; jv < C::NVF; ++jv) {
+      ml_s[(warp * 2 + 0) * G + hb + jv] = m_run[jv];
+      ml_s[(warp * 2 + 1) * G + hb + jv] = l_run[jv];
     }
   }
-  __syncthreads();  // every copy has landed (producer drained) and every consumer is done
-  // stage the accumulators in the ring
-  float* acc_w = reinterpret_cast<float*>(ring);  // [NCW][G][D]
-  if (warp < kNCW && vg == 0) {
+  __syncthreads();  // every warp is done with the ring and has no copy in flight
+  float* acc_w = reinterpret_cast<float*>(ring);  // [NW][G][D]
+  if (vg == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -410,21 +420,20 @@ __global__ void __launch_bounds__((kNCW + 1) * 32) decode_split_kernel(const Dec
   __syncthreads();
 
   // ---------------------------------------------------- merge the warps, write the split
-  const float* acc_s = reinterpret_cast<const float*>(ring);
   for (int t = threadIdx.x; t < G * D; t += blockDim.x) {
     const int h = t / D, d = t % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kNCW; ++w) M = fmaxf(M, ml_s[(w * 2) * G + h]);
+    for (int w = 0; w < kNW; ++w) M = fmaxf(M, ml_s[(w * 2) * G + h]);
     float L = 0.f, O = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kNCW; ++w) {
+      for (int w = 0; w < kNW; ++w) {
         const float mw = ml_s[(w * 2) * G + h];
         if (mw == -INFINITY) continue;
-        const float f = ex2(mw - M);
-        L += ml_s[(w * 2 + 1) * G + h] * f;
-        O += acc_s[(w * G + h) * D + d] * f;
+        const float fw = ex2(mw - M);
+        L += ml_s[(w * 2 + 1) * G + h] * fw;
+        O += acc_w[(w * G + h) * D + d] * fw;
       }
     }
     const size_t row = (static_cast<size_t>(b) * p.Hq + g * G + h) * p.max_splits + sigma;
@@ -471,8 +480,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p,
 template <int D, int ELT, int G>
 size_t decode_smem_bytes() {
   using C = DecodeCfg<D, ELT, G>;
-  return C::RING + 2 * C::STAGES * sizeof(uint64_t) + (kNCW * 16 * G + kNCW * G + kNCW * 2 * G) * sizeof(float) +
-         (kMaxBps + 4) * sizeof(int);
+  return C::RING + kNW * kNBUF * sizeof(uint64_t) +
+         (kNW * 16 * C::TB * G + kNW * G + kNW * 2 * G) * sizeof(float) + kMaxBps * sizeof(int);
 }
 
 template <int D, int ELT, int G>
@@ -482,7 +491,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(p.max_splits, p.Hkv, p.B);
-  kern<<<grid, (kNCW + 1) * 32, smem, s>>>(p);
+  kern<<<grid, kNW * 32, smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_merge_kernel<D><<<p.B * p.Hq, 128, 0, s>>>(p, G, ELT == 1 ? 1 : 0);
