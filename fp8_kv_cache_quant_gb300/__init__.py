@@ -30,7 +30,9 @@ FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT, FAULT_QLEN = 1, 2, 4, 
 EXPORTS = (
     "fkv_status_string", "fkv_version", "kv_quant_cache", "fp8_decode_attn_workspace_size",
     "fp8_decode_attn_num_splits", "fp8_decode_attn", "fkv_prefill_block_n", "fp8_prefill_attn",
+    "fp8_decode_attn_noalloc",
 )
+NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
 class FkvError(RuntimeError):
@@ -71,6 +73,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.fp8_decode_attn.argtypes = [c_vp, c_i32, c_i32, _LayerCache, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
                                     ctypes.c_int, c_f, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_i32, c_vp,
                                     c_vp]
+    lib.fp8_decode_attn_noalloc.restype = ctypes.c_int
+    lib.fp8_decode_attn_noalloc.argtypes = [c_vp, c_i32, c_i32, _LayerCache, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
+                                            ctypes.c_int, c_f, c_i32, c_i32, c_vp, c_i32, c_vp, c_i32, c_vp, c_vp]
     lib.fkv_prefill_block_n.restype = c_i32
     lib.fkv_prefill_block_n.argtypes = [c_i32]
     lib.fp8_prefill_attn.restype = ctypes.c_int
@@ -190,6 +195,25 @@ def fp8_decode_attn(q, cache: LayerCache, block_table, context_lens, q_scale=Non
                              _stream(stream))
     del keep
     _check("fp8_decode_attn", st)
+    return out
+
+
+def fp8_decode_attn_noalloc(q, cache: LayerCache, block_table, context_lens, q_scale=None, k_scale=None,
+                            v_scale=None, gran=SCALE_PER_TENSOR, softmax_scale=0.0, window=0, layer=0,
+                            skip_layer_mask=None, out=None, num_splits=0, fault=None, stream=None):
+    """fp8_decode_attn without a workspace: the library's fixed device scratch is used
+    (see include/fp8kv.h for its size limit and the sharing rule)."""
+    lib = load_library()
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    mp, nl, keep = _mask_arg(skip_layer_mask)
+    st = lib.fp8_decode_attn_noalloc(_ptr(q), B, Hq, cache.c(), _ptr(block_table), int(block_table.shape[1]),
+                                     _ptr(context_lens), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), int(gran),
+                                     float(softmax_scale), int(window), int(layer), mp, nl, _ptr(out),
+                                     int(num_splits), _ptr(fault), _stream(stream))
+    del keep
+    _check("fp8_decode_attn_noalloc", st)
     return out
 
 

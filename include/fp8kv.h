@@ -161,6 +161,38 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads,
                            int32_t num_layers, void* out, void* workspace, size_t workspace_bytes,
                            int32_t num_splits, int32_t* fault, fkv_stream_t stream);
 
+/* Size of the fixed device scratch used by fp8_decode_attn_noalloc (16 MiB per GPU). */
+#define FKV_NOALLOC_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * fp8_decode_attn_noalloc — fp8_decode_attn for callers that cannot provide a workspace.
+ *
+ * The pages have no counterpart: this is a convenience of this library.  Callers such
+ * as plugins inside a framework that owns all device memory, or serving loops that
+ * must never call cudaMalloc/cudaFree (both can synchronise the device), get the same
+ * computation with the split partials kept in a fixed 16 MiB device array of the
+ * library (FKV_NOALLOC_WORKSPACE_BYTES), present on every GPU that loads the library
+ * until the process exits.  Arguments mean what they mean for fp8_decode_attn; there is
+ * no workspace argument.  Nothing is allocated.
+ *
+ *   - Returns FKV_INVALID_ARG when fp8_decode_attn_workspace_size(...) for these sizes
+ *     exceeds FKV_NOALLOC_WORKSPACE_BYTES (use fp8_decode_attn with a caller workspace
+ *     for such sizes), and every error fp8_decode_attn returns.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls share the one array: calls whose kernels overlap on the GPU (other
+ *     streams, other host threads) race on it and produce wrong results.  Calls in one
+ *     stream are ordered and safe; each call writes every scratch byte it later reads.
+ */
+fkv_status fp8_decode_attn_noalloc(const void* q, int32_t batch, int32_t num_q_heads,
+                                   fkv_layer_cache cache, const int32_t* block_table,
+                                   int32_t max_blocks, const int32_t* context_lens,
+                                   const float* q_scale, const float* k_scale, const float* v_scale,
+                                   fkv_scale_gran gran, float softmax_scale, int32_t window,
+                                   int32_t layer, const uint8_t* skip_layer_mask, int32_t num_layers,
+                                   void* out, int32_t num_splits, int32_t* fault,
+                                   fkv_stream_t stream);
+
 /* Keys per tile of fp8_prefill_attn (its online-softmax and P-rounding granularity). */
 int32_t fkv_prefill_block_n(int32_t head_dim);
 
