@@ -204,11 +204,50 @@ fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t 
                             float softmax_scale, int32_t causal, int32_t window, int32_t promote_every,
                             int32_t layer, const uint8_t* skip_layer_mask, int32_t num_layers, void* out,
                             int32_t* fault, fkv_stream_t stream) {
-  (void)q; (void)cu_seqlens_q; (void)batch; (void)num_q_heads; (void)max_q_len; (void)cache;
-  (void)block_table; (void)max_blocks; (void)context_lens; (void)q_scale; (void)k_scale; (void)v_scale;
-  (void)gran; (void)softmax_scale; (void)causal; (void)window; (void)promote_every; (void)layer;
-  (void)skip_layer_mask; (void)num_layers; (void)out; (void)fault; (void)stream;
-  return FKV_UNSUPPORTED;
+  if (batch < 0 || num_q_heads <= 0 || max_q_len < 0 || max_blocks <= 0) return FKV_INVALID_ARG;
+  if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
+  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0) return FKV_INVALID_ARG;
+  if (num_q_heads % cache.num_kv_heads != 0) return FKV_INVALID_ARG;
+  if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
+  if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
+  if (!(softmax_scale >= 0.f) || std::isinf(softmax_scale)) return FKV_INVALID_ARG;
+  if (window < 0) return FKV_INVALID_ARG;
+  if (window != 0 || promote_every != 1) return FKV_UNSUPPORTED;
+  fkv_status st = FKV_OK;
+  const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
+  if (st != FKV_OK) return st;
+  if (bf16) return FKV_UNSUPPORTED;  // skip (bf16) layers have no FP8 prefill here
+  if (batch > 65535 || num_q_heads > 65535) return FKV_UNSUPPORTED;
+  if (batch == 0 || max_q_len == 0) return FKV_OK;
+  if (!q || !cu_seqlens_q || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || !out ||
+      !q_scale || !k_scale || !v_scale)
+    return FKV_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(cache.k_cache, 16) || !aligned(cache.v_cache, 16) ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(cu_seqlens_q, 4))
+    return FKV_INVALID_ARG;
+  fkv::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.cu_q = cu_seqlens_q;
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.per_head = gran == FKV_SCALE_PER_HEAD;
+  p.B = batch;
+  p.Hq = num_q_heads;
+  p.Hkv = cache.num_kv_heads;
+  p.num_blocks = cache.num_blocks;
+  p.max_blocks = max_blocks;
+  p.n_qtiles = (max_q_len + 127) / 128;
+  const float tau = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache.head_dim));
+  p.sm_scale_log2 = tau * 1.4426950408889634f;
+  p.causal = causal != 0;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.fault = fault;
+  return from_cuda(fkv::launch_prefill(p, cache.head_dim, cache.k_cache, cache.v_cache,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

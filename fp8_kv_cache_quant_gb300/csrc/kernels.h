@@ -29,6 +29,24 @@ struct DecodeParams {
   int32_t* fault;
 };
 
+struct PrefillParams {
+  const __nv_bfloat16* q;       // [total_q][Hq][D]
+  const int32_t* cu_q;          // [B + 1]
+  const int32_t* block_table;   // [B][max_blocks]
+  const int32_t* context_lens;  // [B]
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  int per_head;
+  int B, Hq, Hkv, num_blocks, max_blocks, n_qtiles;
+  float sm_scale_log2;
+  int causal;
+  __nv_bfloat16* out;           // [total_q][Hq][D]
+  int32_t* fault;
+};
+
+cudaError_t launch_prefill(const PrefillParams& p, int D, void* k_cache, void* v_cache, cudaStream_t s);
+
 cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* slots, int n_tokens,
                                   const fkv_layer_cache& cache, const float* ks, const float* vs,
                                   int per_head, bool bf16_layer, int32_t* fault, cudaStream_t s,

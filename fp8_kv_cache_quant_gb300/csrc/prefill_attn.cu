@@ -1,3 +1,530 @@
-// FP8 prefill attention on tcgen05 tensor cores (kernel added separately).
+// FP8 prefill (chunked) attention on tcgen05 tensor cores, two-level accumulation.
+//
+// The vLLM blog "FP8 KV-Cache and Attention quantization in vLLM": with an FP8 KV cache
+// the whole attention runs in FP8, the QK and the Score*V matrix products included
+// (引言); FP8 tensor cores accumulate imprecisely over long contractions, so each partial
+// accumulation is promoted into a true FP32 register (section "Kernel 与 vLLM 改进",
+// paragraph "Two-level accumulation"); head_dim 256 puts the most pressure on that
+// scheme (section "大 Head Dimension 的限制").
+//
+// CTA = (128-query tile, query head h, sequence b); 6 warps:
+//   warps 0-3  quantise the Q tile to e4m3 into shared memory (prologue); then per
+//              128-key tile, thread i owns query row i (TMEM lane i): load S from TMEM,
+//              scale, mask, online softmax (running max m, unrounded sum l), write
+//              P8 = e4m3(p * 448) into shared memory, and promote the tile's P.V
+//              partial from TMEM into the FP32 accumulator O = O * alpha + O_tile;
+//              epilogue O * v_s / (448 * l) -> bf16.
+//   warp 4     TMA: each 16-token block of K and V is one box [16][D] of the paged pool
+//              (4-D tensor map: D, slot-in-block, KV head, block), 8 boxes per tile.
+//   warp 5     allocates TMEM, issues S = Q8 K8^T and O_tile = P8 V8 with
+//              tcgen05.mma kind::f8f6f4 (FP32 accumulation in TMEM), commits to
+//              mbarriers.
+// TMEM columns: S [0, 128), O_tile [128, 128 + DN), O [128 + DN, 128 + DN + D); for
+// head_dim 256 the P.V product runs as two N = 128 halves through one O_tile.
+// Every wait is bounded in time; a timeout records FKV_FAULT_TIMEOUT, lets the CTA's
+// copies and MMAs drain and returns.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
+
+namespace fkv {
+
+constexpr uint64_t kPrefillWaitNs = 200000000ull;  // 200 ms per wait
+
+FKV_DEV bool wait_ns(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > kPrefillWaitNs) return false;
+  }
+}
+
+// Warp-uniform forms: tcgen05.ld / st are warp-collective, so every lane of a warp must
+// take the same branch around them.
+FKV_DEV bool wait_warp(uint64_t* bar, uint32_t parity) {
+  const bool ok = wait_ns(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+FKV_DEV bool abort_warp(volatile int* flag) { return __any_sync(0xffffffffu, *flag != 0); }
+
+template <int D>
+struct PrefillCfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int RB = D < 128 ? D : 128;      // bytes of one swizzled row
+  static constexpr int NSUB = D / RB;               // sub-tiles along head_dim
+  static constexpr int SWZ = RB == 128 ? 2 : 4;     // descriptor swizzle mode (128 B / 64 B)
+  static constexpr int SUB = BM * RB;               // bytes of one 128-row sub-tile
+  static constexpr int TILE = BM * D;               // bytes of a Q, K or V tile
+  static constexpr int NS = 2;                      // K/V stages
+  static constexpr int DN = D < 128 ? D : 128;      // N of one P.V product
+  static constexpr int NH = D / DN;
+  static constexpr int TM_S = 0, TM_OT = 128, TM_OA = 128 + DN;
+  static constexpr int TM_COLS = (128 + DN + D) <= 256 ? 256 : 512;
+  // shared memory layout (bytes)
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_P = OFF_V + NS * TILE;
+  static constexpr int OFF_BAR = OFF_P + BM * BN;
+  static constexpr int NBAR = 8 + 4 * NS;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
+  static constexpr uint32_t IDESC_QK = idesc_e4m3_f32(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, DN, 0, 1);
+  static_assert(128 + DN + D <= 512, "TMEM budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv) {
+  using C = PrefillCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sP = smem + C::OFF_P;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* s_full = bars + 1;
+  uint64_t* s_free = bars + 2;
+  uint64_t* p_full = bars + 3;
+  uint64_t* p_free = bars + 4;
+  uint64_t* o_full = bars + 5;
+  uint64_t* o_free = bars + 6;
+  uint64_t* mma_done = bars + 7;
+  uint64_t* k_full = bars + 8;
+  uint64_t* k_empty = k_full + C::NS;
+  uint64_t* v_full = k_empty + C::NS;
+  uint64_t* v_empty = v_full + C::NS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // longest (latest) query tiles first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int G = p.Hq / p.Hkv;
+  const int g = h / G;
+
+  // ------------------------------------------------------------ sequence geometry
+  const int r0 = p.cu_q[b];
+  const int Lq = p.cu_q[b + 1] - r0;
+  int T = p.context_lens[b];
+  if (T < 0 || T > p.max_blocks * 16) {
+    if (qt == 0 && h == 0 && threadIdx.x == 0) raise_fault(p.fault, FKV_FAULT_CONTEXT);
+    T = T < 0 ? 0 : p.max_blocks * 16;
+  }
+  if (Lq > T || Lq < 0) {
+    if (qt == 0 && h == 0 && threadIdx.x == 0) raise_fault(p.fault, FKV_FAULT_QLEN);
+    return;
+  }
+  const int q0 = qt * C::BM;  // first row of the tile within the sequence
+  if (q0 >= Lq) return;
+  const int rows = min(C::BM, Lq - q0);
+  const int pos0 = T - Lq + q0;  // absolute position of the tile's first query
+  const int kv_end = p.causal ? min(T, pos0 + rows) : T;  // keys [0, kv_end) matter
+  const int n_t = (kv_end + C::BN - 1) / C::BN;
+  const int nblk_seq = (T + 15) >> 4;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 128);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(p_full, 128);
+    mbar_init(p_free, 1);
+    mbar_init(o_full, 1);
+    mbar_init(o_free, 128);
+    mbar_init(mma_done, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    *abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, C::TM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    // ============================================================ softmax warpgroup
+    const int i = threadIdx.x;                 // query row within the tile
+    const bool row_ok = i < rows;
+    const int pos = pos0 + i;                  // its absolute position
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // ---- prologue: Q row -> e4m3 codes in the swizzled Q tile
+    {
+      const float qs = p.q_scale[p.per_head ? h : 0];
+      const float iq = __frcp_rn(qs);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D);
+#pragma unroll 4
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (row_ok) {
+          const uint4 a = src[2 * c], bq = src[2 * c + 1];
+          const uint32_t in[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 x0 = bf16x2_to_f2(in[2 * j]), x1 = bf16x2_to_f2(in[2 * j + 1]);
+            const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(x0.x, iq), __fmul_rn(x0.y, iq));
+            const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(x1.x, iq), __fmul_rn(x1.y, iq));
+            w[j] = lo | (hi << 16);
+          }
+        }
+        const int byte = c * 16;
+        const int sub = byte / C::RB;
+        const uint32_t lin = static_cast<uint32_t>(i * C::RB + (byte % C::RB));
+        *reinterpret_cast<uint4*>(sQ + sub * C::SUB + swz(lin, C::RB)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    const float cst = p.sm_scale_log2 * p.q_scale[p.per_head ? h : 0] * p.k_scale[p.per_head ? g : 0];
+    float m = -INFINITY, l = 0.f;
+    int npv = 0;
+    for (int t = 0; t < n_t; ++t) {
+      if (abort_warp(abort_s)) break;
+      if (!wait_warp(s_full, t & 1)) {
+        raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+        *abort_s = 1;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(lane_base + C::TM_S + 32 * c, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[32 * c + j] = v[j];
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(s_free);
+      // scale into the base-2 domain and mask: keys beyond the context, and beyond the
+      // row's own position when causal (rows past the chunk see every key)
+      const int kbase = t * C::BN;
+      const int lim = (p.causal && row_ok) ? min(T, pos + 1) : T;
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 128; ++j) {
+        s[j] = (kbase + j < lim) ? s[j] * cst : -INFINITY;
+        tmax = fmaxf(tmax, s[j]);
+      }
+      const float mn = fmaxf(m, tmax);
+      const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
+      const float msafe = (mn == -INFINITY) ? 0.f : mn;
+      float lsum = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int j = 0; j < 128; j += 4) {
+        const float a0 = ex2(s[j] - msafe), a1 = ex2(s[j + 1] - msafe);
+        const float a2 = ex2(s[j + 2] - msafe), a3 = ex2(s[j + 3] - msafe);
+        lsum += (a0 + a1) + (a2 + a3);
+        const uint32_t lo = f32x2_to_e4m3x2(a0 * 448.f, a1 * 448.f);
+        const uint32_t hi = f32x2_to_e4m3x2(a2 * 448.f, a3 * 448.f);
+        pk[j / 4] = lo | (hi << 16);
+      }
+      l = l * alpha + lsum;
+      m = mn;
+      // P row -> swizzled P tile, once the previous tile's P.V has read it
+      if (t > 0 && !wait_warp(p_free, (t - 1) & 1)) {
+        raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+        *abort_s = 1;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t lin = static_cast<uint32_t>(i * 128 + c * 16);
+        *reinterpret_cast<uint4*>(sP + swz(lin, 128)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(p_full);
+      // promote the tile's P.V partial: O = O * alpha + O_tile (FP32)
+      bool ok = true;
+      for (int hn = 0; hn < C::NH; ++hn) {
+        if (!wait_warp(o_full, npv & 1)) {
+          ok = false;
+          break;
+        }
+        ++npv;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < C::DN / 32; ++c) {
+          float ot[32], oa[32];
+          tmem_ld32(lane_base + C::TM_OT + 32 * c, ot);
+          if (t > 0) tmem_ld32(lane_base + C::TM_OA + hn * C::DN + 32 * c, oa);
+          tmem_ld_wait();
+          if (t > 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) oa[j] = fmaf(oa[j], alpha, ot[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) oa[j] = ot[j];
+          }
+          tmem_st32(lane_base + C::TM_OA + hn * C::DN + 32 * c, oa);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(o_free);
+      }
+      if (!ok) {
+        raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+        *abort_s = 1;
+        break;
+      }
+    }
+    // ---- epilogue: O * v_s / (448 l) -> bf16 (every lane loads; rows past the chunk do not store)
+    if (!abort_warp(abort_s)) {
+      const float vs = p.v_scale[p.per_head ? g : 0];
+      const float f = (l > 0.f) ? vs / (448.f * l) : 0.f;
+      __nv_bfloat16* dst = p.out + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float oa[32];
+        tmem_ld32(lane_base + C::TM_OA + 32 * c, oa);
+        tmem_ld_wait();
+        if (row_ok) {
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 y = __floats2bfloat162_rn(oa[2 * j] * f, oa[2 * j + 1] * f);
+            w[j] = *reinterpret_cast<uint32_t*>(&y);
+          }
+          uint4* o4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        }
+      }
+    }
+  } else if (warp == 4) {
+    // ============================================================ TMA producer
+    const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+    int last_use[C::NS];
+#pragma unroll
+    for (int s = 0; s < C::NS; ++s) last_use[s] = -1;
+    for (int t = 0; t < n_t; ++t) {
+      int stop = *abort_s;
+      if (lane == 0 && (t & 7) == 7 && p.fault && (*reinterpret_cast<volatile int*>(p.fault) & FKV_FAULT_TIMEOUT))
+        stop = 1;  // another CTA gave up: stop early
+      if (__any_sync(0xffffffffu, stop != 0)) {
+        *abort_s = 1;
+        break;
+      }
+      // 8 block ids of the tile; blocks past the context read block 0 (their keys are masked)
+      int id = 0;
+      if (lane < 8) {
+        const int lb = t * 8 + lane;
+        if (lb < nblk_seq) {
+          id = trow[lb];
+          if (id < 0 || id >= p.num_blocks) {
+            raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
+            id = 0;
+          }
+        }
+      }
+      int ids[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ids[j] = __shfl_sync(0xffffffffu, id, j);
+      const int st = t % C::NS, use = t / C::NS;
+      bool ok = true;
+      if (lane == 0) {
+        if (use > 0) ok = wait_ns(&k_empty[st], (use - 1) & 1);
+        if (ok) {
+          mbar_arrive_expect_tx(&k_full[st], C::TILE);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int s = 0; s < C::NSUB; ++s)
+              tma_load_4d(sK + st * C::TILE + s * C::SUB + j * 16 * C::RB, &tmk, s * C::RB, 0, g, ids[j], &k_full[st]);
+          if (use > 0) ok = wait_ns(&v_empty[st], (use - 1) & 1);
+          if (ok) {
+            mbar_arrive_expect_tx(&v_full[st], C::TILE);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+              for (int s = 0; s < C::NSUB; ++s)
+                tma_load_4d(sV + st * C::TILE + s * C::SUB + j * 16 * C::RB, &tmv, s * C::RB, 0, g, ids[j],
+                            &v_full[st]);
+          }
+          last_use[st] = use;
+        }
+        if (!ok) {
+          raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+          *abort_s = 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+    }
+    // let every issued copy land before the CTA can exit
+    if (lane == 0) {
+      for (int s = 0; s < C::NS; ++s) {
+        if (last_use[s] < 0) continue;
+        wait_ns(&k_full[s], last_use[s] & 1);
+        wait_ns(&v_full[s], last_use[s] & 1);
+      }
+    }
+  } else {
+    // ============================================================ MMA issuer (warp 5)
+    const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV), sPa = smem_u32(sP);
+    bool ok = wait_warp(q_full, 0);
+    int npv = 0;
+    for (int t = 0; ok && t < n_t; ++t) {
+      if (abort_warp(abort_s)) break;
+      const int st = t % C::NS, use = t / C::NS;
+      ok = wait_warp(&k_full[st], use & 1) && (t == 0 || wait_warp(s_free, (t - 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+          const int byte = kk * 32;
+          const uint32_t off = (byte / C::RB) * C::SUB + (byte % C::RB);
+          const uint64_t ad = smem_desc(sQa + off, 16, 8 * C::RB, C::SWZ);
+          const uint64_t bd = smem_desc(sKa + st * C::TILE + off, 16, 8 * C::RB, C::SWZ);
+          umma_f8(tmem + C::TM_S, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);
+        umma_commit(&k_empty[st]);
+      }
+      __syncwarp();
+      ok = wait_warp(p_full, t & 1) && wait_warp(&v_full[st], use & 1);
+      if (!ok) break;
+      // keys past the context may hold stale bytes (NaN codes): zero their V rows, since
+      // 0 * NaN would poison the product even though their P is 0
+      const int kbase = t * C::BN;
+      if (kbase + C::BN > T) {
+        const int first = max(T - kbase, 0);
+        const int chunks = C::RB / 16;
+        const int items = (C::BN - first) * C::NSUB * chunks;
+        for (int it = lane; it < items; it += 32) {
+          const int c = it % chunks;
+          const int s = (it / chunks) % C::NSUB;
+          const int r = first + it / (chunks * C::NSUB);
+          *reinterpret_cast<uint4*>(sV + st * C::TILE + s * C::SUB + r * C::RB + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      for (int hn = 0; hn < C::NH; ++hn) {
+        if (npv > 0 && !wait_warp(o_free, (npv - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 32; ++kk) {
+            const uint64_t ad = smem_desc(sPa + kk * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(sVa + st * C::TILE + hn * C::SUB + kk * 32 * C::RB, 8 * C::RB, 8 * C::RB,
+                                          C::SWZ);
+            umma_f8(tmem + C::TM_OT, ad, bd, C::IDESC_PV, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(o_full);
+        }
+        __syncwarp();
+        ++npv;
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        umma_commit(&v_empty[st]);
+        umma_commit(p_free);
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+      *abort_s = 1;
+    }
+    // every MMA issued by this warp completes before TMEM is released
+    if (lane == 0) {
+      umma_commit(mma_done);
+      wait_ns(mma_done, 0);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 4-D map over one pool: (D bytes, 16 slots, KV heads, blocks), box (RB bytes, 16, 1, 1).
+bool make_pool_map(CUtensorMap* map, void* base, int D, int Hkv, int num_blocks, int rb) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), 16, static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(16) * D,
+                                 static_cast<cuuint64_t>(16) * D * Hkv};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(rb), 16, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_prefill_t(const PrefillParams& p, void* kc, void* vc, cudaStream_t s) {
+  using C = PrefillCfg<D>;
+  CUtensorMap tmk, tmv;
+  if (!make_pool_map(&tmk, kc, D, p.Hkv, p.num_blocks, C::RB) ||
+      !make_pool_map(&tmv, vc, D, p.Hkv, p.num_blocks, C::RB))
+    return cudaErrorInvalidValue;
+  auto kern = prefill_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_qtiles, p.Hq, p.B);
+  kern<<<grid, 192, C::SMEM, s>>>(p, tmk, tmv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, int D, void* kc, void* vc, cudaStream_t s) {
+  if (D == 64) return launch_prefill_t<64>(p, kc, vc, s);
+  if (D == 128) return launch_prefill_t<128>(p, kc, vc, s);
+  if (D == 256) return launch_prefill_t<256>(p, kc, vc, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fkv

@@ -1,0 +1,143 @@
+"""fp8_prefill_attn (tcgen05 FP8 prefill, two-level accumulation) against the oracle's
+tile-exact FP8 emulation (128-key tiles, P rounded as e4m3(p*448), unrounded denominator).
+
+Tolerance: max-abs 2e-2 and relative L2 1e-2.  Small cases cover head_dim 64/128/256,
+GQA groups, per-tensor and per-head scales, causal and non-causal, ragged chunks that are
+the tail of a longer context, and NaN-coded stale bytes in partly filled blocks; the two
+large workloads are checked on sampled rows in the benchmark's launch configuration.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from helpers import assert_close, build_layer, to_dev
+from oracle import attention
+
+f = pytest.importorskip("fp8_kv_cache_quant_gb300")
+pytestmark = pytest.mark.gpu
+
+
+def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0):
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(T_list, np.int32)
+    table, nb = synth.block_table(ctx, seed=seed, extra_blocks=3)
+    n = int(ctx.sum())
+    k = torch.from_numpy((rng.standard_normal((n, Hkv, D)) * scale_k).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((n, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    cu = np.concatenate([[0], np.cumsum(Lq_list)]).astype(np.int32)
+    q = torch.from_numpy(rng.standard_normal((int(cu[-1]), Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    if gran:
+        qs, ks, vs = synth.amax_scales(q, 1), synth.amax_scales(k, 1), synth.amax_scales(v, 1)
+    else:
+        qs = torch.tensor([0.5]); ks = torch.tensor([1.0]); vs = torch.tensor([0.25])
+    cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran, False, sentinel=0xFF)
+    fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = f.fp8_prefill_attn(q.cuda(), to_dev(cu), int(max(Lq_list)), cache, to_dev(table), to_dev(ctx), to_dev(qs),
+                             to_dev(ks), to_dev(vs), gran, causal=causal, fault=fault)
+    torch.cuda.synchronize()
+    assert int(fault.item()) == 0, f"fault bits {int(fault.item())}"
+    cs = np.concatenate([[0], np.cumsum(ctx)])
+    kl = [synth.bf16_to_f64(k[cs[b]:cs[b + 1]]) for b in range(len(ctx))]
+    vl = [synth.bf16_to_f64(v[cs[b]:cs[b + 1]]) for b in range(len(ctx))]
+    ref = attention.prefill_attention(synth.bf16_to_f64(q), cu, kl, vl, qs.numpy(), ks.numpy(), vs.numpy(),
+                                      block_n=f.fkv_prefill_block_n(D), causal=causal)
+    return out.float().cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,T_list,Lq_list,gran,causal", [
+    (128, 2, 1, [200], [200], 0, True),
+    (128, 4, 2, [300, 129, 64], [300, 1, 64], 1, True),
+    (64, 8, 2, [500, 77], [180, 77], 1, True),
+    (256, 2, 1, [390, 130], [390, 100], 1, True),
+    (128, 4, 1, [257], [40], 0, False),
+    (64, 2, 2, [16, 1000], [16, 300], 0, True),
+    (256, 8, 1, [640], [256], 1, True),
+])
+def test_prefill_small_parity(D, Hq, Hkv, T_list, Lq_list, gran, causal):
+    got, ref = _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed=D + Hq + sum(T_list))
+    assert_close(got, ref, what=f"D={D} Hq={Hq} Hkv={Hkv} T={T_list} Lq={Lq_list} causal={causal}")
+
+
+def test_prefill_query_longer_than_context_faults():
+    D, Hq = 64, 2
+    ctx = np.array([32], np.int32)
+    table, nb = synth.block_table(ctx, seed=1)
+    cache = f.LayerCache.empty(nb, 1, D)
+    cache.k_cache.zero_()
+    cache.v_cache.zero_()
+    q = torch.zeros((40, Hq, D), dtype=torch.bfloat16, device="cuda")
+    cu = to_dev(np.array([0, 40], np.int32))
+    one = torch.ones(1, device="cuda")
+    fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+    f.fp8_prefill_attn(q, cu, 40, cache, to_dev(table), to_dev(ctx), one, one, one, 0, fault=fault)
+    torch.cuda.synchronize()
+    assert int(fault.item()) & f.FAULT_QLEN
+
+
+def _sample_rows(cu, per_seq, rng):
+    rows = []
+    for b in range(len(cu) - 1):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        pick = set(rng.choice(np.arange(lo, hi), min(per_seq, hi - lo), replace=False).tolist())
+        pick |= {lo, hi - 1, min(lo + 127, hi - 1), min(lo + 128, hi - 1)}
+        rows += sorted(pick)
+    return rows
+
+
+def test_workload5_prefill_d256_sampled():
+    """head_dim 256, 4 x 32768 causal, per-head scales: sampled rows of every head."""
+    w = synth.WORKLOADS[5]
+    data = synth.prefill_data(w, device="cuda")
+    ctx = np.full(w.batch, w.seq_len, np.int32)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    cache = f.LayerCache.empty(nb, w.num_kv_heads, w.head_dim)
+    f.kv_quant_cache(data.k, data.v, to_dev(synth.slot_mapping(table, ctx)), cache, data.k_scale, data.v_scale,
+                     f.SCALE_PER_HEAD)
+    cu = np.arange(w.batch + 1, dtype=np.int32) * w.seq_len
+    out = f.fp8_prefill_attn(data.q, to_dev(cu), w.seq_len, cache, to_dev(table), to_dev(ctx), data.q_scale,
+                             data.k_scale, data.v_scale, f.SCALE_PER_HEAD, causal=True).float().cpu().numpy()
+    rows = _sample_rows(cu, 12, np.random.default_rng(5))
+    kl = [synth.bf16_to_f64(data.k[cu[b]:cu[b + 1]]) for b in range(w.batch)]
+    vl = [synth.bf16_to_f64(data.v[cu[b]:cu[b + 1]]) for b in range(w.batch)]
+    qh = synth.bf16_to_f64(data.q[torch.as_tensor(rows, device="cuda")])
+    # the oracle sees only the sampled rows (others NaN); gather them into a compact query array
+    q_full = np.full((int(cu[-1]), w.num_q_heads, w.head_dim), 0.0)
+    q_full[rows] = qh
+    ref = attention.prefill_attention(q_full, cu, kl, vl, data.q_scale.cpu().numpy(), data.k_scale.cpu().numpy(),
+                                      data.v_scale.cpu().numpy(), block_n=f.fkv_prefill_block_n(w.head_dim),
+                                      rows=rows)
+    assert_close(out[rows], ref[rows], what="workload 5 prefill")
+
+
+def test_workload4_prefill_chunk_sampled():
+    """The 4096-query FP8 prefill chunk at the tail of the 131072-key needle cache."""
+    w = synth.WORKLOADS[4]
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    data = synth.decode_layer(w, 0, ctx, device="cuda")
+    cache = build_layer(f, ctx, table, nb, data.k, data.v, data.k_scale.cpu().numpy(), data.v_scale.cpu().numpy(),
+                        f.SCALE_PER_TENSOR, False)
+    qp = synth.prefill_query(w, 0, device="cuda")
+    L = w.prefill_chunk
+    cu = np.array([0, L], np.int32)
+    out = f.fp8_prefill_attn(qp, to_dev(cu), L, cache, to_dev(table), to_dev(ctx), data.q_scale, data.k_scale,
+                             data.v_scale, f.SCALE_PER_TENSOR, causal=True).float().cpu().numpy()
+    rows = _sample_rows(cu, 10, np.random.default_rng(4))
+    heads = [0, 13, 40, 63]
+    G = w.group
+    one = np.ones(1, np.float32)
+    T = int(ctx[0])
+    got, ref = [], []
+    for g in sorted(set(h // G for h in heads)):
+        kb = [synth.bf16_to_f64(data.k[:T, g:g + 1])]
+        vb = [synth.bf16_to_f64(data.v[:T, g:g + 1])]
+        hs = [h for h in heads if h // G == g]
+        q_full = np.zeros((L, len(hs), w.head_dim))
+        q_full[rows] = synth.bf16_to_f64(qp[torch.as_tensor(rows, device="cuda")][:, hs])
+        r = attention.prefill_attention(q_full, cu, kb, vb, one, one, one, block_n=f.fkv_prefill_block_n(w.head_dim),
+                                        rows=rows)
+        for j, h in enumerate(hs):
+            got.append(out[rows, h])
+            ref.append(r[rows, j])
+    assert_close(np.array(got), np.array(ref), what="workload 4 prefill chunk")
