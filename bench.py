@@ -236,6 +236,77 @@ def _time_graph(g, stream, steps, warmup, barrier):
     return e0.elapsed_time(e1) / steps
 
 
+def _fp8_dense_peak():
+    """FP8 dense tensor peak: the measured bf16 GEMM peak times the nominal fp8/bf16 ratio 2."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return 2.0 * float(json.load(fh)["bf16_tflops"]), "measured bf16_tflops x 2 (nominal fp8/bf16)"
+    return 2.0 * 1900.0, "fallback 1.9 PFLOP/s bf16 x 2"
+
+
+def time_prefill(f, workload_id, device, iters, warmup):
+    """Time fp8_prefill_attn on a prefill workload: the head_dim-256 causal batch (5) or the
+    4096-query chunk over the 131072-key cache (4).  Algorithmic FLOPs = 4 * D * unmasked
+    (query, key) pairs per head."""
+    import numpy as np
+    import torch
+    import synth
+    if workload_id == 5:
+        w = synth.WORKLOADS[5]
+        data = synth.prefill_data(w, device=device)
+        ctx = np.full(w.batch, w.seq_len, np.int32)
+        table, nb = synth.block_table(ctx, seed=w.seed)
+        cache = f.LayerCache.empty(nb, w.num_kv_heads, w.head_dim, device=device)
+        f.kv_quant_cache(data.k, data.v, torch.from_numpy(synth.slot_mapping(table, ctx)).to(device), cache,
+                         data.k_scale, data.v_scale, f.SCALE_PER_HEAD)
+        cu = torch.from_numpy(np.arange(w.batch + 1, dtype=np.int32) * w.seq_len).to(device)
+        q, qs, ks, vs, L, gran = data.q, data.q_scale, data.k_scale, data.v_scale, w.seq_len, f.SCALE_PER_HEAD
+        flops = 4 * w.head_dim * w.num_q_heads * w.batch * (w.seq_len * (w.seq_len + 1) // 2)
+        name = w.name
+        del data.k, data.v
+    else:
+        w = synth.WORKLOADS[4]
+        ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+        table, nb = synth.block_table(ctx, seed=w.seed)
+        data = synth.decode_layer(w, 0, ctx, device=device)
+        cache = f.LayerCache.empty(nb, w.num_kv_heads, w.head_dim, device=device)
+        f.kv_quant_cache(data.k, data.v, torch.from_numpy(synth.slot_mapping(table, ctx)).to(device), cache,
+                         data.k_scale, data.v_scale, f.SCALE_PER_TENSOR)
+        del data.k, data.v
+        q = synth.prefill_query(w, 0, device=device)
+        L = w.prefill_chunk
+        cu = torch.tensor([0, L], dtype=torch.int32, device=device)
+        qs, ks, vs, gran = data.q_scale, data.k_scale, data.v_scale, f.SCALE_PER_TENSOR
+        T = int(ctx[0])
+        flops = 4 * w.head_dim * w.num_q_heads * (L * (T - L) + L * (L + 1) // 2)
+        name = w.name + f"-prefill{L}"
+    tbl = torch.from_numpy(table).to(device)
+    cx = torch.from_numpy(ctx).to(device)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(device)
+
+    def call():
+        f.fp8_prefill_attn(q, cu, L, cache, tbl, cx, qs, ks, vs, gran, out=out, stream=stream)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        call()
+    e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    peak, kind = _fp8_dense_peak()
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"workload": name, "ms": ms, "flops": flops, "iters": iters,
+            "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": kind}}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 def oracle_sample(workload_id: int, keys: int, heads: int):
@@ -380,6 +451,12 @@ def run_ours(args):
                      "fp8_over_bf16_step_time": ms_fp8 / ms_bf,
                      "kv_bytes_fp8": kv_fp8, "kv_bytes_bf16": kv_bf}
 
+    prefill = None
+    if not args.no_prefill:
+        torch.cuda.synchronize()
+        prefill = [time_prefill(f, wid, device, iters=min(args.steps, 10), warmup=3) for wid in (5, 4)]
+        torch.cuda.synchronize()
+
     cpu = None
     if rank == 0 and not args.no_cpu:
         keys = int(sum(int(t) for t in fp8.ctx))
@@ -413,6 +490,7 @@ def run_ours(args):
             "gpu_launches": fp8.launches_per_step() * args.steps,
             "clocks": clocks.summary(),
             "bf16": bf16_info,
+            "prefill": prefill,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -430,6 +508,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

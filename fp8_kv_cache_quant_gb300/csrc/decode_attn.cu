@@ -21,6 +21,8 @@
 // The warps' states are merged in shared memory and written as (o / l, log2-sum-exp).
 // Every wait is bounded in time; on a timeout the CTA records FKV_FAULT_TIMEOUT, lets
 // its in-flight copies land and returns.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -73,6 +75,7 @@ struct DecodeCfg {
   static_assert(LPK >= 2 && LPK <= 32, "lanes per key");
   static_assert(LPV >= 1 && LPV <= 32, "lanes per value row");
   static_assert(G * VPL <= 64 && G * EPL <= 64, "register budget");
+  static_assert(NVF == 1, "every lane ends the QK reduction with one whole score");
   static_assert(kNW * G * D * 4 <= RING, "the warps' accumulators are merged inside the ring");
 };
 
@@ -173,31 +176,11 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
   const int vg = lane / C::LPV;                 // key sub-group of the PV mapping
   const int dv = (lane % C::LPV) * C::VPL;      // first element of the lane's PV slice
 
-  // softmax constant per head: softmax_scale * log2(e) * q_s * k_s
-  float cst[G];
-  {
-    const float ks = ELT == 1 ? p.k_scale[p.per_head ? g : 0] : 1.f;
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-      cst[h] = p.sm_scale_log2 * (ELT == 1 ? p.q_scale[p.per_head ? h0 + h : 0] * ks : 1.f);
-  }
-  // query slice, quantised to e4m3 (exact float values of the codes) for FP8 layers
-  float2 qf[G][C::EPL / 2];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const __nv_bfloat16* qp = p.q + (static_cast<size_t>(b) * p.Hq + h0 + h) * D + dq;
-    const float iq = ELT == 1 ? __frcp_rn(p.q_scale[p.per_head ? h0 + h : 0]) : 1.f;
-#pragma unroll
-    for (int e = 0; e < C::EPL / 2; ++e) {
-      float2 x = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(qp + 2 * e));
-      if constexpr (ELT == 1) {
-        const uint16_t c = f32x2_to_e4m3x2(__fmul_rn(x.x, iq), __fmul_rn(x.y, iq));
-        x = __half22float2(e4m3x2_to_h2(c));
-      }
-      qf[h][e] = x;
-    }
-  }
-  // heads of this lane after the transposing reduction: hb .. hb+NVF-1
+  // Heads of a lane.  The transposing reduction below halves the lane's G partial dot
+  // products at every shuffle level, keeping the lower half of its slots and receiving
+  // the partner's upper half.  For that to need no selects, lane slot j holds query head
+  // j ^ hb, where hb collects the lane bits of the halving levels; after the reduction
+  // slot 0 holds the full score of head hb.
   int hb = 0;
   {
     int nv = G;
@@ -210,25 +193,38 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
     }
   }
   const bool dup0 = (C::LPK <= G) ? true : ((lane % C::LPK) % (C::LPK / G) == 0);
-  float cl[C::NVF];
+  // softmax constant of head hb: softmax_scale * log2(e) * q_s * k_s
+  const float cl = p.sm_scale_log2 *
+                   (ELT == 1 ? p.q_scale[p.per_head ? h0 + hb : 0] * p.k_scale[p.per_head ? g : 0] : 1.f);
+  // query slice in slot order, quantised to e4m3 (exact values of the codes) on FP8 layers
+  float2 qf[G][C::EPL / 2];
 #pragma unroll
-  for (int j = 0; j < C::NVF; ++j) {
-    cl[j] = cst[0];
+  for (int j = 0; j < G; ++j) {
+    const int h = j ^ hb;
+    const __nv_bfloat16* qp = p.q + (static_cast<size_t>(b) * p.Hq + h0 + h) * D + dq;
+    const float iq = ELT == 1 ? __frcp_rn(p.q_scale[p.per_head ? h0 + h : 0]) : 1.f;
 #pragma unroll
-    for (int h = 1; h < G; ++h)
-      if (h == hb + j) cl[j] = cst[h];
+    for (int e = 0; e < C::EPL / 2; ++e) {
+      float2 x = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(qp + 2 * e));
+      if constexpr (ELT == 1) {
+        const uint16_t c = f32x2_to_e4m3x2(__fmul_rn(x.x, iq), __fmul_rn(x.y, iq));
+        x = __half22float2(e4m3x2_to_h2(c));
+      }
+      qf[j][e] = x;
+    }
   }
 
-  float m_run[C::NVF], l_run[C::NVF];
-#pragma unroll
-  for (int i = 0; i < C::NVF; ++i) { m_run[i] = -INFINITY; l_run[i] = 0.f; }
+  float m_run = -INFINITY, l_run = 0.f;
   float2 acc[G][C::VPL / 2 > 0 ? C::VPL / 2 : 1];
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
 
+  // per-warp probabilities of the current tile: float (bf16 layers) or (p, p) half2 pairs
+  // (e4m3 layers, for the packed f16 P.V products); both 4 bytes per (key, head)
   float* pw = p_s + warp * 16 * C::TB * G;
+  __half2* pwh = reinterpret_cast<__half2*>(pw);
   float* aw = alpha_s + warp * G;
   int issued = min(kNBUF, max(0, (ntiles - warp + kNW - 1) / kNW));
   int k = 0;
@@ -245,77 +241,83 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
     const uint8_t* tile = wring + buf * C::TILE_BYTES;
     const int nb = min(C::TB, nblk - t * C::TB);
     const int key0 = (blk_first + t * C::TB) * 16;  // absolute position of the tile's first key
+    const bool interior = nb == C::TB && key0 >= r.lo && key0 + 16 * C::TB <= r.T;
 
     // ---------------- QK
-    float sc[C::TB][C::ROUNDS][C::NVF];
+    float sc[C::TB][C::ROUNDS];
+    auto qk = [&](auto all_valid) {
 #pragma unroll
-    for (int j = 0; j < C::TB; ++j) {
-      const uint8_t* kb = tile + j * 2 * C::CHUNK;
+      for (int j = 0; j < C::TB; ++j) {
+        const uint8_t* kb = tile + j * 2 * C::CHUNK;
 #pragma unroll
-      for (int rr = 0; rr < C::ROUNDS; ++rr) {
-        const int key = rr * C::KPR + kq;
-        uint32_t w[C::EPL * ELT / 4 > 0 ? C::EPL * ELT / 4 : 1];
-        load_bytes<C::EPL * ELT>(kb + key * D * ELT + dq * ELT, w);
-        float2 kf[C::EPL / 2];
-        to_f2<ELT, C::EPL>(w, kf);
-        float v[G];
+        for (int rr = 0; rr < C::ROUNDS; ++rr) {
+          const int key = rr * C::KPR + kq;
+          uint32_t w[C::EPL * ELT / 4 > 0 ? C::EPL * ELT / 4 : 1];
+          load_bytes<C::EPL * ELT>(kb + key * D * ELT + dq * ELT, w);
+          float2 kf[C::EPL / 2];
+          to_f2<ELT, C::EPL>(w, kf);
+          float v[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float2 a = make_float2(0.f, 0.f);
+          for (int h = 0; h < G; ++h) {
+            float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < C::EPL / 2; ++e) a = __ffma2_rn(qf[h][e], kf[e], a);
-          v[h] = a.x + a.y;
-        }
-        // transposing reduction across the LPK lanes of this key
-        int nv = G;
+            for (int e = 0; e < C::EPL / 2; ++e) a = __ffma2_rn(qf[h][e], kf[e], a);
+            v[h] = a.x + a.y;
+          }
+          // select-free transposing reduction across the LPK lanes of this key
+          int nv = G;
 #pragma unroll
-        for (int off = C::LPK / 2; off >= 1; off >>= 1) {
-          if (nv > 1) {
-            const bool up = lane & off;
+          for (int off = C::LPK / 2; off >= 1; off >>= 1) {
+            if (nv > 1) {
 #pragma unroll
-            for (int q2 = 0; q2 < nv / 2; ++q2) {
-              const float send = up ? v[q2] : v[q2 + nv / 2];
-              const float keep = up ? v[q2 + nv / 2] : v[q2];
-              v[q2] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+              for (int q2 = 0; q2 < nv / 2; ++q2) v[q2] += __shfl_xor_sync(0xffffffffu, v[q2 + nv / 2], off);
+              nv >>= 1;
+            } else {
+              v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
             }
-            nv >>= 1;
+          }
+          if constexpr (decltype(all_valid)::value) {
+            sc[j][rr] = v[0] * cl;
           } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+            const int kabs = key0 + j * 16 + key;
+            const bool valid = j < nb && kabs >= r.lo && kabs < r.T;
+            sc[j][rr] = valid ? v[0] * cl : -INFINITY;
           }
         }
-        const int kabs = key0 + j * 16 + key;
-        const bool valid = j < nb && kabs >= r.lo && kabs < r.T;
-#pragma unroll
-        for (int jv = 0; jv < C::NVF; ++jv) sc[j][rr][jv] = valid ? v[jv] * cl[jv] : -INFINITY;
       }
-    }
+    };
+    if (interior) qk(std::true_type{});
+    else qk(std::false_type{});
 
     // ---------------- softmax (base 2) over the tile's keys
-#pragma unroll
-    for (int jv = 0; jv < C::NVF; ++jv) {
+    {
       float mx = -INFINITY;
 #pragma unroll
       for (int j = 0; j < C::TB; ++j)
 #pragma unroll
-        for (int rr = 0; rr < C::ROUNDS; ++rr) mx = fmaxf(mx, sc[j][rr][jv]);
+        for (int rr = 0; rr < C::ROUNDS; ++rr) mx = fmaxf(mx, sc[j][rr]);
 #pragma unroll
       for (int off = C::LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mn = fmaxf(m_run[jv], mx);
-      const float alpha = (m_run[jv] == -INFINITY) ? 0.f : ex2(m_run[jv] - mn);
-      m_run[jv] = mn;
+      const float mn = fmaxf(m_run, mx);
+      const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mn);
+      m_run = mn;
       float sum = 0.f;
 #pragma unroll
       for (int j = 0; j < C::TB; ++j)
 #pragma unroll
         for (int rr = 0; rr < C::ROUNDS; ++rr) {
-          const float pv = ex2(sc[j][rr][jv] - mn);
+          const float pv = ex2(sc[j][rr] - mn);
           sum += pv;
-          if (dup0) pw[(j * 16 + rr * C::KPR + kq) * G + hb + jv] = pv;
+          if (dup0) {
+            const int idx = (j * 16 + rr * C::KPR + kq) * G + hb;
+            if constexpr (ELT == 1) pwh[idx] = __float2half2_rn(pv);
+            else pw[idx] = pv;
+          }
         }
 #pragma unroll
       for (int off = C::LPK; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      l_run[jv] = l_run[jv] * alpha + sum;
-      if (dup0 && kq == 0) aw[hb + jv] = alpha;
+      l_run = l_run * alpha + sum;
+      if (dup0 && kq == 0) aw[hb] = alpha;
     }
     __syncwarp();
 
@@ -333,11 +335,21 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
         }
       }
     }
+    // e4m3 layers: the tile's P.V partial (at most 16 products per element and lane) is
+    // summed in packed f16 on the exact f16 values of the V codes and P rounded to f16,
+    // then promoted into the FP32 accumulator (two-level accumulation).  bf16 layers
+    // multiply and accumulate in FP32.
+    __half2 acc16[G][C::VPL / 2 > 0 ? C::VPL / 2 : 1];
+    if constexpr (ELT == 1) {
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < C::VPL / 2; ++e) acc16[h][e] = __float2half2_rn(0.f);
+    }
 #pragma unroll
     for (int j = 0; j < C::TB; ++j) {
       if (j >= nb) break;
       const uint8_t* vb = tile + j * 2 * C::CHUNK + C::CHUNK;
-      const float* pj = pw + j * 16 * G;
       // keys of this block inside [lo, T); the bytes of the other keys may be stale (even
       // NaN codes), so they are skipped rather than weighted by p = 0.
       const int kb0 = key0 + j * 16;
@@ -345,25 +357,56 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
       auto pv_key = [&](int key) {
         uint32_t w[C::VPL * ELT / 4 > 0 ? C::VPL * ELT / 4 : 1];
         load_bytes<C::VPL * ELT>(vb + key * D * ELT + dv * ELT, w);
-        float2 vf[C::VPL / 2];
-        to_f2<ELT, C::VPL>(w, vf);
-        const float* pk = pj + key * G;
-        float pv[G];
-        if constexpr (G % 4 == 0) {
+        const int pidx = (j * 16 + key) * G;
+        if constexpr (ELT == 1) {
+          __half2 vh[C::VPL / 2];
+          if constexpr (C::VPL >= 4) {
 #pragma unroll
-          for (int h = 0; h < G; h += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(pk + h);
-            pv[h] = x.x; pv[h + 1] = x.y; pv[h + 2] = x.z; pv[h + 3] = x.w;
+            for (int i = 0; i < C::VPL / 4; ++i) {
+              vh[2 * i] = e4m3x2_to_h2(static_cast<uint16_t>(w[i] & 0xFFFFu));
+              vh[2 * i + 1] = e4m3x2_to_h2(static_cast<uint16_t>(w[i] >> 16));
+            }
+          } else {
+            vh[0] = e4m3x2_to_h2(static_cast<uint16_t>(w[0] & 0xFFFFu));
           }
+          __half2 ph[G];
+          if constexpr (G % 4 == 0) {
+#pragma unroll
+            for (int h = 0; h < G; h += 4) {
+              const uint4 x = *reinterpret_cast<const uint4*>(pwh + pidx + h);
+              ph[h] = *reinterpret_cast<const __half2*>(&x.x);
+              ph[h + 1] = *reinterpret_cast<const __half2*>(&x.y);
+              ph[h + 2] = *reinterpret_cast<const __half2*>(&x.z);
+              ph[h + 3] = *reinterpret_cast<const __half2*>(&x.w);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < G; ++h) ph[h] = pwh[pidx + h];
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < C::VPL / 2; ++e) acc16[h][e] = __hfma2(ph[h], vh[e], acc16[h][e]);
         } else {
+          float2 vf[C::VPL / 2];
+          to_f2<ELT, C::VPL>(w, vf);
+          float pv[G];
+          if constexpr (G % 4 == 0) {
 #pragma unroll
-          for (int h = 0; h < G; ++h) pv[h] = pk[h];
-        }
+            for (int h = 0; h < G; h += 4) {
+              const float4 x = *reinterpret_cast<const float4*>(pw + pidx + h);
+              pv[h] = x.x; pv[h + 1] = x.y; pv[h + 2] = x.z; pv[h + 3] = x.w;
+            }
+          } else {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float2 p2 = make_float2(pv[h], pv[h]);
+            for (int h = 0; h < G; ++h) pv[h] = pw[pidx + h];
+          }
 #pragma unroll
-          for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+          for (int h = 0; h < G; ++h) {
+            const float2 p2 = make_float2(pv[h], pv[h]);
+#pragma unroll
+            for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+          }
         }
       };
       if (kv_lo == 0 && kv_hi == 16) {
@@ -376,6 +419,16 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
           if (key >= kv_lo && key < kv_hi) pv_key(key);
         }
       }
+    }
+    if constexpr (ELT == 1) {
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < C::VPL / 2; ++e) {
+          const float2 x = __half22float2(acc16[h][e]);
+          acc[h][e].x += x.x;
+          acc[h][e].y += x.y;
+        }
     }
     __syncwarp();
     // the buffer is free again: refill it with this warp's tile k + NBUF
@@ -402,11 +455,8 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
       }
   }
   if (dup0 && kq == 0) {
-#pragma unroll
-    for (int jv = 0; jv < C::NVF; ++jv) {
-      ml_s[(warp * 2 + 0) * G + hb + jv] = m_run[jv];
-      ml_s[(warp * 2 + 1) * G + hb + jv] = l_run[jv];
-    }
+    ml_s[(warp * 2 + 0) * G + hb] = m_run;
+    ml_s[(warp * 2 + 1) * G + hb] = l_run;
   }
   __syncthreads();  // every warp is done with the ring and has no copy in flight
   float* acc_w = reinterpret_cast<float*>(ring);  // [NW][G][D]

@@ -30,7 +30,12 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--bf16", action="store_true", help="bf16 pool (the skip-layer path) instead of e4m3")
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--prefill", action="store_true",
+                    help="run fp8_prefill_attn on the head_dim-256 prefill shape instead (batch 1)")
+    ap.add_argument("--seq", type=int, default=8192, help="prefill sequence length")
     a = ap.parse_args()
+    if a.prefill:
+        return run_prefill(a)
     w = synth.WORKLOADS[a.workload]
     dev = torch.device("cuda:0")
     ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
@@ -52,6 +57,32 @@ def main():
                           num_splits=a.splits)
     torch.cuda.synchronize()
     print("profile_case done", w.name, "layer", a.layer, "bf16" if a.bf16 else "e4m3")
+
+
+def run_prefill(a):
+    import numpy as np
+    import torch
+
+    import fp8_kv_cache_quant_gb300 as f
+    import synth
+
+    w = synth.WORKLOADS[5]
+    dev = torch.device("cuda:0")
+    data = synth.prefill_data(w, device=dev, seq_len=a.seq, batch=1)
+    ctx = np.array([a.seq], np.int32)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    cache = f.LayerCache.empty(nb, w.num_kv_heads, w.head_dim, device=dev)
+    f.kv_quant_cache(data.k, data.v, torch.from_numpy(synth.slot_mapping(table, ctx)).to(dev), cache, data.k_scale,
+                     data.v_scale, f.SCALE_PER_HEAD)
+    cu = torch.tensor([0, a.seq], dtype=torch.int32, device=dev)
+    tbl = torch.from_numpy(table).to(dev)
+    cx = torch.from_numpy(ctx).to(dev)
+    out = torch.empty_like(data.q)
+    for _ in range(a.iters):
+        f.fp8_prefill_attn(data.q, cu, a.seq, cache, tbl, cx, data.q_scale, data.k_scale, data.v_scale,
+                           f.SCALE_PER_HEAD, out=out)
+    torch.cuda.synchronize()
+    print("profile_case done prefill", a.seq)
 
 
 if __name__ == "__main__":

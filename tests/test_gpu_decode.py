@@ -83,8 +83,12 @@ def test_split_count_invariance_and_permutation():
         outs[s] = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(one), to_dev(one),
                                     to_dev(one), 0, num_splits=s).float().cpu().numpy()
     assert np.all(np.isfinite(outs[1]))
+    # different split counts group the keys differently; the per-tile f16 P.V partials
+    # then round differently, at about 1e-3 of the output's scale
+    scale = float(np.max(np.abs(outs[1])))
     for s in (2, 7, 0):
-        np.testing.assert_allclose(outs[s], outs[1], rtol=2.0 ** -7, atol=1e-6)
+        np.testing.assert_allclose(outs[s], outs[1], rtol=0, atol=2e-3 * scale)
+        assert np.linalg.norm(outs[s] - outs[1]) <= 2e-3 * np.linalg.norm(outs[1])
     # the same data under another physical block permutation: bit-identical output
     table2, nb2 = synth.block_table(ctx, seed=99, extra_blocks=3)
     cache2 = build_layer(f, ctx, table2, nb2, k, v, one, one, 0, False, sentinel=0x7F)
