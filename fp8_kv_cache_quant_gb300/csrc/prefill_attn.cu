@@ -50,6 +50,12 @@ FKV_DEV bool wait_warp(uint64_t* bar, uint32_t parity) {
 }
 FKV_DEV bool abort_warp(volatile int* flag) { return __any_sync(0xffffffffu, *flag != 0); }
 
+FKV_DEV float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 template <int D>
 struct PrefillCfg {
   static constexpr int BM = 128, BN = 128;
@@ -58,27 +64,33 @@ struct PrefillCfg {
   static constexpr int SWZ = RB == 128 ? 2 : 4;     // descriptor swizzle mode (128 B / 64 B)
   static constexpr int SUB = BM * RB;               // bytes of one 128-row sub-tile
   static constexpr int TILE = BM * D;               // bytes of a Q, K or V tile
-  static constexpr int NS = 2;                      // K/V stages
+  static constexpr int NS = D <= 128 ? 3 : 2;       // K/V stages
   static constexpr int DN = D < 128 ? D : 128;      // N of one P.V product
   static constexpr int NH = D / DN;
-  static constexpr int TM_S = 0, TM_OT = 128, TM_OA = 128 + DN;
-  static constexpr int TM_COLS = (128 + DN + D) <= 256 ? 256 : 512;
+  static constexpr int SBUF = D <= 128 ? 2 : 1;     // S buffers in TMEM
+  static constexpr int TM_OT = 128 * SBUF, TM_OA = TM_OT + DN;
+  static constexpr int TM_COLS = (TM_OA + D) <= 256 ? 256 : 512;
   // shared memory layout (bytes)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_P = OFF_V + NS * TILE;
-  static constexpr int OFF_BAR = OFF_P + BM * BN;
-  static constexpr int NBAR = 8 + 4 * NS;
+  static constexpr int OFF_P = OFF_V + NS * TILE;           // two P tiles
+  static constexpr int OFF_A = OFF_P + 2 * BM * BN;         // alpha [2][128] floats
+  static constexpr int OFF_L = OFF_A + 2 * BM * 4;          // l [128] floats
+  static constexpr int OFF_BAR = OFF_L + BM * 4;
+  static constexpr int NBAR = 17 + 4 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_QK = idesc_e4m3_f32(128, 128, 0, 0);
   static constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, DN, 0, 1);
-  static_assert(128 + DN + D <= 512, "TMEM budget");
+  static_assert(TM_OA + D <= 512, "TMEM budget");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
+constexpr int kPrefillThreads = 320;  // softmax WG, correction WG, TMA warp, MMA warp
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
   using C = PrefillCfg<D>;
@@ -88,16 +100,21 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sP = smem + C::OFF_P;
+  float* sAlpha = reinterpret_cast<float*>(smem + C::OFF_A);
+  float* sL = reinterpret_cast<float*>(smem + C::OFF_L);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* s_full = bars + 1;
-  uint64_t* s_free = bars + 2;
-  uint64_t* p_full = bars + 3;
-  uint64_t* p_free = bars + 4;
-  uint64_t* o_full = bars + 5;
-  uint64_t* o_free = bars + 6;
-  uint64_t* mma_done = bars + 7;
-  uint64_t* k_full = bars + 8;
+  uint64_t* s_full = bars + 1;      // [2]
+  uint64_t* s_free = bars + 3;      // [2]
+  uint64_t* p_full = bars + 5;      // [2]
+  uint64_t* p_free = bars + 7;      // [2]
+  uint64_t* o_full = bars + 9;
+  uint64_t* o_free = bars + 10;
+  uint64_t* l_full = bars + 11;
+  uint64_t* mma_done = bars + 12;
+  uint64_t* a_full = bars + 13;     // [2] alpha of a tile published in slot t % 2
+  uint64_t* a_free = bars + 15;     // [2] ... and read by the correction warpgroup
+  uint64_t* k_full = bars + 17;
   uint64_t* k_empty = k_full + C::NS;
   uint64_t* v_full = k_empty + C::NS;
   uint64_t* v_empty = v_full + C::NS;
@@ -132,12 +149,19 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 128);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(p_full, 128);
-    mbar_init(p_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&p_free[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&a_full[i], 128);
+      mbar_init(&a_free[i], 128);
+    }
     mbar_init(o_full, 1);
     mbar_init(o_free, 128);
+    mbar_init(l_full, 128);
     mbar_init(mma_done, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&k_full[s], 1);
@@ -148,7 +172,7 @@ __global__ void __launch_bounds__(192, 1)
     *abort_s = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, C::TM_COLS);
     tmem_relinquish();
     tc_fence_before();
@@ -159,14 +183,13 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp < 4) {
     // ============================================================ softmax warpgroup
-    const int i = threadIdx.x;                 // query row within the tile
+    const int i = threadIdx.x;                 // query row within the tile (TMEM lane i)
     const bool row_ok = i < rows;
     const int pos = pos0 + i;                  // its absolute position
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     // ---- prologue: Q row -> e4m3 codes in the swizzled Q tile
     {
-      const float qs = p.q_scale[p.per_head ? h : 0];
-      const float iq = __frcp_rn(qs);
+      const float iq = __frcp_rn(p.q_scale[p.per_head ? h : 0]);
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D);
 #pragma unroll 4
       for (int c = 0; c < D / 16; ++c) {
@@ -191,73 +214,121 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(q_full);
     }
     const float cst = p.sm_scale_log2 * p.q_scale[p.per_head ? h : 0] * p.k_scale[p.per_head ? g : 0];
+    const int lim_row = (p.causal && row_ok) ? min(T, pos + 1) : T;  // keys [0, lim_row) visible
     float m = -INFINITY, l = 0.f;
-    int npv = 0;
+    bool ok = true;
     for (int t = 0; t < n_t; ++t) {
-      if (abort_warp(abort_s)) break;
-      if (!wait_warp(s_full, t & 1)) {
-        raise_fault(p.fault, FKV_FAULT_TIMEOUT);
-        *abort_s = 1;
-        break;
-      }
+      if (abort_warp(abort_s)) { ok = false; break; }
+      const int sb = t % C::SBUF;
+      if (!wait_warp(&s_full[sb], (t / C::SBUF) & 1)) { ok = false; break; }
       tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(lane_base + C::TM_S + 32 * c, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) s[32 * c + j] = v[j];
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(s_free);
-      // scale into the base-2 domain and mask: keys beyond the context, and beyond the
-      // row's own position when causal (rows past the chunk see every key)
-      const int kbase = t * C::BN;
-      const int lim = (p.causal && row_ok) ? min(T, pos + 1) : T;
+      const int lim = lim_row - t * C::BN;  // columns [0, lim) of this tile are visible
+      const bool full = lim >= C::BN;       // interior tile for this row: nothing masked
+      const uint32_t sc = lane_base + 128 * sb;
+      // pass 1: row max of the scaled, masked scores (cst > 0, so the raw maximum scales).
+      // The TMEM loads are warp-collective: every lane issues them; only the arithmetic
+      // depends on the row's own mask.
       float tmax = -INFINITY;
+      {
+        float mx = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 128; ++j) {
-        s[j] = (kbase + j < lim) ? s[j] * cst : -INFINITY;
-        tmax = fmaxf(tmax, s[j]);
+        for (int hf = 0; hf < 2; ++hf) {
+          float v0[32], v1[32];
+          tmem_ld32(sc + 64 * hf, v0);
+          tmem_ld32(sc + 64 * hf + 32, v1);
+          tmem_ld_wait();
+          if (full) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) mx = fmax3(mx, fmax3(v0[j], v0[j + 1], v1[j]), v1[j + 1]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int c0 = 64 * hf + j, c1 = c0 + 32;
+              tmax = fmaxf(tmax, c0 < lim ? v0[j] * cst : -INFINITY);
+              tmax = fmaxf(tmax, c1 < lim ? v1[j] * cst : -INFINITY);
+            }
+          }
+        }
+        if (full) tmax = mx * cst;
       }
       const float mn = fmaxf(m, tmax);
       const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
       const float msafe = (mn == -INFINITY) ? 0.f : mn;
-      float lsum = 0.f;
-      uint32_t pk[32];
+      // P tile t%2 is free once the P.V of tile t-2 completed
+      const int pb = t & 1;
+      if (t >= 2 && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+      uint8_t* P = sP + pb * C::BM * C::BN;
+      // pass 2: p = 2^(s*cst - m), its unrounded sum, and P8 = e4m3(p * 448) into the P tile
+      float2 lsum2 = make_float2(0.f, 0.f);
+      const float2 cst2 = make_float2(cst, cst), nm2 = make_float2(-msafe, -msafe);
+      const float2 k448 = make_float2(448.f, 448.f);
 #pragma unroll
-      for (int j = 0; j < 128; j += 4) {
-        const float a0 = ex2(s[j] - msafe), a1 = ex2(s[j + 1] - msafe);
-        const float a2 = ex2(s[j + 2] - msafe), a3 = ex2(s[j + 3] - msafe);
-        lsum += (a0 + a1) + (a2 + a3);
-        const uint32_t lo = f32x2_to_e4m3x2(a0 * 448.f, a1 * 448.f);
-        const uint32_t hi = f32x2_to_e4m3x2(a2 * 448.f, a3 * 448.f);
-        pk[j / 4] = lo | (hi << 16);
+      for (int hf = 0; hf < 2; ++hf) {
+        float v[64];
+        {
+          float v0[32], v1[32];
+          tmem_ld32(sc + 64 * hf, v0);
+          tmem_ld32(sc + 64 * hf + 32, v1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) { v[j] = v0[j]; v[32 + j] = v1[j]; }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          float2 x0 = __ffma2_rn(make_float2(v[j], v[j + 1]), cst2, nm2);
+          float2 x1 = __ffma2_rn(make_float2(v[j + 2], v[j + 3]), cst2, nm2);
+          x0.x = ex2(x0.x); x0.y = ex2(x0.y); x1.x = ex2(x1.x); x1.y = ex2(x1.y);
+          if (!full) {
+            const int c = 64 * hf + j;
+            if (c >= lim) x0.x = 0.f;
+            if (c + 1 >= lim) x0.y = 0.f;
+            if (c + 2 >= lim) x1.x = 0.f;
+            if (c + 3 >= lim) x1.y = 0.f;
+          }
+          lsum2 = __fadd2_rn(lsum2, __fadd2_rn(x0, x1));
+          const float2 y0 = __fmul2_rn(x0, k448), y1 = __fmul2_rn(x1, k448);
+          pk[j / 4] = static_cast<uint32_t>(f32x2_to_e4m3x2(y0.x, y0.y)) |
+                      (static_cast<uint32_t>(f32x2_to_e4m3x2(y1.x, y1.y)) << 16);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t lin = static_cast<uint32_t>(i * 128 + (4 * hf + c) * 16);
+          *reinterpret_cast<uint4*>(P + swz(lin, 128)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
       }
+      const float lsum = lsum2.x + lsum2.y;
+      tc_fence_before();
+      mbar_arrive(&s_free[sb]);
       l = l * alpha + lsum;
       m = mn;
-      // P row -> swizzled P tile, once the previous tile's P.V has read it
-      if (t > 0 && !wait_warp(p_free, (t - 1) & 1)) {
-        raise_fault(p.fault, FKV_FAULT_TIMEOUT);
-        *abort_s = 1;
-        break;
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t lin = static_cast<uint32_t>(i * 128 + c * 16);
-        *reinterpret_cast<uint4*>(sP + swz(lin, 128)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      }
+      // alpha slot t%2 is free once the correction warpgroup has read tile t-2's alpha
+      if (t >= 2 && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+      sAlpha[pb * C::BM + i] = alpha;
+      mbar_arrive(&a_full[pb]);
       fence_proxy_async_smem();
-      mbar_arrive(p_full);
-      // promote the tile's P.V partial: O = O * alpha + O_tile (FP32)
-      bool ok = true;
+      mbar_arrive(&p_full[pb]);
+    }
+    if (!ok) {
+      if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+      *abort_s = 1;
+    }
+    sL[i] = l;
+    mbar_arrive(l_full);
+  } else if (warp < 8) {
+    // ============================================================ correction warpgroup
+    const int i = threadIdx.x - 128;           // query row (TMEM lane i)
+    const bool row_ok = i < rows;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16);
+    int npv = 0;
+    bool ok = true;
+    for (int t = 0; t < n_t; ++t) {
+      if (abort_warp(abort_s)) { ok = false; break; }
+      if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+      const float alpha = sAlpha[(t & 1) * C::BM + i];
+      mbar_arrive(&a_free[t & 1]);
       for (int hn = 0; hn < C::NH; ++hn) {
-        if (!wait_warp(o_full, npv & 1)) {
-          ok = false;
-          break;
-        }
+        if (!wait_warp(o_full, npv & 1)) { ok = false; break; }
         ++npv;
         tc_fence_after();
 #pragma unroll
@@ -279,14 +350,15 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         mbar_arrive(o_free);
       }
-      if (!ok) {
-        raise_fault(p.fault, FKV_FAULT_TIMEOUT);
-        *abort_s = 1;
-        break;
-      }
+      if (!ok) break;
+    }
+    if (!ok) {
+      if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+      *abort_s = 1;
     }
     // ---- epilogue: O * v_s / (448 l) -> bf16 (every lane loads; rows past the chunk do not store)
-    if (!abort_warp(abort_s)) {
+    if (wait_warp(l_full, 0) && !abort_warp(abort_s)) {
+      const float l = sL[i];
       const float vs = p.v_scale[p.per_head ? g : 0];
       const float f = (l > 0.f) ? vs / (448.f * l) : 0.f;
       __nv_bfloat16* dst = p.out + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D;
@@ -308,7 +380,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ============================================================ TMA producer
     const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
     int last_use[C::NS];
@@ -377,15 +449,14 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    // ============================================================ MMA issuer (warp 5)
+    // ============================================================ MMA issuer (warp 9)
     const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV), sPa = smem_u32(sP);
-    bool ok = wait_warp(q_full, 0);
     int npv = 0;
-    for (int t = 0; ok && t < n_t; ++t) {
-      if (abort_warp(abort_s)) break;
-      const int st = t % C::NS, use = t / C::NS;
-      ok = wait_warp(&k_full[st], use & 1) && (t == 0 || wait_warp(s_free, (t - 1) & 1));
-      if (!ok) break;
+    // S(t) = Q8 K8^T into S buffer t % SBUF
+    auto issue_qk = [&](int t) -> bool {
+      const int st = t % C::NS, sb = t % C::SBUF;
+      if (!wait_warp(&k_full[st], (t / C::NS) & 1)) return false;
+      if (t >= C::SBUF && !wait_warp(&s_free[sb], ((t / C::SBUF) - 1) & 1)) return false;
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
@@ -394,14 +465,19 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t off = (byte / C::RB) * C::SUB + (byte % C::RB);
           const uint64_t ad = smem_desc(sQa + off, 16, 8 * C::RB, C::SWZ);
           const uint64_t bd = smem_desc(sKa + st * C::TILE + off, 16, 8 * C::RB, C::SWZ);
-          umma_f8(tmem + C::TM_S, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          umma_f8(tmem + 128 * sb, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
         }
-        umma_commit(s_full);
+        umma_commit(&s_full[sb]);
         umma_commit(&k_empty[st]);
       }
       __syncwarp();
-      ok = wait_warp(p_full, t & 1) && wait_warp(&v_full[st], use & 1);
-      if (!ok) break;
+      return true;
+    };
+    // O_tile = P8(t) V8(t), in NH products of N = DN
+    auto issue_pv = [&](int t) -> bool {
+      const int st = t % C::NS, pb = t & 1;
+      if (!wait_warp(&p_full[pb], (t >> 1) & 1)) return false;
+      if (!wait_warp(&v_full[st], (t / C::NS) & 1)) return false;
       // keys past the context may hold stale bytes (NaN codes): zero their V rows, since
       // 0 * NaN would poison the product even though their P is 0
       const int kbase = t * C::BN;
@@ -419,15 +495,12 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
       }
       for (int hn = 0; hn < C::NH; ++hn) {
-        if (npv > 0 && !wait_warp(o_free, (npv - 1) & 1)) {
-          ok = false;
-          break;
-        }
+        if (npv > 0 && !wait_warp(o_free, (npv - 1) & 1)) return false;
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < C::BN / 32; ++kk) {
-            const uint64_t ad = smem_desc(sPa + kk * 32, 16, 1024, 2);
+            const uint64_t ad = smem_desc(sPa + pb * C::BM * C::BN + kk * 32, 16, 1024, 2);
             const uint64_t bd = smem_desc(sVa + st * C::TILE + hn * C::SUB + kk * 32 * C::RB, 8 * C::RB, 8 * C::RB,
                                           C::SWZ);
             umma_f8(tmem + C::TM_OT, ad, bd, C::IDESC_PV, kk > 0 ? 1u : 0u);
@@ -437,12 +510,18 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         ++npv;
       }
-      if (!ok) break;
       if (lane == 0) {
         umma_commit(&v_empty[st]);
-        umma_commit(p_free);
+        umma_commit(&p_free[pb]);
       }
       __syncwarp();
+      return true;
+    };
+    bool ok = wait_warp(q_full, 0) && issue_qk(0);
+    for (int t = 0; ok && t < n_t; ++t) {
+      if (abort_warp(abort_s)) break;
+      if (t + 1 < n_t) ok = issue_qk(t + 1);  // S of the next tile overlaps this tile's softmax
+      if (ok) ok = issue_pv(t);
     }
     if (!ok) {
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
@@ -456,7 +535,7 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   }
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TM_COLS);
   }
@@ -514,7 +593,7 @@ cudaError_t launch_prefill_t(const PrefillParams& p, void* kc, void* vc, cudaStr
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_qtiles, p.Hq, p.B);
-  kern<<<grid, 192, C::SMEM, s>>>(p, tmk, tmv);
+  kern<<<grid, kPrefillThreads, C::SMEM, s>>>(p, tmk, tmv);
   return cudaGetLastError();
 }
 
