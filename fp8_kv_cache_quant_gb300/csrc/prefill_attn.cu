@@ -68,6 +68,10 @@ struct PrefillCfg {
   static constexpr int DN = D < 128 ? D : 128;      // N of one P.V product
   static constexpr int NH = D / DN;
   static constexpr int SBUF = D <= 128 ? 2 : 1;     // S buffers in TMEM
+  // unrolling of the softmax / correction chunk loops: full for head_dim <= 128 (the
+  // softmax is the critical path there), none for 256 (code size of four warp roles)
+  static constexpr int UNR = D <= 128 ? 4 : 1;
+  static constexpr bool ONE_LOAD = D <= 128;        // S row loaded once into registers
   static constexpr int TM_OT = 128 * SBUF, TM_OA = TM_OT + DN;
   static constexpr int TM_COLS = (TM_OA + D) <= 256 ? 256 : 512;
   // shared memory layout (bytes)
@@ -225,31 +229,46 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const int lim = lim_row - t * C::BN;  // columns [0, lim) of this tile are visible
       const bool full = lim >= C::BN;       // interior tile for this row: nothing masked
       const uint32_t sc = lane_base + 128 * sb;
-      // pass 1: row max of the scaled, masked scores (cst > 0, so the raw maximum scales).
-      // The TMEM loads are warp-collective: every lane issues them; only the arithmetic
-      // depends on the row's own mask.
+      float vall[C::ONE_LOAD ? 128 : 1];
       float tmax = -INFINITY;
-      {
-        float mx = -INFINITY;
+      if constexpr (C::ONE_LOAD) {
+        // head_dim <= 128: the whole S row in registers, one TMEM wait; S is released at once
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float v0[32], v1[32];
-          tmem_ld32(sc + 64 * hf, v0);
-          tmem_ld32(sc + 64 * hf + 32, v1);
-          tmem_ld_wait();
-          if (full) {
+        for (int c = 0; c < 4; ++c) tmem_ld32(sc + 32 * c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&s_free[sb]);
+        if (full) {
+          float mx = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) mx = fmax3(mx, fmax3(v0[j], v0[j + 1], v1[j]), v1[j + 1]);
-          } else {
+          for (int j = 0; j < 128; j += 4) mx = fmax3(mx, fmax3(vall[j], vall[j + 1], vall[j + 2]), vall[j + 3]);
+          tmax = mx * cst;
+        } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int c0 = 64 * hf + j, c1 = c0 + 32;
-              tmax = fmaxf(tmax, c0 < lim ? v0[j] * cst : -INFINITY);
-              tmax = fmaxf(tmax, c1 < lim ? v1[j] * cst : -INFINITY);
+          for (int j = 0; j < 128; ++j) tmax = fmaxf(tmax, j < lim ? vall[j] * cst : -INFINITY);
+        }
+      } else {
+        // pass 1: row max of the scaled, masked scores (cst > 0, so the raw maximum scales).
+        // The TMEM loads are warp-collective: every lane issues them; only the arithmetic
+        // depends on the row's own mask.  Loops run over 32-column chunks and are not
+        // unrolled at that level, to keep the warp roles' code small.
+        {
+          float mx = -INFINITY;
+  #pragma unroll C::UNR
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(sc + 32 * c, v);
+            tmem_ld_wait();
+            if (full) {
+  #pragma unroll
+              for (int j = 0; j < 32; j += 4) mx = fmax3(mx, fmax3(v[j], v[j + 1], v[j + 2]), v[j + 3]);
+            } else {
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, 32 * c + j < lim ? v[j] * cst : -INFINITY);
             }
           }
+          if (full) tmax = mx * cst;
         }
-        if (full) tmax = mx * cst;
       }
       const float mn = fmaxf(m, tmax);
       const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
@@ -258,33 +277,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const int pb = t & 1;
       if (t >= 2 && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
       uint8_t* P = sP + pb * C::BM * C::BN;
-      // pass 2: p = 2^(s*cst - m), its unrounded sum, and P8 = e4m3(p * 448) into the P tile
+      // pass 2: p = 2^(s*cst - m), its unrounded sum, and P8 = e4m3(p * 448) into the P tile;
+      // the next chunk's TMEM load is in flight while the current one is processed
       float2 lsum2 = make_float2(0.f, 0.f);
       const float2 cst2 = make_float2(cst, cst), nm2 = make_float2(-msafe, -msafe);
       const float2 k448 = make_float2(448.f, 448.f);
+      auto chunk = [&](const float (&v)[32], int c) {
+        uint32_t pk[8];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v[64];
-        {
-          float v0[32], v1[32];
-          tmem_ld32(sc + 64 * hf, v0);
-          tmem_ld32(sc + 64 * hf + 32, v1);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) { v[j] = v0[j]; v[32 + j] = v1[j]; }
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 64; j += 4) {
+        for (int j = 0; j < 32; j += 4) {
           float2 x0 = __ffma2_rn(make_float2(v[j], v[j + 1]), cst2, nm2);
           float2 x1 = __ffma2_rn(make_float2(v[j + 2], v[j + 3]), cst2, nm2);
           x0.x = ex2(x0.x); x0.y = ex2(x0.y); x1.x = ex2(x1.x); x1.y = ex2(x1.y);
           if (!full) {
-            const int c = 64 * hf + j;
-            if (c >= lim) x0.x = 0.f;
-            if (c + 1 >= lim) x0.y = 0.f;
-            if (c + 2 >= lim) x1.x = 0.f;
-            if (c + 3 >= lim) x1.y = 0.f;
+            const int col = 32 * c + j;
+            if (col >= lim) x0.x = 0.f;
+            if (col + 1 >= lim) x0.y = 0.f;
+            if (col + 2 >= lim) x1.x = 0.f;
+            if (col + 3 >= lim) x1.y = 0.f;
           }
           lsum2 = __fadd2_rn(lsum2, __fadd2_rn(x0, x1));
           const float2 y0 = __fmul2_rn(x0, k448), y1 = __fmul2_rn(x1, k448);
@@ -292,14 +302,34 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                       (static_cast<uint32_t>(f32x2_to_e4m3x2(y1.x, y1.y)) << 16);
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t lin = static_cast<uint32_t>(i * 128 + (4 * hf + c) * 16);
-          *reinterpret_cast<uint4*>(P + swz(lin, 128)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t lin = static_cast<uint32_t>(i * 128 + (2 * c + q) * 16);
+          *reinterpret_cast<uint4*>(P + swz(lin, 128)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      };
+      if constexpr (C::ONE_LOAD) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) chunk(*reinterpret_cast<const float(*)[32]>(vall + 32 * c), c);
+      } else {
+        {
+          float va[32], vb[32];
+          tmem_ld32(sc, va);
+  #pragma unroll C::UNR
+          for (int c = 0; c < 4; c += 2) {
+            tmem_ld_wait();
+            tmem_ld32(sc + 32 * (c + 1), vb);
+            chunk(va, c);
+            tmem_ld_wait();
+            if (c + 2 < 4) tmem_ld32(sc + 32 * (c + 2), va);
+            chunk(vb, c + 1);
+          }
         }
       }
       const float lsum = lsum2.x + lsum2.y;
-      tc_fence_before();
-      mbar_arrive(&s_free[sb]);
+      if constexpr (!C::ONE_LOAD) {
+        tc_fence_before();
+        mbar_arrive(&s_free[sb]);
+      }
       l = l * alpha + lsum;
       m = mn;
       // alpha slot t%2 is free once the correction warpgroup has read tile t-2's alpha
@@ -331,7 +361,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (!wait_warp(o_full, npv & 1)) { ok = false; break; }
         ++npv;
         tc_fence_after();
-#pragma unroll
+#pragma unroll C::UNR
         for (int c = 0; c < C::DN / 32; ++c) {
           float ot[32], oa[32];
           tmem_ld32(lane_base + C::TM_OT + 32 * c, ot);
