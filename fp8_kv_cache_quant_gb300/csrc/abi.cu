@@ -42,7 +42,7 @@ bool supported_group(int32_t G, int32_t D) {
 struct DecodePlan {
   int bps = 0;
   int max_splits = 0;
-  size_t o_bytes = 0, lse_bytes = 0;
+  size_t o_bytes = 0, lse_bytes = 0, cnt_bytes = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -73,6 +73,7 @@ bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_bloc
   const size_t rows = static_cast<size_t>(B) * Hq * plan->max_splits;
   plan->o_bytes = align256(rows * D * sizeof(float));
   plan->lse_bytes = align256(rows * sizeof(float));
+  plan->cnt_bytes = align256(static_cast<size_t>(std::max(B, 1)) * Hkv * sizeof(int32_t));
   return true;
 }
 
@@ -123,7 +124,7 @@ size_t fp8_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_
   DecodePlan plan;
   if (!supported_head_dim(head_dim)) return 0;
   if (!plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks, window, num_splits, &plan)) return 0;
-  return plan.o_bytes + plan.lse_bytes;
+  return plan.o_bytes + plan.lse_bytes + plan.cnt_bytes;
 }
 
 int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
@@ -165,7 +166,7 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads, fk
   DecodePlan plan;
   if (!plan_decode(batch, num_q_heads, cache.num_kv_heads, cache.head_dim, max_blocks, window, num_splits, &plan))
     return FKV_UNSUPPORTED;
-  if (workspace_bytes < plan.o_bytes + plan.lse_bytes) return FKV_INVALID_ARG;
+  if (workspace_bytes < plan.o_bytes + plan.lse_bytes + plan.cnt_bytes) return FKV_INVALID_ARG;
 
   DecodeParams p;
   std::memset(&p, 0, sizeof(p));
@@ -190,8 +191,13 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads, fk
   p.max_splits = plan.max_splits;
   p.o_part = static_cast<float*>(workspace);
   p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.o_bytes);
+  p.done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plan.o_bytes + plan.lse_bytes);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.fault = fault;
+  // split-completion counters start at zero on every call
+  if (cudaMemsetAsync(p.done, 0, static_cast<size_t>(batch) * cache.num_kv_heads * sizeof(int32_t),
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FKV_CUDA_ERROR;
   return from_cuda(fkv::launch_decode(p, cache.head_dim, bf16, G, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -77,6 +77,7 @@ struct DecodeCfg {
   static_assert(G * VPL <= 64 && G * EPL <= 64, "register budget");
   static_assert(NVF == 1, "every lane ends the QK reduction with one whole score");
   static_assert(kNW * G * D * 4 <= RING, "the warps' accumulators are merged inside the ring");
+  static_assert(RING / 4 >= 2 * G + 8 * G, "the merge keeps at least 8 split weights per head in the ring");
 };
 
 template <int N>
@@ -125,7 +126,13 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
   const int sigma = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqRange r = seq_range(p, b, sigma == 0 && g == 0 && threadIdx.x == 0);
-  if (sigma >= r.nsplit) return;  // uniform over the CTA
+  if (sigma >= r.nsplit) {  // uniform over the CTA
+    if (sigma == 0) {  // a sequence without keys: zero output rows
+      for (int t = threadIdx.x; t < G * D; t += blockDim.x)
+        p.out[(static_cast<size_t>(b) * p.Hq + g * G + t / D) * D + t % D] = __float2bfloat16(0.f);
+    }
+    return;
+  }
   const int blk_first = r.blk_begin + sigma * p.bps;
   const int nblk = min(p.bps, r.blk_end - blk_first);
   const int ntiles = (nblk + C::TB - 1) / C::TB;
@@ -194,10 +201,16 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
   }
   const bool dup0 = (C::LPK <= G) ? true : ((lane % C::LPK) % (C::LPK / G) == 0);
   // softmax constant of head hb: softmax_scale * log2(e) * q_s * k_s
+  // On e4m3 layers the QK partial products are summed in packed f16 on exact operands:
+  // query codes times 2^-8 and key codes are f16 values, so each product is exact and at
+  // most 448 * 448 / 256 = 784; each lane adds 8 products per half in f16 and promotes
+  // the two halves into FP32 before the cross-lane reduction (two-level accumulation).
+  // The 2^8 returns in the softmax constant.
   const float cl = p.sm_scale_log2 *
-                   (ELT == 1 ? p.q_scale[p.per_head ? h0 + hb : 0] * p.k_scale[p.per_head ? g : 0] : 1.f);
-  // query slice in slot order, quantised to e4m3 (exact values of the codes) on FP8 layers
-  float2 qf[G][C::EPL / 2];
+                   (ELT == 1 ? 256.f * p.q_scale[p.per_head ? h0 + hb : 0] * p.k_scale[p.per_head ? g : 0] : 1.f);
+  // query slice in slot order (e4m3 codes * 2^-8 as half2 on FP8 layers, float2 on bf16 layers)
+  float2 qf[ELT == 1 ? 1 : G][C::EPL / 2];
+  __half2 qh[ELT == 1 ? G : 1][C::EPL / 2];
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const int h = j ^ hb;
@@ -205,12 +218,13 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
     const float iq = ELT == 1 ? __frcp_rn(p.q_scale[p.per_head ? h0 + h : 0]) : 1.f;
 #pragma unroll
     for (int e = 0; e < C::EPL / 2; ++e) {
-      float2 x = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(qp + 2 * e));
+      const float2 x = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(qp + 2 * e));
       if constexpr (ELT == 1) {
         const uint16_t c = f32x2_to_e4m3x2(__fmul_rn(x.x, iq), __fmul_rn(x.y, iq));
-        x = __half22float2(e4m3x2_to_h2(c));
+        qh[j][e] = __hmul2(e4m3x2_to_h2(c), __float2half2_rn(0.00390625f));  // exact: times 2^-8
+      } else {
+        qf[j][e] = x;
       }
-      qf[j][e] = x;
     }
   }
 
@@ -254,15 +268,36 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
           const int key = rr * C::KPR + kq;
           uint32_t w[C::EPL * ELT / 4 > 0 ? C::EPL * ELT / 4 : 1];
           load_bytes<C::EPL * ELT>(kb + key * D * ELT + dq * ELT, w);
-          float2 kf[C::EPL / 2];
-          to_f2<ELT, C::EPL>(w, kf);
           float v[G];
+          if constexpr (ELT == 1) {
+            __half2 kh[C::EPL / 2];
+            if constexpr (C::EPL >= 4) {
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float2 a = make_float2(0.f, 0.f);
+              for (int i = 0; i < C::EPL / 4; ++i) {
+                kh[2 * i] = e4m3x2_to_h2(static_cast<uint16_t>(w[i] & 0xFFFFu));
+                kh[2 * i + 1] = e4m3x2_to_h2(static_cast<uint16_t>(w[i] >> 16));
+              }
+            } else {
+              kh[0] = e4m3x2_to_h2(static_cast<uint16_t>(w[0] & 0xFFFFu));
+            }
 #pragma unroll
-            for (int e = 0; e < C::EPL / 2; ++e) a = __ffma2_rn(qf[h][e], kf[e], a);
-            v[h] = a.x + a.y;
+            for (int h = 0; h < G; ++h) {
+              __half2 a = __hmul2(qh[h][0], kh[0]);
+#pragma unroll
+              for (int e = 1; e < C::EPL / 2; ++e) a = __hfma2(qh[h][e], kh[e], a);
+              const float2 af = __half22float2(a);
+              v[h] = af.x + af.y;
+            }
+          } else {
+            float2 kf[C::EPL / 2];
+            to_f2<ELT, C::EPL>(w, kf);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int e = 0; e < C::EPL / 2; ++e) a = __ffma2_rn(qf[h][e], kf[e], a);
+              v[h] = a.x + a.y;
+            }
           }
           // select-free transposing reduction across the LPK lanes of this key
           int nv = G;
@@ -490,41 +525,75 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
     p.o_part[row * D + d] = L > 0.f ? O / L : 0.f;
     if (d == 0) p.lse_part[row] = L > 0.f ? M + lg2(L) : -INFINITY;
   }
-}
 
-// Merge the splits of one (sequence, query head): o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
-// times the V scale, to bf16.  FP32 throughout.
-template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p, int G, int apply_vscale) {
-  const int bh = blockIdx.x;
-  const int b = bh / p.Hq, h = bh % p.Hq;
-  const SeqRange r = seq_range(p, b, false);
-  const size_t row0 = static_cast<size_t>(bh) * p.max_splits;
-  __shared__ float w_s[1024];
-  __shared__ float red_s[2];
-  const int ns = min(r.nsplit, 1024);
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, p.lse_part[row0 + s]);
-  float W = 0.f;
-  for (int s = threadIdx.x; s < ns; s += blockDim.x) {
-    const float l = p.lse_part[row0 + s];
-    w_s[s] = (l == -INFINITY) ? 0.f : ex2(l - M);
-  }
+  // ---------------------------------------------------- the last split of (b, g) merges
+  // o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M), times the V scale, to bf16: the
+  // FP32 second level of the accumulation.
+  volatile int* last_s = ids_s;  // the block ids are no longer needed
+  __threadfence();
   __syncthreads();
-  for (int s = 0; s < ns; ++s) W += w_s[s];
-  const float vs = apply_vscale ? p.v_scale[p.per_head ? h / G : 0] : 1.f;
-  const float inv = (W > 0.f) ? vs / W : 0.f;
-  for (int d = threadIdx.x * 2; d < D; d += blockDim.x * 2) {
-    float2 o = make_float2(0.f, 0.f);
-    for (int s = 0; s < ns; ++s) {
-      const float2 x = *reinterpret_cast<const float2*>(p.o_part + (row0 + s) * D + d);
-      o.x += w_s[s] * x.x;
-      o.y += w_s[s] * x.y;
-    }
-    __nv_bfloat162 y = __floats2bfloat162_rn(o.x * inv, o.y * inv);
-    *reinterpret_cast<__nv_bfloat162*>(p.out + static_cast<size_t>(bh) * D + d) = y;
+  if (threadIdx.x == 0) *last_s = atomicAdd(&p.done[b * p.Hkv + g], 1) == r.nsplit - 1;
+  __syncthreads();
+  if (!*last_s) return;
+  __threadfence();
+  // per head: M = max_s lse_s and 1 / sum_s 2^(lse_s - M) (times the V scale)
+  float* ms_s = reinterpret_cast<float*>(ring);       // [G]
+  float* inv_s = ms_s + G;                            // [G]
+  float* w_s = inv_s + G;                             // [G][CH] weights of a chunk of splits
+  constexpr int CH = (C::RING / 4 - 2 * G) / G < 256 ? (C::RING / 4 - 2 * G) / G : 256;
+  const float vs = ELT == 1 ? p.v_scale[p.per_head ? g : 0] : 1.f;
+  const int ns = r.nsplit;
+  for (int t = threadIdx.x; t < G; t += blockDim.x) {
+    const size_t row0 = (static_cast<size_t>(b) * p.Hq + g * G + t) * p.max_splits;
+    float M = -INFINITY;
+    for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(p.lse_part + row0 + s2));
+    float W = 0.f;
+    if (M != -INFINITY)
+      for (int s2 = 0; s2 < ns; ++s2) {
+        const float lv = __ldcg(p.lse_part + row0 + s2);
+        W += (lv == -INFINITY) ? 0.f : ex2(lv - M);
+      }
+    ms_s[t] = M;
+    inv_s[t] = (W > 0.f) ? vs / W : 0.f;
   }
-  (void)red_s;
+  constexpr int PAIRS = (G * D / 2 + kNW * 32 - 1) / (kNW * 32);  // output pairs per thread
+  float2 o[PAIRS];
+#pragma unroll
+  for (int k2 = 0; k2 < PAIRS; ++k2) o[k2] = make_float2(0.f, 0.f);
+  for (int c0 = 0; c0 < ns; c0 += CH) {
+    const int nc = min(CH, ns - c0);
+    __syncthreads();
+    for (int t = threadIdx.x; t < G * nc; t += blockDim.x) {
+      const int h = t / nc, j = t % nc;
+      const float lv = __ldcg(p.lse_part + (static_cast<size_t>(b) * p.Hq + g * G + h) * p.max_splits + c0 + j);
+      w_s[h * CH + j] = (lv == -INFINITY) ? 0.f : ex2(lv - ms_s[h]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k2 = 0; k2 < PAIRS; ++k2) {
+      const int t = threadIdx.x + k2 * kNW * 32;
+      if (t < G * D / 2) {
+        const int h = t / (D / 2), d = 2 * (t % (D / 2));
+        const float* src = p.o_part + ((static_cast<size_t>(b) * p.Hq + g * G + h) * p.max_splits + c0) * D + d;
+        for (int j = 0; j < nc; ++j) {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + static_cast<size_t>(j) * D));
+          const float wv = w_s[h * CH + j];
+          o[k2].x += wv * x.x;
+          o[k2].y += wv * x.y;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k2 = 0; k2 < PAIRS; ++k2) {
+    const int t = threadIdx.x + k2 * kNW * 32;
+    if (t < G * D / 2) {
+      const int h = t / (D / 2), d = 2 * (t % (D / 2));
+      const float inv = inv_s[h];
+      *reinterpret_cast<__nv_bfloat162*>(p.out + (static_cast<size_t>(b) * p.Hq + g * G + h) * D + d) =
+          __floats2bfloat162_rn(o[k2].x * inv, o[k2].y * inv);
+    }
+  }
 }
 
 template <int D, int ELT, int G>
@@ -542,9 +611,6 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   dim3 grid(p.max_splits, p.Hkv, p.B);
   kern<<<grid, kNW * 32, smem, s>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  decode_merge_kernel<D><<<p.B * p.Hq, 128, 0, s>>>(p, G, ELT == 1 ? 1 : 0);
   return cudaGetLastError();
 }
 

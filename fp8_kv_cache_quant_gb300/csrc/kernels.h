@@ -25,6 +25,7 @@ struct DecodeParams {
   int max_splits;
   float* o_part;        // [B][Hq][max_splits][D]
   float* lse_part;      // [B][Hq][max_splits], base 2
+  int32_t* done;        // [B][Hkv] splits finished (zeroed before the launch)
   __nv_bfloat16* out;   // [B][Hq][D]
   int32_t* fault;
 };
