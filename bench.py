@@ -142,7 +142,7 @@ def decode_bytes(w, ctx, layer_is_bf16):
 
 
 class DecodeState:
-    def __init__(self, f, w, device, all_bf16=False):
+    def __init__(self, f, w, device, all_bf16=False, no_skip=False):
         import numpy as np
         import torch
         import synth
@@ -150,7 +150,12 @@ class DecodeState:
         self.f = f
         self.ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
         self.table, self.nb = synth.block_table(self.ctx, seed=w.seed)
-        self.mask = np.ones(w.num_layers, np.uint8) if all_bf16 else w.skip_mask()
+        if all_bf16:
+            self.mask = np.ones(w.num_layers, np.uint8)
+        elif no_skip:
+            self.mask = np.zeros(w.num_layers, np.uint8)
+        else:
+            self.mask = w.skip_mask()
         self.bf16 = [bool(x) for x in self.mask]
         self.gran = f.SCALE_PER_HEAD if w.scale_mode == "amax" else f.SCALE_PER_TENSOR
         self.table_d = torch.from_numpy(self.table).to(device)
@@ -199,7 +204,8 @@ class DecodeState:
                               workspace=self.ws)
 
     def launches_per_step(self):
-        return 3 * len(self.layers)
+        # kv_quant_cache and decode_split_kernel per layer (the split-counter reset is a memset node)
+        return 2 * len(self.layers)
 
     def step_bytes(self):
         return sum(x["decode"] + x["write"] for x in self.bytes)
@@ -307,6 +313,80 @@ def time_prefill(f, workload_id, device, iters, warmup):
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": kind}}
 
 
+def linear_fit(xs, ys):
+    """Least-squares line y = slope * x + intercept (the blog's ITL fit)."""
+    n = len(xs)
+    mx = sum(xs) / n
+    my = sum(ys) / n
+    sxx = sum((x - mx) ** 2 for x in xs)
+    sxy = sum((x - mx) * (y - my) for x, y in zip(xs, ys))
+    slope = sxy / sxx
+    return slope, my - slope * mx
+
+
+def break_even(slope_a, icpt_a, slope_b, icpt_b):
+    """Context length where line a (e.g. FP8) drops below line b (e.g. BF16); None if it never does."""
+    if slope_b <= slope_a:
+        return None
+    return (icpt_a - icpt_b) / (slope_b - slope_a)
+
+
+def dist_barrier(dist, world):
+    if world > 1:
+        dist.barrier()
+
+
+def dist_max(dist, world, x, device):
+    """Maximum of a float over the ranks (all-reduce MAX)."""
+    if world == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+SWEEP_T = (256, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 125000)
+
+
+def itl_sweep(f, device, steps, warmup, lengths=SWEEP_T):
+    """The ITL-slope proxy: per-step decode time of all layers at batch 1 versus the cached
+    context T, for an e4m3 cache and for a bf16 cache, with least-squares lines (the blog's
+    ITL = slope * input_len + intercept) and the break-even context.  Shapes: the
+    Llama-3.1-8B-shaped stack (32 layers, 32/8 heads, head_dim 128) and the gpt-oss-20b-shaped
+    hybrid stack (24 layers, window-128 layers every other layer), the latter with and
+    without the sliding-window layers kept bf16."""
+    import dataclasses
+    import torch
+    import synth
+    out = {}
+    shapes = {"llama8b": (synth.WORKLOADS[2], [("fp8", {}), ("bf16", {"all_bf16": True})]),
+              "gptoss20b-hybrid": (synth.WORKLOADS[3], [("fp8-skip-sw", {}), ("fp8", {"no_skip": True}),
+                                                        ("bf16", {"all_bf16": True})])}
+    stream = torch.cuda.Stream(device)
+    for name, (base, variants) in shapes.items():
+        res = {v: [] for v, _ in variants}
+        for T in lengths:
+            w = dataclasses.replace(base, batch=1, ctx_lo=T, ctx_hi=T, name=f"{base.name}-b1-t{T}")
+            for v, kw in variants:
+                st = DecodeState(f, w, device, **kw)
+                g = _graph(st.step, stream)
+                ms = _time_graph(g, stream, steps, warmup, lambda: None)
+                res[v].append(ms * 1e3)
+                del g, st
+                torch.cuda.empty_cache()
+        entry = {"T": list(lengths), "us_per_step": res}
+        fits = {v: linear_fit(list(lengths), ys) for v, ys in res.items()}
+        entry["slope_us_per_1k_tokens"] = {v: fi[0] * 1e3 for v, fi in fits.items()}
+        entry["intercept_us"] = {v: fi[1] for v, fi in fits.items()}
+        ref = fits["bf16"]
+        entry["slope_ratio_vs_bf16"] = {v: fi[0] / ref[0] for v, fi in fits.items() if v != "bf16"}
+        entry["break_even_tokens"] = {v: break_even(fi[0], fi[1], ref[0], ref[1])
+                                      for v, fi in fits.items() if v != "bf16"}
+        out[name] = entry
+    return out
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 def oracle_sample(workload_id: int, keys: int, heads: int):
@@ -389,17 +469,20 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=device)
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        dist_barrier(dist, world)
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return dist_max(dist, world, x, device)
 
     f.load_library()
+    if args.sweep:
+        res = itl_sweep(f, device, steps=max(3, min(args.steps, 50)), warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"sweep": "ITL-slope proxy (decode step time vs cached context, batch 1)",
+                              "unit": "us", "results": res}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
     w = synth.WORKLOADS[args.workload]
     stream = torch.cuda.Stream(device)
 
@@ -481,7 +564,7 @@ def run_ours(args):
                        "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
             "us_per_step": ms_fp8 * 1e3,
             "pct_of_hbm_peak": value / peak,
-            "roofline": {"bound": "hbm", "kernel": "fp8_decode_attn (decode_split_kernel + decode_merge_kernel)",
+            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel (fp8_decode_attn, merge fused)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
                          "algorithmic_bytes_per_launch": dec_bytes, "launch_ms": dec_launch_ms},
@@ -509,6 +592,7 @@ def main():
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="ITL-slope sweep instead of the benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

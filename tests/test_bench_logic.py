@@ -1,0 +1,96 @@
+"""Host logic of the benchmark (CPU only): ITL fits and break-even against the numbers the
+vLLM blog prints (tests/golden/itl_fits.txt), byte accounting, the oracle sample of the
+reference arm, and the max-over-ranks timing with two gloo ranks."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "itl_fits.txt")
+
+
+def _golden_rows():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            name, sb, ib, sf, i_f, be, tol, ratio = line.split()
+            rows.append((name, float(sb), float(ib), float(sf), float(i_f), float(be), float(tol), float(ratio)))
+    return rows
+
+
+def test_break_even_and_slope_ratio_match_the_blog():
+    rows = _golden_rows()
+    assert len(rows) == 3
+    for name, sb, ib, sf, i_f, be, tol, ratio in rows:
+        got = bench.break_even(sf, i_f, sb, ib)
+        assert abs(got - be) <= tol * be, (name, got, be)
+        assert abs(sf / sb - ratio) <= 0.006, (name, sf / sb, ratio)
+
+
+def test_break_even_none_when_fp8_is_not_cheaper():
+    assert bench.break_even(2.0, 1.0, 1.0, 0.0) is None
+
+
+def test_linear_fit_recovers_line():
+    xs = [256, 1024, 4096, 16384, 125000]
+    ys = [3.2e-3 * x + 41.0 for x in xs]
+    s, c = bench.linear_fit(xs, ys)
+    assert abs(s - 3.2e-3) < 1e-12 and abs(c - 41.0) < 1e-9
+    rng = np.random.default_rng(0)
+    ys2 = [y + e for y, e in zip(ys, rng.standard_normal(len(xs)) * 0.01)]
+    s2, _ = bench.linear_fit(xs, ys2)
+    assert abs(s2 - 3.2e-3) < 1e-6
+
+
+def test_decode_bytes_accounting():
+    w = synth.WORKLOADS[3]
+    ctx = np.array([8192, 20000], np.int32)
+    import dataclasses
+    w2 = dataclasses.replace(w, batch=2)
+    per = bench.decode_bytes(w2, ctx, [bool(x) for x in w2.skip_mask()])
+    # full layer 0 (e4m3): every key, 2 (K, V) * 8 heads * 64 bytes
+    assert per[0]["kv"] == sum(2 * 8 * 64 * int(t) for t in ctx)
+    # window layer 1 (bf16, skip mask): the last 128 keys, 2 bytes each
+    assert per[1]["kv"] == 2 * (2 * 8 * 64 * 2 * 128)
+    assert per[0]["write"] == 2 * 8 * 64 * (2 * 2 + 2 * 1)
+
+
+def test_oracle_sample_of_the_reference_arm():
+    dt, nbytes = bench.oracle_sample(2, 512, 4)
+    assert dt > 0 and nbytes == 2 * 1 * 128 * 512
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    bench.dist_barrier(dist, world)
+    got = bench.dist_max(dist, world, 1.5 + rank, torch.device("cpu"))
+    bench.dist_barrier(dist, world)
+    q.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+    assert res == {0: 2.5, 1: 2.5}
