@@ -123,9 +123,9 @@ constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
 FKV_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;  // sleep rather than spin
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
   }
 }
 
