@@ -273,10 +273,7 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
             __half2 kh[C::EPL / 2];
             if constexpr (C::EPL >= 4) {
 #pragma unroll
-              for (int i = 0; i < C::EPL / 4; ++i) {
-                kh[2 * i] = e4m3x2_to_h2(static_cast<uint16_t>(w[i] & 0xFFFFu));
-                kh[2 * i + 1] = e4m3x2_to_h2(static_cast<uint16_t>(w[i] >> 16));
-              }
+              for (int i = 0; i < C::EPL / 4; ++i) e4m3x4_to_h2x2(w[i], kh[2 * i], kh[2 * i + 1]);
             } else {
               kh[0] = e4m3x2_to_h2(static_cast<uint16_t>(w[0] & 0xFFFFu));
             }
@@ -397,10 +394,7 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
           __half2 vh[C::VPL / 2];
           if constexpr (C::VPL >= 4) {
 #pragma unroll
-            for (int i = 0; i < C::VPL / 4; ++i) {
-              vh[2 * i] = e4m3x2_to_h2(static_cast<uint16_t>(w[i] & 0xFFFFu));
-              vh[2 * i + 1] = e4m3x2_to_h2(static_cast<uint16_t>(w[i] >> 16));
-            }
+            for (int i = 0; i < C::VPL / 4; ++i) e4m3x4_to_h2x2(w[i], vh[2 * i], vh[2 * i + 1]);
           } else {
             vh[0] = e4m3x2_to_h2(static_cast<uint16_t>(w[0] & 0xFFFFu));
           }
