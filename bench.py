@@ -251,7 +251,7 @@ def _fp8_dense_peak():
     return 2.0 * 1900.0, "fallback 1.9 PFLOP/s bf16 x 2"
 
 
-def time_prefill(f, workload_id, device, iters, warmup):
+def time_prefill(f, workload_id, device, iters, warmup, promote_every=(1,)):
     """Time fp8_prefill_attn on a prefill workload: the head_dim-256 causal batch (5) or the
     4096-query chunk over the 131072-key cache (4).  Algorithmic FLOPs = 4 * D * unmasked
     (query, key) pairs per head."""
@@ -292,25 +292,28 @@ def time_prefill(f, workload_id, device, iters, warmup):
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(device)
 
-    def call():
-        f.fp8_prefill_attn(q, cu, L, cache, tbl, cx, qs, ks, vs, gran, out=out, stream=stream)
-
-    for _ in range(warmup):
-        call()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(iters):
-        call()
-    e1.record(stream)
-    e1.synchronize()
-    ms = e0.elapsed_time(e1) / iters
+    res = []
     peak, kind = _fp8_dense_peak()
-    achieved = flops / (ms * 1e-3) / 1e12
-    return {"workload": name, "ms": ms, "flops": flops, "iters": iters,
-            "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": kind}}
+    for pe in promote_every:
+        def call():
+            f.fp8_prefill_attn(q, cu, L, cache, tbl, cx, qs, ks, vs, gran, out=out, stream=stream, promote_every=pe)
+
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            call()
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        achieved = flops / (ms * 1e-3) / 1e12
+        res.append({"workload": name, "promote_every": pe, "ms": ms, "flops": flops, "iters": iters,
+                    "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved, "peak": peak,
+                                 "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": kind}})
+    return res
 
 
 def linear_fit(xs, ys):
@@ -537,7 +540,8 @@ def run_ours(args):
     prefill = None
     if not args.no_prefill:
         torch.cuda.synchronize()
-        prefill = [time_prefill(f, wid, device, iters=min(args.steps, 10), warmup=3) for wid in (5, 4)]
+        prefill = (time_prefill(f, 5, device, iters=min(args.steps, 10), warmup=3, promote_every=(1, 0)) +
+                   time_prefill(f, 4, device, iters=min(args.steps, 10), warmup=3, promote_every=(1, 4, 0)))
         torch.cuda.synchronize()
 
     cpu = None

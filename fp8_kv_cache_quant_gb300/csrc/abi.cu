@@ -217,8 +217,9 @@ fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t 
   if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
   if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
   if (!(softmax_scale >= 0.f) || std::isinf(softmax_scale)) return FKV_INVALID_ARG;
-  if (window < 0) return FKV_INVALID_ARG;
-  if (window != 0 || promote_every != 1) return FKV_UNSUPPORTED;
+  if (window < 0 || promote_every < 0) return FKV_INVALID_ARG;
+  if (window != 0) return FKV_UNSUPPORTED;
+  if (promote_every >= 2 && cache.head_dim > 128) return FKV_UNSUPPORTED;  // TMEM holds one 128-column O_tile
   fkv_status st = FKV_OK;
   const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
   if (st != FKV_OK) return st;
@@ -250,6 +251,7 @@ fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t 
   const float tau = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache.head_dim));
   p.sm_scale_log2 = tau * 1.4426950408889634f;
   p.causal = causal != 0;
+  p.promote_every = promote_every;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.fault = fault;
   return from_cuda(fkv::launch_prefill(p, cache.head_dim, cache.k_cache, cache.v_cache,

@@ -42,6 +42,7 @@ struct PrefillParams {
   int B, Hq, Hkv, num_blocks, max_blocks, n_qtiles;
   float sm_scale_log2;
   int causal;
+  int promote_every;            // 1: every tile; N >= 2: every N tiles; 0: never
   __nv_bfloat16* out;           // [total_q][Hq][D]
   int32_t* fault;
 };

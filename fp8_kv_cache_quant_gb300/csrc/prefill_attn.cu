@@ -352,35 +352,97 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16);
     int npv = 0;
     bool ok = true;
-    for (int t = 0; t < n_t; ++t) {
-      if (abort_warp(abort_s)) { ok = false; break; }
-      if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
-      const float alpha = sAlpha[(t & 1) * C::BM + i];
-      mbar_arrive(&a_free[t & 1]);
-      for (int hn = 0; hn < C::NH; ++hn) {
-        if (!wait_warp(o_full, npv & 1)) { ok = false; break; }
-        ++npv;
-        tc_fence_after();
+    const int pe = p.promote_every;
+    if (pe == 1) {
+      // two-level accumulation every tile: O = O * alpha + O_tile after each P.V
+      for (int t = 0; t < n_t; ++t) {
+        if (abort_warp(abort_s)) { ok = false; break; }
+        if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+        const float alpha = sAlpha[(t & 1) * C::BM + i];
+        mbar_arrive(&a_free[t & 1]);
+        for (int hn = 0; hn < C::NH; ++hn) {
+          if (!wait_warp(o_full, npv & 1)) { ok = false; break; }
+          ++npv;
+          tc_fence_after();
 #pragma unroll C::UNR
-        for (int c = 0; c < C::DN / 32; ++c) {
-          float ot[32], oa[32];
-          tmem_ld32(lane_base + C::TM_OT + 32 * c, ot);
-          if (t > 0) tmem_ld32(lane_base + C::TM_OA + hn * C::DN + 32 * c, oa);
-          tmem_ld_wait();
-          if (t > 0) {
+          for (int c = 0; c < C::DN / 32; ++c) {
+            float ot[32], oa[32];
+            tmem_ld32(lane_base + C::TM_OT + 32 * c, ot);
+            if (t > 0) tmem_ld32(lane_base + C::TM_OA + hn * C::DN + 32 * c, oa);
+            tmem_ld_wait();
+            if (t > 0) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) oa[j] = fmaf(oa[j], alpha, ot[j]);
-          } else {
+              for (int j = 0; j < 32; ++j) oa[j] = fmaf(oa[j], alpha, ot[j]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) oa[j] = ot[j];
+              for (int j = 0; j < 32; ++j) oa[j] = ot[j];
+            }
+            tmem_st32(lane_base + C::TM_OA + hn * C::DN + 32 * c, oa);
           }
-          tmem_st32(lane_base + C::TM_OA + hn * C::DN + 32 * c, oa);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(o_free);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(o_free);
+        if (!ok) break;
       }
-      if (!ok) break;
+    } else {
+      // promote every pe tiles (pe >= 2, one P.V product per tile) or never (pe == 0: the
+      // tensor core accumulates the whole contraction into O).  The running sum the next
+      // P.V accumulates into is rescaled in place when a row's maximum moved.
+      const uint32_t acc_col = pe == 0 ? C::TM_OA : C::TM_OT;
+      const int acc_cols = pe == 0 ? D : C::DN;
+      float A = 1.f;         // product of the alphas since the last promotion
+      bool have_o = false;   // O holds promoted groups
+      for (int t = 0; t < n_t; ++t) {
+        if (abort_warp(abort_s)) { ok = false; break; }
+        if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+        const float alpha = sAlpha[(t & 1) * C::BM + i];
+        mbar_arrive(&a_free[t & 1]);
+        A *= alpha;
+        const bool start = pe == 0 ? t == 0 : (t % pe) == 0;
+        if (!start) {
+          // P.V(t-1) completed at the previous o_full wait
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+            for (int c = 0; c < acc_cols / 32; ++c) {
+              float x[32];
+              tmem_ld32(lane_base + acc_col + 32 * c, x);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) x[j] *= alpha;
+              tmem_st32(lane_base + acc_col + 32 * c, x);
+            }
+            tmem_st_wait();
+          }
+          tc_fence_before();
+          mbar_arrive(o_free);
+        }
+        if (!wait_warp(o_full, t & 1)) { ok = false; break; }
+        tc_fence_after();
+        const bool last = pe != 0 && ((t + 1) % pe == 0 || t == n_t - 1);
+        if (last) {
+#pragma unroll 1
+          for (int c = 0; c < C::DN / 32; ++c) {
+            float ot[32], oa[32];
+            tmem_ld32(lane_base + C::TM_OT + 32 * c, ot);
+            if (have_o) tmem_ld32(lane_base + C::TM_OA + 32 * c, oa);
+            tmem_ld_wait();
+            if (have_o) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) oa[j] = fmaf(oa[j], A, ot[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) oa[j] = ot[j];
+            }
+            tmem_st32(lane_base + C::TM_OA + 32 * c, oa);
+          }
+          tmem_st_wait();
+          have_o = true;
+          A = 1.f;
+          tc_fence_before();
+          mbar_arrive(o_free);
+        }
+      }
     }
     if (!ok) {
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
@@ -524,21 +586,44 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      for (int hn = 0; hn < C::NH; ++hn) {
-        if (npv > 0 && !wait_warp(o_free, (npv - 1) & 1)) return false;
+      if (p.promote_every == 1) {
+        for (int hn = 0; hn < C::NH; ++hn) {
+          if (npv > 0 && !wait_warp(o_free, (npv - 1) & 1)) return false;
+          tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int kk = 0; kk < C::BN / 32; ++kk) {
+              const uint64_t ad = smem_desc(sPa + pb * C::BM * C::BN + kk * 32, 16, 1024, 2);
+              const uint64_t bd = smem_desc(sVa + st * C::TILE + hn * C::SUB + kk * 32 * C::RB, 8 * C::RB,
+                                            8 * C::RB, C::SWZ);
+              umma_f8(tmem + C::TM_OT, ad, bd, C::IDESC_PV, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(o_full);
+          }
+          __syncwarp();
+          ++npv;
+        }
+      } else {
+        // the running sum (O_tile, or O when never promoted) is ready once the correction
+        // warpgroup has promoted or rescaled it for this tile
+        if (t > 0 && !wait_warp(o_free, (t - 1) & 1)) return false;
         tc_fence_after();
+        const int pe = p.promote_every;
+        const bool fresh = pe == 0 ? t == 0 : (t % pe) == 0;
         if (lane == 0) {
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 32; ++kk) {
-            const uint64_t ad = smem_desc(sPa + pb * C::BM * C::BN + kk * 32, 16, 1024, 2);
-            const uint64_t bd = smem_desc(sVa + st * C::TILE + hn * C::SUB + kk * 32 * C::RB, 8 * C::RB, 8 * C::RB,
-                                          C::SWZ);
-            umma_f8(tmem + C::TM_OT, ad, bd, C::IDESC_PV, kk > 0 ? 1u : 0u);
-          }
+          for (int hn = 0; hn < C::NH; ++hn)
+#pragma unroll
+            for (int kk = 0; kk < C::BN / 32; ++kk) {
+              const uint64_t ad = smem_desc(sPa + pb * C::BM * C::BN + kk * 32, 16, 1024, 2);
+              const uint64_t bd = smem_desc(sVa + st * C::TILE + hn * C::SUB + kk * 32 * C::RB, 8 * C::RB,
+                                            8 * C::RB, C::SWZ);
+              const uint32_t dst = pe == 0 ? tmem + C::TM_OA + hn * C::DN : tmem + C::TM_OT;
+              umma_f8(dst, ad, bd, C::IDESC_PV, (kk > 0 || !fresh) ? 1u : 0u);
+            }
           umma_commit(o_full);
         }
         __syncwarp();
-        ++npv;
       }
       if (lane == 0) {
         umma_commit(&v_empty[st]);

@@ -214,8 +214,12 @@ int32_t fkv_prefill_block_n(int32_t head_dim);
  *   max_q_len     host upper bound of every Lq_b (sizes the grid)
  *   causal        non-zero for causal masking
  *   window        must be 0 (sliding-window prefill is not implemented: FKV_UNSUPPORTED)
- *   promote_every must be 1 (two-level accumulation every tile); other values are
- *                 FKV_UNSUPPORTED
+ *   promote_every 1: promote each tile's P.V partial into the FP32 accumulator (two-level
+ *                 accumulation, the default); N >= 2: let the tensor core accumulate N tiles
+ *                 (rescaled in place when a row's maximum moves) before promoting (head_dim
+ *                 <= 128, else FKV_UNSUPPORTED); 0: never promote — the tensor core accumulates
+ *                 the whole contraction (the blog's "大 Head Dimension 的限制": accumulate
+ *                 every N steps, or disable two-level accumulation); negative: FKV_INVALID_ARG
  *   out           device bf16 [total_q][num_q_heads][head_dim]
  * head_dim in {64, 128, 256}; skip (bf16) layers are FKV_UNSUPPORTED.
  */

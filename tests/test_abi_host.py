@@ -111,3 +111,8 @@ def test_prefill_validation(lib):
     # a bf16 (skip) layer has no FP8 prefill
     assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 0, 1, 0, mask, 1, p, None, None) == f.UNSUPPORTED
     assert f.fkv_prefill_block_n(128) == 128 and f.fkv_prefill_block_n(100) == 0
+    # promote_every: negative is invalid; N >= 2 needs head_dim <= 128; windows are not implemented
+    assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 0, -1, 0, None, 0, p, None, None) == f.INVALID_ARG
+    assert pre(p, p, 1, 8, 16, _cache(D=256), p, 4, p, p, p, p, 0, 0.0, 1, 0, 2, 0, None, 0, p, None, None) == f.UNSUPPORTED
+    assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 64, 1, 0, None, 0, p, None, None) == f.UNSUPPORTED
+    assert pre(p, p, 0, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 0, 0, 0, None, 0, p, None, None) == f.OK

@@ -18,7 +18,7 @@ f = pytest.importorskip("fp8_kv_cache_quant_gb300")
 pytestmark = pytest.mark.gpu
 
 
-def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0):
+def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0, promote_every=1):
     rng = np.random.default_rng(seed)
     ctx = np.asarray(T_list, np.int32)
     table, nb = synth.block_table(ctx, seed=seed, extra_blocks=3)
@@ -34,7 +34,7 @@ def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0):
     cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran, False, sentinel=0xFF)
     fault = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = f.fp8_prefill_attn(q.cuda(), to_dev(cu), int(max(Lq_list)), cache, to_dev(table), to_dev(ctx), to_dev(qs),
-                             to_dev(ks), to_dev(vs), gran, causal=causal, fault=fault)
+                             to_dev(ks), to_dev(vs), gran, causal=causal, fault=fault, promote_every=promote_every)
     torch.cuda.synchronize()
     assert int(fault.item()) == 0, f"fault bits {int(fault.item())}"
     cs = np.concatenate([[0], np.cumsum(ctx)])
@@ -57,6 +57,14 @@ def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0):
 def test_prefill_small_parity(D, Hq, Hkv, T_list, Lq_list, gran, causal):
     got, ref = _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed=D + Hq + sum(T_list))
     assert_close(got, ref, what=f"D={D} Hq={Hq} Hkv={Hkv} T={T_list} Lq={Lq_list} causal={causal}")
+
+
+@pytest.mark.parametrize("D,promote_every", [(128, 0), (128, 2), (128, 3), (64, 4), (64, 0), (256, 0)])
+def test_prefill_promote_every_variants(D, promote_every):
+    """The tensor core accumulating N tiles (or the whole contraction) before promotion
+    computes the same attention; the oracle is the same, only rounding differs."""
+    got, ref = _run(D, 4, 2, [700, 300], [700, 130], 1, True, seed=D + promote_every, promote_every=promote_every)
+    assert_close(got, ref, what=f"D={D} promote_every={promote_every}")
 
 
 def test_prefill_query_longer_than_context_faults():
@@ -110,8 +118,10 @@ def test_workload5_prefill_d256_sampled():
     assert_close(out[rows], ref[rows], what="workload 5 prefill")
 
 
-def test_workload4_prefill_chunk_sampled():
-    """The 4096-query FP8 prefill chunk at the tail of the 131072-key needle cache."""
+@pytest.mark.parametrize("promote_every", [1, 0])
+def test_workload4_prefill_chunk_sampled(promote_every):
+    """The 4096-query FP8 prefill chunk at the tail of the 131072-key needle cache: a contraction
+    over ~130k keys, with two-level accumulation (1) and without it (0)."""
     w = synth.WORKLOADS[4]
     ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
     table, nb = synth.block_table(ctx, seed=w.seed)
@@ -122,7 +132,8 @@ def test_workload4_prefill_chunk_sampled():
     L = w.prefill_chunk
     cu = np.array([0, L], np.int32)
     out = f.fp8_prefill_attn(qp, to_dev(cu), L, cache, to_dev(table), to_dev(ctx), data.q_scale, data.k_scale,
-                             data.v_scale, f.SCALE_PER_TENSOR, causal=True).float().cpu().numpy()
+                             data.v_scale, f.SCALE_PER_TENSOR, causal=True,
+                             promote_every=promote_every).float().cpu().numpy()
     rows = _sample_rows(cu, 10, np.random.default_rng(4))
     heads = [0, 13, 40, 63]
     G = w.group
