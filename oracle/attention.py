@@ -128,7 +128,7 @@ def decode_attention_contiguous(q_b, k_seq, v_seq, q_scale, k_scale, v_scale, *,
     return res
 
 
-def _tile_walk(Qt, K, V, qpos, kpos0, block_n, tau, p_quant):
+def _tile_walk(Qt, K, V, qpos, kpos0, block_n, tau, p_quant, window=0):
     """Online softmax over key tiles for a set of query rows of one head.
 
     Qt: [R][D] dequantised queries at absolute positions qpos [R]; K, V: [T][D]
@@ -144,6 +144,8 @@ def _tile_walk(Qt, K, V, qpos, kpos0, block_n, tau, p_quant):
     S = (Qt @ K.T) * tau                      # [R][T]
     kabs = kpos0 + np.arange(T)
     valid = kabs[None, :] <= qpos[:, None]
+    if window > 0:
+        valid &= kabs[None, :] >= (qpos[:, None] - window + 1)
     S = np.where(valid, S, -np.inf)
     m = np.full(R, -np.inf)
     l = np.zeros(R)
@@ -175,14 +177,15 @@ def _tile_walk(Qt, K, V, qpos, kpos0, block_n, tau, p_quant):
 
 def prefill_attention(q, cu_seqlens, k_seq_list, v_seq_list, q_scale, k_scale, v_scale, *, block_n: int,
                       fp8: bool = True, p_quant: bool = True, softmax_scale: float = 0.0,
-                      causal: bool = True, rows=None):
+                      causal: bool = True, rows=None, window: int = 0):
     """Prefill (chunked) attention with the kernel's tile walk.
 
     q: float64 [sum Lq][Hq][D]; cu_seqlens: [B+1]; k_seq_list[b] / v_seq_list[b]:
     float64 [T_b][Hkv][D] bf16 values of the whole context of sequence b (the oracle
     quantises them with the cache-write rule).  ``rows`` optionally restricts the
     computed query rows to a list of global row indices (others are NaN).
-    Non-causal means every row sees the whole context.
+    Non-causal means every row sees the whole context.  A window W > 0 keeps, for the row
+    at position p, only keys [p - W + 1, p] (R6: the last W keys, its own included).
     Returns float64 [sum Lq][Hq][D].
     """
     q = np.asarray(q, dtype=np.float64)
@@ -216,5 +219,5 @@ def prefill_attention(q, cu_seqlens, k_seq_list, v_seq_list, q_scale, k_scale, v
                     Qt = e4m3.decode(e4m3.quantize(q[sel, h], qs)) * qs
                 else:
                     Qt = q[sel, h]
-                out[sel, h] = _tile_walk(Qt, K[:kmax], V[:kmax], qpos, 0, block_n, tau, p_quant and fp8)
+                out[sel, h] = _tile_walk(Qt, K[:kmax], V[:kmax], qpos, 0, block_n, tau, p_quant and fp8, window)
     return out

@@ -274,3 +274,28 @@ def test_prefill_tail_rows_equal_decode():
         dec = attention.decode_attention_contiguous(q[row], K[0][:ctx], V[0][:ctx], s, s, s)
         for h in range(Hq):
             np.testing.assert_allclose(pre[row, h], dec[h], rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_window_matches_banded_sdpa_and_decode():
+    # R6: with window W, the row at position p sees keys [p - W + 1, p]
+    rng = np.random.default_rng(24)
+    Hq, Hkv, D, W = 4, 2, 16, 37
+    T, Lq = 150, 60
+    K = [_bf16(rng.standard_normal((T, Hkv, D)))]
+    V = [_bf16(rng.standard_normal((T, Hkv, D)))]
+    q = _bf16(rng.standard_normal((Lq, Hq, D)))
+    one = np.ones(1, np.float32)
+    got = attention.prefill_attention(q, [0, Lq], K, V, one, one, one, block_n=32, fp8=False, window=W)
+    qpos = T - Lq + np.arange(Lq)
+    kpos = np.arange(T)
+    mask = torch.from_numpy((kpos[None, :] <= qpos[:, None]) & (kpos[None, :] >= qpos[:, None] - W + 1))
+    qt = torch.from_numpy(q).permute(1, 0, 2)
+    kt = torch.from_numpy(K[0]).permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)
+    vt = torch.from_numpy(V[0]).permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+    # the last row equals decode over the last W keys (fp8, unrounded P)
+    pre = attention.prefill_attention(q, [0, Lq], K, V, one, one, one, block_n=32, p_quant=False, window=W)
+    dec = attention.decode_attention_contiguous(q[Lq - 1], K[0], V[0], one, one, one, window=W)
+    for h in range(Hq):
+        np.testing.assert_allclose(pre[Lq - 1, h], dec[h], rtol=1e-12, atol=1e-13)
