@@ -218,17 +218,17 @@ fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t 
   if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
   if (!(softmax_scale >= 0.f) || std::isinf(softmax_scale)) return FKV_INVALID_ARG;
   if (window < 0 || promote_every < 0) return FKV_INVALID_ARG;
-  if (window != 0) return FKV_UNSUPPORTED;
+  if (window > 0 && !causal) return FKV_UNSUPPORTED;                        // a window is causal
   if (promote_every >= 2 && cache.head_dim > 128) return FKV_UNSUPPORTED;  // TMEM holds one 128-column O_tile
   fkv_status st = FKV_OK;
   const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
   if (st != FKV_OK) return st;
-  if (bf16) return FKV_UNSUPPORTED;  // skip (bf16) layers have no FP8 prefill here
+  if (bf16 && cache.head_dim > 128) return FKV_UNSUPPORTED;  // bf16 tiles of head_dim 256 exceed shared memory
   if (batch > 65535 || num_q_heads > 65535) return FKV_UNSUPPORTED;
   if (batch == 0 || max_q_len == 0) return FKV_OK;
-  if (!q || !cu_seqlens_q || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || !out ||
-      !q_scale || !k_scale || !v_scale)
+  if (!q || !cu_seqlens_q || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || !out)
     return FKV_INVALID_ARG;
+  if (!bf16 && (!q_scale || !k_scale || !v_scale)) return FKV_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(cache.k_cache, 16) || !aligned(cache.v_cache, 16) ||
       !aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(cu_seqlens_q, 4))
     return FKV_INVALID_ARG;
@@ -252,9 +252,10 @@ fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t 
   p.sm_scale_log2 = tau * 1.4426950408889634f;
   p.causal = causal != 0;
   p.promote_every = promote_every;
+  p.window = window;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.fault = fault;
-  return from_cuda(fkv::launch_prefill(p, cache.head_dim, cache.k_cache, cache.v_cache,
+  return from_cuda(fkv::launch_prefill(p, cache.head_dim, bf16, cache.k_cache, cache.v_cache,
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -43,11 +43,13 @@ struct PrefillParams {
   float sm_scale_log2;
   int causal;
   int promote_every;            // 1: every tile; N >= 2: every N tiles; 0: never
+  int window;                   // 0 = full, else the last `window` keys of each query
   __nv_bfloat16* out;           // [total_q][Hq][D]
   int32_t* fault;
 };
 
-cudaError_t launch_prefill(const PrefillParams& p, int D, void* k_cache, void* v_cache, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams& p, int D, bool bf16_layer, void* k_cache, void* v_cache,
+                           cudaStream_t s);
 
 cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* slots, int n_tokens,
                                   const fkv_layer_cache& cache, const float* ks, const float* vs,

@@ -56,17 +56,23 @@ FKV_DEV float fmax3(float a, float b, float c) {
   return r;
 }
 
-template <int D>
+template <int D, bool BF>
 struct PrefillCfg {
   static constexpr int BM = 128, BN = 128;
-  static constexpr int RB = D < 128 ? D : 128;      // bytes of one swizzled row
-  static constexpr int NSUB = D / RB;               // sub-tiles along head_dim
+  static constexpr int ES = BF ? 2 : 1;             // bytes per element (bf16 / e4m3)
+  static constexpr int DB = D * ES;                 // bytes of one Q / K / V row
+  static constexpr int RB = DB < 128 ? DB : 128;    // bytes of one swizzled row
+  static constexpr int NSUB = DB / RB;              // sub-tiles along head_dim
+  static constexpr int EPS = RB / ES;               // elements of a sub-tile row: N of one P.V product
   static constexpr int SWZ = RB == 128 ? 2 : 4;     // descriptor swizzle mode (128 B / 64 B)
   static constexpr int SUB = BM * RB;               // bytes of one 128-row sub-tile
-  static constexpr int TILE = BM * D;               // bytes of a Q, K or V tile
-  static constexpr int NS = D <= 128 ? 3 : 2;       // K/V stages
-  static constexpr int DN = D < 128 ? D : 128;      // N of one P.V product
-  static constexpr int NH = D / DN;
+  static constexpr int TILE = BM * DB;              // bytes of a Q, K or V tile
+  static constexpr int NS = (!BF && D <= 128) ? 3 : 2;  // K/V stages
+  static constexpr int DN = D < 128 ? D : 128;      // O_tile width (elements) of one P.V pass
+  static constexpr int NH = D / DN;                 // P.V passes
+  static constexpr int PB = BN * ES;                // bytes of one P row
+  static constexpr int PTILE = BM * PB;             // bytes of one P tile
+  static constexpr int KSTEP = 32 / ES;             // keys (P columns) of one P.V k-step (32 bytes)
   static constexpr int SBUF = D <= 128 ? 2 : 1;     // S buffers in TMEM
   // unrolling of the softmax / correction chunk loops: full for head_dim <= 128 (the
   // softmax is the critical path there), none for 256 (code size of four warp roles)
@@ -79,25 +85,32 @@ struct PrefillCfg {
   static constexpr int OFF_K = OFF_Q + TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_P = OFF_V + NS * TILE;           // two P tiles
-  static constexpr int OFF_A = OFF_P + 2 * BM * BN;         // alpha [2][128] floats
+  static constexpr int OFF_A = OFF_P + 2 * PTILE;           // alpha [2][128] floats
   static constexpr int OFF_L = OFF_A + 2 * BM * 4;          // l [128] floats
   static constexpr int OFF_BAR = OFF_L + BM * 4;
   static constexpr int NBAR = 17 + 4 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
-  static constexpr uint32_t IDESC_QK = idesc_e4m3_f32(128, 128, 0, 0);
-  static constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, DN, 0, 1);
+  static constexpr uint32_t IDESC_QK = BF ? idesc_bf16_f32(128, 128, 0, 0) : idesc_e4m3_f32(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = BF ? idesc_bf16_f32(128, EPS, 0, 1) : idesc_e4m3_f32(128, EPS, 0, 1);
   static_assert(TM_OA + D <= 512, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
+// One MMA of the element type: e4m3 (kind::f8f6f4) or bf16 (kind::f16), FP32 accumulation.
+template <bool BF>
+FKV_DEV void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  if constexpr (BF) umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+  else umma_f8(d_tmem, adesc, bdesc, idesc, accumulate);
+}
+
 constexpr int kPrefillThreads = 320;  // softmax WG, correction WG, TMA warp, MMA warp
 
-template <int D>
+template <int D, bool BF, bool WIN>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<D, BF>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::OFF_Q;
@@ -147,8 +160,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   if (q0 >= Lq) return;
   const int rows = min(C::BM, Lq - q0);
   const int pos0 = T - Lq + q0;  // absolute position of the tile's first query
-  const int kv_end = p.causal ? min(T, pos0 + rows) : T;  // keys [0, kv_end) matter
-  const int n_t = (kv_end + C::BN - 1) / C::BN;
+  const int kv_end = p.causal ? min(T, pos0 + rows) : T;  // keys [kv_lo, kv_end) matter
+  const int kv_lo = WIN ? max(0, pos0 - p.window + 1) : 0;
+  const int tb = kv_lo / C::BN;                               // first key tile
+  const int n_t = (kv_end + C::BN - 1) / C::BN - tb;          // tiles u = 0 .. n_t-1 are tb + u
   const int nblk_seq = (T + 15) >> 4;
 
   if (threadIdx.x == 0) {
@@ -191,34 +206,42 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const bool row_ok = i < rows;
     const int pos = pos0 + i;                  // its absolute position
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    // ---- prologue: Q row -> e4m3 codes in the swizzled Q tile
+    // ---- prologue: Q row -> e4m3 codes (bf16 values on bf16 layers) in the swizzled Q tile
     {
-      const float iq = __frcp_rn(p.q_scale[p.per_head ? h : 0]);
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D);
+      const float iq = BF ? 1.f : __frcp_rn(p.q_scale[p.per_head ? h : 0]);
 #pragma unroll 4
-      for (int c = 0; c < D / 16; ++c) {
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
+      for (int c = 0; c < C::DB / 16; ++c) {
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
         if (row_ok) {
-          const uint4 a = src[2 * c], bq = src[2 * c + 1];
-          const uint32_t in[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+          if constexpr (BF) {
+            out = src[c];
+          } else {
+            const uint4 a = src[2 * c], bq = src[2 * c + 1];
+            const uint32_t in[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+            uint32_t w[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 x0 = bf16x2_to_f2(in[2 * j]), x1 = bf16x2_to_f2(in[2 * j + 1]);
-            const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(x0.x, iq), __fmul_rn(x0.y, iq));
-            const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(x1.x, iq), __fmul_rn(x1.y, iq));
-            w[j] = lo | (hi << 16);
+            for (int j = 0; j < 4; ++j) {
+              const float2 x0 = bf16x2_to_f2(in[2 * j]), x1 = bf16x2_to_f2(in[2 * j + 1]);
+              const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(x0.x, iq), __fmul_rn(x0.y, iq));
+              const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(x1.x, iq), __fmul_rn(x1.y, iq));
+              w[j] = lo | (hi << 16);
+            }
+            out = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
         const int byte = c * 16;
         const int sub = byte / C::RB;
         const uint32_t lin = static_cast<uint32_t>(i * C::RB + (byte % C::RB));
-        *reinterpret_cast<uint4*>(sQ + sub * C::SUB + swz(lin, C::RB)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(sQ + sub * C::SUB + swz(lin, C::RB)) = out;
       }
       fence_proxy_async_smem();
       mbar_arrive(q_full);
     }
-    const float cst = p.sm_scale_log2 * p.q_scale[p.per_head ? h : 0] * p.k_scale[p.per_head ? g : 0];
-    const int lim_row = (p.causal && row_ok) ? min(T, pos + 1) : T;  // keys [0, lim_row) visible
+    const float cst = BF ? p.sm_scale_log2
+                         : p.sm_scale_log2 * p.q_scale[p.per_head ? h : 0] * p.k_scale[p.per_head ? g : 0];
+    const int lim_row = (p.causal && row_ok) ? min(T, pos + 1) : T;  // keys [lo_row, lim_row) visible
+    const int lo_row = (WIN && row_ok) ? max(0, pos - p.window + 1) : 0;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < n_t; ++t) {
@@ -226,8 +249,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const int sb = t % C::SBUF;
       if (!wait_warp(&s_full[sb], (t / C::SBUF) & 1)) { ok = false; break; }
       tc_fence_after();
-      const int lim = lim_row - t * C::BN;  // columns [0, lim) of this tile are visible
-      const bool full = lim >= C::BN;       // interior tile for this row: nothing masked
+      const int kbase = (tb + t) * C::BN;
+      const int lim = lim_row - kbase;      // columns [lo, lim) of this tile are visible
+      // full-attention instantiations fold the lower bound away (it costs the softmax
+      // warps dearly when it is a run-time value)
+      const int lo = WIN ? lo_row - kbase : -(1 << 30);
+      const bool full = lim >= C::BN && (!WIN || lo <= 0);  // interior tile for this row: nothing masked
       const uint32_t sc = lane_base + 128 * sb;
       float vall[C::ONE_LOAD ? 128 : 1];
       float tmax = -INFINITY;
@@ -245,7 +272,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           tmax = mx * cst;
         } else {
 #pragma unroll
-          for (int j = 0; j < 128; ++j) tmax = fmaxf(tmax, j < lim ? vall[j] * cst : -INFINITY);
+          for (int j = 0; j < 128; ++j) tmax = fmaxf(tmax, (j < lim && j >= lo) ? vall[j] * cst : -INFINITY);
         }
       } else {
         // pass 1: row max of the scaled, masked scores (cst > 0, so the raw maximum scales).
@@ -264,7 +291,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               for (int j = 0; j < 32; j += 4) mx = fmax3(mx, fmax3(v[j], v[j + 1], v[j + 2]), v[j + 3]);
             } else {
   #pragma unroll
-              for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, 32 * c + j < lim ? v[j] * cst : -INFINITY);
+              for (int j = 0; j < 32; ++j) {
+                const int col = 32 * c + j;
+                tmax = fmaxf(tmax, (col < lim && col >= lo) ? v[j] * cst : -INFINITY);
+              }
             }
           }
           if (full) tmax = mx * cst;
@@ -276,14 +306,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       // P tile t%2 is free once the P.V of tile t-2 completed
       const int pb = t & 1;
       if (t >= 2 && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
-      uint8_t* P = sP + pb * C::BM * C::BN;
+      uint8_t* P = sP + pb * C::PTILE;
       // pass 2: p = 2^(s*cst - m), its unrounded sum, and P8 = e4m3(p * 448) into the P tile;
       // the next chunk's TMEM load is in flight while the current one is processed
       float2 lsum2 = make_float2(0.f, 0.f);
       const float2 cst2 = make_float2(cst, cst), nm2 = make_float2(-msafe, -msafe);
       const float2 k448 = make_float2(448.f, 448.f);
       auto chunk = [&](const float (&v)[32], int c) {
-        uint32_t pk[8];
+        uint32_t pk[8 * C::ES];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           float2 x0 = __ffma2_rn(make_float2(v[j], v[j + 1]), cst2, nm2);
@@ -291,20 +321,29 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           x0.x = ex2(x0.x); x0.y = ex2(x0.y); x1.x = ex2(x1.x); x1.y = ex2(x1.y);
           if (!full) {
             const int col = 32 * c + j;
-            if (col >= lim) x0.x = 0.f;
-            if (col + 1 >= lim) x0.y = 0.f;
-            if (col + 2 >= lim) x1.x = 0.f;
-            if (col + 3 >= lim) x1.y = 0.f;
+            if (col >= lim || col < lo) x0.x = 0.f;
+            if (col + 1 >= lim || col + 1 < lo) x0.y = 0.f;
+            if (col + 2 >= lim || col + 2 < lo) x1.x = 0.f;
+            if (col + 3 >= lim || col + 3 < lo) x1.y = 0.f;
           }
           lsum2 = __fadd2_rn(lsum2, __fadd2_rn(x0, x1));
-          const float2 y0 = __fmul2_rn(x0, k448), y1 = __fmul2_rn(x1, k448);
-          pk[j / 4] = static_cast<uint32_t>(f32x2_to_e4m3x2(y0.x, y0.y)) |
-                      (static_cast<uint32_t>(f32x2_to_e4m3x2(y1.x, y1.y)) << 16);
+          if constexpr (BF) {
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(x0.x, x0.y), b1 = __floats2bfloat162_rn(x1.x, x1.y);
+            pk[j / 2] = *reinterpret_cast<uint32_t*>(&b0);
+            pk[j / 2 + 1] = *reinterpret_cast<uint32_t*>(&b1);
+          } else {
+            const float2 y0 = __fmul2_rn(x0, k448), y1 = __fmul2_rn(x1, k448);
+            pk[j / 4] = static_cast<uint32_t>(f32x2_to_e4m3x2(y0.x, y0.y)) |
+                        (static_cast<uint32_t>(f32x2_to_e4m3x2(y1.x, y1.y)) << 16);
+          }
         }
+        // 32 columns = 32 * ES bytes of the P row, in 16-byte pieces
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint32_t lin = static_cast<uint32_t>(i * 128 + (2 * c + q) * 16);
-          *reinterpret_cast<uint4*>(P + swz(lin, 128)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int q = 0; q < 2 * C::ES; ++q) {
+          const int byte = 32 * C::ES * c + 16 * q;
+          const uint32_t lin = static_cast<uint32_t>(i * 128 + (byte % 128));
+          *reinterpret_cast<uint4*>(P + (byte / 128) * (C::BM * 128) + swz(lin, 128)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       };
       if constexpr (C::ONE_LOAD) {
@@ -451,8 +490,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // ---- epilogue: O * v_s / (448 l) -> bf16 (every lane loads; rows past the chunk do not store)
     if (wait_warp(l_full, 0) && !abort_warp(abort_s)) {
       const float l = sL[i];
-      const float vs = p.v_scale[p.per_head ? g : 0];
-      const float f = (l > 0.f) ? vs / (448.f * l) : 0.f;
+      const float vs = BF ? 1.f : p.v_scale[p.per_head ? g : 0];
+      const float f = (l > 0.f) ? vs / ((BF ? 1.f : 448.f) * l) : 0.f;
       __nv_bfloat16* dst = p.out + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -489,7 +528,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       // 8 block ids of the tile; blocks past the context read block 0 (their keys are masked)
       int id = 0;
       if (lane < 8) {
-        const int lb = t * 8 + lane;
+        const int lb = (tb + t) * 8 + lane;
         if (lb < nblk_seq) {
           id = trow[lb];
           if (id < 0 || id >= p.num_blocks) {
@@ -552,18 +591,34 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk) {
+        for (int kk = 0; kk < C::DB / 32; ++kk) {
           const int byte = kk * 32;
           const uint32_t off = (byte / C::RB) * C::SUB + (byte % C::RB);
           const uint64_t ad = smem_desc(sQa + off, 16, 8 * C::RB, C::SWZ);
           const uint64_t bd = smem_desc(sKa + st * C::TILE + off, 16, 8 * C::RB, C::SWZ);
-          umma_f8(tmem + 128 * sb, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          umma<BF>(tmem + 128 * sb, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[sb]);
         umma_commit(&k_empty[st]);
       }
       __syncwarp();
       return true;
+    };
+    // One P.V pass: the DN output columns hn*DN .. of O_tile (or O) from P(t) and V(t), one
+    // product of N = EPS per V sub-tile and per 32-byte k-step of P.
+    auto issue_pv_pass = [&](int st, int pb, int hn, uint32_t dst, bool fresh) {
+#pragma unroll
+      for (int kk = 0; kk < C::PB / 32; ++kk) {
+        const int pbyte = kk * 32;
+        const uint64_t ad = smem_desc(sPa + pb * C::PTILE + (pbyte / 128) * (C::BM * 128) + (pbyte % 128), 16, 1024, 2);
+#pragma unroll
+        for (int j = 0; j < C::DN / C::EPS; ++j) {
+          const int sub = hn * (C::DN / C::EPS) + j;
+          const uint64_t bd = smem_desc(sVa + st * C::TILE + sub * C::SUB + kk * C::KSTEP * C::RB, 8 * C::RB,
+                                        8 * C::RB, C::SWZ);
+          umma<BF>(dst + j * C::EPS, ad, bd, C::IDESC_PV, (kk > 0 || !fresh) ? 1u : 0u);
+        }
+      }
     };
     // O_tile = P8(t) V8(t), in NH products of N = DN
     auto issue_pv = [&](int t) -> bool {
@@ -572,7 +627,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (!wait_warp(&v_full[st], (t / C::NS) & 1)) return false;
       // keys past the context may hold stale bytes (NaN codes): zero their V rows, since
       // 0 * NaN would poison the product even though their P is 0
-      const int kbase = t * C::BN;
+      const int kbase = (tb + t) * C::BN;
       if (kbase + C::BN > T) {
         const int first = max(T - kbase, 0);
         const int chunks = C::RB / 16;
@@ -590,16 +645,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int hn = 0; hn < C::NH; ++hn) {
           if (npv > 0 && !wait_warp(o_free, (npv - 1) & 1)) return false;
           tc_fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int kk = 0; kk < C::BN / 32; ++kk) {
-              const uint64_t ad = smem_desc(sPa + pb * C::BM * C::BN + kk * 32, 16, 1024, 2);
-              const uint64_t bd = smem_desc(sVa + st * C::TILE + hn * C::SUB + kk * 32 * C::RB, 8 * C::RB,
-                                            8 * C::RB, C::SWZ);
-              umma_f8(tmem + C::TM_OT, ad, bd, C::IDESC_PV, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(o_full);
-          }
+          if (lane == 0) issue_pv_pass(st, pb, hn, tmem + C::TM_OT, true);
+          if (lane == 0) umma_commit(o_full);
           __syncwarp();
           ++npv;
         }
@@ -613,14 +660,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (lane == 0) {
 #pragma unroll
           for (int hn = 0; hn < C::NH; ++hn)
-#pragma unroll
-            for (int kk = 0; kk < C::BN / 32; ++kk) {
-              const uint64_t ad = smem_desc(sPa + pb * C::BM * C::BN + kk * 32, 16, 1024, 2);
-              const uint64_t bd = smem_desc(sVa + st * C::TILE + hn * C::SUB + kk * 32 * C::RB, 8 * C::RB,
-                                            8 * C::RB, C::SWZ);
-              const uint32_t dst = pe == 0 ? tmem + C::TM_OA + hn * C::DN : tmem + C::TM_OT;
-              umma_f8(dst, ad, bd, C::IDESC_PV, (kk > 0 || !fresh) ? 1u : 0u);
-            }
+            issue_pv_pass(st, pb, hn, pe == 0 ? tmem + C::TM_OA + hn * C::DN : tmem + C::TM_OT, fresh);
           umma_commit(o_full);
         }
         __syncwarp();
@@ -697,14 +737,14 @@ bool make_pool_map(CUtensorMap* map, void* base, int D, int Hkv, int num_blocks,
   return r == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool BF, bool WIN>
 cudaError_t launch_prefill_t(const PrefillParams& p, void* kc, void* vc, cudaStream_t s) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<D, BF>;
   CUtensorMap tmk, tmv;
-  if (!make_pool_map(&tmk, kc, D, p.Hkv, p.num_blocks, C::RB) ||
-      !make_pool_map(&tmv, vc, D, p.Hkv, p.num_blocks, C::RB))
+  if (!make_pool_map(&tmk, kc, C::DB, p.Hkv, p.num_blocks, C::RB) ||
+      !make_pool_map(&tmv, vc, C::DB, p.Hkv, p.num_blocks, C::RB))
     return cudaErrorInvalidValue;
-  auto kern = prefill_kernel<D>;
+  auto kern = prefill_kernel<D, BF, WIN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_qtiles, p.Hq, p.B);
@@ -712,12 +752,22 @@ cudaError_t launch_prefill_t(const PrefillParams& p, void* kc, void* vc, cudaStr
   return cudaGetLastError();
 }
 
+template <int D, bool BF>
+cudaError_t launch_prefill_w(const PrefillParams& p, void* kc, void* vc, cudaStream_t s) {
+  return p.window > 0 ? launch_prefill_t<D, BF, true>(p, kc, vc, s) : launch_prefill_t<D, BF, false>(p, kc, vc, s);
+}
+
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillParams& p, int D, void* kc, void* vc, cudaStream_t s) {
-  if (D == 64) return launch_prefill_t<64>(p, kc, vc, s);
-  if (D == 128) return launch_prefill_t<128>(p, kc, vc, s);
-  if (D == 256) return launch_prefill_t<256>(p, kc, vc, s);
+cudaError_t launch_prefill(const PrefillParams& p, int D, bool bf16_layer, void* kc, void* vc, cudaStream_t s) {
+  if (bf16_layer) {
+    if (D == 64) return launch_prefill_w<64, true>(p, kc, vc, s);
+    if (D == 128) return launch_prefill_w<128, true>(p, kc, vc, s);
+    return cudaErrorInvalidValue;
+  }
+  if (D == 64) return launch_prefill_w<64, false>(p, kc, vc, s);
+  if (D == 128) return launch_prefill_w<128, false>(p, kc, vc, s);
+  if (D == 256) return launch_prefill_w<256, false>(p, kc, vc, s);
   return cudaErrorInvalidValue;
 }
 

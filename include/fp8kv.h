@@ -213,7 +213,9 @@ int32_t fkv_prefill_block_n(int32_t head_dim);
  *   cu_seqlens_q  device int32 [batch + 1], non-decreasing, starting at 0
  *   max_q_len     host upper bound of every Lq_b (sizes the grid)
  *   causal        non-zero for causal masking
- *   window        must be 0 (sliding-window prefill is not implemented: FKV_UNSUPPORTED)
+ *   window        0 = full attention; W > 0 keeps, for the row at position p, the keys
+ *                 [p - W + 1, p] only (sliding window, causal != 0 required, else
+ *                 FKV_UNSUPPORTED; tiles wholly before the CTA's first live key are skipped)
  *   promote_every 1: promote each tile's P.V partial into the FP32 accumulator (two-level
  *                 accumulation, the default); N >= 2: let the tensor core accumulate N tiles
  *                 (rescaled in place when a row's maximum moves) before promoting (head_dim
@@ -221,7 +223,10 @@ int32_t fkv_prefill_block_n(int32_t head_dim);
  *                 the whole contraction (the blog's "大 Head Dimension 的限制": accumulate
  *                 every N steps, or disable two-level accumulation); negative: FKV_INVALID_ARG
  *   out           device bf16 [total_q][num_q_heads][head_dim]
- * head_dim in {64, 128, 256}; skip (bf16) layers are FKV_UNSUPPORTED.
+ * head_dim in {64, 128, 256}.  Skip (bf16) layers — the layer's bit set in skip_layer_mask —
+ * read the bf16 pool and run the same kernel on bf16 operands (kind::f16 MMA, P rounded to
+ * bf16, no scales: q_scale/k_scale/v_scale may be NULL); they support head_dim 64 and 128
+ * (256: FKV_UNSUPPORTED, the bf16 tiles exceed shared memory).
  */
 fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t batch,
                             int32_t num_q_heads, int32_t max_q_len, fkv_layer_cache cache,

@@ -108,11 +108,20 @@ def test_prefill_validation(lib):
     pre = lib.fp8_prefill_attn
     p = 1 << 12
     mask = (ctypes.c_uint8 * 1)(1)
-    # a bf16 (skip) layer has no FP8 prefill
-    assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 0, 1, 0, mask, 1, p, None, None) == f.UNSUPPORTED
+    # a bf16 (skip) layer runs the bf16 prefill for head_dim 64 / 128 (no scales needed); 256 does not fit
+    assert pre(p, p, 1, 8, 16, _cache(D=256), p, 4, p, p, p, p, 0, 0.0, 1, 0, 1, 0, mask, 1, p, None,
+               None) == f.UNSUPPORTED
+    assert pre(p, p, 0, 8, 16, _cache(), p, 4, p, None, None, None, 0, 0.0, 1, 0, 1, 0, mask, 1, p, None,
+               None) == f.OK
     assert f.fkv_prefill_block_n(128) == 128 and f.fkv_prefill_block_n(100) == 0
-    # promote_every: negative is invalid; N >= 2 needs head_dim <= 128; windows are not implemented
+    # promote_every: negative is invalid; N >= 2 needs head_dim <= 128
     assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 0, -1, 0, None, 0, p, None, None) == f.INVALID_ARG
     assert pre(p, p, 1, 8, 16, _cache(D=256), p, 4, p, p, p, p, 0, 0.0, 1, 0, 2, 0, None, 0, p, None, None) == f.UNSUPPORTED
-    assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 64, 1, 0, None, 0, p, None, None) == f.UNSUPPORTED
+    # a sliding window is causal: negative is invalid, non-causal is unsupported
+    assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, -1, 1, 0, None, 0, p, None, None) == f.INVALID_ARG
+    assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 0, 64, 1, 0, None, 0, p, None, None) == f.UNSUPPORTED
+    assert pre(p, p, 0, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 64, 1, 0, None, 0, p, None, None) == f.OK
+    # an fp8 layer needs its scales
+    assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, None, p, p, 0, 0.0, 1, 0, 1, 0, None, 0, p, None,
+               None) == f.INVALID_ARG
     assert pre(p, p, 0, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 0, 0, 0, None, 0, p, None, None) == f.OK

@@ -1,5 +1,6 @@
 """fp8_prefill_attn (tcgen05 FP8 prefill, two-level accumulation) against the oracle's
-tile-exact FP8 emulation (128-key tiles, P rounded as e4m3(p*448), unrounded denominator).
+tile-exact FP8 emulation (128-key tiles, P rounded as e4m3(p*448), unrounded denominator);
+skip layers' bf16 prefill against the oracle's unquantised attention; sliding windows.
 
 Tolerance: max-abs 2e-2 and relative L2 1e-2.  Small cases cover head_dim 64/128/256,
 GQA groups, per-tensor and per-head scales, causal and non-causal, ragged chunks that are
@@ -18,7 +19,7 @@ f = pytest.importorskip("fp8_kv_cache_quant_gb300")
 pytestmark = pytest.mark.gpu
 
 
-def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0, promote_every=1):
+def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0, promote_every=1, bf16=False, window=0):
     rng = np.random.default_rng(seed)
     ctx = np.asarray(T_list, np.int32)
     table, nb = synth.block_table(ctx, seed=seed, extra_blocks=3)
@@ -31,17 +32,20 @@ def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0, promote_e
         qs, ks, vs = synth.amax_scales(q, 1), synth.amax_scales(k, 1), synth.amax_scales(v, 1)
     else:
         qs = torch.tensor([0.5]); ks = torch.tensor([1.0]); vs = torch.tensor([0.25])
-    cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran, False, sentinel=0xFF)
+    cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran, bf16, sentinel=0xFF)
     fault = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = f.fp8_prefill_attn(q.cuda(), to_dev(cu), int(max(Lq_list)), cache, to_dev(table), to_dev(ctx), to_dev(qs),
-                             to_dev(ks), to_dev(vs), gran, causal=causal, fault=fault, promote_every=promote_every)
+    # a bf16 (skip) layer takes no scales (its kernel instantiation reads none)
+    sc = (None, None, None) if bf16 else (to_dev(qs), to_dev(ks), to_dev(vs))
+    out = f.fp8_prefill_attn(q.cuda(), to_dev(cu), int(max(Lq_list)), cache, to_dev(table), to_dev(ctx), *sc, gran,
+                             causal=causal, window=window, fault=fault, promote_every=promote_every, layer=0,
+                             skip_layer_mask=[1] if bf16 else None)
     torch.cuda.synchronize()
     assert int(fault.item()) == 0, f"fault bits {int(fault.item())}"
     cs = np.concatenate([[0], np.cumsum(ctx)])
     kl = [synth.bf16_to_f64(k[cs[b]:cs[b + 1]]) for b in range(len(ctx))]
     vl = [synth.bf16_to_f64(v[cs[b]:cs[b + 1]]) for b in range(len(ctx))]
     ref = attention.prefill_attention(synth.bf16_to_f64(q), cu, kl, vl, qs.numpy(), ks.numpy(), vs.numpy(),
-                                      block_n=f.fkv_prefill_block_n(D), causal=causal)
+                                      block_n=f.fkv_prefill_block_n(D), causal=causal, fp8=not bf16, window=window)
     return out.float().cpu().numpy(), ref
 
 
@@ -65,6 +69,37 @@ def test_prefill_promote_every_variants(D, promote_every):
     computes the same attention; the oracle is the same, only rounding differs."""
     got, ref = _run(D, 4, 2, [700, 300], [700, 130], 1, True, seed=D + promote_every, promote_every=promote_every)
     assert_close(got, ref, what=f"D={D} promote_every={promote_every}")
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,T_list,Lq_list,gran,causal,promote_every", [
+    (128, 2, 1, [200], [200], 0, True, 1),
+    (128, 4, 2, [300, 129, 64], [300, 1, 64], 1, True, 1),
+    (64, 8, 2, [500, 77], [180, 77], 1, True, 1),
+    (128, 4, 1, [257], [40], 0, False, 1),
+    (64, 2, 2, [16, 1000], [16, 300], 0, True, 1),
+    (128, 4, 2, [700, 300], [700, 130], 1, True, 0),
+    (128, 4, 2, [700, 300], [700, 130], 1, True, 3),
+    (64, 4, 2, [700, 300], [700, 130], 1, True, 2),
+])
+def test_prefill_bf16_skip_layer_parity(D, Hq, Hkv, T_list, Lq_list, gran, causal, promote_every):
+    """A skip layer's bf16 prefill (kind::f16 MMA on the bf16 pool) against the oracle's
+    full-precision attention over the same bf16 values; the kernel rounds P to bf16."""
+    got, ref = _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed=7 * D + Hq + sum(T_list),
+                    promote_every=promote_every, bf16=True)
+    assert_close(got, ref, what=f"bf16 D={D} T={T_list} Lq={Lq_list} causal={causal} pe={promote_every}")
+
+
+@pytest.mark.parametrize("D,bf16,window,promote_every", [
+    (128, False, 1, 1), (128, False, 100, 1), (128, False, 128, 1), (128, False, 300, 1), (128, False, 5000, 1),
+    (64, False, 257, 1), (256, False, 200, 1), (256, False, 200, 0), (128, False, 300, 0), (64, False, 77, 3),
+    (128, True, 1, 1), (128, True, 300, 1), (64, True, 129, 1), (128, True, 250, 0),
+])
+def test_prefill_sliding_window_parity(D, bf16, window, promote_every):
+    """Sliding-window prefill: each row attends the last `window` keys up to its own
+    position; whole chunks and tails, windows shorter and longer than a key tile."""
+    got, ref = _run(D, 4, 2, [900, 400, 50], [900, 170, 50], 1, True, seed=D + window + promote_every,
+                    promote_every=promote_every, bf16=bf16, window=window)
+    assert_close(got, ref, what=f"window={window} D={D} bf16={bf16} pe={promote_every}")
 
 
 def test_prefill_query_longer_than_context_faults():
