@@ -390,6 +390,77 @@ def itl_sweep(f, device, steps, warmup, lengths=SWEEP_T):
     return out
 
 
+def quadratic_fit(xs, ys):
+    """Least-squares TTFT = a * L^2 + b * L + c (the blog's quadratic TTFT model).  The
+    lengths are scaled by 1/1000 for the solve, so the normal matrix stays well conditioned."""
+    import numpy as np
+    x = np.asarray(xs, dtype=np.float64) / 1000.0
+    A = np.stack([x * x, x, np.ones_like(x)], axis=1)
+    a, b, c = np.linalg.lstsq(A, np.asarray(ys, dtype=np.float64), rcond=None)[0]
+    return float(a) / 1e6, float(b) / 1e3, float(c)
+
+
+def ttft_sweep(f, device, steps, warmup, lengths=SWEEP_T):
+    """The TTFT proxy: one layer's prefill of a single prompt of L tokens (cache write of
+    its K/V + causal attention over it) versus L, fitted with TTFT = a L^2 + b L + c, for
+    an e4m3 cache (two-level accumulation, and without promotion) and a bf16 cache.
+    Shapes: Llama-3.1-8B-shaped (32/8 heads, head_dim 128) and the head_dim-256 shape
+    (8/1 heads) whose FP8/BF16 ratio of the quadratic coefficient the blog reports as ~1.6
+    with two-level accumulation on H100.  The prompts of all lengths are prefixes of one
+    seeded draw.  No L2 flush: the step is tensor-bound and re-reads its own inputs."""
+    import dataclasses
+    import numpy as np
+    import torch
+    import synth
+    Lmax = max(lengths)
+    shapes = {
+        "llama8b": synth.PrefillWorkload("llama8b-prefill-h32x8-d128", 1, Lmax, 32, 8, 128, seed=1),
+        "hd256": dataclasses.replace(synth.WORKLOADS[5], batch=1, seq_len=Lmax, name="prefill-h8x1-d256"),
+    }
+    variants = [("fp8", 1, False), ("fp8-no-promote", 0, False), ("bf16", 1, True)]
+    stream = torch.cuda.Stream(device)
+    out = {}
+    for name, w in shapes.items():
+        data = synth.prefill_data(w, device=device)
+        ctx_max = np.array([Lmax], np.int32)
+        table, nb = synth.block_table(ctx_max, seed=w.seed)
+        slots = torch.from_numpy(synth.slot_mapping(table, ctx_max)).to(device)
+        tbl = torch.from_numpy(table).to(device)
+        res = {v: [] for v, _, _ in variants}
+        for v, pe, bf in variants:
+            cache = f.LayerCache.empty(nb, w.num_kv_heads, w.head_dim, bf16=bf, device=device)
+            mask = [1] if bf else None
+            qs, ks, vs = (None, None, None) if bf else (data.q_scale, data.k_scale, data.v_scale)
+            outb = torch.empty_like(data.q)
+            for L in lengths:
+                cu = torch.tensor([0, L], dtype=torch.int32, device=device)
+                cx = torch.tensor([L], dtype=torch.int32, device=device)
+
+                def step():
+                    f.kv_quant_cache(data.k[:L], data.v[:L], slots[:L], cache, ks, vs, f.SCALE_PER_HEAD, layer=0,
+                                     skip_layer_mask=mask, stream=stream)
+                    f.fp8_prefill_attn(data.q[:L], cu, L, cache, tbl, cx, qs, ks, vs, f.SCALE_PER_HEAD, causal=True,
+                                       promote_every=pe, layer=0, skip_layer_mask=mask, out=outb[:L], stream=stream)
+
+                g = _graph(step, stream)
+                res[v].append(_time_graph(g, stream, steps, warmup, lambda: None))
+                del g
+            del cache, outb
+            torch.cuda.empty_cache()
+        fits = {v: quadratic_fit(lengths, ys) for v, ys in res.items()}
+        flops = [4 * w.head_dim * w.num_q_heads * (L * (L + 1) // 2) for L in lengths]
+        out[name] = {
+            "L": list(lengths), "ms": res,
+            "attn_tflops": {v: [fl / (ms * 1e-3) / 1e12 for fl, ms in zip(flops, ys)] for v, ys in res.items()},
+            "fit_ms": {v: {"a_per_tok2": a, "b_per_tok": b, "c": c} for v, (a, b, c) in fits.items()},
+            "a_ratio_vs_bf16": {v: fits[v][0] / fits["bf16"][0] for v in fits if v != "bf16"},
+            "ttft_ratio_vs_bf16_at_max": {v: res[v][-1] / res["bf16"][-1] for v in res if v != "bf16"},
+        }
+        del data
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 def oracle_sample(workload_id: int, keys: int, heads: int):
@@ -478,11 +549,17 @@ def run_ours(args):
         return dist_max(dist, world, x, device)
 
     f.load_library()
-    if args.sweep:
-        res = itl_sweep(f, device, steps=max(3, min(args.steps, 50)), warmup=args.warmup)
-        if rank == 0:
-            print(json.dumps({"sweep": "ITL-slope proxy (decode step time vs cached context, batch 1)",
-                              "unit": "us", "results": res}), flush=True)
+    if args.sweep or args.ttft:
+        if args.sweep:
+            res = itl_sweep(f, device, steps=max(3, min(args.steps, 50)), warmup=args.warmup)
+            if rank == 0:
+                print(json.dumps({"sweep": "ITL-slope proxy (decode step time vs cached context, batch 1)",
+                                  "unit": "us", "results": res}), flush=True)
+        if args.ttft:
+            res = ttft_sweep(f, device, steps=max(2, min(args.steps, 5)), warmup=min(args.warmup, 3))
+            if rank == 0:
+                print(json.dumps({"sweep": "TTFT proxy (one layer's prompt prefill: cache write + causal "
+                                  "attention, vs prompt length)", "unit": "ms", "results": res}), flush=True)
         if world > 1:
             dist.destroy_process_group()
         return 0
@@ -597,6 +674,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="ITL-slope sweep instead of the benchmark line")
+    ap.add_argument("--ttft", action="store_true", help="TTFT quadratic-fit sweep instead of the benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -223,7 +223,6 @@ fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t 
   fkv_status st = FKV_OK;
   const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
   if (st != FKV_OK) return st;
-  if (bf16 && cache.head_dim > 128) return FKV_UNSUPPORTED;  // bf16 tiles of head_dim 256 exceed shared memory
   if (batch > 65535 || num_q_heads > 65535) return FKV_UNSUPPORTED;
   if (batch == 0 || max_q_len == 0) return FKV_OK;
   if (!q || !cu_seqlens_q || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || !out)

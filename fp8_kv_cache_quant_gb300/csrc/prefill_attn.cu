@@ -7,20 +7,23 @@
 // paragraph "Two-level accumulation"); head_dim 256 puts the most pressure on that
 // scheme (section "大 Head Dimension 的限制").
 //
-// CTA = (128-query tile, query head h, sequence b); 6 warps:
-//   warps 0-3  quantise the Q tile to e4m3 into shared memory (prologue); then per
-//              128-key tile, thread i owns query row i (TMEM lane i): load S from TMEM,
-//              scale, mask, online softmax (running max m, unrounded sum l), write
-//              P8 = e4m3(p * 448) into shared memory, and promote the tile's P.V
-//              partial from TMEM into the FP32 accumulator O = O * alpha + O_tile;
-//              epilogue O * v_s / (448 * l) -> bf16.
-//   warp 4     TMA: each 16-token block of K and V is one box [16][D] of the paged pool
-//              (4-D tensor map: D, slot-in-block, KV head, block), 8 boxes per tile.
-//   warp 5     allocates TMEM, issues S = Q8 K8^T and O_tile = P8 V8 with
-//              tcgen05.mma kind::f8f6f4 (FP32 accumulation in TMEM), commits to
-//              mbarriers.
-// TMEM columns: S [0, 128), O_tile [128, 128 + DN), O [128 + DN, 128 + DN + D); for
-// head_dim 256 the P.V product runs as two N = 128 halves through one O_tile.
+// CTA = (128-query tile, query head h, sequence b); 10 warps:
+//   warps 0-3  softmax warpgroup: quantise the Q tile to e4m3 into shared memory (bf16
+//              layers copy it); then per key tile, thread i owns query row i (TMEM lane
+//              i): load S from TMEM, scale, mask (causal, sliding window), online softmax
+//              (running max m, unrounded sum l), write P8 = e4m3(p * 448) (bf16 layers:
+//              P rounded to bf16) into shared memory, publish the tile's alpha.
+//   warps 4-7  correction warpgroup: promote the tile's P.V partial from TMEM into the
+//              FP32 accumulator O = O * alpha + O_tile (every tile, every N tiles, or
+//              never); epilogue O * v_s / (448 * l) -> bf16.
+//   warp 8     TMA: each 16-token block of K and V is one box [16][row bytes] of the
+//              paged pool (4-D tensor map: row bytes, slot-in-block, KV head, block).
+//   warp 9     allocates TMEM, issues S = Q8 K8^T and O_tile = P8 V8 with tcgen05.mma
+//              (kind::f8f6f4 for e4m3, kind::f16 for bf16; FP32 accumulation in TMEM),
+//              commits to mbarriers.
+// Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns: S [0, 128 * SBUF),
+// O_tile [TM_OT, TM_OT + DN), O [TM_OA, TM_OA + D); for head_dim 256 the P.V product runs
+// as two N = 128 halves through one O_tile.
 // Every wait is bounded in time; a timeout records FKV_FAULT_TIMEOUT, lets the CTA's
 // copies and MMAs drain and returns.
 #include <mutex>
@@ -58,15 +61,21 @@ FKV_DEV float fmax3(float a, float b, float c) {
 
 template <int D, bool BF>
 struct PrefillCfg {
-  static constexpr int BM = 128, BN = 128;
   static constexpr int ES = BF ? 2 : 1;             // bytes per element (bf16 / e4m3)
+  // 128 queries per CTA; 128 keys per tile, or 64 for bf16 head_dim 256, whose 128-key
+  // K and V tiles would not fit next to the Q tile in shared memory
+  static constexpr int BM = 128, BN = (BF && D > 128) ? 64 : 128;
+  static constexpr int NBLK = BN / 16;              // 16-token pool blocks per key tile
+  static constexpr int NCH = BN / 32;               // 32-column chunks of an S row
   static constexpr int DB = D * ES;                 // bytes of one Q / K / V row
   static constexpr int RB = DB < 128 ? DB : 128;    // bytes of one swizzled row
   static constexpr int NSUB = DB / RB;              // sub-tiles along head_dim
   static constexpr int EPS = RB / ES;               // elements of a sub-tile row: N of one P.V product
   static constexpr int SWZ = RB == 128 ? 2 : 4;     // descriptor swizzle mode (128 B / 64 B)
-  static constexpr int SUB = BM * RB;               // bytes of one 128-row sub-tile
-  static constexpr int TILE = BM * DB;              // bytes of a Q, K or V tile
+  static constexpr int SUB = BM * RB;               // bytes of one 128-row Q sub-tile
+  static constexpr int TILE = BM * DB;              // bytes of the Q tile
+  static constexpr int KSUB = BN * RB;              // bytes of one BN-row K / V sub-tile
+  static constexpr int KTILE = BN * DB;             // bytes of a K or V tile
   static constexpr int NS = (!BF && D <= 128) ? 3 : 2;  // K/V stages
   static constexpr int DN = D < 128 ? D : 128;      // O_tile width (elements) of one P.V pass
   static constexpr int NH = D / DN;                 // P.V passes
@@ -83,18 +92,19 @@ struct PrefillCfg {
   // shared memory layout (bytes)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + TILE;
-  static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_P = OFF_V + NS * TILE;           // two P tiles
+  static constexpr int OFF_V = OFF_K + NS * KTILE;
+  static constexpr int OFF_P = OFF_V + NS * KTILE;          // two P tiles
   static constexpr int OFF_A = OFF_P + 2 * PTILE;           // alpha [2][128] floats
   static constexpr int OFF_L = OFF_A + 2 * BM * 4;          // l [128] floats
   static constexpr int OFF_BAR = OFF_L + BM * 4;
   static constexpr int NBAR = 17 + 4 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
-  static constexpr uint32_t IDESC_QK = BF ? idesc_bf16_f32(128, 128, 0, 0) : idesc_e4m3_f32(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_QK = BF ? idesc_bf16_f32(128, BN, 0, 0) : idesc_e4m3_f32(128, BN, 0, 0);
   static constexpr uint32_t IDESC_PV = BF ? idesc_bf16_f32(128, EPS, 0, 1) : idesc_e4m3_f32(128, EPS, 0, 1);
   static_assert(TM_OA + D <= 512, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(!ONE_LOAD || BN == 128, "the one-load softmax holds a 128-column S row");
 };
 
 // One MMA of the element type: e4m3 (kind::f8f6f4) or bf16 (kind::f16), FP32 accumulation.
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         {
           float mx = -INFINITY;
   #pragma unroll C::UNR
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < C::NCH; ++c) {
             float v[32];
             tmem_ld32(sc + 32 * c, v);
             tmem_ld_wait();
@@ -354,12 +364,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           float va[32], vb[32];
           tmem_ld32(sc, va);
   #pragma unroll C::UNR
-          for (int c = 0; c < 4; c += 2) {
+          for (int c = 0; c < C::NCH; c += 2) {
             tmem_ld_wait();
             tmem_ld32(sc + 32 * (c + 1), vb);
             chunk(va, c);
             tmem_ld_wait();
-            if (c + 2 < 4) tmem_ld32(sc + 32 * (c + 2), va);
+            if (c + 2 < C::NCH) tmem_ld32(sc + 32 * (c + 2), va);
             chunk(vb, c + 1);
           }
         }
@@ -525,10 +535,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         *abort_s = 1;
         break;
       }
-      // 8 block ids of the tile; blocks past the context read block 0 (their keys are masked)
+      // NBLK block ids of the tile; blocks past the context read block 0 (their keys are masked)
       int id = 0;
-      if (lane < 8) {
-        const int lb = (tb + t) * 8 + lane;
+      if (lane < C::NBLK) {
+        const int lb = (tb + t) * C::NBLK + lane;
         if (lb < nblk_seq) {
           id = trow[lb];
           if (id < 0 || id >= p.num_blocks) {
@@ -537,28 +547,29 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           }
         }
       }
-      int ids[8];
+      int ids[C::NBLK];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ids[j] = __shfl_sync(0xffffffffu, id, j);
+      for (int j = 0; j < C::NBLK; ++j) ids[j] = __shfl_sync(0xffffffffu, id, j);
       const int st = t % C::NS, use = t / C::NS;
       bool ok = true;
       if (lane == 0) {
         if (use > 0) ok = wait_ns(&k_empty[st], (use - 1) & 1);
         if (ok) {
-          mbar_arrive_expect_tx(&k_full[st], C::TILE);
+          mbar_arrive_expect_tx(&k_full[st], C::KTILE);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
+          for (int j = 0; j < C::NBLK; ++j)
 #pragma unroll
             for (int s = 0; s < C::NSUB; ++s)
-              tma_load_4d(sK + st * C::TILE + s * C::SUB + j * 16 * C::RB, &tmk, s * C::RB, 0, g, ids[j], &k_full[st]);
+              tma_load_4d(sK + st * C::KTILE + s * C::KSUB + j * 16 * C::RB, &tmk, s * C::RB, 0, g, ids[j],
+                          &k_full[st]);
           if (use > 0) ok = wait_ns(&v_empty[st], (use - 1) & 1);
           if (ok) {
-            mbar_arrive_expect_tx(&v_full[st], C::TILE);
+            mbar_arrive_expect_tx(&v_full[st], C::KTILE);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < C::NBLK; ++j)
 #pragma unroll
               for (int s = 0; s < C::NSUB; ++s)
-                tma_load_4d(sV + st * C::TILE + s * C::SUB + j * 16 * C::RB, &tmv, s * C::RB, 0, g, ids[j],
+                tma_load_4d(sV + st * C::KTILE + s * C::KSUB + j * 16 * C::RB, &tmv, s * C::RB, 0, g, ids[j],
                             &v_full[st]);
           }
           last_use[st] = use;
@@ -593,9 +604,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < C::DB / 32; ++kk) {
           const int byte = kk * 32;
-          const uint32_t off = (byte / C::RB) * C::SUB + (byte % C::RB);
-          const uint64_t ad = smem_desc(sQa + off, 16, 8 * C::RB, C::SWZ);
-          const uint64_t bd = smem_desc(sKa + st * C::TILE + off, 16, 8 * C::RB, C::SWZ);
+          const uint32_t qoff = (byte / C::RB) * C::SUB + (byte % C::RB);
+          const uint32_t koff = (byte / C::RB) * C::KSUB + (byte % C::RB);
+          const uint64_t ad = smem_desc(sQa + qoff, 16, 8 * C::RB, C::SWZ);
+          const uint64_t bd = smem_desc(sKa + st * C::KTILE + koff, 16, 8 * C::RB, C::SWZ);
           umma<BF>(tmem + 128 * sb, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[sb]);
@@ -614,7 +626,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
         for (int j = 0; j < C::DN / C::EPS; ++j) {
           const int sub = hn * (C::DN / C::EPS) + j;
-          const uint64_t bd = smem_desc(sVa + st * C::TILE + sub * C::SUB + kk * C::KSTEP * C::RB, 8 * C::RB,
+          const uint64_t bd = smem_desc(sVa + st * C::KTILE + sub * C::KSUB + kk * C::KSTEP * C::RB, 8 * C::RB,
                                         8 * C::RB, C::SWZ);
           umma<BF>(dst + j * C::EPS, ad, bd, C::IDESC_PV, (kk > 0 || !fresh) ? 1u : 0u);
         }
@@ -636,7 +648,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           const int c = it % chunks;
           const int s = (it / chunks) % C::NSUB;
           const int r = first + it / (chunks * C::NSUB);
-          *reinterpret_cast<uint4*>(sV + st * C::TILE + s * C::SUB + r * C::RB + c * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sV + st * C::KTILE + s * C::KSUB + r * C::RB + c * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -763,6 +775,7 @@ cudaError_t launch_prefill(const PrefillParams& p, int D, bool bf16_layer, void*
   if (bf16_layer) {
     if (D == 64) return launch_prefill_w<64, true>(p, kc, vc, s);
     if (D == 128) return launch_prefill_w<128, true>(p, kc, vc, s);
+    if (D == 256) return launch_prefill_w<256, true>(p, kc, vc, s);
     return cudaErrorInvalidValue;
   }
   if (D == 64) return launch_prefill_w<64, false>(p, kc, vc, s);

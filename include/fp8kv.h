@@ -225,8 +225,8 @@ int32_t fkv_prefill_block_n(int32_t head_dim);
  *   out           device bf16 [total_q][num_q_heads][head_dim]
  * head_dim in {64, 128, 256}.  Skip (bf16) layers — the layer's bit set in skip_layer_mask —
  * read the bf16 pool and run the same kernel on bf16 operands (kind::f16 MMA, P rounded to
- * bf16, no scales: q_scale/k_scale/v_scale may be NULL); they support head_dim 64 and 128
- * (256: FKV_UNSUPPORTED, the bf16 tiles exceed shared memory).
+ * bf16, no scales: q_scale/k_scale/v_scale may be NULL); at head_dim 256 their key tiles
+ * hold 64 keys (128-key bf16 tiles do not fit in shared memory).
  */
 fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t batch,
                             int32_t num_q_heads, int32_t max_q_len, fkv_layer_cache cache,

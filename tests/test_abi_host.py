@@ -108,9 +108,9 @@ def test_prefill_validation(lib):
     pre = lib.fp8_prefill_attn
     p = 1 << 12
     mask = (ctypes.c_uint8 * 1)(1)
-    # a bf16 (skip) layer runs the bf16 prefill for head_dim 64 / 128 (no scales needed); 256 does not fit
-    assert pre(p, p, 1, 8, 16, _cache(D=256), p, 4, p, p, p, p, 0, 0.0, 1, 0, 1, 0, mask, 1, p, None,
-               None) == f.UNSUPPORTED
+    # a bf16 (skip) layer runs the bf16 prefill and needs no scales; its head_dim 256 is accepted
+    assert pre(p, p, 0, 8, 16, _cache(D=256), p, 4, p, None, None, None, 0, 0.0, 1, 0, 1, 0, mask, 1, p, None,
+               None) == f.OK
     assert pre(p, p, 0, 8, 16, _cache(), p, 4, p, None, None, None, 0, 0.0, 1, 0, 1, 0, mask, 1, p, None,
                None) == f.OK
     assert f.fkv_prefill_block_n(128) == 128 and f.fkv_prefill_block_n(100) == 0

@@ -1,5 +1,6 @@
 """Host logic of the benchmark (CPU only): ITL fits and break-even against the numbers the
-vLLM blog prints (tests/golden/itl_fits.txt), byte accounting, the oracle sample of the
+vLLM blog prints (tests/golden/itl_fits.txt), the TTFT quadratic fit and the head_dim-256
+ratios (tests/golden/gemma_hd256_fits.txt), byte accounting, the oracle sample of the
 reference arm, and the max-over-ranks timing with two gloo ranks."""
 import os
 import socket
@@ -33,6 +34,28 @@ def test_break_even_and_slope_ratio_match_the_blog():
         got = bench.break_even(sf, i_f, sb, ib)
         assert abs(got - be) <= tol * be, (name, got, be)
         assert abs(sf / sb - ratio) <= 0.006, (name, sf / sb, ratio)
+
+
+def test_gemma_hd256_ratios_match_the_blog():
+    """The FP8/BF16 ratios the sweeps report are fp8 over bf16 coefficients, as the blog's."""
+    rows = {}
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "gemma_hd256_fits.txt")):
+        if line.strip() and not line.startswith("#"):
+            name, bf, fp, ratio, tol = line.split()
+            rows[name] = (float(bf), float(fp), float(ratio), float(tol))
+    for name, (bf, fp, ratio, tol) in rows.items():
+        assert abs(fp / bf - ratio) <= tol, (name, fp / bf, ratio)
+
+
+def test_quadratic_fit_recovers_the_blog_coefficient():
+    xs = list(bench.SWEEP_T)
+    a, b, c = 1.12e-06, 2.0e-4, 35.0
+    ys = [a * x * x + b * x + c for x in xs]
+    fa, fb, fc = bench.quadratic_fit(xs, ys)
+    assert abs(fa - a) < 1e-12 and abs(fb - b) < 1e-8 and abs(fc - c) < 1e-5
+    rng = np.random.default_rng(1)
+    noisy = [y * (1 + 1e-3 * e) for y, e in zip(ys, rng.standard_normal(len(xs)))]
+    assert abs(bench.quadratic_fit(xs, noisy)[0] / a - 1) < 5e-3
 
 
 def test_break_even_none_when_fp8_is_not_cheaper():

@@ -80,10 +80,15 @@ def test_prefill_promote_every_variants(D, promote_every):
     (128, 4, 2, [700, 300], [700, 130], 1, True, 0),
     (128, 4, 2, [700, 300], [700, 130], 1, True, 3),
     (64, 4, 2, [700, 300], [700, 130], 1, True, 2),
+    (256, 2, 1, [390, 130], [390, 100], 1, True, 1),
+    (256, 8, 1, [640], [256], 0, True, 1),
+    (256, 4, 1, [333], [70], 0, False, 1),
+    (256, 4, 2, [700, 300], [700, 130], 1, True, 0),
 ])
 def test_prefill_bf16_skip_layer_parity(D, Hq, Hkv, T_list, Lq_list, gran, causal, promote_every):
     """A skip layer's bf16 prefill (kind::f16 MMA on the bf16 pool) against the oracle's
-    full-precision attention over the same bf16 values; the kernel rounds P to bf16."""
+    full-precision attention over the same bf16 values; the kernel rounds P to bf16.
+    head_dim 256 runs 64-key tiles."""
     got, ref = _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed=7 * D + Hq + sum(T_list),
                     promote_every=promote_every, bf16=True)
     assert_close(got, ref, what=f"bf16 D={D} T={T_list} Lq={Lq_list} causal={causal} pe={promote_every}")
@@ -93,6 +98,7 @@ def test_prefill_bf16_skip_layer_parity(D, Hq, Hkv, T_list, Lq_list, gran, causa
     (128, False, 1, 1), (128, False, 100, 1), (128, False, 128, 1), (128, False, 300, 1), (128, False, 5000, 1),
     (64, False, 257, 1), (256, False, 200, 1), (256, False, 200, 0), (128, False, 300, 0), (64, False, 77, 3),
     (128, True, 1, 1), (128, True, 300, 1), (64, True, 129, 1), (128, True, 250, 0),
+    (256, True, 1, 1), (256, True, 65, 1), (256, True, 512, 0),
 ])
 def test_prefill_sliding_window_parity(D, bf16, window, promote_every):
     """Sliding-window prefill: each row attends the last `window` keys up to its own
