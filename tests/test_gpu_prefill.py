@@ -134,8 +134,26 @@ def _sample_rows(cu, per_seq, rng):
     return rows
 
 
+def _errors(got, ref):
+    d = got - ref
+    return float(np.abs(d).max()), float(np.sqrt((d * d).sum() / (ref * ref).sum()))
+
+
+def _check_promote_variants(outs, ref, what):
+    """Every promote_every variant within the parity bar, and skipping promotion no less
+    accurate than promoting every tile beyond rounding noise: the tensor core's TMEM
+    accumulator is FP32 on this hardware (the blog: on B200 the accumulation issue is fixed)."""
+    errs = {}
+    for pe, got in outs.items():
+        assert_close(got, ref, what=f"{what} promote_every={pe}")
+        errs[pe] = _errors(got, ref)
+        print(f"{what} promote_every={pe}: max-abs {errs[pe][0]:.3e} rel-L2 {errs[pe][1]:.3e}")
+    assert errs[0][1] <= 2.0 * errs[1][1] + 1e-4, errs
+
+
 def test_workload5_prefill_d256_sampled():
-    """head_dim 256, 4 x 32768 causal, per-head scales: sampled rows of every head."""
+    """head_dim 256, 4 x 32768 causal, per-head scales: sampled rows of every head, for
+    two-level accumulation every tile (1) and none (0)."""
     w = synth.WORKLOADS[5]
     data = synth.prefill_data(w, device="cuda")
     ctx = np.full(w.batch, w.seq_len, np.int32)
@@ -144,9 +162,12 @@ def test_workload5_prefill_d256_sampled():
     f.kv_quant_cache(data.k, data.v, to_dev(synth.slot_mapping(table, ctx)), cache, data.k_scale, data.v_scale,
                      f.SCALE_PER_HEAD)
     cu = np.arange(w.batch + 1, dtype=np.int32) * w.seq_len
-    out = f.fp8_prefill_attn(data.q, to_dev(cu), w.seq_len, cache, to_dev(table), to_dev(ctx), data.q_scale,
-                             data.k_scale, data.v_scale, f.SCALE_PER_HEAD, causal=True).float().cpu().numpy()
     rows = _sample_rows(cu, 12, np.random.default_rng(5))
+    outs = {}
+    for pe in (1, 0):
+        out = f.fp8_prefill_attn(data.q, to_dev(cu), w.seq_len, cache, to_dev(table), to_dev(ctx), data.q_scale,
+                                 data.k_scale, data.v_scale, f.SCALE_PER_HEAD, causal=True, promote_every=pe)
+        outs[pe] = out.float().cpu().numpy()[rows]
     kl = [synth.bf16_to_f64(data.k[cu[b]:cu[b + 1]]) for b in range(w.batch)]
     vl = [synth.bf16_to_f64(data.v[cu[b]:cu[b + 1]]) for b in range(w.batch)]
     qh = synth.bf16_to_f64(data.q[torch.as_tensor(rows, device="cuda")])
@@ -156,13 +177,12 @@ def test_workload5_prefill_d256_sampled():
     ref = attention.prefill_attention(q_full, cu, kl, vl, data.q_scale.cpu().numpy(), data.k_scale.cpu().numpy(),
                                       data.v_scale.cpu().numpy(), block_n=f.fkv_prefill_block_n(w.head_dim),
                                       rows=rows)
-    assert_close(out[rows], ref[rows], what="workload 5 prefill")
+    _check_promote_variants(outs, ref[rows], "workload 5 prefill")
 
 
-@pytest.mark.parametrize("promote_every", [1, 0])
-def test_workload4_prefill_chunk_sampled(promote_every):
+def test_workload4_prefill_chunk_sampled():
     """The 4096-query FP8 prefill chunk at the tail of the 131072-key needle cache: a contraction
-    over ~130k keys, with two-level accumulation (1) and without it (0)."""
+    over ~130k keys, with two-level accumulation every tile (1), every 4 tiles (4) and none (0)."""
     w = synth.WORKLOADS[4]
     ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
     table, nb = synth.block_table(ctx, seed=w.seed)
@@ -172,15 +192,18 @@ def test_workload4_prefill_chunk_sampled(promote_every):
     qp = synth.prefill_query(w, 0, device="cuda")
     L = w.prefill_chunk
     cu = np.array([0, L], np.int32)
-    out = f.fp8_prefill_attn(qp, to_dev(cu), L, cache, to_dev(table), to_dev(ctx), data.q_scale, data.k_scale,
-                             data.v_scale, f.SCALE_PER_TENSOR, causal=True,
-                             promote_every=promote_every).float().cpu().numpy()
     rows = _sample_rows(cu, 10, np.random.default_rng(4))
     heads = [0, 13, 40, 63]
+    full = {}
+    for pe in (1, 4, 0):
+        full[pe] = f.fp8_prefill_attn(qp, to_dev(cu), L, cache, to_dev(table), to_dev(ctx), data.q_scale,
+                                      data.k_scale, data.v_scale, f.SCALE_PER_TENSOR, causal=True,
+                                      promote_every=pe).float().cpu().numpy()
     G = w.group
     one = np.ones(1, np.float32)
     T = int(ctx[0])
-    got, ref = [], []
+    outs = {pe: [] for pe in full}
+    ref = []
     for g in sorted(set(h // G for h in heads)):
         kb = [synth.bf16_to_f64(data.k[:T, g:g + 1])]
         vb = [synth.bf16_to_f64(data.v[:T, g:g + 1])]
@@ -190,6 +213,7 @@ def test_workload4_prefill_chunk_sampled(promote_every):
         r = attention.prefill_attention(q_full, cu, kb, vb, one, one, one, block_n=f.fkv_prefill_block_n(w.head_dim),
                                         rows=rows)
         for j, h in enumerate(hs):
-            got.append(out[rows, h])
+            for pe in full:
+                outs[pe].append(full[pe][rows, h])
             ref.append(r[rows, j])
-    assert_close(np.array(got), np.array(ref), what="workload 4 prefill chunk")
+    _check_promote_variants({pe: np.array(v) for pe, v in outs.items()}, np.array(ref), "workload 4 prefill chunk")
