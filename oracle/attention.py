@@ -14,13 +14,20 @@ Readings where the pages are silent (each is exercised by the tests):
   R6  a window W keeps exactly the last W keys, the current one included;
   R7  decode quantises Q with its scale (1.0 when uncalibrated);
   R8  softmax scale 1/sqrt(D);
-  R9  decode keeps P in FP32 (no FP8 rounding of the probabilities);
+  R9  decode keeps P exact (``p_quant=False``), or, for a decode whose Score*V product
+      runs on FP8 tensor cores (``p_quant=True``), rounds P per key tile as prefill does
+      (R11) with the tiles of the kernel's splits (R23);
   R10 the prefill softmax denominator sums the unrounded p;
   R11 prefill rounds P to e4m3 as e4m3(p * 448) and divides by 448 again;
   R13 prefill query i of a sequence with context T and Lq queries sits at absolute
-      position T - Lq + i (the chunk is the tail of the context).
+      position T - Lq + i (the chunk is the tail of the context);
+  R23 a split-K decode with FP8 P splits the key range [lo, T) into runs of
+      ``split_blocks`` pool blocks starting at block lo // block_size; each split walks
+      its keys in tiles of ``block_n`` starting at its first block, with its own running
+      maximum, and the splits' (acc, m, l) are merged exactly.
 
-The decode oracle computes the unsplit softmax (split-K is exactly the same sum).
+With exact P the decode oracle computes the unsplit softmax (split-K is exactly the same
+sum).
 The prefill oracle walks the keys in the kernel's tiles because the e4m3 rounding of
 p depends on the running maximum at each tile; with ``p_quant=False`` it is the plain
 softmax definition.
@@ -56,14 +63,43 @@ def softmax_attend(qv, K, V, tau):
     return w @ V, w
 
 
+def split_decode(qv, K, V, T, lo, tau, *, split_blocks, block_n, p_quant, block_size=16):
+    """One query over keys lo .. T-1 (dequantised K, V [T - lo][D]) as a split-K decode
+    (R23): splits of ``split_blocks`` blocks from block lo // block_size, each walked in
+    tiles of ``block_n`` from its first block with its own running maximum (P rounded
+    as e4m3(p * 448) / 448 when ``p_quant``), then merged:
+    o = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s,  M = max_s m_s."""
+    blk0, blk1 = lo // block_size, (T + block_size - 1) // block_size
+    qpos = np.array([T - 1])
+    accs, ms, ls = [], [], []
+    for b0 in range(blk0, blk1, split_blocks):
+        b1 = min(b0 + split_blocks, blk1)
+        a, z = max(lo, b0 * block_size), min(T, b1 * block_size)
+        if z <= a:
+            continue
+        acc, m, l = _tile_walk(np.asarray(qv)[None, :], K[a - lo:z - lo], V[a - lo:z - lo], qpos, a, block_n, tau,
+                               p_quant, tile0=b0 * block_size, state=True)
+        accs.append(acc[0]); ms.append(m[0]); ls.append(l[0])
+    if not ms:
+        return np.zeros(V.shape[1])
+    M = max(ms)
+    w = [math.exp(mi - M) for mi in ms]
+    num = sum(wi * ai for wi, ai in zip(w, accs))
+    den = sum(wi * li for wi, li in zip(w, ls))
+    return num / den
+
+
 def decode_attention(q, k_pool, v_pool, block_table, context_lens, q_scale, k_scale, v_scale, *,
-                     fp8: bool = True, softmax_scale: float = 0.0, window: int = 0, block_size: int = 16):
+                     fp8: bool = True, softmax_scale: float = 0.0, window: int = 0, block_size: int = 16,
+                     p_quant: bool = False, split_blocks: int = 0, block_n: int = 128):
     """Paged decode attention, one query per sequence.
 
     q: float64 [B][Hq][D] (bf16 values).  k_pool / v_pool: uint8 e4m3 codes
     ``[nb][Hkv][bs][D]`` when ``fp8``, else float64 values of the bf16 pool.
     context_lens[b] counts every key of sequence b, the current token included.
     Returns float64 [B][Hq][D]; a sequence with no key gives a zero row.
+    ``split_blocks`` > 0 computes it as the split-K decode of R23 (``p_quant`` rounds P,
+    on e4m3 layers only); 0 is the plain softmax.
     """
     q = np.asarray(q, dtype=np.float64)
     B, Hq, D = q.shape
@@ -86,15 +122,21 @@ def decode_attention(q, k_pool, v_pool, block_table, context_lens, q_scale, k_sc
                     qv = e4m3.decode(e4m3.quantize(q[b, h], qs)) * qs
                 else:
                     qv = q[b, h]
-                out[b, h], _ = softmax_attend(qv, K, V, tau)
+                if split_blocks > 0:
+                    out[b, h] = split_decode(qv, K, V, T, lo, tau, split_blocks=split_blocks, block_n=block_n,
+                                             p_quant=p_quant and fp8, block_size=block_size)
+                else:
+                    out[b, h], _ = softmax_attend(qv, K, V, tau)
     return out
 
 
 def decode_attention_contiguous(q_b, k_seq, v_seq, q_scale, k_scale, v_scale, *, fp8=True,
-                                softmax_scale=0.0, window=0, heads=None):
+                                softmax_scale=0.0, window=0, heads=None, p_quant=False, split_blocks=0,
+                                block_n=128):
     """Decode attention of ONE sequence from its contiguous bf16 K/V ([T][Hkv][D],
     float64 values): the oracle quantises K/V itself with the same rule as the cache
-    write, then attends.  Used at full workload sizes on sampled sequences/heads.
+    write, then attends (as the split-K decode of R23 when ``split_blocks`` > 0).  Used
+    at full workload sizes on sampled sequences/heads.
     Returns {h: float64[D]} for the requested query heads (default: all)."""
     Hq, D = q_b.shape
     T, Hkv, _ = k_seq.shape
@@ -124,20 +166,26 @@ def decode_attention_contiguous(q_b, k_seq, v_seq, q_scale, k_scale, v_scale, *,
             qv = e4m3.decode(e4m3.quantize(q_b[h], qs)) * qs
         else:
             qv = q_b[h]
-        res[h], _ = softmax_attend(qv, K, V, tau)
+        if split_blocks > 0:
+            res[h] = split_decode(qv, K, V, T, lo, tau, split_blocks=split_blocks, block_n=block_n,
+                                  p_quant=p_quant and fp8)
+        else:
+            res[h], _ = softmax_attend(qv, K, V, tau)
     return res
 
 
-def _tile_walk(Qt, K, V, qpos, kpos0, block_n, tau, p_quant, window=0):
+def _tile_walk(Qt, K, V, qpos, kpos0, block_n, tau, p_quant, window=0, tile0=0, state=False):
     """Online softmax over key tiles for a set of query rows of one head.
 
     Qt: [R][D] dequantised queries at absolute positions qpos [R]; K, V: [T][D]
-    dequantised keys/values at absolute positions kpos0 .. kpos0+T-1.  Tiles are the
-    absolute key ranges [t*block_n, (t+1)*block_n).  Row r sees keys <= qpos[r].
+    dequantised keys/values at absolute positions kpos0 .. kpos0+T-1 (kpos0 >= tile0).
+    Tiles are the key ranges [tile0 + t*block_n, tile0 + (t+1)*block_n).  Row r sees
+    keys <= qpos[r].
     For each tile: m_t = max(m_{t-1}, tile max); p = exp(s - m_t);
     l = l e^{m_{t-1}-m_t} + sum p (unrounded p, R10);
     acc = acc e^{m_{t-1}-m_t} + sum e4m3(p*448)/448 * v (R11, two-level: the tile's
     partial is added into the running float accumulator).
+    Returns acc / l, or with ``state`` the unnormalised (acc, m, l) (natural-log max).
     """
     R, D = Qt.shape
     T = K.shape[0]
@@ -150,11 +198,11 @@ def _tile_walk(Qt, K, V, qpos, kpos0, block_n, tau, p_quant, window=0):
     m = np.full(R, -np.inf)
     l = np.zeros(R)
     acc = np.zeros((R, V.shape[1]))
-    t_first = kpos0 // block_n
-    t_last = (kpos0 + T - 1) // block_n
+    t_first = (kpos0 - tile0) // block_n
+    t_last = (kpos0 + T - 1 - tile0) // block_n
     for t in range(t_first, t_last + 1):
-        a = max(t * block_n, kpos0) - kpos0
-        b = min((t + 1) * block_n, kpos0 + T) - kpos0
+        a = max(tile0 + t * block_n, kpos0) - kpos0
+        b = min(tile0 + (t + 1) * block_n, kpos0 + T) - kpos0
         st = S[:, a:b]
         tmax = np.max(st, axis=1)
         m_new = np.maximum(m, tmax)
@@ -170,6 +218,8 @@ def _tile_walk(Qt, K, V, qpos, kpos0, block_n, tau, p_quant, window=0):
             pq = p
         acc = acc * alpha[:, None] + pq @ V[a:b]
         m = np.where(live, m_new, m)
+    if state:
+        return acc, m, l
     with np.errstate(invalid="ignore", divide="ignore"):
         out = np.where(l[:, None] > 0, acc / np.where(l > 0, l, 1.0)[:, None], 0.0)
     return out

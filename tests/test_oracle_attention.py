@@ -299,3 +299,122 @@ def test_prefill_window_matches_banded_sdpa_and_decode():
     dec = attention.decode_attention_contiguous(q[Lq - 1], K[0], V[0], one, one, one, window=W)
     for h in range(Hq):
         np.testing.assert_allclose(pre[Lq - 1, h], dec[h], rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- split-K decode (R23)
+
+def _dequant(K, V, qv_raw, qs, ks, vs):
+    K8 = e4m3.decode(e4m3.quantize(K, ks)) * ks
+    V8 = e4m3.decode(e4m3.quantize(V, vs)) * vs
+    qv = e4m3.decode(e4m3.quantize(qv_raw, qs)) * qs
+    return qv, K8, V8
+
+
+@pytest.mark.parametrize("split_blocks", [1, 2, 3, 8])
+@pytest.mark.parametrize("window", [0, 37])
+def test_split_decode_with_exact_p_is_sdpa(split_blocks, window):
+    """With exact P, splitting the keys and merging (acc, m, l) is the plain softmax:
+    float64 scaled_dot_product_attention over the dequantised window."""
+    rng = np.random.default_rng(20 + split_blocks + window)
+    D, T = 8, 150
+    lo = max(0, T - window) if window else 0
+    qv, K, V = _dequant(rng.standard_normal((T, D)) * 2, rng.standard_normal((T, D)), rng.standard_normal(D),
+                        np.float32(0.5), np.float32(0.75), np.float32(0.25))
+    tau = 1 / math.sqrt(D)
+    got = attention.split_decode(qv, K[lo:], V[lo:], T, lo, tau, split_blocks=split_blocks, block_n=32,
+                                 p_quant=False, block_size=16)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(qv)[None, None], torch.from_numpy(K[lo:])[None], torch.from_numpy(V[lo:])[None],
+        scale=tau)[0, 0].numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def _closed_form_fp8p(qv, K, V, T, lo, tau, split_blocks, block_n, bs):
+    """Non-iterative statement of the split-K decode with FP8 P: key j of split s, tile t
+    (tiles counted from the split's first block) gets the P code of e^(s_j - m) with m the
+    maximum over the split's keys up to the end of tile t, and the weight
+    dec(code) / 448 * e^(m - M); the denominator is sum_j e^(s_j - M), M the global max."""
+    kpos = np.arange(lo, T)
+    s = (K @ qv) * tau
+    M = s.max()
+    blk0 = lo // bs
+    w = np.zeros(len(kpos))
+    for j, kp in enumerate(kpos):
+        split = (kp // bs - blk0) // split_blocks
+        origin = (blk0 + split * split_blocks) * bs
+        split_end = min((blk0 + (split + 1) * split_blocks) * bs, T)
+        tile_end = min(origin + ((kp - origin) // block_n + 1) * block_n, split_end)
+        m_run = s[(kpos >= max(origin, lo)) & (kpos < tile_end)].max()
+        code = e4m3.encode(e4m3.fl32(e4m3.fl32(np.exp(s[j] - m_run)) * 448.0))
+        w[j] = e4m3.decode(code) / 448.0 * math.exp(m_run - M)
+    return (w @ V) / np.exp(s - M).sum()
+
+
+@pytest.mark.parametrize("T,window,split_blocks,block_n", [
+    (20, 0, 4, 32),      # one split, one partial tile: the single-tile direct formula
+    (150, 0, 4, 32),     # splits of two 32-key tiles
+    (150, 0, 3, 32),     # a split of 48 keys: a full tile and a partial one
+    (300, 70, 2, 16),    # window starting inside block 14: split origins not tile-aligned
+    (300, 200, 5, 32),   # window, splits of 80 keys (2.5 tiles)
+    (257, 0, 16, 128),   # the kernel's shape: 128-key tiles, 256-key splits, a 1-key tail
+])
+def test_split_decode_fp8p_matches_closed_form(T, window, split_blocks, block_n):
+    rng = np.random.default_rng(T + window + split_blocks)
+    D = 8
+    lo = max(0, T - window) if window else 0
+    # strongly varying scores so that running maxima move between tiles and splits
+    qv, K, V = _dequant(rng.standard_normal((T, D)) * 3, rng.standard_normal((T, D)), rng.standard_normal(D) * 2,
+                        np.float32(0.5), np.float32(1.0), np.float32(0.25))
+    tau = 1 / math.sqrt(D)
+    got = attention.split_decode(qv, K[lo:], V[lo:], T, lo, tau, split_blocks=split_blocks, block_n=block_n,
+                                 p_quant=True, block_size=16)
+    ref = _closed_form_fp8p(qv, K[lo:], V[lo:], T, lo, tau, split_blocks, block_n, 16)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+    # the rounding is visible: exact P differs by more than rounding noise
+    exact = attention.split_decode(qv, K[lo:], V[lo:], T, lo, tau, split_blocks=split_blocks, block_n=block_n,
+                                   p_quant=False, block_size=16)
+    assert np.abs(got - exact).max() > 1e-6
+
+
+def test_split_decode_fp8p_depends_on_the_tile_origin():
+    """Tiles start at each split's first block, not at absolute multiples of block_n: with
+    a window the two readings give different P codes, and the oracle follows the first."""
+    rng = np.random.default_rng(3)
+    D, T, window = 8, 300, 180
+    lo = T - window              # 120: the first split starts at key 112, 16 past a multiple of 32
+    q = rng.standard_normal(D)
+    # scores that rise along the keys, so that the running maximum moves in almost every tile
+    K = rng.standard_normal((T, D)) + np.outer(np.arange(T) / 20.0, q / np.linalg.norm(q))
+    qv, K, V = _dequant(K, rng.standard_normal((T, D)), q, np.float32(0.5), np.float32(1.0), np.float32(0.25))
+    tau = 1 / math.sqrt(D)
+    got = attention.split_decode(qv, K[lo:], V[lo:], T, lo, tau, split_blocks=64, block_n=32, p_quant=True)
+    # absolute tiles: one tile walk over the window with tile0 = 0
+    acc, m, l = attention._tile_walk(qv[None], K[lo:], V[lo:], np.array([T - 1]), lo, 32, tau, True, state=True)
+    absolute = acc[0] / l[0]
+    assert np.abs(got - absolute).max() > 1e-6
+    ref = _closed_form_fp8p(qv, K[lo:], V[lo:], T, lo, tau, 64, 32, 16)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_decode_attention_split_mode_is_the_split_walk():
+    """The paged entry point routes through the split walk per (sequence, head)."""
+    rng = np.random.default_rng(4)
+    Hq, Hkv, D = 4, 2, 8
+    T_list = [1, 40, 150]
+    q = _bf16(rng.standard_normal((len(T_list), Hq, D)) * 2)
+    K = [_bf16(rng.standard_normal((t, Hkv, D)) * 3) for t in T_list]
+    V = [_bf16(rng.standard_normal((t, Hkv, D))) for t in T_list]
+    qs = np.array([0.5, 1.0, 0.25, 2.0], np.float32)
+    ks = np.array([0.75, 0.125], np.float32)
+    vs = np.array([1.5, 0.5], np.float32)
+    kp, vp, table = _paged(K, V, T_list, rng, True, ks, vs)
+    got = attention.decode_attention(q, kp, vp, table, T_list, qs, ks, vs, window=100, p_quant=True, split_blocks=2,
+                                     block_n=16)
+    tau = 1 / math.sqrt(D)
+    for b, T in enumerate(T_list):
+        lo = max(0, T - 100)
+        for h in range(Hq):
+            g = h // 2
+            qv, K8, V8 = _dequant(K[b][:, g], V[b][:, g], q[b, h], qs[h], ks[g], vs[g])
+            ref = _closed_form_fp8p(qv, K8[lo:], V8[lo:], T, lo, tau, 2, 16, 16)
+            np.testing.assert_allclose(got[b, h], ref, rtol=1e-12, atol=1e-13)
