@@ -30,7 +30,7 @@ FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT, FAULT_QLEN = 1, 2, 4, 
 EXPORTS = (
     "fkv_status_string", "fkv_version", "kv_quant_cache", "fp8_decode_attn_workspace_size",
     "fp8_decode_attn_num_splits", "fp8_decode_attn", "fkv_prefill_block_n", "fp8_prefill_attn",
-    "fp8_decode_attn_noalloc",
+    "fp8_decode_attn_noalloc", "fp8_decode_attn_split_blocks", "fkv_decode_block_n",
 )
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
@@ -69,6 +69,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.fp8_decode_attn_workspace_size.argtypes = [c_i32] * 7
     lib.fp8_decode_attn_num_splits.restype = c_i32
     lib.fp8_decode_attn_num_splits.argtypes = [c_i32] * 7
+    lib.fp8_decode_attn_split_blocks.restype = c_i32
+    lib.fp8_decode_attn_split_blocks.argtypes = [c_i32] * 7
+    lib.fkv_decode_block_n.restype = c_i32
+    lib.fkv_decode_block_n.argtypes = [c_i32, c_i32]
     lib.fp8_decode_attn.restype = ctypes.c_int
     lib.fp8_decode_attn.argtypes = [c_vp, c_i32, c_i32, _LayerCache, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
                                     ctypes.c_int, c_f, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_i32, c_vp,
@@ -169,6 +173,16 @@ def fp8_decode_attn_num_splits(batch, num_q_heads, num_kv_heads, head_dim, max_b
                                num_splits=0) -> int:
     return int(load_library().fp8_decode_attn_num_splits(batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
                                                           window, num_splits))
+
+
+def fp8_decode_attn_split_blocks(batch, num_q_heads, num_kv_heads, head_dim, max_blocks, window=0,
+                                 num_splits=0) -> int:
+    return int(load_library().fp8_decode_attn_split_blocks(batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
+                                                            window, num_splits))
+
+
+def fkv_decode_block_n(head_dim: int, bf16_layer: bool = False) -> int:
+    return int(load_library().fkv_decode_block_n(head_dim, int(bool(bf16_layer))))
 
 
 def decode_workspace(batch, num_q_heads, cache: LayerCache, max_blocks, window=0, num_splits=0, device="cuda"):

@@ -22,7 +22,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
-SOURCES = ["abi.cu", "kv_quant_cache.cu", "decode_attn.cu", "prefill_attn.cu", "decode_noalloc.cu"]
+SOURCES = ["abi.cu", "kv_quant_cache.cu", "decode_attn.cu", "decode_tc.cu", "prefill_attn.cu", "decode_noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -47,9 +47,12 @@ struct DecodePlan {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Split-K plan.  Blocks per split (bps) are chosen so that the whole grid holds about
-// 16 CTAs per SM when num_splits is 0, within [8, 128] blocks; a requested num_splits
-// sets bps = ceil(blocks / num_splits).  At most 1024 splits per sequence.
+// Split-K plan.  Blocks per split (bps) are multiples of 8 (whole 128-key tiles of the
+// tensor-core decode) up to 128, with at most 1024 splits per sequence.  A requested
+// num_splits sets bps = ceil(blocks / num_splits), rounded up.  Otherwise bps minimises
+// the estimated time waves * bps, where a wave is one CTA on every resident slot
+// (3 per SM) and the grid has B * Hkv * ceil(blocks / bps) CTAs: the longest split
+// sets a wave's time, and a partly filled last wave costs as much as a full one.
 bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_blocks, int32_t window,
                  int32_t num_splits, DecodePlan* plan) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks <= 0 || window < 0 || num_splits < 0) return false;
@@ -60,13 +63,22 @@ bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_bloc
     bps = (nblk_max + num_splits - 1) / num_splits;
   } else {
     const long long units = static_cast<long long>(std::max(B, 1)) * Hkv;
-    const long long target = static_cast<long long>(current_num_sms()) * 16;
-    bps = (units * nblk_max + target - 1) / target;
-    bps = std::max<long long>(bps, 8);
+    const long long slots = static_cast<long long>(current_num_sms()) * 3;
+    long long best = -1, best_cost = 0;
+    for (long long c = 8; c <= 128; c += 8) {
+      const long long ctas = units * ((nblk_max + c - 1) / c);
+      const long long cost = (ctas + slots - 1) / slots * std::min(c, nblk_max);
+      if (best < 0 || cost < best_cost || (cost == best_cost && c > best)) {
+        best = c;
+        best_cost = cost;
+      }
+    }
+    bps = best;
   }
   bps = std::min<long long>(bps, 128);
   bps = std::max<long long>(bps, (nblk_max + 1023) / 1024);
   bps = std::max<long long>(bps, 1);
+  bps = (bps + 7) / 8 * 8;
   if (bps > 128) return false;  // context too long for 1024 splits of 128 blocks
   plan->bps = static_cast<int>(bps);
   plan->max_splits = static_cast<int>((nblk_max + bps - 1) / bps);
@@ -125,6 +137,18 @@ size_t fp8_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_
   if (!supported_head_dim(head_dim)) return 0;
   if (!plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks, window, num_splits, &plan)) return 0;
   return plan.o_bytes + plan.lse_bytes + plan.cnt_bytes;
+}
+
+int32_t fp8_decode_attn_split_blocks(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t max_blocks, int32_t window,
+                                     int32_t num_splits) {
+  DecodePlan plan;
+  if (!plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks, window, num_splits, &plan)) return 0;
+  return plan.bps;
+}
+
+int32_t fkv_decode_block_n(int32_t head_dim, int32_t bf16_layer) {
+  return fkv::decode_uses_tensor_cores(head_dim, bf16_layer != 0) ? 128 : 0;
 }
 
 int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
@@ -198,7 +222,9 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads, fk
   if (cudaMemsetAsync(p.done, 0, static_cast<size_t>(batch) * cache.num_kv_heads * sizeof(int32_t),
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FKV_CUDA_ERROR;
-  return from_cuda(fkv::launch_decode(p, cache.head_dim, bf16, G, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fkv::decode_uses_tensor_cores(cache.head_dim, bf16)) return from_cuda(fkv::launch_decode_tc(p, cache.head_dim, G, s));
+  return from_cuda(fkv::launch_decode(p, cache.head_dim, bf16, G, s));
 }
 
 int32_t fkv_prefill_block_n(int32_t head_dim) { return supported_head_dim(head_dim) ? 128 : 0; }

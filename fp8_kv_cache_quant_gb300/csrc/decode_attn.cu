@@ -24,31 +24,10 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "kernels.h"
 
 namespace fkv {
-
-// Per-sequence key range in blocks; shared by the split and the merge kernels.
-struct SeqRange {
-  int T, lo, blk_begin, blk_end, nsplit;
-};
-
-FKV_DEV SeqRange seq_range(const DecodeParams& p, int b, bool report) {
-  SeqRange r;
-  int T = p.context_lens[b];
-  const int cap = p.max_blocks * 16;
-  if (T < 0 || T > cap) {
-    if (report) raise_fault(p.fault, FKV_FAULT_CONTEXT);
-    T = T < 0 ? 0 : cap;
-  }
-  r.T = T;
-  r.lo = p.window > 0 ? max(0, T - p.window) : 0;
-  r.blk_begin = r.lo >> 4;
-  r.blk_end = (T + 15) >> 4;
-  const int nb = r.blk_end - r.blk_begin;
-  r.nsplit = nb > 0 ? (nb + p.bps - 1) / p.bps : 0;
-  return r;
-}
 
 constexpr int kNW = 4;           // warps per CTA; every warp prefetches and consumes its own tiles
 constexpr int kNBUF = 2;         // tile buffers per warp (one in use, one in flight)

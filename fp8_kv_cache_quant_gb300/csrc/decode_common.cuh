@@ -1,0 +1,96 @@
+// Pieces shared by the split-K decode kernels: the per-sequence key range in pool blocks
+// and the FP32 merge of the splits' partial results.
+#pragma once
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fkv {
+
+// Keys [lo, T) of sequence b, as blocks [blk_begin, blk_end), in nsplit splits of p.bps
+// blocks.  A context longer than the block table can address is clamped (and reported).
+struct SeqRange {
+  int T, lo, blk_begin, blk_end, nsplit;
+};
+
+FKV_DEV SeqRange seq_range(const DecodeParams& p, int b, bool report) {
+  SeqRange r;
+  int T = p.context_lens[b];
+  const int cap = p.max_blocks * 16;
+  if (T < 0 || T > cap) {
+    if (report) raise_fault(p.fault, FKV_FAULT_CONTEXT);
+    T = T < 0 ? 0 : cap;
+  }
+  r.T = T;
+  r.lo = p.window > 0 ? max(0, T - p.window) : 0;
+  r.blk_begin = r.lo >> 4;
+  r.blk_end = (T + 15) >> 4;
+  const int nb = r.blk_end - r.blk_begin;
+  r.nsplit = nb > 0 ? (nb + p.bps - 1) / p.bps : 0;
+  return r;
+}
+
+// The second, FP32 level of the split-K accumulation, run by the CTA that finished the
+// last split of (sequence b, KV head g): with lse_s the base-2 log-sum-exp of split s
+// and o_s its normalised output, o = v_s * sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
+// M = max_s lse_s, written as bf16.  Every thread of the CTA calls it (it synchronises);
+// `scratch` holds at least 2 * G + G * CH floats of shared memory.
+template <int D, int G, int NT, int CH>
+FKV_DEV void merge_splits(const DecodeParams& p, int b, int g, int ns, float vs, float* scratch) {
+  float* ms_s = scratch;       // [G] max of lse
+  float* inv_s = ms_s + G;     // [G] v_s / sum of weights
+  float* w_s = inv_s + G;      // [G][CH] weights of a chunk of splits
+  const size_t row_base = (static_cast<size_t>(b) * p.Hq + g * G) * p.max_splits;
+  for (int t = threadIdx.x; t < G; t += NT) {
+    const size_t row0 = row_base + static_cast<size_t>(t) * p.max_splits;
+    float M = -INFINITY;
+    for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(p.lse_part + row0 + s2));
+    float W = 0.f;
+    if (M != -INFINITY)
+      for (int s2 = 0; s2 < ns; ++s2) {
+        const float lv = __ldcg(p.lse_part + row0 + s2);
+        W += (lv == -INFINITY) ? 0.f : ex2(lv - M);
+      }
+    ms_s[t] = M;
+    inv_s[t] = (W > 0.f) ? vs / W : 0.f;
+  }
+  constexpr int PAIRS = (G * D / 2 + NT - 1) / NT;  // output pairs per thread
+  float2 o[PAIRS];
+#pragma unroll
+  for (int k2 = 0; k2 < PAIRS; ++k2) o[k2] = make_float2(0.f, 0.f);
+  for (int c0 = 0; c0 < ns; c0 += CH) {
+    const int nc = min(CH, ns - c0);
+    __syncthreads();
+    for (int t = threadIdx.x; t < G * nc; t += NT) {
+      const int h = t / nc, j = t % nc;
+      const float lv = __ldcg(p.lse_part + row_base + static_cast<size_t>(h) * p.max_splits + c0 + j);
+      w_s[h * CH + j] = (lv == -INFINITY) ? 0.f : ex2(lv - ms_s[h]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k2 = 0; k2 < PAIRS; ++k2) {
+      const int t = threadIdx.x + k2 * NT;
+      if (t < G * D / 2) {
+        const int h = t / (D / 2), d = 2 * (t % (D / 2));
+        const float* src = p.o_part + (row_base + static_cast<size_t>(h) * p.max_splits + c0) * D + d;
+        for (int j = 0; j < nc; ++j) {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + static_cast<size_t>(j) * D));
+          const float wv = w_s[h * CH + j];
+          o[k2].x += wv * x.x;
+          o[k2].y += wv * x.y;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k2 = 0; k2 < PAIRS; ++k2) {
+    const int t = threadIdx.x + k2 * NT;
+    if (t < G * D / 2) {
+      const int h = t / (D / 2), d = 2 * (t % (D / 2));
+      const float inv = inv_s[h];
+      *reinterpret_cast<__nv_bfloat162*>(p.out + (static_cast<size_t>(b) * p.Hq + g * G + h) * D + d) =
+          __floats2bfloat162_rn(o[k2].x * inv, o[k2].y * inv);
+    }
+  }
+}
+
+}  // namespace fkv

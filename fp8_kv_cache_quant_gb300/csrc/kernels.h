@@ -58,4 +58,9 @@ cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* s
 
 cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16_layer, int G, cudaStream_t s);
 
+// e4m3 layers with head_dim 128 / 256 decode on the tensor cores (FP8 P, 128-key tiles);
+// the others on the CUDA cores (P exact).
+bool decode_uses_tensor_cores(int D, bool bf16_layer);
+cudaError_t launch_decode_tc(const DecodeParams& p, int D, int G, cudaStream_t s);
+
 }  // namespace fkv

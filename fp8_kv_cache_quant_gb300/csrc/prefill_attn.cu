@@ -34,25 +34,6 @@
 
 namespace fkv {
 
-constexpr uint64_t kPrefillWaitNs = 200000000ull;  // 200 ms per wait
-
-FKV_DEV bool wait_ns(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;  // sleep rather than spin
-    if (globaltimer_ns() - t0 > kPrefillWaitNs) return false;
-  }
-}
-
-// Warp-uniform forms: tcgen05.ld / st are warp-collective, so every lane of a warp must
-// take the same branch around them.
-FKV_DEV bool wait_warp(uint64_t* bar, uint32_t parity) {
-  const bool ok = wait_ns(bar, parity);
-  return __all_sync(0xffffffffu, ok);
-}
-FKV_DEV bool abort_warp(volatile int* flag) { return __any_sync(0xffffffffu, *flag != 0); }
-
 FKV_DEV float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -732,6 +713,8 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // 4-D map over one pool: (D bytes, 16 slots, KV heads, blocks), box (RB bytes, 16, 1, 1).
 bool make_pool_map(CUtensorMap* map, void* base, int D, int Hkv, int num_blocks, int rb) {
   EncodeTiled enc = encode_fn();
@@ -748,6 +731,8 @@ bool make_pool_map(CUtensorMap* map, void* base, int D, int Hkv, int num_blocks,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int D, bool BF, bool WIN>
 cudaError_t launch_prefill_t(const PrefillParams& p, void* kc, void* vc, cudaStream_t s) {

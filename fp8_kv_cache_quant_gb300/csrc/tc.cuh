@@ -41,6 +41,19 @@ FKV_DEV void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 FKV_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+FKV_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 FKV_DEV void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -117,6 +130,31 @@ FKV_DEV void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// ---------------------------------------------------------------- waits
+
+// Pipeline waits of the tensor-core kernels: bounded in wall-clock time (a timeout makes
+// the caller record FKV_FAULT_TIMEOUT and drain), sleeping with a suspend-time hint
+// rather than spinning.
+constexpr uint64_t kPipeWaitNs = 200000000ull;  // 200 ms per wait
+
+FKV_DEV bool wait_ns(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
+    if (globaltimer_ns() - t0 > kPipeWaitNs) return false;
+  }
+}
+
+// Warp-uniform forms: tcgen05.ld / st are warp-collective, so every lane of a warp must
+// take the same branch around them.
+FKV_DEV bool wait_warp(uint64_t* bar, uint32_t parity) {
+  const bool ok = wait_ns(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+FKV_DEV bool abort_warp(volatile int* flag) { return __any_sync(0xffffffffu, *flag != 0); }
+
+
 // ---------------------------------------------------------------- TMA
 
 FKV_DEV void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w, uint64_t* bar) {
@@ -126,6 +164,19 @@ FKV_DEV void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z,
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Prefetch one tile of a 4-D tensor map into L2 (no shared memory, no completion).
+FKV_DEV void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map), "r"(x), "r"(y),
+               "r"(z), "r"(w)
+               : "memory");
+}
+
+// Host: a 4-D TMA map over one paged pool [num_blocks][Hkv][16][row_bytes] (x = byte in
+// the row, slot, KV head, block), uint8 elements, boxes of [16][box_bytes] with the
+// 128-byte (box_bytes 128) or 64-byte (box_bytes 64) swizzle.  False when the driver
+// entry point is missing or the encoding is rejected.
+bool make_pool_map(CUtensorMap* map, void* base, int row_bytes, int Hkv, int num_blocks, int box_bytes);
 
 // Byte offset inside a swizzled tile for a linear (row-major) byte offset: 128-byte swizzle
 // XORs address bits 4..6 with bits 7..9, 64-byte swizzle bits 4..5 with bits 7..8 (tile

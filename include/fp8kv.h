@@ -127,6 +127,22 @@ int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t n
                                    int32_t num_splits);
 
 /*
+ * Pool blocks per context split of fp8_decode_attn for these sizes (a multiple of 8):
+ * split s of a sequence covers blocks [lo / 16 + s * n, lo / 16 + (s + 1) * n).  0 for
+ * invalid sizes.
+ */
+int32_t fp8_decode_attn_split_blocks(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t max_blocks, int32_t window,
+                                     int32_t num_splits);
+
+/*
+ * Keys per tile over which fp8_decode_attn rounds P to e4m3 for a layer of this head_dim
+ * (bf16_layer != 0: a skip layer), or 0 when that layer's decode keeps P exact.  Tiles
+ * start at each split's first block.
+ */
+int32_t fkv_decode_block_n(int32_t head_dim, int32_t bf16_layer);
+
+/*
  * fp8_decode_attn — one decode step of paged GQA attention for one layer.
  *
  * For every sequence b and query head h (KV head g = h / G): keys j in
@@ -135,10 +151,16 @@ int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t n
  *   s_j = (e4m3(q*1/q_s) * q_s) . (k8_j * k_s[g]) * softmax_scale,
  *   out = sum_j softmax(s)_j * (v8_j * v_s[g])     (bf16 [batch][num_q_heads][head_dim]).
  * The context is split across CTAs (split-K, the blog's decode-tuned configurations);
- * each split keeps its softmax state and P.V sum in FP32 registers and a second kernel
- * merges the splits through their log-sum-exp in FP32 — the two-level accumulation of
- * the blog's "Two-level accumulation" paragraph, so a 100k+ key contraction is summed
- * in true FP32.  Skip layers read a bf16 pool and quantise nothing.
+ * each split keeps its softmax state and P.V sum in FP32, and the CTA that finishes a
+ * (sequence, KV head) last merges the splits through their log-sum-exp in FP32 — the
+ * two-level accumulation of the blog's "Two-level accumulation" paragraph, so a 100k+
+ * key contraction is summed in true FP32.
+ * e4m3 layers with head_dim 128 or 256 run on the tensor cores, FP8 QK and Score*V as in
+ * the blog's FP8 attention: S^T = K8 Q8^T and O^T = V8^T P8^T per 128-key tile with
+ * P8 = e4m3(p * 448) relative to the split's running maximum, the denominator summing
+ * the unrounded p, and each tile's partial promoted into FP32 registers.  Other e4m3
+ * layers (head_dim 64) run on the CUDA cores with P exact.  Skip layers read a bf16
+ * pool, quantise nothing and keep P exact.  fkv_decode_block_n tells which applies.
  *
  *   q             device bf16 [batch][num_q_heads][head_dim]
  *   block_table   device int32 [batch][max_blocks]
@@ -149,7 +171,8 @@ int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t n
  *   out           device bf16 [batch][num_q_heads][head_dim]
  *   workspace     device, >= fp8_decode_attn_workspace_size(...) bytes, 256-byte aligned;
  *                 scratch only (no state is kept across calls)
- *   num_splits    0 = automatic, else the requested number of context splits
+ *   num_splits    0 = automatic, else the requested number of context splits (each split
+ *                 is then rounded up to whole multiples of 8 blocks, so fewer may result)
  * head_dim in {64, 128, 256}; G = num_q_heads / num_kv_heads in {1, 2, 4, 8, 16} with
  * G * head_dim <= 2048.  A sequence with no key gets a zero row.
  */

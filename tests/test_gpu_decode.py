@@ -1,7 +1,9 @@
 """fp8_decode_attn (split-K paged decode + FP32 merge) on the GPU against the oracle.
 
 Tolerance: max-abs 2e-2 and relative L2 1e-2 of the oracle's float64 FP8-emulated
-result.  Small cases cover every head_dim, several GQA group sizes, both scale
+result.  Where the library rounds P (the tensor-core decode: fkv_decode_block_n > 0),
+the oracle walks the same splits and tiles with P rounded (reading R23); elsewhere P is
+exact and the oracle is the plain softmax.  Small cases cover every head_dim, several GQA group sizes, both scale
 granularities, the bf16 skip-layer path, windows, ragged and empty contexts and forced
 split counts; the full-size workloads are checked on sampled sequences and heads in the
 launch configuration the benchmark times.
@@ -18,6 +20,15 @@ from oracle import attention, e4m3, kvcache
 
 f = pytest.importorskip("fp8_kv_cache_quant_gb300")
 pytestmark = pytest.mark.gpu
+
+
+def _oracle_mode(D, bf16_layer, batch, Hq, Hkv, max_blocks, window, num_splits):
+    """Keyword arguments of the oracle's decode matching the library's kernel choice."""
+    bn = f.fkv_decode_block_n(D, bf16_layer)
+    if bn == 0:
+        return {}
+    bps = f.fp8_decode_attn_split_blocks(batch, Hq, Hkv, D, max_blocks, window, num_splits)
+    return dict(p_quant=True, split_blocks=bps, block_n=bn)
 
 
 def _inputs(rng, ctx, Hq, Hkv, D, scale_k=3.0):
@@ -63,16 +74,18 @@ def test_decode_small_parity(D, G, bf16_layer, gran, window, splits):
     out = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(qs), to_dev(ks), to_dev(vs),
                             gran, window=window, skip_layer_mask=mask, num_splits=splits)
     kp, vp = oracle_pools(kvcache, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), bf16_layer)
+    mode = _oracle_mode(D, bf16_layer, len(ctx), Hq, Hkv, table.shape[1], window, splits)
     ref = attention.decode_attention(synth.bf16_to_f64(q), kp, vp, table, ctx, qs.numpy(), ks.numpy(), vs.numpy(),
-                                     fp8=not bf16_layer, window=window)
+                                     fp8=not bf16_layer, window=window, **mode)
     got = out.float().cpu().numpy()
     assert np.all(got[6] == 0), "empty context must give a zero row"
     assert_close(got, ref, what=f"D={D} G={G} bf16={bf16_layer} gran={gran} W={window} splits={splits}")
 
 
-def test_split_count_invariance_and_permutation():
+@pytest.mark.parametrize("D", [128, 64])
+def test_split_count_invariance_and_permutation(D):
     rng = np.random.default_rng(3)
-    Hq, Hkv, D = 32, 8, 128
+    Hq, Hkv = 32, 8
     ctx = np.array([2000, 777, 4096], np.int32)
     table, nb = synth.block_table(ctx, seed=5)
     q, k, v = _inputs(rng, ctx, Hq, Hkv, D)
@@ -83,12 +96,21 @@ def test_split_count_invariance_and_permutation():
         outs[s] = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(one), to_dev(one),
                                     to_dev(one), 0, num_splits=s).float().cpu().numpy()
     assert np.all(np.isfinite(outs[1]))
-    # different split counts group the keys differently; the per-tile f16 P.V partials
-    # then round differently, at about 1e-3 of the output's scale
-    scale = float(np.max(np.abs(outs[1])))
-    for s in (2, 7, 0):
-        np.testing.assert_allclose(outs[s], outs[1], rtol=2.0 ** -7, atol=2e-3 * scale)
-        assert np.linalg.norm(outs[s] - outs[1]) <= 2e-3 * np.linalg.norm(outs[1])
+    if f.fkv_decode_block_n(D) > 0:
+        # P rounded per split and tile: each split count against the oracle walking the
+        # same splits (their P codes differ by design)
+        kp, vp = oracle_pools(kvcache, ctx, table, nb, k, v, one, one, False)
+        for s, o in outs.items():
+            mode = _oracle_mode(D, False, len(ctx), Hq, Hkv, table.shape[1], 0, s)
+            ref = attention.decode_attention(synth.bf16_to_f64(q), kp, vp, table, ctx, one, one, one, **mode)
+            assert_close(o, ref, what=f"num_splits={s}")
+    else:
+        # exact P: different split counts group the keys differently; the per-tile f16
+        # P.V partials then round differently, at about 1e-3 of the output's scale
+        scale = float(np.max(np.abs(outs[1])))
+        for s in (2, 7, 0):
+            np.testing.assert_allclose(outs[s], outs[1], rtol=2.0 ** -7, atol=2e-3 * scale)
+            assert np.linalg.norm(outs[s] - outs[1]) <= 2e-3 * np.linalg.norm(outs[1])
     # the same data under another physical block permutation: bit-identical output
     table2, nb2 = synth.block_table(ctx, seed=99, extra_blocks=3)
     cache2 = build_layer(f, ctx, table2, nb2, k, v, one, one, 0, False, sentinel=0x7F)
@@ -111,20 +133,22 @@ def _decode_layer_check(w, layer, ctx, table, nb, seqs, heads, num_splits=0):
                             num_splits=num_splits).float().cpu().numpy()
     cu = np.concatenate([[0], np.cumsum(ctx)])
     qs, ks, vs = (x.cpu().numpy() for x in (data.q_scale, data.k_scale, data.v_scale))
+    mode = _oracle_mode(w.head_dim, bf16_layer, w.batch, w.num_q_heads, w.num_kv_heads, table.shape[1], window,
+                        num_splits)
     got, ref = [], []
     G = w.group
     for b in seqs:
         T = int(ctx[b])
-        lo = max(0, T - window) if window else 0
         for g in sorted(set(h // G for h in heads)):
             hs = [h for h in heads if h // G == g]
-            kb = synth.bf16_to_f64(data.k[cu[b] + lo:cu[b] + T, g:g + 1])
-            vb = synth.bf16_to_f64(data.v[cu[b] + lo:cu[b] + T, g:g + 1])
+            # the whole context at its absolute positions (the window is cut by the oracle)
+            kb = synth.bf16_to_f64(data.k[cu[b]:cu[b] + T, g:g + 1])
+            vb = synth.bf16_to_f64(data.v[cu[b]:cu[b] + T, g:g + 1])
             qb = synth.bf16_to_f64(data.q[b, g * G:(g + 1) * G])
             sel = lambda a, idx: a if a.size == 1 else a[idx]
             res = attention.decode_attention_contiguous(
                 qb, kb, vb, sel(qs, slice(g * G, (g + 1) * G)), sel(ks, slice(g, g + 1)), sel(vs, slice(g, g + 1)),
-                fp8=not bf16_layer, heads=[h - g * G for h in hs])
+                fp8=not bf16_layer, window=window, heads=[h - g * G for h in hs], **mode)
             for h in hs:
                 got.append(out[b, h])
                 ref.append(res[h - g * G])
