@@ -204,7 +204,7 @@ class DecodeState:
                               workspace=self.ws)
 
     def launches_per_step(self):
-        # kv_quant_cache and decode_split_kernel per layer (the split-counter reset is a memset node)
+        # kv_quant_cache and the decode kernel per layer (the split-counter reset is a memset node)
         return 2 * len(self.layers)
 
     def step_bytes(self):
@@ -598,7 +598,13 @@ def run_ours(args):
     dec_launch_ms = ms_dec / w.num_layers
     peak, peak_kind = _peaks()
     achieved = dec_bytes / (dec_launch_ms * 1e-3) / 1e9
-    traffic = _traffic_record("decode_attn.cu", "decode_attn_llama8b_decode.txt")
+    # the decode kernel this workload's e4m3 layers run: tensor cores (head_dim 128 / 256) or CUDA cores
+    if f.fkv_decode_block_n(w.head_dim) > 0:
+        dec_kernel = "decode_tc_kernel (fp8_decode_attn on tcgen05, merge fused)"
+        traffic = _traffic_record("decode_tc.cu", "decode_tc_llama8b_decode.txt")
+    else:
+        dec_kernel = "decode_split_kernel (fp8_decode_attn on CUDA cores, merge fused)"
+        traffic = _traffic_record("decode_attn.cu", "decode_attn_llama8b_decode.txt")
 
     # the same step with a bf16 cache (all layers), for the FP8-vs-BF16 per-token cost
     bf16_info = None
@@ -645,7 +651,7 @@ def run_ours(args):
                        "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
             "us_per_step": ms_fp8 * 1e3,
             "pct_of_hbm_peak": value / peak,
-            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel (fp8_decode_attn, merge fused)",
+            "roofline": {"bound": "hbm", "kernel": dec_kernel,
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
                          "algorithmic_bytes_per_launch": dec_bytes, "launch_ms": dec_launch_ms},
