@@ -49,6 +49,20 @@ def cache_write(k, v, slots, k_pool, v_pool, k_scale, v_scale, *, skip: bool, bl
     return k_pool, v_pool
 
 
+def clip_count(x, scale) -> int:
+    """Number of elements whose scaled value fl32(x * fl32(1/scale)) lies beyond the e4m3
+    range, |y| > 448, and is therefore clipped to +-448 by the saturating encode — the
+    clipping frequency the KV-cache quantisation explainer asks to watch when it can be
+    observed ("本番投入前の比較" checklist).  NaN is not counted.  ``x``: float64 [n][H][D]
+    (bf16 values); ``scale``: one value or one per head (axis 1)."""
+    x = np.asarray(x, dtype=np.float64)
+    s = np.asarray(scale, dtype=np.float32).reshape(-1)
+    inv = e4m3.reciprocal_f32(s if s.size == 1 else s.reshape(1, -1, 1))
+    y = e4m3.fl32(x * inv)
+    with np.errstate(invalid="ignore"):
+        return int(np.count_nonzero(np.abs(y) > 448.0))
+
+
 def kv_bytes_formula(num_layers, num_kv_heads, head_dim, tokens, batch, elem_bytes) -> int:
     """M_KV = 2 * L * H_KV * D * T * B * S (vLLM-independent explainer "KV Cache量子化とは？",
     section "weight量子化とは別の場所を小さくする", the KV memory formula)."""

@@ -82,6 +82,24 @@ def test_decode_small_parity(D, G, bf16_layer, gran, window, splits):
     assert_close(got, ref, what=f"D={D} G={G} bf16={bf16_layer} gran={gran} W={window} splits={splits}")
 
 
+@pytest.mark.parametrize("Hkv,G,D", [(3, 2, 64), (1, 8, 64), (5, 4, 64), (3, 4, 128)])
+def test_decode_odd_kv_head_counts(Hkv, G, D):
+    """Odd KV head counts and a single KV head, on both decode kernels."""
+    rng = np.random.default_rng(Hkv * 10 + G)
+    Hq = Hkv * G
+    ctx = np.array([300, 1, 1000, 129], np.int32)
+    table, nb = synth.block_table(ctx, seed=7, extra_blocks=2)
+    q, k, v = _inputs(rng, ctx, Hq, Hkv, D)
+    qs, ks, vs = synth.amax_scales(q, 1), synth.amax_scales(k, 1), synth.amax_scales(v, 1)
+    cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), 1, False, sentinel=0xFF)
+    out = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(qs), to_dev(ks), to_dev(vs), 1)
+    kp, vp = oracle_pools(kvcache, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), False)
+    mode = _oracle_mode(D, False, len(ctx), Hq, Hkv, table.shape[1], 0, 0)
+    ref = attention.decode_attention(synth.bf16_to_f64(q), kp, vp, table, ctx, qs.numpy(), ks.numpy(), vs.numpy(),
+                                     **mode)
+    assert_close(out.float().cpu().numpy(), ref, what=f"Hkv={Hkv} G={G} D={D}")
+
+
 @pytest.mark.parametrize("D", [128, 64])
 def test_split_count_invariance_and_permutation(D):
     rng = np.random.default_rng(3)

@@ -56,3 +56,36 @@ def test_memory_formula_matches_pool_bytes():
     tok = int(np.sum(ctx))
     exact = 2 * H * D * tok
     assert 0 <= pool_bytes_one_layer_fp8 - exact < 2 * H * D * 16 * len(ctx)
+
+
+def test_clip_count_hand_values():
+    """Scale 1: 448 is representable (kept); 450, -450, +-inf are clipped; NaN is not a
+    clip.  Scale 0.5 doubles the values: 224 -> 448 (kept), 226 -> 452 (clipped)."""
+    x = np.array([448.0, 450.0, -450.0, 416.0, np.inf, -np.inf, np.nan, 0.0]).reshape(1, 1, -1)
+    assert kvcache.clip_count(x, np.float32(1.0)) == 4
+    y = np.array([224.0, 226.0, -226.0, 100.0]).reshape(1, 1, -1)
+    assert kvcache.clip_count(y, np.float32(0.5)) == 2
+    # one scale per head (axis 1): head 0 at scale 1 keeps 300, head 1 at scale 0.5 clips it
+    z = np.array([[[300.0, 10.0], [300.0, 10.0]]])
+    assert kvcache.clip_count(z, np.array([1.0, 0.5], np.float32)) == 1
+
+
+def test_clip_count_matches_float32_arithmetic_and_the_codec():
+    """Brute force with numpy float32 arithmetic (IEEE single multiply by the single
+    reciprocal), element by element; every clipped element encodes to +-448."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((7, 3, 16)) * 120.0
+    x[0, 1, 3] = 2000.0
+    x[4, 2, 0] = -7000.0
+    x = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).float().numpy().astype(np.float64)
+    s = np.array([0.75, 0.3, 1.25], np.float32)
+    n = 0
+    for idx in np.ndindex(*x.shape):
+        inv = np.float32(1.0) / s[idx[1]]
+        yv = np.float32(x[idx]) * inv
+        if abs(float(yv)) > 448.0:
+            n += 1
+            code = int(e4m3.quantize(np.array([x[idx]]), s[idx[1]])[0])
+            assert code in (0x7E, 0xFE)
+    assert n > 2
+    assert kvcache.clip_count(x, s) == n
