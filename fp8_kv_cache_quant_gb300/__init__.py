@@ -30,7 +30,7 @@ FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT, FAULT_QLEN = 1, 2, 4, 
 EXPORTS = (
     "fkv_status_string", "fkv_version", "kv_quant_cache", "fp8_decode_attn_workspace_size",
     "fp8_decode_attn_num_splits", "fp8_decode_attn", "fkv_prefill_block_n", "fp8_prefill_attn",
-    "fp8_decode_attn_noalloc", "fp8_decode_attn_split_blocks", "fkv_decode_block_n",
+    "fp8_decode_attn_noalloc", "fp8_decode_attn_split_blocks", "fkv_decode_block_n", "kv_quant_cache_clips",
 )
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
@@ -65,6 +65,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kv_quant_cache.restype = ctypes.c_int
     lib.kv_quant_cache.argtypes = [c_vp, c_vp, c_vp, c_i32, _LayerCache, c_vp, c_vp, ctypes.c_int, c_i32, c_vp,
                                    c_i32, c_vp, c_vp]
+    lib.kv_quant_cache_clips.restype = ctypes.c_int
+    lib.kv_quant_cache_clips.argtypes = [c_vp, c_vp, c_vp, c_i32, _LayerCache, c_vp, c_vp, ctypes.c_int, c_i32, c_vp,
+                                         c_i32, c_vp, c_vp, c_vp]
     lib.fp8_decode_attn_workspace_size.restype = c_sz
     lib.fp8_decode_attn_workspace_size.argtypes = [c_i32] * 7
     lib.fp8_decode_attn_num_splits.restype = c_i32
@@ -161,6 +164,22 @@ def kv_quant_cache(k, v, slot_mapping, cache: LayerCache, k_scale=None, v_scale=
                             _ptr(v_scale), int(gran), int(layer), mp, nl, _ptr(fault), _stream(stream))
     del keep
     _check("kv_quant_cache", st)
+
+
+def kv_quant_cache_clips(k, v, slot_mapping, cache: LayerCache, k_scale, v_scale, gran=SCALE_PER_TENSOR,
+                         clip_counts=None, layer=0, skip_layer_mask=None, fault=None, stream=None):
+    """kv_quant_cache that also adds the numbers of clipped K and V elements to
+    ``clip_counts`` (device int64 [2], created zeroed when None); returns it."""
+    lib = load_library()
+    if clip_counts is None:
+        clip_counts = torch.zeros(2, dtype=torch.int64, device=k.device)
+    mp, nl, keep = _mask_arg(skip_layer_mask)
+    st = lib.kv_quant_cache_clips(_ptr(k), _ptr(v), _ptr(slot_mapping), int(k.shape[0]), cache.c(), _ptr(k_scale),
+                                  _ptr(v_scale), int(gran), int(layer), mp, nl, _ptr(clip_counts), _ptr(fault),
+                                  _stream(stream))
+    del keep
+    _check("kv_quant_cache_clips", st)
+    return clip_counts
 
 
 def fp8_decode_attn_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_blocks, window=0,

@@ -91,6 +91,29 @@ bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_bloc
 
 fkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FKV_OK : FKV_CUDA_ERROR; }
 
+fkv_status cache_write(const void* k, const void* v, const int64_t* slot_mapping, int32_t n_tokens,
+                       fkv_layer_cache cache, const float* k_scale, const float* v_scale, fkv_scale_gran gran,
+                       int32_t layer, const uint8_t* skip_layer_mask, int32_t num_layers, int32_t* fault,
+                       fkv_stream_t stream, unsigned long long* clips) {
+  if (n_tokens < 0) return FKV_INVALID_ARG;
+  if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
+  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0) return FKV_INVALID_ARG;
+  if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
+  if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
+  fkv_status st = FKV_OK;
+  const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
+  if (st != FKV_OK) return st;
+  if (n_tokens == 0) return FKV_OK;
+  if (!k || !v || !slot_mapping || !cache.k_cache || !cache.v_cache) return FKV_INVALID_ARG;
+  if (!bf16 && (!k_scale || !v_scale)) return FKV_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache.k_cache, 16) || !aligned(cache.v_cache, 16) ||
+      !aligned(slot_mapping, 8) || !aligned(clips, 8))
+    return FKV_INVALID_ARG;
+  return from_cuda(fkv::launch_kv_quant_cache(k, v, slot_mapping, n_tokens, cache, k_scale, v_scale,
+                                              gran == FKV_SCALE_PER_HEAD, bf16, fault,
+                                              reinterpret_cast<cudaStream_t>(stream), current_num_sms(), clips));
+}
+
 }  // namespace
 
 extern "C" {
@@ -105,29 +128,25 @@ const char* fkv_status_string(fkv_status status) {
   return "unknown status";
 }
 
-int32_t fkv_version(void) { return 100; }
+int32_t fkv_version(void) { return 101; }
+
 
 fkv_status kv_quant_cache(const void* k, const void* v, const int64_t* slot_mapping, int32_t n_tokens,
                           fkv_layer_cache cache, const float* k_scale, const float* v_scale,
                           fkv_scale_gran gran, int32_t layer, const uint8_t* skip_layer_mask,
                           int32_t num_layers, int32_t* fault, fkv_stream_t stream) {
-  if (n_tokens < 0) return FKV_INVALID_ARG;
-  if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
-  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0) return FKV_INVALID_ARG;
-  if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
-  if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
-  fkv_status st = FKV_OK;
-  const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
-  if (st != FKV_OK) return st;
-  if (n_tokens == 0) return FKV_OK;
-  if (!k || !v || !slot_mapping || !cache.k_cache || !cache.v_cache) return FKV_INVALID_ARG;
-  if (!bf16 && (!k_scale || !v_scale)) return FKV_INVALID_ARG;
-  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache.k_cache, 16) || !aligned(cache.v_cache, 16) ||
-      !aligned(slot_mapping, 8))
-    return FKV_INVALID_ARG;
-  return from_cuda(fkv::launch_kv_quant_cache(k, v, slot_mapping, n_tokens, cache, k_scale, v_scale,
-                                              gran == FKV_SCALE_PER_HEAD, bf16, fault,
-                                              reinterpret_cast<cudaStream_t>(stream), current_num_sms()));
+  return cache_write(k, v, slot_mapping, n_tokens, cache, k_scale, v_scale, gran, layer, skip_layer_mask, num_layers,
+                     fault, stream, nullptr);
+}
+
+fkv_status kv_quant_cache_clips(const void* k, const void* v, const int64_t* slot_mapping, int32_t n_tokens,
+                                fkv_layer_cache cache, const float* k_scale, const float* v_scale,
+                                fkv_scale_gran gran, int32_t layer, const uint8_t* skip_layer_mask,
+                                int32_t num_layers, unsigned long long* clip_counts, int32_t* fault,
+                                fkv_stream_t stream) {
+  if (clip_counts == nullptr) return FKV_INVALID_ARG;
+  return cache_write(k, v, slot_mapping, n_tokens, cache, k_scale, v_scale, gran, layer, skip_layer_mask, num_layers,
+                     fault, stream, clip_counts);
 }
 
 size_t fp8_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,

@@ -54,7 +54,7 @@ cudaError_t launch_prefill(const PrefillParams& p, int D, bool bf16_layer, void*
 cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* slots, int n_tokens,
                                   const fkv_layer_cache& cache, const float* ks, const float* vs,
                                   int per_head, bool bf16_layer, int32_t* fault, cudaStream_t s,
-                                  int num_sms);
+                                  int num_sms, unsigned long long* clips);
 
 cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16_layer, int G, cudaStream_t s);
 

@@ -114,6 +114,23 @@ fkv_status kv_quant_cache(const void* k, const void* v, const int64_t* slot_mapp
                           int32_t* fault, fkv_stream_t stream);
 
 /*
+ * kv_quant_cache_clips — kv_quant_cache that also counts clipped elements.
+ *
+ * The KV-cache quantisation explainer's pre-production checklist asks for the clipping
+ * frequency where it can be observed.  Same write as kv_quant_cache; in addition
+ * clip_counts[0] and clip_counts[1] (device uint64, accumulated atomically; the caller
+ * zeroes them) grow by the number of K and V elements whose scaled value
+ * fl32(x * fl32(1/scale)) lies beyond +-448 and is therefore clipped (NaN is not
+ * counted; skip layers clip nothing).  clip_counts NULL or not 8-byte aligned:
+ * FKV_INVALID_ARG.
+ */
+fkv_status kv_quant_cache_clips(const void* k, const void* v, const int64_t* slot_mapping,
+                                int32_t n_tokens, fkv_layer_cache cache, const float* k_scale,
+                                const float* v_scale, fkv_scale_gran gran, int32_t layer,
+                                const uint8_t* skip_layer_mask, int32_t num_layers,
+                                unsigned long long* clip_counts, int32_t* fault, fkv_stream_t stream);
+
+/*
  * Workspace bytes fp8_decode_attn needs for these sizes (same argument meaning as
  * there).  Returns 0 for invalid sizes.
  */

@@ -83,6 +83,15 @@ def test_kv_quant_cache_validation(lib):
     assert st(one, one, one, 0, _cache(), one, one, 0, 0, None, 0, None, None) == f.OK   # nothing to do
 
 
+def test_kv_quant_cache_clips_validation(lib):
+    st = lib.kv_quant_cache_clips
+    one = 1 << 12
+    assert st(one, one, one, 4, _cache(), one, one, 0, 0, None, 0, None, None, None) == f.INVALID_ARG   # no counters
+    assert st(one, one, one, 4, _cache(), one, one, 0, 0, None, 0, one + 4, None, None) == f.INVALID_ARG  # misaligned
+    assert st(one, one, one, 0, _cache(), one, one, 0, 0, None, 0, one, None, None) == f.OK
+    assert st(one, one, one, 4, _cache(D=96), one, one, 0, 0, None, 0, one, None, None) == f.UNSUPPORTED
+
+
 def test_decode_validation(lib):
     d = lib.fp8_decode_attn
     p = 1 << 12

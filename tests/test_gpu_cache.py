@@ -119,3 +119,48 @@ def test_prefill_workload_fill_sampled_blocks():
             got_v = cache.v_cache[pb, 0].cpu().numpy()
             assert np.array_equal(got_k, e4m3.quantize(kx[:, 0], ks[0]))
             assert np.array_equal(got_v, e4m3.quantize(vx[:, 0], vs[0]))
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.0371])
+def test_clip_counts_every_bf16_pattern(scale):
+    """The counting cache write over every bf16 bit pattern: the counts equal the oracle's
+    (integers, exact) and the cache bytes equal those of the plain write."""
+    k = _all_bf16_patterns()
+    v = k.flip(0).contiguous()
+    n, H, D = k.shape
+    s = torch.tensor([scale], dtype=torch.float32, device="cuda")
+    slots = torch.arange(n, dtype=torch.int64, device="cuda")
+    plain = f.LayerCache.empty(n // 16, H, D)
+    f.kv_quant_cache(k.cuda(), v.cuda(), slots, plain, s, s, f.SCALE_PER_TENSOR)
+    counted = f.LayerCache.empty(n // 16, H, D)
+    counts = f.kv_quant_cache_clips(k.cuda(), v.cuda(), slots, counted, s, s, f.SCALE_PER_TENSOR)
+    torch.cuda.synchronize()
+    assert torch.equal(plain.k_cache, counted.k_cache) and torch.equal(plain.v_cache, counted.v_cache)
+    got = counts.cpu().tolist()
+    ref = [kvcache.clip_count(synth.bf16_to_f64(k), np.float32(scale)),
+           kvcache.clip_count(synth.bf16_to_f64(v), np.float32(scale))]
+    assert got == ref and ref[0] > 0
+
+
+def test_clip_counts_per_head_accumulate_and_skip_layers():
+    """Per-head scales with planted outliers; two calls accumulate; a skip layer clips nothing."""
+    rng = np.random.default_rng(12)
+    n, H, D = 300, 4, 128
+    k = torch.from_numpy((rng.standard_normal((n, H, D)) * 40).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy((rng.standard_normal((n, H, D)) * 40).astype(np.float32)).to(torch.bfloat16)
+    k[5, 1, 7] = 30000.0
+    v[77, 3, 0] = -9000.0
+    ks = np.array([0.2, 0.5, 0.1, 1.0], np.float32)
+    vs = np.array([0.3, 0.05, 0.25, 0.5], np.float32)
+    ctx = np.array([n], np.int32)
+    table, nb = synth.block_table(ctx, seed=2)
+    slots = to_dev(synth.slot_mapping(table, ctx))
+    cache = f.LayerCache.empty(nb, H, D)
+    counts = f.kv_quant_cache_clips(k.cuda(), v.cuda(), slots, cache, to_dev(ks), to_dev(vs), f.SCALE_PER_HEAD)
+    counts = f.kv_quant_cache_clips(k.cuda(), v.cuda(), slots, cache, to_dev(ks), to_dev(vs), f.SCALE_PER_HEAD,
+                                    clip_counts=counts)
+    ref = [kvcache.clip_count(synth.bf16_to_f64(k), ks), kvcache.clip_count(synth.bf16_to_f64(v), vs)]
+    assert counts.cpu().tolist() == [2 * ref[0], 2 * ref[1]] and ref[0] > 1 and ref[1] > 1
+    bf = f.LayerCache.empty(nb, H, D, bf16=True)
+    c2 = f.kv_quant_cache_clips(k.cuda(), v.cuda(), slots, bf, None, None, f.SCALE_PER_TENSOR, skip_layer_mask=[1])
+    assert c2.cpu().tolist() == [0, 0]
