@@ -21,6 +21,8 @@ Readings where the pages are silent (each is exercised by the tests):
   R11 prefill rounds P to e4m3 as e4m3(p * 448) and divides by 448 again;
   R13 prefill query i of a sequence with context T and Lq queries sits at absolute
       position T - Lq + i (the chunk is the tail of the context);
+  R25 an e5m2 layer stores K and V as e5m2 codes (scales as for e4m3) and attends with
+      the bf16 query and exact P: the codes are dequantised, nothing else is rounded;
   R23 a split-K decode with FP8 P splits the key range [lo, T) into runs of
       ``split_blocks`` pool blocks starting at block lo // block_size; each split walks
       its keys in tiles of ``block_n`` starting at its first block, with its own running
@@ -38,7 +40,7 @@ import math
 
 import numpy as np
 
-from . import e4m3
+from . import e4m3, e5m2
 from .kvcache import head_scale
 
 
@@ -48,9 +50,9 @@ def _gather(pool, table_row, positions, g, block_size):
     return pool[blk, g, off, :]
 
 
-def _dequant_rows(rows, scale, fp8: bool):
+def _dequant_rows(rows, scale, fp8: bool, fmt: str = "e4m3"):
     if fp8:
-        return e4m3.decode(rows) * scale
+        return (e5m2 if fmt == "e5m2" else e4m3).decode(rows) * scale
     return np.asarray(rows, dtype=np.float64)
 
 
@@ -91,7 +93,7 @@ def split_decode(qv, K, V, T, lo, tau, *, split_blocks, block_n, p_quant, block_
 
 def decode_attention(q, k_pool, v_pool, block_table, context_lens, q_scale, k_scale, v_scale, *,
                      fp8: bool = True, softmax_scale: float = 0.0, window: int = 0, block_size: int = 16,
-                     p_quant: bool = False, split_blocks: int = 0, block_n: int = 128):
+                     p_quant: bool = False, split_blocks: int = 0, block_n: int = 128, fmt: str = "e4m3"):
     """Paged decode attention, one query per sequence.
 
     q: float64 [B][Hq][D] (bf16 values).  k_pool / v_pool: uint8 e4m3 codes
@@ -99,7 +101,8 @@ def decode_attention(q, k_pool, v_pool, block_table, context_lens, q_scale, k_sc
     context_lens[b] counts every key of sequence b, the current token included.
     Returns float64 [B][Hq][D]; a sequence with no key gives a zero row.
     ``split_blocks`` > 0 computes it as the split-K decode of R23 (``p_quant`` rounds P,
-    on e4m3 layers only); 0 is the plain softmax.
+    on e4m3 layers only); 0 is the plain softmax.  ``fmt`` "e5m2" reads e5m2 pools with
+    the bf16 query and exact P (R25).
     """
     q = np.asarray(q, dtype=np.float64)
     B, Hq, D = q.shape
@@ -114,17 +117,17 @@ def decode_attention(q, k_pool, v_pool, block_table, context_lens, q_scale, k_sc
             continue
         pos = np.arange(lo, T, dtype=np.int64)
         for g in range(Hkv):
-            K = _dequant_rows(_gather(k_pool, block_table[b], pos, g, block_size), head_scale(k_scale, g), fp8)
-            V = _dequant_rows(_gather(v_pool, block_table[b], pos, g, block_size), head_scale(v_scale, g), fp8)
+            K = _dequant_rows(_gather(k_pool, block_table[b], pos, g, block_size), head_scale(k_scale, g), fp8, fmt)
+            V = _dequant_rows(_gather(v_pool, block_table[b], pos, g, block_size), head_scale(v_scale, g), fp8, fmt)
             for h in range(g * G, (g + 1) * G):
-                if fp8:
+                if fp8 and fmt == "e4m3":
                     qs = head_scale(q_scale, h)
                     qv = e4m3.decode(e4m3.quantize(q[b, h], qs)) * qs
                 else:
                     qv = q[b, h]
                 if split_blocks > 0:
                     out[b, h] = split_decode(qv, K, V, T, lo, tau, split_blocks=split_blocks, block_n=block_n,
-                                             p_quant=p_quant and fp8, block_size=block_size)
+                                             p_quant=p_quant and fp8 and fmt == "e4m3", block_size=block_size)
                 else:
                     out[b, h], _ = softmax_attend(qv, K, V, tau)
     return out

@@ -15,7 +15,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import e4m3
+from . import e4m3, e5m2
 
 
 def head_scale(scale, h: int) -> float:
@@ -24,14 +24,17 @@ def head_scale(scale, h: int) -> float:
     return float(s[0] if s.size == 1 else s[h])
 
 
-def cache_write(k, v, slots, k_pool, v_pool, k_scale, v_scale, *, skip: bool, block_size: int = 16):
+def cache_write(k, v, slots, k_pool, v_pool, k_scale, v_scale, *, skip: bool, block_size: int = 16,
+                fmt: str = "e4m3"):
     """Write tokens into the pools in place.
 
     k, v: float64 [n][H_kv][D] holding bf16 values (or, for ``skip``, uint16 bf16
     bit patterns may be passed instead).  k_pool / v_pool: uint8 codes
-    ``[nb][H_kv][bs][D]`` (e4m3 layer) or uint16 bf16 bits (skip layer).
-    Every byte not addressed by a non-negative slot keeps its prior value.
+    ``[nb][H_kv][bs][D]`` (an FP8 layer, format ``fmt``: "e4m3" or "e5m2") or uint16
+    bf16 bits (skip layer).  Every byte not addressed by a non-negative slot keeps its
+    prior value.
     """
+    codec = {"e4m3": e4m3, "e5m2": e5m2}[fmt]
     slots = np.asarray(slots, dtype=np.int64)
     n, H, D = np.shape(k)
     for t in range(n):
@@ -44,23 +47,23 @@ def cache_write(k, v, slots, k_pool, v_pool, k_scale, v_scale, *, skip: bool, bl
                 k_pool[blk, h, off, :] = k[t, h]
                 v_pool[blk, h, off, :] = v[t, h]
             else:
-                k_pool[blk, h, off, :] = e4m3.quantize(k[t, h], head_scale(k_scale, h))
-                v_pool[blk, h, off, :] = e4m3.quantize(v[t, h], head_scale(v_scale, h))
+                k_pool[blk, h, off, :] = codec.quantize(k[t, h], head_scale(k_scale, h))
+                v_pool[blk, h, off, :] = codec.quantize(v[t, h], head_scale(v_scale, h))
     return k_pool, v_pool
 
 
-def clip_count(x, scale) -> int:
-    """Number of elements whose scaled value fl32(x * fl32(1/scale)) lies beyond the e4m3
-    range, |y| > 448, and is therefore clipped to +-448 by the saturating encode — the
-    clipping frequency the KV-cache quantisation explainer asks to watch when it can be
-    observed ("本番投入前の比較" checklist).  NaN is not counted.  ``x``: float64 [n][H][D]
-    (bf16 values); ``scale``: one value or one per head (axis 1)."""
+def clip_count(x, scale, limit: float = e4m3.E4M3_MAX) -> int:
+    """Number of elements whose scaled value fl32(x * fl32(1/scale)) lies beyond the FP8
+    range, |y| > limit (448 for e4m3, 57344 for e5m2), and is therefore clipped by the
+    saturating encode — the clipping frequency the KV-cache quantisation explainer asks
+    to watch when it can be observed ("本番投入前の比較" checklist).  NaN is not counted.
+    ``x``: float64 [n][H][D] (bf16 values); ``scale``: one value or one per head (axis 1)."""
     x = np.asarray(x, dtype=np.float64)
     s = np.asarray(scale, dtype=np.float32).reshape(-1)
     inv = e4m3.reciprocal_f32(s if s.size == 1 else s.reshape(1, -1, 1))
     y = e4m3.fl32(x * inv)
     with np.errstate(invalid="ignore"):
-        return int(np.count_nonzero(np.abs(y) > 448.0))
+        return int(np.count_nonzero(np.abs(y) > limit))
 
 
 def kv_bytes_formula(num_layers, num_kv_heads, head_dim, tokens, batch, elem_bytes) -> int:

@@ -418,3 +418,51 @@ def test_decode_attention_split_mode_is_the_split_walk():
             qv, K8, V8 = _dequant(K[b][:, g], V[b][:, g], q[b, h], qs[h], ks[g], vs[g])
             ref = _closed_form_fp8p(qv, K8[lo:], V8[lo:], T, lo, tau, 2, 16, 16)
             np.testing.assert_allclose(got[b, h], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_e5m2_decode_matches_loops_and_sdpa():
+    """An e5m2 layer (R25): the codes dequantised with their scales, the bf16 query, exact
+    softmax — pure-Python loops with the e5m2 codec, and float64 SDPA."""
+    from oracle import e5m2
+    rng = np.random.default_rng(31)
+    Hq, Hkv, D = 4, 2, 8
+    T_list = [1, 9, 40]
+    q = _bf16(rng.standard_normal((len(T_list), Hq, D)) * 2)
+    K = [_bf16(rng.standard_normal((t, Hkv, D)) * 300) for t in T_list]
+    V = [_bf16(rng.standard_normal((t, Hkv, D)) * 50) for t in T_list]
+    ks = np.array([0.5, 2.0], np.float32)
+    vs = np.array([0.25, 1.0], np.float32)
+    one = np.ones(1, np.float32)
+    B = len(T_list)
+    nblk = [(t + BS - 1) // BS for t in T_list]
+    table = np.full((B, max(nblk)), -1, np.int64)
+    nb = sum(nblk)
+    perm = rng.permutation(nb)
+    off = 0
+    for b in range(B):
+        table[b, :nblk[b]] = perm[off:off + nblk[b]]
+        off += nblk[b]
+    kp = np.zeros((nb, Hkv, BS, D), np.uint8)
+    vp = np.zeros((nb, Hkv, BS, D), np.uint8)
+    for b in range(B):
+        pos = np.arange(T_list[b])
+        kvcache.cache_write(K[b], V[b], table[b, pos // BS] * BS + pos % BS, kp, vp, ks, vs, skip=False, fmt="e5m2")
+    got = attention.decode_attention(q, kp, vp, table, T_list, one, ks, vs, fmt="e5m2")
+    tau = 1 / math.sqrt(D)
+    for b, T in enumerate(T_list):
+        for h in range(Hq):
+            g = h // 2
+            Kd = [[float(e5m2.decode(e5m2.quantize(np.array([K[b][j][g][d]]), ks[g]))[0]) * float(ks[g])
+                   for d in range(D)] for j in range(T)]
+            Vd = [[float(e5m2.decode(e5m2.quantize(np.array([V[b][j][g][d]]), vs[g]))[0]) * float(vs[g])
+                   for d in range(D)] for j in range(T)]
+            sc = [sum(q[b, h, d] * Kd[j][d] for d in range(D)) * tau for j in range(T)]
+            mx = max(sc)
+            w = [math.exp(x - mx) for x in sc]
+            z = sum(w)
+            loop = [sum(w[j] * Vd[j][d] for j in range(T)) / z for d in range(D)]
+            np.testing.assert_allclose(got[b, h], loop, rtol=1e-12, atol=1e-12)
+            sd = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(q[b, h], dtype=torch.float64)[None, None], torch.tensor(Kd, dtype=torch.float64)[None],
+                torch.tensor(Vd, dtype=torch.float64)[None], scale=tau)[0, 0]
+            np.testing.assert_allclose(got[b, h], sd.numpy(), rtol=1e-10, atol=1e-12)
