@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_PKG, "libfp8kv.so")
 
 OK, INVALID_ARG, UNSUPPORTED, CUDA_ERROR = 0, 1, 2, 3
 SCALE_PER_TENSOR, SCALE_PER_HEAD = 0, 1
+KV_E4M3, KV_E5M2 = 0, 1
 FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT, FAULT_QLEN = 1, 2, 4, 8, 16
 
 # Entry points declared by include/fp8kv.h (checked by the tests).
@@ -43,7 +44,8 @@ class FkvError(RuntimeError):
 
 class _LayerCache(ctypes.Structure):
     _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
-                ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+                ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_format", ctypes.c_int32)]
 
 
 _lib = None
@@ -117,10 +119,12 @@ def _stream(stream) -> Optional[int]:
 
 @dataclasses.dataclass
 class LayerCache:
-    """One layer's K/V pools: uint8 (e4m3) or bfloat16 tensors [num_blocks][Hkv][16][D]."""
+    """One layer's K/V pools: uint8 (FP8 codes of ``kv_format``: KV_E4M3 or KV_E5M2) or
+    bfloat16 tensors [num_blocks][Hkv][16][D]."""
 
     k_cache: torch.Tensor
     v_cache: torch.Tensor
+    kv_format: int = 0
 
     @property
     def num_blocks(self):
@@ -140,13 +144,14 @@ class LayerCache:
 
     def c(self) -> _LayerCache:
         return _LayerCache(self.k_cache.data_ptr(), self.v_cache.data_ptr(), self.num_blocks, self.block_size,
-                           self.num_kv_heads, self.head_dim)
+                           self.num_kv_heads, self.head_dim, self.kv_format)
 
     @staticmethod
-    def empty(num_blocks, num_kv_heads, head_dim, bf16=False, device="cuda", block_size=16):
+    def empty(num_blocks, num_kv_heads, head_dim, bf16=False, device="cuda", block_size=16, kv_format=0):
         dt = torch.bfloat16 if bf16 else torch.uint8
         shape = (num_blocks, num_kv_heads, block_size, head_dim)
-        return LayerCache(torch.empty(shape, dtype=dt, device=device), torch.empty(shape, dtype=dt, device=device))
+        return LayerCache(torch.empty(shape, dtype=dt, device=device), torch.empty(shape, dtype=dt, device=device),
+                          kv_format)
 
 
 def _mask_arg(skip_layer_mask):
@@ -200,8 +205,9 @@ def fp8_decode_attn_split_blocks(batch, num_q_heads, num_kv_heads, head_dim, max
                                                             window, num_splits))
 
 
-def fkv_decode_block_n(head_dim: int, bf16_layer: bool = False) -> int:
-    return int(load_library().fkv_decode_block_n(head_dim, int(bool(bf16_layer))))
+def fkv_decode_block_n(head_dim: int, bf16_layer: bool = False, kv_format: int = 0) -> int:
+    kind = 1 if bf16_layer else (2 if kv_format == KV_E5M2 else 0)
+    return int(load_library().fkv_decode_block_n(head_dim, kind))
 
 
 def decode_workspace(batch, num_q_heads, cache: LayerCache, max_blocks, window=0, num_splits=0, device="cuda"):

@@ -34,6 +34,11 @@ bool layer_is_bf16(int32_t layer, const uint8_t* mask, int32_t num_layers, fkv_s
 
 bool supported_head_dim(int32_t d) { return d == 64 || d == 128 || d == 256; }
 
+bool valid_format(const fkv_layer_cache& c) { return c.kv_format == FKV_KV_E4M3 || c.kv_format == FKV_KV_E5M2; }
+
+// Element type of a layer's pools for the decode kernels: 1 e4m3, 2 bf16, 3 e5m2.
+int layer_elt(bool bf16, const fkv_layer_cache& c) { return bf16 ? 2 : (c.kv_format == FKV_KV_E5M2 ? 3 : 1); }
+
 bool supported_group(int32_t G, int32_t D) {
   if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16)) return false;
   return G * D <= 2048;
@@ -97,7 +102,7 @@ fkv_status cache_write(const void* k, const void* v, const int64_t* slot_mapping
                        fkv_stream_t stream, unsigned long long* clips) {
   if (n_tokens < 0) return FKV_INVALID_ARG;
   if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
-  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0) return FKV_INVALID_ARG;
+  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0 || !valid_format(cache)) return FKV_INVALID_ARG;
   if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
   if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
   fkv_status st = FKV_OK;
@@ -166,8 +171,9 @@ int32_t fp8_decode_attn_split_blocks(int32_t batch, int32_t num_q_heads, int32_t
   return plan.bps;
 }
 
-int32_t fkv_decode_block_n(int32_t head_dim, int32_t bf16_layer) {
-  return fkv::decode_uses_tensor_cores(head_dim, bf16_layer != 0) ? 128 : 0;
+int32_t fkv_decode_block_n(int32_t head_dim, int32_t layer_kind) {
+  const int elt = layer_kind == 0 ? 1 : layer_kind == 1 ? 2 : layer_kind == 2 ? 3 : 0;
+  return elt != 0 && fkv::decode_uses_tensor_cores(head_dim, elt) ? 128 : 0;
 }
 
 int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
@@ -188,7 +194,7 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads, fk
   if (batch < 0 || num_q_heads <= 0 || max_blocks <= 0 || window < 0 || num_splits < 0)
     return FKV_INVALID_ARG;
   if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
-  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0) return FKV_INVALID_ARG;
+  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0 || !valid_format(cache)) return FKV_INVALID_ARG;
   if (num_q_heads % cache.num_kv_heads != 0) return FKV_INVALID_ARG;
   if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
   const int G = num_q_heads / cache.num_kv_heads;
@@ -242,8 +248,9 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads, fk
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FKV_CUDA_ERROR;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (fkv::decode_uses_tensor_cores(cache.head_dim, bf16)) return from_cuda(fkv::launch_decode_tc(p, cache.head_dim, G, s));
-  return from_cuda(fkv::launch_decode(p, cache.head_dim, bf16, G, s));
+  const int elt = layer_elt(bf16, cache);
+  if (fkv::decode_uses_tensor_cores(cache.head_dim, elt)) return from_cuda(fkv::launch_decode_tc(p, cache.head_dim, G, s));
+  return from_cuda(fkv::launch_decode(p, cache.head_dim, elt, G, s));
 }
 
 int32_t fkv_prefill_block_n(int32_t head_dim) { return supported_head_dim(head_dim) ? 128 : 0; }
@@ -257,7 +264,7 @@ fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t 
                             int32_t* fault, fkv_stream_t stream) {
   if (batch < 0 || num_q_heads <= 0 || max_q_len < 0 || max_blocks <= 0) return FKV_INVALID_ARG;
   if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
-  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0) return FKV_INVALID_ARG;
+  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0 || !valid_format(cache)) return FKV_INVALID_ARG;
   if (num_q_heads % cache.num_kv_heads != 0) return FKV_INVALID_ARG;
   if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
   if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
@@ -268,6 +275,7 @@ fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t 
   fkv_status st = FKV_OK;
   const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
   if (st != FKV_OK) return st;
+  if (!bf16 && cache.kv_format == FKV_KV_E5M2) return FKV_UNSUPPORTED;  // e5m2 layers: decode only
   if (batch > 65535 || num_q_heads > 65535) return FKV_UNSUPPORTED;
   if (batch == 0 || max_q_len == 0) return FKV_OK;
   if (!q || !cu_seqlens_q || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || !out)

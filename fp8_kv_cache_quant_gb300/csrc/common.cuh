@@ -28,6 +28,23 @@ FKV_DEV uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Two float32 values -> two e5m2 codes, round-to-nearest-even, saturating to +-57344
+// (PTX cvt.rn.satfinite.e5m2x2.f32).  Returns (code(hi) << 8) | code(lo).
+FKV_DEV uint16_t f32x2_to_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four e5m2 codes (low byte first) -> float32 pairs.  An e5m2 code is the upper byte of
+// a binary16, so each code shifted into the high byte of a half is its exact value.
+FKV_DEV void e5m2x4_to_f2(uint32_t w, float2& lo, float2& hi) {
+  const uint32_t h01 = ((w & 0x000000FFu) << 8) | ((w & 0x0000FF00u) << 16);
+  const uint32_t h23 = ((w >> 8) & 0x0000FF00u) | (w & 0xFF000000u);
+  lo = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  hi = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+}
+
 // Two e4m3 codes (low byte first) -> half2 (exact: every e4m3 value is an f16 value).
 FKV_DEV __half2 e4m3x2_to_h2(uint16_t v) {
   uint32_t r;

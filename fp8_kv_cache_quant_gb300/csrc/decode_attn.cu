@@ -33,13 +33,16 @@ constexpr int kNW = 4;           // warps per CTA; every warp prefetches and con
 constexpr int kNBUF = 2;         // tile buffers per warp (one in use, one in flight)
 constexpr int kMaxBps = 128;     // blocks per split, upper bound (table ids staged in smem)
 
+// ELT: the pool's element type — 1 e4m3 (f16 partial sums of exact code products), 2 bf16,
+// 3 e5m2 (the codes widened to FP32, the query unquantised, P exact: as bf16 layers).
 template <int D, int ELT, int G>
 struct DecodeCfg {
-  static constexpr int CHUNK = 16 * D * ELT;                  // bytes of one (block, head) chunk
+  static constexpr int ES = ELT == 2 ? 2 : 1;                 // bytes per element
+  static constexpr int CHUNK = 16 * D * ES;                   // bytes of one (block, head) chunk
   static constexpr int TB = CHUNK <= 2048 ? 2 : 1;            // 16-key blocks per tile
   static constexpr int TILE_BYTES = TB * 2 * CHUNK;           // K and V of a tile
   static constexpr int RING = kNW * kNBUF * TILE_BYTES;
-  // QK mapping: EPL elements (EPL*ELT bytes) of one key per lane
+  // QK mapping: EPL elements (EPL*ES bytes) of one key per lane
   static constexpr int EPL = ELT == 1 ? (G <= 4 ? 16 : (G == 8 ? 8 : 4)) : (G <= 8 ? 8 : 4);
   static constexpr int LPK = D / EPL;                         // lanes per key
   static constexpr int KPR = 32 / LPK;                        // keys per round
@@ -74,7 +77,7 @@ FKV_DEV void load_bytes(const uint8_t* p, uint32_t (&w)[N / 4 > 0 ? N / 4 : 1]) 
   }
 }
 
-// Convert N elements (e4m3 or bf16) held in words to float2 pairs.
+// Convert N elements (e4m3, bf16 or e5m2) held in words to float2 pairs.
 template <int ELT, int N>
 FKV_DEV void to_f2(const uint32_t* w, float2* out) {
   if constexpr (ELT == 1) {
@@ -83,6 +86,14 @@ FKV_DEV void to_f2(const uint32_t* w, float2* out) {
       for (int i = 0; i < N / 4; ++i) e4m3x4_to_f2(w[i], out[2 * i], out[2 * i + 1]);
     } else {
       out[0] = __half22float2(e4m3x2_to_h2(static_cast<uint16_t>(w[0] & 0xFFFFu)));
+    }
+  } else if constexpr (ELT == 3) {
+    if constexpr (N >= 4) {
+#pragma unroll
+      for (int i = 0; i < N / 4; ++i) e5m2x4_to_f2(w[i], out[2 * i], out[2 * i + 1]);
+    } else {
+      float2 unused;
+      e5m2x4_to_f2(w[0] & 0xFFFFu, out[0], unused);
     }
   } else {
 #pragma unroll
@@ -186,7 +197,9 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
   // the two halves into FP32 before the cross-lane reduction (two-level accumulation).
   // The 2^8 returns in the softmax constant.
   const float cl = p.sm_scale_log2 *
-                   (ELT == 1 ? 256.f * p.q_scale[p.per_head ? h0 + hb : 0] * p.k_scale[p.per_head ? g : 0] : 1.f);
+                   (ELT == 1   ? 256.f * p.q_scale[p.per_head ? h0 + hb : 0] * p.k_scale[p.per_head ? g : 0]
+                    : ELT == 3 ? p.k_scale[p.per_head ? g : 0]
+                               : 1.f);
   // query slice in slot order (e4m3 codes * 2^-8 as half2 on FP8 layers, float2 on bf16 layers)
   float2 qf[ELT == 1 ? 1 : G][C::EPL / 2];
   __half2 qh[ELT == 1 ? G : 1][C::EPL / 2];
@@ -245,8 +258,8 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
 #pragma unroll
         for (int rr = 0; rr < C::ROUNDS; ++rr) {
           const int key = rr * C::KPR + kq;
-          uint32_t w[C::EPL * ELT / 4 > 0 ? C::EPL * ELT / 4 : 1];
-          load_bytes<C::EPL * ELT>(kb + key * D * ELT + dq * ELT, w);
+          uint32_t w[C::EPL * C::ES / 4 > 0 ? C::EPL * C::ES / 4 : 1];
+          load_bytes<C::EPL * C::ES>(kb + key * D * C::ES + dq * C::ES, w);
           float v[G];
           if constexpr (ELT == 1) {
             __half2 kh[C::EPL / 2];
@@ -366,8 +379,8 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
       const int kb0 = key0 + j * 16;
       const int kv_lo = max(r.lo - kb0, 0), kv_hi = min(r.T - kb0, 16);
       auto pv_key = [&](int key) {
-        uint32_t w[C::VPL * ELT / 4 > 0 ? C::VPL * ELT / 4 : 1];
-        load_bytes<C::VPL * ELT>(vb + key * D * ELT + dv * ELT, w);
+        uint32_t w[C::VPL * C::ES / 4 > 0 ? C::VPL * C::ES / 4 : 1];
+        load_bytes<C::VPL * C::ES>(vb + key * D * C::ES + dv * C::ES, w);
         const int pidx = (j * 16 + key) * G;
         if constexpr (ELT == 1) {
           __half2 vh[C::VPL / 2];
@@ -514,7 +527,7 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
   float* inv_s = ms_s + G;                            // [G]
   float* w_s = inv_s + G;                             // [G][CH] weights of a chunk of splits
   constexpr int CH = (C::RING / 4 - 2 * G) / G < 256 ? (C::RING / 4 - 2 * G) / G : 256;
-  const float vs = ELT == 1 ? p.v_scale[p.per_head ? g : 0] : 1.f;
+  const float vs = ELT != 2 ? p.v_scale[p.per_head ? g : 0] : 1.f;
   const int ns = r.nsplit;
   for (int t = threadIdx.x; t < G; t += blockDim.x) {
     const size_t row0 = (static_cast<size_t>(b) * p.Hq + g * G + t) * p.max_splits;
@@ -601,10 +614,18 @@ cudaError_t launch_decode_g(const DecodeParams& p, int G, cudaStream_t s) {
   }
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16_layer, int G, cudaStream_t s) {
-  if (D == 64) return bf16_layer ? launch_decode_g<64, 2>(p, G, s) : launch_decode_g<64, 1>(p, G, s);
-  if (D == 128) return bf16_layer ? launch_decode_g<128, 2>(p, G, s) : launch_decode_g<128, 1>(p, G, s);
-  if (D == 256) return bf16_layer ? launch_decode_g<256, 2>(p, G, s) : launch_decode_g<256, 1>(p, G, s);
+template <int D>
+cudaError_t launch_decode_d(const DecodeParams& p, int elt, int G, cudaStream_t s) {
+  if (elt == 1) return launch_decode_g<D, 1>(p, G, s);
+  if (elt == 2) return launch_decode_g<D, 2>(p, G, s);
+  if (elt == 3) return launch_decode_g<D, 3>(p, G, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int D, int elt, int G, cudaStream_t s) {
+  if (D == 64) return launch_decode_d<64>(p, elt, G, s);
+  if (D == 128) return launch_decode_d<128>(p, elt, G, s);
+  if (D == 256) return launch_decode_d<256>(p, elt, G, s);
   return cudaErrorInvalidValue;
 }
 

@@ -557,7 +557,7 @@ cudaError_t launch_decode_tc_g(const DecodeParams& p, int G, cudaStream_t s) {
 
 }  // namespace
 
-bool decode_uses_tensor_cores(int D, bool bf16_layer) { return !bf16_layer && (D == 128 || D == 256); }
+bool decode_uses_tensor_cores(int D, int elt) { return elt == 1 && (D == 128 || D == 256); }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int D, int G, cudaStream_t s) {
   if (D == 128) return launch_decode_tc_g<128>(p, G, s);

@@ -56,11 +56,12 @@ cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* s
                                   int per_head, bool bf16_layer, int32_t* fault, cudaStream_t s,
                                   int num_sms, unsigned long long* clips);
 
-cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16_layer, int G, cudaStream_t s);
+// elt: the pool's element type, 1 e4m3, 2 bf16, 3 e5m2
+cudaError_t launch_decode(const DecodeParams& p, int D, int elt, int G, cudaStream_t s);
 
-// e4m3 layers with head_dim 128 / 256 decode on the tensor cores (FP8 P, 128-key tiles);
-// the others on the CUDA cores (P exact).
-bool decode_uses_tensor_cores(int D, bool bf16_layer);
+// e4m3 layers (elt 1) with head_dim 128 / 256 decode on the tensor cores (FP8 P, 128-key
+// tiles); the others on the CUDA cores (P exact).
+bool decode_uses_tensor_cores(int D, int elt);
 cudaError_t launch_decode_tc(const DecodeParams& p, int D, int G, cudaStream_t s);
 
 }  // namespace fkv

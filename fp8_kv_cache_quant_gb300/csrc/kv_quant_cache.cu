@@ -1,5 +1,5 @@
-// kv_quant_cache: bf16 K/V of new tokens -> paged e4m3 pool (or a bf16 copy for skip
-// layers).  The cache write of the vLLM blog "FP8 KV-Cache and Attention quantization
+// kv_quant_cache: bf16 K/V of new tokens -> paged e4m3 (or e5m2) pool, or a bf16 copy for
+// skip layers.  The cache write of the vLLM blog "FP8 KV-Cache and Attention quantization
 // in vLLM" (section "Kernel 与 vLLM 改进", paragraph "Per-Head Scales": the write takes a
 // per-KV-head scale array instead of one scalar; paragraph "跳过 Layer": skipped layers
 // stay bf16).
@@ -15,7 +15,7 @@
 
 namespace fkv {
 
-template <bool kBf16, bool kCount>
+template <bool kBf16, bool kCount, bool kE5>
 __global__ void __launch_bounds__(256) kv_quant_cache_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
     int n_tokens, int H, int D, uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
@@ -55,17 +55,22 @@ __global__ void __launch_bounds__(256) kv_quant_cache_kernel(
         const float2 v0 = bf16x2_to_f2(vw[2 * j]), v1 = bf16x2_to_f2(vw[2 * j + 1]);
         const float ky[4] = {__fmul_rn(k0.x, ik), __fmul_rn(k0.y, ik), __fmul_rn(k1.x, ik), __fmul_rn(k1.y, ik)};
         const float vy[4] = {__fmul_rn(v0.x, iv), __fmul_rn(v0.y, iv), __fmul_rn(v1.x, iv), __fmul_rn(v1.y, iv)};
+        constexpr float kLimit = kE5 ? 57344.f : 448.f;  // largest finite code of the format
         if constexpr (kCount) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            kclip += fabsf(ky[e]) > 448.f ? 1u : 0u;  // NaN compares false: not a clip
-            vclip += fabsf(vy[e]) > 448.f ? 1u : 0u;
+            kclip += fabsf(ky[e]) > kLimit ? 1u : 0u;  // NaN compares false: not a clip
+            vclip += fabsf(vy[e]) > kLimit ? 1u : 0u;
           }
         }
-        const uint32_t klo = f32x2_to_e4m3x2(ky[0], ky[1]);
-        const uint32_t khi = f32x2_to_e4m3x2(ky[2], ky[3]);
-        const uint32_t vlo = f32x2_to_e4m3x2(vy[0], vy[1]);
-        const uint32_t vhi = f32x2_to_e4m3x2(vy[2], vy[3]);
+        auto enc = [](float a, float b2) -> uint32_t {
+          if constexpr (kE5) return f32x2_to_e5m2x2(a, b2);
+          else return f32x2_to_e4m3x2(a, b2);
+        };
+        const uint32_t klo = enc(ky[0], ky[1]);
+        const uint32_t khi = enc(ky[2], ky[3]);
+        const uint32_t vlo = enc(vy[0], vy[1]);
+        const uint32_t vhi = enc(vy[2], vy[3]);
         ko[j] = klo | (khi << 16);
         vo[j] = vlo | (vhi << 16);
       }
@@ -88,6 +93,7 @@ cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* s
                                   const fkv_layer_cache& cache, const float* ks, const float* vs,
                                   int per_head, bool bf16_layer, int32_t* fault, cudaStream_t s,
                                   int num_sms, unsigned long long* clips) {
+  const bool e5 = !bf16_layer && cache.kv_format == FKV_KV_E5M2;
   const long long total = static_cast<long long>(n_tokens) * cache.num_kv_heads * (cache.head_dim / 8);
   if (total == 0) return cudaSuccess;
   const int threads = 256;
@@ -95,8 +101,11 @@ cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* s
   const long long cap = static_cast<long long>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   const long long capacity = static_cast<long long>(cache.num_blocks) * cache.block_size;
-  auto kern = bf16_layer ? kv_quant_cache_kernel<true, false>
-                         : (clips != nullptr ? kv_quant_cache_kernel<false, true> : kv_quant_cache_kernel<false, false>);
+  auto kern = bf16_layer ? kv_quant_cache_kernel<true, false, false>
+               : e5      ? (clips != nullptr ? kv_quant_cache_kernel<false, true, true>
+                                             : kv_quant_cache_kernel<false, false, true>)
+                         : (clips != nullptr ? kv_quant_cache_kernel<false, true, false>
+                                             : kv_quant_cache_kernel<false, false, false>);
   kern<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, n_tokens, cache.num_kv_heads, cache.head_dim,
       static_cast<uint8_t*>(cache.k_cache), static_cast<uint8_t*>(cache.v_cache), capacity, ks, vs, per_head, fault,

@@ -70,9 +70,16 @@ typedef enum {
 #define FKV_FAULT_TIMEOUT 8  /* an in-kernel pipeline wait exceeded 1 s: work abandoned        */
 #define FKV_FAULT_QLEN 16    /* prefill: query length > context length: sequence skipped     */
 
+/* FP8 format of a layer's pools (fkv_layer_cache.kv_format). */
+typedef enum {
+  FKV_KV_E4M3 = 0, /* e4m3 "fn": the format of the FP8 attention (default) */
+  FKV_KV_E5M2 = 1  /* e5m2 (vLLM's other FP8 KV-cache format): dequantised, attended in bf16 precision */
+} fkv_kv_format;
+
 /* One layer of the paged cache.  k_cache / v_cache: device pools, 16-byte aligned,
- * [num_blocks][num_kv_heads][block_size][head_dim] of e4m3 (1 byte) or bf16 (2 bytes),
- * the element type being chosen per layer by the skip-layer mask. */
+ * [num_blocks][num_kv_heads][block_size][head_dim] of FP8 codes (1 byte, format
+ * kv_format) or bf16 (2 bytes): a layer named by the skip-layer mask is bf16 whatever
+ * kv_format says. */
 typedef struct {
   void* k_cache;
   void* v_cache;
@@ -80,6 +87,7 @@ typedef struct {
   int32_t block_size;
   int32_t num_kv_heads;
   int32_t head_dim;
+  int32_t kv_format; /* fkv_kv_format */
 } fkv_layer_cache;
 
 /* Human-readable name of a status code (static string). */
@@ -104,8 +112,9 @@ int32_t fkv_version(void);
  *   layer, skip_layer_mask (host uint8 [num_layers], may be NULL = no skipped layer),
  *   num_layers    skip_layer_mask[layer] != 0 selects the bf16 pool format
  *   fault         device int32 or NULL
- * Each element is e4m3(fl32(x * fl32(1/scale))) (round-to-nearest-even, saturating);
- * every other byte of the pools keeps its value.
+ * Each element is e4m3(fl32(x * fl32(1/scale))) (round-to-nearest-even, saturating;
+ * e5m2 likewise on pools with cache.kv_format FKV_KV_E5M2, saturating to +-57344); every
+ * other byte of the pools keeps its value.
  */
 fkv_status kv_quant_cache(const void* k, const void* v, const int64_t* slot_mapping,
                           int32_t n_tokens, fkv_layer_cache cache, const float* k_scale,
@@ -120,8 +129,9 @@ fkv_status kv_quant_cache(const void* k, const void* v, const int64_t* slot_mapp
  * frequency where it can be observed.  Same write as kv_quant_cache; in addition
  * clip_counts[0] and clip_counts[1] (device uint64, accumulated atomically; the caller
  * zeroes them) grow by the number of K and V elements whose scaled value
- * fl32(x * fl32(1/scale)) lies beyond +-448 and is therefore clipped (NaN is not
- * counted; skip layers clip nothing).  clip_counts NULL or not 8-byte aligned:
+ * fl32(x * fl32(1/scale)) lies beyond the format's largest finite value (448 for
+ * e4m3, 57344 for e5m2) and is therefore clipped (NaN is not counted; skip layers clip
+ * nothing).  clip_counts NULL or not 8-byte aligned:
  * FKV_INVALID_ARG.
  */
 fkv_status kv_quant_cache_clips(const void* k, const void* v, const int64_t* slot_mapping,
@@ -154,10 +164,10 @@ int32_t fp8_decode_attn_split_blocks(int32_t batch, int32_t num_q_heads, int32_t
 
 /*
  * Keys per tile over which fp8_decode_attn rounds P to e4m3 for a layer of this head_dim
- * (bf16_layer != 0: a skip layer), or 0 when that layer's decode keeps P exact.  Tiles
- * start at each split's first block.
+ * and kind (0: e4m3 pools, 1: a skip layer's bf16 pools, 2: e5m2 pools), or 0 when that
+ * layer's decode keeps P exact.  Tiles start at each split's first block.
  */
-int32_t fkv_decode_block_n(int32_t head_dim, int32_t bf16_layer);
+int32_t fkv_decode_block_n(int32_t head_dim, int32_t layer_kind);
 
 /*
  * fp8_decode_attn — one decode step of paged GQA attention for one layer.
@@ -177,7 +187,9 @@ int32_t fkv_decode_block_n(int32_t head_dim, int32_t bf16_layer);
  * P8 = e4m3(p * 448) relative to the split's running maximum, the denominator summing
  * the unrounded p, and each tile's partial promoted into FP32 registers.  Other e4m3
  * layers (head_dim 64) run on the CUDA cores with P exact.  Skip layers read a bf16
- * pool, quantise nothing and keep P exact.  fkv_decode_block_n tells which applies.
+ * pool, quantise nothing and keep P exact; e5m2 layers (cache.kv_format) dequantise
+ * their codes with the scales and attend with the bf16 query and exact P on the CUDA
+ * cores.  fkv_decode_block_n tells which applies.
  *
  *   q             device bf16 [batch][num_q_heads][head_dim]
  *   block_table   device int32 [batch][max_blocks]
@@ -263,6 +275,7 @@ int32_t fkv_prefill_block_n(int32_t head_dim);
  *                 the whole contraction (the blog's "大 Head Dimension 的限制": accumulate
  *                 every N steps, or disable two-level accumulation); negative: FKV_INVALID_ARG
  *   out           device bf16 [total_q][num_q_heads][head_dim]
+ * e5m2 layers (cache.kv_format FKV_KV_E5M2, not skipped) are FKV_UNSUPPORTED.
  * head_dim in {64, 128, 256}.  Skip (bf16) layers — the layer's bit set in skip_layer_mask —
  * read the bf16 pool and run the same kernel on bf16 operands (kind::f16 MMA, P rounded to
  * bf16, no scales: q_scale/k_scale/v_scale may be NULL); at head_dim 256 their key tiles

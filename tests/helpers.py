@@ -37,10 +37,10 @@ def to_dev(x, dtype=None):
     return t.cuda()
 
 
-def build_layer(f, ctx, table, num_blocks, k, v, ks, vs, gran, bf16_layer, sentinel=None):
+def build_layer(f, ctx, table, num_blocks, k, v, ks, vs, gran, bf16_layer, sentinel=None, kv_format=0):
     """Allocate one layer's pools and fill them with kv_quant_cache (all positions)."""
     H, D = k.shape[1], k.shape[2]
-    cache = f.LayerCache.empty(num_blocks, H, D, bf16=bf16_layer)
+    cache = f.LayerCache.empty(num_blocks, H, D, bf16=bf16_layer, kv_format=kv_format)
     if sentinel is not None:
         cache.k_cache.view(torch.uint8).fill_(sentinel)
         cache.v_cache.view(torch.uint8).fill_(sentinel)
@@ -55,7 +55,7 @@ def seq_slices(ctx):
     return [(int(cu[b]), int(cu[b + 1])) for b in range(len(ctx))]
 
 
-def oracle_pools(oracle_kvcache, ctx, table, num_blocks, k, v, ks, vs, bf16_layer):
+def oracle_pools(oracle_kvcache, ctx, table, num_blocks, k, v, ks, vs, bf16_layer, fmt="e4m3"):
     """The oracle's own pools, written by the oracle's cache write from the bf16 inputs."""
     H, D = k.shape[1], k.shape[2]
     if bf16_layer:
@@ -66,5 +66,5 @@ def oracle_pools(oracle_kvcache, ctx, table, num_blocks, k, v, ks, vs, bf16_laye
         vp = np.zeros((num_blocks, H, 16, D), np.uint8)
     slots = synth.slot_mapping(table, ctx)
     oracle_kvcache.cache_write(synth.bf16_to_f64(k), synth.bf16_to_f64(v), slots, kp, vp,
-                               np.asarray(ks, np.float32), np.asarray(vs, np.float32), skip=bf16_layer)
+                               np.asarray(ks, np.float32), np.asarray(vs, np.float32), skip=bf16_layer, fmt=fmt)
     return kp, vp

@@ -64,8 +64,8 @@ def test_split_planning(lib):
     assert f.fp8_decode_attn_workspace_size(1, 8, 2, 96, 10) == 0      # unsupported head_dim
 
 
-def _cache(D=128, bs=16, nb=4, H=2, k=1 << 20, v=1 << 21):
-    return f._LayerCache(k, v, nb, bs, H, D)
+def _cache(D=128, bs=16, nb=4, H=2, k=1 << 20, v=1 << 21, fmt=0):
+    return f._LayerCache(k, v, nb, bs, H, D, fmt)
 
 
 def test_kv_quant_cache_validation(lib):
@@ -81,6 +81,23 @@ def test_kv_quant_cache_validation(lib):
     mask = (ctypes.c_uint8 * 2)(0, 1)
     assert st(one, one, one, 4, _cache(), one, one, 0, 5, mask, 2, None, None) == f.INVALID_ARG
     assert st(one, one, one, 0, _cache(), one, one, 0, 0, None, 0, None, None) == f.OK   # nothing to do
+
+
+def test_kv_format_validation(lib):
+    one = 1 << 12
+    p = one
+    # an unknown FP8 format is invalid everywhere
+    assert lib.kv_quant_cache(one, one, one, 4, _cache(fmt=7), one, one, 0, 0, None, 0, None, None) == f.INVALID_ARG
+    assert lib.fp8_prefill_attn(p, p, 1, 8, 16, _cache(fmt=2), p, 4, p, p, p, p, 0, 0.0, 1, 0, 1, 0, None, 0, p, None,
+                                None) == f.INVALID_ARG
+    # e5m2 layers have no prefill here; a skip layer is bf16 whatever its format field says
+    assert lib.fp8_prefill_attn(p, p, 1, 8, 16, _cache(fmt=1), p, 4, p, p, p, p, 0, 0.0, 1, 0, 1, 0, None, 0, p, None,
+                                None) == f.UNSUPPORTED
+    mask = (ctypes.c_uint8 * 1)(1)
+    assert lib.fp8_prefill_attn(p, p, 0, 8, 16, _cache(fmt=1), p, 4, p, None, None, None, 0, 0.0, 1, 0, 1, 0, mask, 1, p,
+                                None, None) == f.OK
+    # e5m2 layers decode on the CUDA cores with P exact
+    assert f.fkv_decode_block_n(128, kv_format=f.KV_E5M2) == 0 and f.fkv_decode_block_n(128) == 128
 
 
 def test_kv_quant_cache_clips_validation(lib):

@@ -164,3 +164,24 @@ def test_clip_counts_per_head_accumulate_and_skip_layers():
     bf = f.LayerCache.empty(nb, H, D, bf16=True)
     c2 = f.kv_quant_cache_clips(k.cuda(), v.cuda(), slots, bf, None, None, f.SCALE_PER_TENSOR, skip_layer_mask=[1])
     assert c2.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.0371, 3.5])
+def test_e5m2_codec_every_bf16_pattern(scale):
+    """Every bf16 bit pattern through the e5m2 cache write (pools with kv_format KV_E5M2),
+    bit-exact against the oracle's e5m2 codec, with the clip counts at the e5m2 limit."""
+    from oracle import e5m2
+    k = _all_bf16_patterns()
+    v = k.flip(0).contiguous()
+    n, H, D = k.shape
+    cache = f.LayerCache.empty(n // 16, H, D, kv_format=f.KV_E5M2)
+    slots = torch.arange(n, dtype=torch.int64, device="cuda")
+    s = torch.tensor([scale], dtype=torch.float32, device="cuda")
+    counts = f.kv_quant_cache_clips(k.cuda(), v.cuda(), slots, cache, s, s, f.SCALE_PER_TENSOR)
+    got_k = cache.k_cache.cpu().numpy().reshape(n, D)
+    got_v = cache.v_cache.cpu().numpy().reshape(n, D)
+    kx, vx = synth.bf16_to_f64(k), synth.bf16_to_f64(v)
+    assert np.array_equal(got_k, e5m2.quantize(kx.reshape(n, D), np.float32(scale)))
+    assert np.array_equal(got_v, e5m2.quantize(vx.reshape(n, D), np.float32(scale)))
+    assert counts.cpu().tolist() == [kvcache.clip_count(kx, np.float32(scale), limit=e5m2.E5M2_MAX),
+                                     kvcache.clip_count(vx, np.float32(scale), limit=e5m2.E5M2_MAX)]

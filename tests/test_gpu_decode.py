@@ -82,6 +82,35 @@ def test_decode_small_parity(D, G, bf16_layer, gran, window, splits):
     assert_close(got, ref, what=f"D={D} G={G} bf16={bf16_layer} gran={gran} W={window} splits={splits}")
 
 
+@pytest.mark.parametrize("D,G,gran,window,splits", [
+    (128, 4, 1, 0, 0), (64, 8, 0, 0, 3), (256, 2, 1, 0, 0), (128, 16, 0, 100, 0), (64, 4, 1, 40, 2),
+])
+def test_decode_e5m2_layers(D, G, gran, window, splits):
+    """e5m2 pools (kv_format KV_E5M2): the codes dequantised with their scales, the bf16
+    query and exact P (R25) on the CUDA cores, against the oracle's e5m2 decode."""
+    rng = np.random.default_rng(D + G + window)
+    Hkv = 2
+    Hq = Hkv * G
+    ctx = np.array([1, 15, 16, 17, 300, 1000, 0, 129], np.int32)
+    table, nb = synth.block_table(ctx, seed=13, extra_blocks=2)
+    q, k, v = _inputs(rng, ctx, Hq, Hkv, D, scale_k=40.0)
+    if gran:
+        ks, vs = synth.amax_scales(k, 1) * (448.0 / 57344.0), synth.amax_scales(v, 1) * (448.0 / 57344.0)
+    else:
+        ks = torch.tensor([0.01]); vs = torch.tensor([0.002])
+    qs = torch.ones(1)
+    cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran, False, sentinel=0xFF,
+                        kv_format=f.KV_E5M2)
+    out = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(qs), to_dev(ks), to_dev(vs), gran,
+                            window=window, num_splits=splits)
+    kp, vp = oracle_pools(kvcache, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), False, fmt="e5m2")
+    ref = attention.decode_attention(synth.bf16_to_f64(q), kp, vp, table, ctx, qs.numpy(), ks.numpy(), vs.numpy(),
+                                     window=window, fmt="e5m2")
+    got = out.float().cpu().numpy()
+    assert np.all(got[6] == 0), "empty context must give a zero row"
+    assert_close(got, ref, what=f"e5m2 D={D} G={G} gran={gran} W={window} splits={splits}")
+
+
 @pytest.mark.parametrize("Hkv,G,D", [(3, 2, 64), (1, 8, 64), (5, 4, 64), (3, 4, 128)])
 def test_decode_odd_kv_head_counts(Hkv, G, D):
     """Odd KV head counts and a single KV head, on both decode kernels."""

@@ -72,7 +72,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     need = f.fp8_decode_attn_workspace_size(512, 32, 8, 128, 8192, 0, 64)
     assert need > f.NOALLOC_WORKSPACE_BYTES
     p = 1 << 12
-    cache = f._LayerCache(p, p, 100, 16, 8, 128)
+    cache = f._LayerCache(p, p, 100, 16, 8, 128, 0)
     st = lib.fp8_decode_attn_noalloc(p, 512, 32, cache, p, 8192, p, p, p, p, 0, 0.0, 0, 0, None, 0, p, 64, None,
                                      None)
     assert st == f.INVALID_ARG
