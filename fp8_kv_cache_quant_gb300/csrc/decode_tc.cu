@@ -1,5 +1,5 @@
-// Paged GQA decode attention on tcgen05 tensor cores, for e4m3 layers with head_dim 128
-// or 256: split-K over the context, FP8 QK and Score*V products with FP32 accumulation in
+// Paged GQA decode attention on tcgen05 tensor cores, for e4m3 layers with head_dim 64,
+// 128 or 256: split-K over the context, FP8 QK and Score*V products with FP32 accumulation in
 // tensor memory, two-level accumulation, FP32 merge of the splits.
 //
 // The vLLM blog "FP8 KV-Cache and Attention quantization in vLLM": with an FP8 KV cache
@@ -13,6 +13,8 @@
 //   S^T [128 keys][16]   = K8 [128 keys][D]   . Q8^T [D][16]        (K, Q8 K-major)
 //   O^T [128 d][16]     += V8^T [128 d][128 keys] . P8^T [128 keys][16]   (V MN-major)
 // so the cache tiles are the A operands exactly as TMA lands them from the pool.
+// head_dim 64 uses 64-byte rows (64-byte swizzle) and an M = 64 P.V product, whose
+// accumulator row r sits in TMEM lane 32 (r / 16) + r % 16.
 //
 // CTA = (split, KV head g, sequence b), 10 warps:
 //   warps 0-3  softmax: quantise the G query rows to e4m3 (prologue); per 128-key tile
@@ -42,12 +44,15 @@ template <int D, int G>
 struct DecodeTcCfg {
   static constexpr int BN = 128;               // keys per tile (M of S^T)
   static constexpr int NP = 16;                // query heads padded to the MMA's N
-  static constexpr int NSUB = D / 128;         // 128-byte column blocks of a K / V row
-  static constexpr int KSUB = BN * 128;        // bytes of one column block of a K / V tile
+  static constexpr int RB = D < 128 ? D : 128; // bytes of one swizzled row
+  static constexpr int SWZ = RB == 128 ? 2 : 4;  // descriptor swizzle mode (128 / 64 bytes)
+  static constexpr int NSUB = D / RB;          // column blocks of a K / V row
+  static constexpr int KSUB = BN * RB;         // bytes of one column block of a K / V tile
   static constexpr int KTILE = BN * D;         // bytes of a K or V tile
-  static constexpr int NS = 2;                 // K / V stages (small CTAs: 3 per SM at head_dim 128)
+  static constexpr int MPV = D < 128 ? D : 128;  // M of one P.V product (head_dim rows)
+  static constexpr int NS = D == 64 ? 4 : 2;   // K / V stages (small CTAs: 3 per SM up to head_dim 128)
   static constexpr int MAX_BPS = 128;          // blocks per split (their ids staged in shared memory)
-  static constexpr int QSUB = NP * 128;        // bytes of one column block of the Q8 tile
+  static constexpr int QSUB = NP * RB;         // bytes of one column block of the Q8 tile
   static constexpr int PTILE = NP * BN;        // bytes of one P8^T tile
   static constexpr int TM_S = 0;               // S^T buffers: TMEM columns [0, 2 * NP)
   static constexpr int TM_O = 2 * NP;          // O_tile^T buffers: [TM_O, TM_O + 2 * NSUB * NP)
@@ -65,18 +70,18 @@ struct DecodeTcCfg {
   static constexpr int OFF_MISC = OFF_IDS + MAX_BPS * 4;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_QK = idesc_e4m3_f32(128, NP, 0, 0);  // K8 and Q8 K-major
-  static constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, NP, 1, 0);  // V8 MN-major, P8 K-major
+  static constexpr uint32_t IDESC_PV = idesc_e4m3_f32(MPV, NP, 1, 0);  // V8 MN-major, P8 K-major
   // merge scratch (in the K stages, free by then): 2 G + G * CH floats
   static constexpr int CH = (NS * KTILE / 4 - 2 * G) / G < 256 ? (NS * KTILE / 4 - 2 * G) / G : 256;
   static_assert(G >= 1 && G <= NP, "query heads per KV head");
-  static_assert(D == 128 || D == 256, "head_dim");
+  static_assert(D == 64 || D == 128 || D == 256, "head_dim");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
 constexpr int kDecodeTcThreads = 320;  // softmax warpgroup, correction warpgroup, TMA warp, MMA warp
 
 template <int D, int G>
-__global__ void __launch_bounds__(kDecodeTcThreads, (D == 128 && G <= 8) ? 3 : 1)
+__global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1)
     decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
   using C = DecodeTcCfg<D, G>;
@@ -203,8 +208,8 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D == 128 && G <= 8) ? 3 : 1
           w4 = make_uint4(w[0], w[1], w[2], w[3]);
         }
         const int byte = c * 16;
-        *reinterpret_cast<uint4*>(sQ + (byte / 128) * C::QSUB + swz(static_cast<uint32_t>(row * 128 + byte % 128), 128)) =
-            w4;
+        *reinterpret_cast<uint4*>(sQ + (byte / C::RB) * C::QSUB +
+                                  swz(static_cast<uint32_t>(row * C::RB + byte % C::RB), C::RB)) = w4;
       }
       if constexpr (G < C::NP) {
         for (int x = i; x < 2 * (C::NP - G) * 8; x += 128) {
@@ -311,8 +316,12 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D == 128 && G <= 8) ? 3 : 1
     if (ok) mbar_arrive(l_full);
   } else if (warp < 8) {
     // ============================================================ correction warpgroup
-    const int i = threadIdx.x - 128;  // head_dim row i (and 128 + i) of O (TMEM lane i)
+    const int i = threadIdx.x - 128;  // TMEM lane i
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16);
+    // the head_dim row this lane holds (and 128 + it): lane i itself for M = 128; for the
+    // M = 64 product of head_dim 64, lanes 0-15 of each warp hold rows 16 (warp - 4) + lane
+    const bool has_row = C::MPV == 128 || lane < 16;
+    const int d = C::MPV == 128 ? i : (warp - 4) * 16 + lane;
     float acc[C::NSUB][G];
 #pragma unroll
     for (int h = 0; h < G; ++h)
@@ -352,8 +361,10 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D == 128 && G <= 8) ? 3 : 1
         const float L = ml_s[C::NP + h];
         const size_t row = (static_cast<size_t>(b) * p.Hq + g * G + h) * p.max_splits + sigma;
         const float inv = L > 0.f ? 1.f / (448.f * L) : 0.f;  // P8 carries the factor 448
+        if (has_row) {
 #pragma unroll
-        for (int s2 = 0; s2 < C::NSUB; ++s2) p.o_part[row * D + s2 * 128 + i] = acc[s2][h] * inv;
+          for (int s2 = 0; s2 < C::NSUB; ++s2) p.o_part[row * D + s2 * 128 + d] = acc[s2][h] * inv;
+        }
         if (i == 0) p.lse_part[row] = L > 0.f ? ml_s[h] + lg2(L) : -INFINITY;
       }
     } else if (ok) {
@@ -383,7 +394,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D == 128 && G <= 8) ? 3 : 1
       if (lane < nblk) {
 #pragma unroll
         for (int s = 0; s < C::NSUB; ++s)
-          tma_load_4d(sK + st * C::KTILE + s * C::KSUB + lane * 16 * 128, &tmk, s * 128, 0, g, ids_s[8 * t + lane],
+          tma_load_4d(sK + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmk, s * C::RB, 0, g, ids_s[8 * t + lane],
                       &k_full[st]);
       }
       last_use[st] = use;
@@ -421,7 +432,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D == 128 && G <= 8) ? 3 : 1
         if (lane < nblk) {
 #pragma unroll
           for (int s = 0; s < C::NSUB; ++s)
-            tma_load_4d(sV + st * C::KTILE + s * C::KSUB + lane * 16 * 128, &tmv, s * 128, 0, g, ids_s[8 * tv + lane],
+            tma_load_4d(sV + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmv, s * C::RB, 0, g, ids_s[8 * tv + lane],
                         &v_full[st]);
         }
         v_last[st] = tv / C::NS;
@@ -437,8 +448,9 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D == 128 && G <= 8) ? 3 : 1
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk) {
             const int byte = kk * 32;
-            const uint64_t ad = smem_desc(sKa + st * C::KTILE + (byte / 128) * C::KSUB + byte % 128, 16, 1024, 2);
-            const uint64_t bd = smem_desc(sQa + (byte / 128) * C::QSUB + byte % 128, 16, 1024, 2);
+            const uint64_t ad =
+                smem_desc(sKa + st * C::KTILE + (byte / C::RB) * C::KSUB + byte % C::RB, 16, 8 * C::RB, C::SWZ);
+            const uint64_t bd = smem_desc(sQa + (byte / C::RB) * C::QSUB + byte % C::RB, 16, 8 * C::RB, C::SWZ);
             umma_f8(tmem + C::TM_S + sb * C::NP, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[sb]);
@@ -460,12 +472,13 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D == 128 && G <= 8) ? 3 : 1
         const int kbase = (bb + 8 * tp) * 16;
         if (kbase + C::BN > T) {
           const int first = max(T - kbase, 0);
-          const int items = (C::BN - first) * C::NSUB * 8;
+          constexpr int CPR = C::RB / 16;  // 16-byte chunks per row
+          const int items = (C::BN - first) * C::NSUB * CPR;
           for (int it = lane; it < items; it += 32) {
-            const int c = it & 7;
-            const int s = (it >> 3) % C::NSUB;
-            const int rr = first + (it >> 3) / C::NSUB;
-            *reinterpret_cast<uint4*>(sV + st * C::KTILE + s * C::KSUB + rr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            const int c = it % CPR;
+            const int s = (it / CPR) % C::NSUB;
+            const int rr = first + (it / CPR) / C::NSUB;
+            *reinterpret_cast<uint4*>(sV + st * C::KTILE + s * C::KSUB + rr * C::RB + c * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -477,7 +490,8 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D == 128 && G <= 8) ? 3 : 1
           for (int s = 0; s < C::NSUB; ++s)
 #pragma unroll
             for (int kk = 0; kk < C::BN / 32; ++kk) {
-              const uint64_t ad = smem_desc(sVa + st * C::KTILE + s * C::KSUB + kk * 32 * 128, 1024, 1024, 2);
+              const uint64_t ad = smem_desc(sVa + st * C::KTILE + s * C::KSUB + kk * 32 * C::RB, 8 * C::RB, 8 * C::RB,
+                                            C::SWZ);
               const uint64_t bd = smem_desc(sPa + pb * C::PTILE + kk * 32, 16, 1024, 2);
               umma_f8(tmem + C::TM_O + (pb * C::NSUB + s) * C::NP, ad, bd, C::IDESC_PV, kk > 0 ? 1u : 0u);
             }
@@ -532,8 +546,8 @@ cudaError_t launch_decode_tc_t(const DecodeParams& p, cudaStream_t s) {
   using C = DecodeTcCfg<D, G>;
   if (p.bps > C::MAX_BPS || p.bps % 8 != 0) return cudaErrorInvalidValue;  // whole tiles, ids staged in smem
   CUtensorMap tmk, tmv;
-  if (!make_pool_map(&tmk, const_cast<uint8_t*>(p.k_cache), D, p.Hkv, p.num_blocks, 128) ||
-      !make_pool_map(&tmv, const_cast<uint8_t*>(p.v_cache), D, p.Hkv, p.num_blocks, 128))
+  if (!make_pool_map(&tmk, const_cast<uint8_t*>(p.k_cache), D, p.Hkv, p.num_blocks, C::RB) ||
+      !make_pool_map(&tmv, const_cast<uint8_t*>(p.v_cache), D, p.Hkv, p.num_blocks, C::RB))
     return cudaErrorInvalidValue;
   auto kern = decode_tc_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -557,9 +571,10 @@ cudaError_t launch_decode_tc_g(const DecodeParams& p, int G, cudaStream_t s) {
 
 }  // namespace
 
-bool decode_uses_tensor_cores(int D, int elt) { return elt == 1 && (D == 128 || D == 256); }
+bool decode_uses_tensor_cores(int D, int elt) { return elt == 1 && (D == 64 || D == 128 || D == 256); }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int D, int G, cudaStream_t s) {
+  if (D == 64) return launch_decode_tc_g<64>(p, G, s);
   if (D == 128) return launch_decode_tc_g<128>(p, G, s);
   if (D == 256) return launch_decode_tc_g<256>(p, G, s);
   return cudaErrorInvalidValue;

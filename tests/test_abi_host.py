@@ -55,8 +55,8 @@ def test_split_planning(lib):
     for auto in (f.fp8_decode_attn_split_blocks(8, 32, 8, 128, 1536), f.fp8_decode_attn_split_blocks(1, 64, 8, 128, 8192)):
         assert auto % 8 == 0 and 8 <= auto <= 128
     # which decodes round P (tensor cores, 128-key tiles) and which keep it exact
-    assert f.fkv_decode_block_n(128) == 128 and f.fkv_decode_block_n(256) == 128
-    assert f.fkv_decode_block_n(64) == 0 and f.fkv_decode_block_n(128, True) == 0
+    assert f.fkv_decode_block_n(128) == 128 and f.fkv_decode_block_n(256) == 128 and f.fkv_decode_block_n(64) == 128
+    assert f.fkv_decode_block_n(128, True) == 0 and f.fkv_decode_block_n(64, True) == 0
     # a window bounds the splits by the window's blocks
     assert f.fp8_decode_attn_num_splits(8, 64, 8, 64, 2048, 128, 0) <= 9
     # 128k keys fit in 1024 splits

@@ -249,7 +249,9 @@ def test_fault_bits_block_id_and_context():
     table, nb = synth.block_table(ctx, seed=1)
     q, k, v = _inputs(rng, ctx, 8, 2, 64)
     one = np.ones(1, np.float32)
-    cache = build_layer(f, ctx, table, nb, k, v, one, one, 0, False)
+    # every pool byte initialised (code 0 = +0.0): the clamped context below reads slots
+    # no token was written to, and the output must stay finite
+    cache = build_layer(f, ctx, table, nb, k, v, one, one, 0, False, sentinel=0x00)
     bad = table.copy()
     bad[0, 1] = nb + 100
     fault = torch.zeros(1, dtype=torch.int32, device="cuda")
