@@ -133,7 +133,11 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
   const int n_t = (be - bb + 7) / 8;
   const int T = r.T;
 
-  if (threadIdx.x == 0) {
+  // The K-producer warp sets up the barriers and, before the CTA-wide barrier, issues the
+  // K and V copies of the first NS tiles, so that the first HBM latency overlaps the rest
+  // of the prologue (TMEM allocation, block-id staging, the query's quantisation).
+  const int n0 = min(C::NS, n_t);  // tiles whose copies go out in the prologue
+  if (warp == 8 && lane == 0) {
     mbar_init(q_full, 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -160,15 +164,44 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     *abort_s = 0;
     fence_mbar_init();
   }
+  if (warp == 8) {
+    __syncwarp();
+    const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks + bb;
+    int id = 0;
+    if (lane < 8 * n0 && lane < be - bb) {  // block `lane` of the split
+      id = trow[lane];
+      if (id < 0 || id >= p.num_blocks) {
+        raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
+        id = 0;
+      }
+      ids_s[lane] = id;
+    }
+    for (int t = 0; t < n0; ++t) {
+      const int nblk = min(8, be - bb - 8 * t);
+      const int idt = __shfl_sync(0xffffffffu, id, 8 * t + (lane & 7));
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&k_full[t], nblk * 16 * D);
+        mbar_arrive_expect_tx(&v_full[t], nblk * 16 * D);
+      }
+      __syncwarp();
+      if (lane < nblk) {
+#pragma unroll
+        for (int s = 0; s < C::NSUB; ++s) {
+          tma_load_4d(sK + t * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmk, s * C::RB, 0, g, idt, &k_full[t]);
+          tma_load_4d(sV + t * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmv, s * C::RB, 0, g, idt, &v_full[t]);
+        }
+      }
+    }
+  }
   if (warp == 9) {
     tmem_alloc(tmem_slot, C::TM_COLS);
     tmem_relinquish();
     tc_fence_before();
   }
-  // the split's block ids, checked once (an id out of range reads block 0 and is reported)
+  // the split's other block ids, checked once (an id out of range reads block 0 and is reported)
   {
     const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks + bb;
-    for (int j = threadIdx.x; j < be - bb; j += blockDim.x) {
+    for (int j = 8 * n0 + threadIdx.x; j < be - bb; j += blockDim.x) {
       int id = trow[j];
       if (id < 0 || id >= p.num_blocks) {
         raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
@@ -379,8 +412,8 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     // lanes at once.
     int last_use[C::NS];
 #pragma unroll
-    for (int s = 0; s < C::NS; ++s) last_use[s] = -1;
-    for (int t = 0; t < n_t; ++t) {
+    for (int s = 0; s < C::NS; ++s) last_use[s] = s < n0 ? 0 : -1;  // the prologue's copies
+    for (int t = n0; t < n_t; ++t) {
       if (abort_warp(abort_s)) break;
       const int st = t % C::NS, use = t / C::NS;
       if (use > 0 && !wait_warp(&k_empty[st], (use - 1) & 1)) {
@@ -410,10 +443,10 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     // they become possible, the V loads, the S^T products and the P.V products, so that
     // a late K tile never holds back a P.V (and the V stage it frees) or vice versa.
     const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV), sPa = smem_u32(sP);
-    int tq = 0, tp = 0, tv = 0;  // next S^T, P.V and V load to issue
+    int tq = 0, tp = 0, tv = n0;  // next S^T, P.V and V load to issue (the first n0 V loads: prologue)
     int v_last[C::NS];
 #pragma unroll
-    for (int s = 0; s < C::NS; ++s) v_last[s] = -1;
+    for (int s = 0; s < C::NS; ++s) v_last[s] = s < n0 ? 0 : -1;
     bool ok = wait_warp(q_full, 0);
     uint64_t t_progress = globaltimer_ns();
     while (ok && tp < n_t) {
