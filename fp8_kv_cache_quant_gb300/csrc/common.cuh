@@ -45,41 +45,6 @@ FKV_DEV void e5m2x4_to_f2(uint32_t w, float2& lo, float2& hi) {
   hi = __half22float2(*reinterpret_cast<const __half2*>(&h23));
 }
 
-// Two e4m3 codes (low byte first) -> half2 (exact: every e4m3 value is an f16 value).
-FKV_DEV __half2 e4m3x2_to_h2(uint16_t v) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-  return *reinterpret_cast<__half2*>(&r);
-}
-
-// Four e4m3 codes packed little-endian in a word -> two half2 (codes 0,1 and 2,3), exact.
-// The word is split into its 16-bit halves by register moves, without integer operations.
-FKV_DEV void e4m3x4_to_h2x2(uint32_t w, __half2& lo, __half2& hi) {
-  uint32_t a, b;
-  asm("{\n\t.reg .b16 l, h;\n\t"
-      "mov.b32 {l, h}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-      : "=r"(a), "=r"(b)
-      : "r"(w));
-  lo = *reinterpret_cast<__half2*>(&a);
-  hi = *reinterpret_cast<__half2*>(&b);
-}
-
-// Four e4m3 codes packed little-endian in a word -> four floats (exact).
-FKV_DEV void e4m3x4_to_f32(uint32_t w, float& a, float& b, float& c, float& d) {
-  float2 lo = __half22float2(e4m3x2_to_h2(static_cast<uint16_t>(w & 0xFFFFu)));
-  float2 hi = __half22float2(e4m3x2_to_h2(static_cast<uint16_t>(w >> 16)));
-  a = lo.x; b = lo.y; c = hi.x; d = hi.y;
-}
-
-FKV_DEV void e4m3x4_to_f2(uint32_t w, float2& lo, float2& hi) {
-  __half2 a, b;
-  e4m3x4_to_h2x2(w, a, b);
-  lo = __half22float2(a);
-  hi = __half22float2(b);
-}
-
 // Two bf16 packed in a word -> float2 (exact).
 FKV_DEV float2 bf16x2_to_f2(uint32_t w) {
   float2 r;

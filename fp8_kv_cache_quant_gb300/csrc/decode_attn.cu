@@ -1,22 +1,23 @@
-// Paged GQA decode attention over an e4m3 (or bf16) KV pool, split-K over the context,
-// FP32 softmax state and P.V sums, then an FP32 log-sum-exp merge of the splits.
+// Paged GQA decode attention on the CUDA cores for the layers whose pools are not e4m3:
+// bf16 (skip layers) and e5m2.  Split-K over the context, FP32 softmax state and P.V
+// sums, then an FP32 log-sum-exp merge of the splits.  (e4m3 layers decode on the tensor
+// cores, decode_tc.cu.)
 //
 // The vLLM blog "FP8 KV-Cache and Attention quantization in vLLM": the decode step must
 // read every cached token, so its cost is the cache bytes (section "性能 Benchmark");
-// the blog tunes dedicated decode configurations (section "Kernel 与 vLLM 改进", "优化
-// FA3 FP8 tile size") and promotes partial sums into true FP32 registers ("Two-level
-// accumulation").  Here each split's partial output lives in FP32 registers and the
-// splits are merged in FP32, so a 128k-key contraction never accumulates in a reduced
-// precision register.
+// skipped layers stay bf16 (section "Kernel 与 vLLM 改进", paragraph "跳过 Layer"); each
+// split's partial output lives in FP32 registers and the splits are merged in FP32
+// ("Two-level accumulation").  vLLM also keeps FP8 caches as e5m2 ("量子化が vLLM の推論
+// 性能に与える影響", "KV キャッシュの量子化"); those codes are widened exactly to FP32 here.
 //
 // CTA = (split, KV head g, sequence b); it serves all G query heads of g, so each K/V
-// byte is read from HBM once.  Warp NCW (the producer) copies each 16-token block's
-// contiguous K chunk and V chunk ([block][g][16][D] in the pool) into a shared-memory
-// ring with cp.async.bulk, completion counted on an mbarrier per stage.  Consumer warp
-// w takes blocks w, w+NCW, ...; per block:
-//   QK : lanes split (key, d-slice); FP32 FMAs on exact e4m3->f32 values; a transposing
-//        shuffle reduction leaves each lane with whole scores;
-//   softmax: running max m and sum l per head (base-2 domain), rescale factor per block;
+// byte is read from HBM once.  Each of the 4 warps owns two tile buffers in shared
+// memory and refills one with cp.async.bulk (each 16-token block's K chunk and V chunk,
+// [block][g][16][D] in the pool, completion on an mbarrier) while it computes the other;
+// warp w takes tiles w, w + 4, ...  Per tile:
+//   QK : lanes split (key, d-slice); FP32 FMAs; a select-free transposing shuffle
+//        reduction leaves each lane with the whole score of one head;
+//   softmax: running max m and sum l per head (base-2 domain), rescale factor per tile;
 //   PV : lanes split (key sub-group, d-slice); acc[h][d] += p[h][key] * v[key][d].
 // The warps' states are merged in shared memory and written as (o / l, log2-sum-exp).
 // Every wait is bounded in time; on a timeout the CTA records FKV_FAULT_TIMEOUT, lets
@@ -33,23 +34,24 @@ constexpr int kNW = 4;           // warps per CTA; every warp prefetches and con
 constexpr int kNBUF = 2;         // tile buffers per warp (one in use, one in flight)
 constexpr int kMaxBps = 128;     // blocks per split, upper bound (table ids staged in smem)
 
-// ELT: the pool's element type — 1 e4m3 (f16 partial sums of exact code products), 2 bf16,
-// 3 e5m2 (the codes widened to FP32, the query unquantised, P exact: as bf16 layers).
+// ELT: the pool's element type — 2 bf16, 3 e5m2 (the codes widened to FP32 with the K/V
+// scales applied; the query unquantised and P exact, as on bf16 layers).
 template <int D, int ELT, int G>
 struct DecodeCfg {
+  static_assert(ELT == 2 || ELT == 3, "bf16 or e5m2 pools");
   static constexpr int ES = ELT == 2 ? 2 : 1;                 // bytes per element
   static constexpr int CHUNK = 16 * D * ES;                   // bytes of one (block, head) chunk
   static constexpr int TB = CHUNK <= 2048 ? 2 : 1;            // 16-key blocks per tile
   static constexpr int TILE_BYTES = TB * 2 * CHUNK;           // K and V of a tile
   static constexpr int RING = kNW * kNBUF * TILE_BYTES;
   // QK mapping: EPL elements (EPL*ES bytes) of one key per lane
-  static constexpr int EPL = ELT == 1 ? (G <= 4 ? 16 : (G == 8 ? 8 : 4)) : (G <= 8 ? 8 : 4);
+  static constexpr int EPL = G <= 8 ? 8 : 4;
   static constexpr int LPK = D / EPL;                         // lanes per key
   static constexpr int KPR = 32 / LPK;                        // keys per round
   static constexpr int ROUNDS = 16 / KPR;                     // rounds per block
   static constexpr int NVF = G > LPK ? G / LPK : 1;           // scores per lane per round
   // PV mapping: VPL elements of one value row per lane
-  static constexpr int VPL0 = ELT == 1 ? (G <= 4 ? 8 : (G == 8 ? 4 : 2)) : (G <= 4 ? 4 : 2);
+  static constexpr int VPL0 = G <= 4 ? 4 : 2;
   static constexpr int VPL = VPL0 > D / 32 ? VPL0 : D / 32;
   static constexpr int LPV = D / VPL;                         // lanes per value row
   static constexpr int KPV = 32 / LPV;                        // keys in parallel
@@ -77,17 +79,10 @@ FKV_DEV void load_bytes(const uint8_t* p, uint32_t (&w)[N / 4 > 0 ? N / 4 : 1]) 
   }
 }
 
-// Convert N elements (e4m3, bf16 or e5m2) held in words to float2 pairs.
+// Convert N elements (bf16 or e5m2) held in words to float2 pairs.
 template <int ELT, int N>
 FKV_DEV void to_f2(const uint32_t* w, float2* out) {
-  if constexpr (ELT == 1) {
-    if constexpr (N >= 4) {
-#pragma unroll
-      for (int i = 0; i < N / 4; ++i) e4m3x4_to_f2(w[i], out[2 * i], out[2 * i + 1]);
-    } else {
-      out[0] = __half22float2(e4m3x2_to_h2(static_cast<uint16_t>(w[0] & 0xFFFFu)));
-    }
-  } else if constexpr (ELT == 3) {
+  if constexpr (ELT == 3) {
     if constexpr (N >= 4) {
 #pragma unroll
       for (int i = 0; i < N / 4; ++i) e5m2x4_to_f2(w[i], out[2 * i], out[2 * i + 1]);
@@ -190,34 +185,16 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
     }
   }
   const bool dup0 = (C::LPK <= G) ? true : ((lane % C::LPK) % (C::LPK / G) == 0);
-  // softmax constant of head hb: softmax_scale * log2(e) * q_s * k_s
-  // On e4m3 layers the QK partial products are summed in packed f16 on exact operands:
-  // query codes times 2^-8 and key codes are f16 values, so each product is exact and at
-  // most 448 * 448 / 256 = 784; each lane adds 8 products per half in f16 and promotes
-  // the two halves into FP32 before the cross-lane reduction (two-level accumulation).
-  // The 2^8 returns in the softmax constant.
-  const float cl = p.sm_scale_log2 *
-                   (ELT == 1   ? 256.f * p.q_scale[p.per_head ? h0 + hb : 0] * p.k_scale[p.per_head ? g : 0]
-                    : ELT == 3 ? p.k_scale[p.per_head ? g : 0]
-                               : 1.f);
-  // query slice in slot order (e4m3 codes * 2^-8 as half2 on FP8 layers, float2 on bf16 layers)
-  float2 qf[ELT == 1 ? 1 : G][C::EPL / 2];
-  __half2 qh[ELT == 1 ? G : 1][C::EPL / 2];
+  // softmax constant: softmax_scale * log2(e), times the K scale on e5m2 layers
+  const float cl = p.sm_scale_log2 * (ELT == 3 ? p.k_scale[p.per_head ? g : 0] : 1.f);
+  // query slice in slot order, FP32
+  float2 qf[G][C::EPL / 2];
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const int h = j ^ hb;
     const __nv_bfloat16* qp = p.q + (static_cast<size_t>(b) * p.Hq + h0 + h) * D + dq;
-    const float iq = ELT == 1 ? __frcp_rn(p.q_scale[p.per_head ? h0 + h : 0]) : 1.f;
 #pragma unroll
-    for (int e = 0; e < C::EPL / 2; ++e) {
-      const float2 x = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(qp + 2 * e));
-      if constexpr (ELT == 1) {
-        const uint16_t c = f32x2_to_e4m3x2(__fmul_rn(x.x, iq), __fmul_rn(x.y, iq));
-        qh[j][e] = __hmul2(e4m3x2_to_h2(c), __float2half2_rn(0.00390625f));  // exact: times 2^-8
-      } else {
-        qf[j][e] = x;
-      }
-    }
+    for (int e = 0; e < C::EPL / 2; ++e) qf[j][e] = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(qp + 2 * e));
   }
 
   float m_run = -INFINITY, l_run = 0.f;
@@ -227,10 +204,8 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
 #pragma unroll
     for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
 
-  // per-warp probabilities of the current tile: float (bf16 layers) or (p, p) half2 pairs
-  // (e4m3 layers, for the packed f16 P.V products); both 4 bytes per (key, head)
+  // per-warp probabilities of the current tile, one float per (key, head)
   float* pw = p_s + warp * 16 * C::TB * G;
-  __half2* pwh = reinterpret_cast<__half2*>(pw);
   float* aw = alpha_s + warp * G;
   int issued = min(kNBUF, max(0, (ntiles - warp + kNW - 1) / kNW));
   int k = 0;
@@ -261,32 +236,14 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
           uint32_t w[C::EPL * C::ES / 4 > 0 ? C::EPL * C::ES / 4 : 1];
           load_bytes<C::EPL * C::ES>(kb + key * D * C::ES + dq * C::ES, w);
           float v[G];
-          if constexpr (ELT == 1) {
-            __half2 kh[C::EPL / 2];
-            if constexpr (C::EPL >= 4) {
+          float2 kf[C::EPL / 2];
+          to_f2<ELT, C::EPL>(w, kf);
 #pragma unroll
-              for (int i = 0; i < C::EPL / 4; ++i) e4m3x4_to_h2x2(w[i], kh[2 * i], kh[2 * i + 1]);
-            } else {
-              kh[0] = e4m3x2_to_h2(static_cast<uint16_t>(w[0] & 0xFFFFu));
-            }
+          for (int h = 0; h < G; ++h) {
+            float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              __half2 a = __hmul2(qh[h][0], kh[0]);
-#pragma unroll
-              for (int e = 1; e < C::EPL / 2; ++e) a = __hfma2(qh[h][e], kh[e], a);
-              const float2 af = __half22float2(a);
-              v[h] = af.x + af.y;
-            }
-          } else {
-            float2 kf[C::EPL / 2];
-            to_f2<ELT, C::EPL>(w, kf);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-              for (int e = 0; e < C::EPL / 2; ++e) a = __ffma2_rn(qf[h][e], kf[e], a);
-              v[h] = a.x + a.y;
-            }
+            for (int e = 0; e < C::EPL / 2; ++e) a = __ffma2_rn(qf[h][e], kf[e], a);
+            v[h] = a.x + a.y;
           }
           // select-free transposing reduction across the LPK lanes of this key
           int nv = G;
@@ -332,11 +289,7 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
         for (int rr = 0; rr < C::ROUNDS; ++rr) {
           const float pv = ex2(sc[j][rr] - mn);
           sum += pv;
-          if (dup0) {
-            const int idx = (j * 16 + rr * C::KPR + kq) * G + hb;
-            if constexpr (ELT == 1) pwh[idx] = __float2half2_rn(pv);
-            else pw[idx] = pv;
-          }
+          if (dup0) pw[(j * 16 + rr * C::KPR + kq) * G + hb] = pv;
         }
 #pragma unroll
       for (int off = C::LPK; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
@@ -359,17 +312,7 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
         }
       }
     }
-    // e4m3 layers: the tile's P.V partial (at most 16 products per element and lane) is
-    // summed in packed f16 on the exact f16 values of the V codes and P rounded to f16,
-    // then promoted into the FP32 accumulator (two-level accumulation).  bf16 layers
-    // multiply and accumulate in FP32.
-    __half2 acc16[G][C::VPL / 2 > 0 ? C::VPL / 2 : 1];
-    if constexpr (ELT == 1) {
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < C::VPL / 2; ++e) acc16[h][e] = __float2half2_rn(0.f);
-    }
+    // P.V in FP32
 #pragma unroll
     for (int j = 0; j < C::TB; ++j) {
       if (j >= nb) break;
@@ -382,52 +325,24 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
         uint32_t w[C::VPL * C::ES / 4 > 0 ? C::VPL * C::ES / 4 : 1];
         load_bytes<C::VPL * C::ES>(vb + key * D * C::ES + dv * C::ES, w);
         const int pidx = (j * 16 + key) * G;
-        if constexpr (ELT == 1) {
-          __half2 vh[C::VPL / 2];
-          if constexpr (C::VPL >= 4) {
+        float2 vf[C::VPL / 2];
+        to_f2<ELT, C::VPL>(w, vf);
+        float pv[G];
+        if constexpr (G % 4 == 0) {
 #pragma unroll
-            for (int i = 0; i < C::VPL / 4; ++i) e4m3x4_to_h2x2(w[i], vh[2 * i], vh[2 * i + 1]);
-          } else {
-            vh[0] = e4m3x2_to_h2(static_cast<uint16_t>(w[0] & 0xFFFFu));
+          for (int h = 0; h < G; h += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(pw + pidx + h);
+            pv[h] = x.x; pv[h + 1] = x.y; pv[h + 2] = x.z; pv[h + 3] = x.w;
           }
-          __half2 ph[G];
-          if constexpr (G % 4 == 0) {
-#pragma unroll
-            for (int h = 0; h < G; h += 4) {
-              const uint4 x = *reinterpret_cast<const uint4*>(pwh + pidx + h);
-              ph[h] = *reinterpret_cast<const __half2*>(&x.x);
-              ph[h + 1] = *reinterpret_cast<const __half2*>(&x.y);
-              ph[h + 2] = *reinterpret_cast<const __half2*>(&x.z);
-              ph[h + 3] = *reinterpret_cast<const __half2*>(&x.w);
-            }
-          } else {
-#pragma unroll
-            for (int h = 0; h < G; ++h) ph[h] = pwh[pidx + h];
-          }
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < C::VPL / 2; ++e) acc16[h][e] = __hfma2(ph[h], vh[e], acc16[h][e]);
         } else {
-          float2 vf[C::VPL / 2];
-          to_f2<ELT, C::VPL>(w, vf);
-          float pv[G];
-          if constexpr (G % 4 == 0) {
 #pragma unroll
-            for (int h = 0; h < G; h += 4) {
-              const float4 x = *reinterpret_cast<const float4*>(pw + pidx + h);
-              pv[h] = x.x; pv[h + 1] = x.y; pv[h + 2] = x.z; pv[h + 3] = x.w;
-            }
-          } else {
+          for (int h = 0; h < G; ++h) pv[h] = pw[pidx + h];
+        }
 #pragma unroll
-            for (int h = 0; h < G; ++h) pv[h] = pw[pidx + h];
-          }
+        for (int h = 0; h < G; ++h) {
+          const float2 p2 = make_float2(pv[h], pv[h]);
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float2 p2 = make_float2(pv[h], pv[h]);
-#pragma unroll
-            for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
-          }
+          for (int e = 0; e < C::VPL / 2; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
         }
       };
       if (kv_lo == 0 && kv_hi == 16) {
@@ -440,16 +355,6 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
           if (key >= kv_lo && key < kv_hi) pv_key(key);
         }
       }
-    }
-    if constexpr (ELT == 1) {
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < C::VPL / 2; ++e) {
-          const float2 x = __half22float2(acc16[h][e]);
-          acc[h][e].x += x.x;
-          acc[h][e].y += x.y;
-        }
     }
     __syncwarp();
     // the buffer is free again: refill it with this warp's tile k + NBUF
@@ -522,64 +427,9 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
   __syncthreads();
   if (!*last_s) return;
   __threadfence();
-  // per head: M = max_s lse_s and 1 / sum_s 2^(lse_s - M) (times the V scale)
-  float* ms_s = reinterpret_cast<float*>(ring);       // [G]
-  float* inv_s = ms_s + G;                            // [G]
-  float* w_s = inv_s + G;                             // [G][CH] weights of a chunk of splits
   constexpr int CH = (C::RING / 4 - 2 * G) / G < 256 ? (C::RING / 4 - 2 * G) / G : 256;
-  const float vs = ELT != 2 ? p.v_scale[p.per_head ? g : 0] : 1.f;
-  const int ns = r.nsplit;
-  for (int t = threadIdx.x; t < G; t += blockDim.x) {
-    const size_t row0 = (static_cast<size_t>(b) * p.Hq + g * G + t) * p.max_splits;
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(p.lse_part + row0 + s2));
-    float W = 0.f;
-    if (M != -INFINITY)
-      for (int s2 = 0; s2 < ns; ++s2) {
-        const float lv = __ldcg(p.lse_part + row0 + s2);
-        W += (lv == -INFINITY) ? 0.f : ex2(lv - M);
-      }
-    ms_s[t] = M;
-    inv_s[t] = (W > 0.f) ? vs / W : 0.f;
-  }
-  constexpr int PAIRS = (G * D / 2 + kNW * 32 - 1) / (kNW * 32);  // output pairs per thread
-  float2 o[PAIRS];
-#pragma unroll
-  for (int k2 = 0; k2 < PAIRS; ++k2) o[k2] = make_float2(0.f, 0.f);
-  for (int c0 = 0; c0 < ns; c0 += CH) {
-    const int nc = min(CH, ns - c0);
-    __syncthreads();
-    for (int t = threadIdx.x; t < G * nc; t += blockDim.x) {
-      const int h = t / nc, j = t % nc;
-      const float lv = __ldcg(p.lse_part + (static_cast<size_t>(b) * p.Hq + g * G + h) * p.max_splits + c0 + j);
-      w_s[h * CH + j] = (lv == -INFINITY) ? 0.f : ex2(lv - ms_s[h]);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k2 = 0; k2 < PAIRS; ++k2) {
-      const int t = threadIdx.x + k2 * kNW * 32;
-      if (t < G * D / 2) {
-        const int h = t / (D / 2), d = 2 * (t % (D / 2));
-        const float* src = p.o_part + ((static_cast<size_t>(b) * p.Hq + g * G + h) * p.max_splits + c0) * D + d;
-        for (int j = 0; j < nc; ++j) {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + static_cast<size_t>(j) * D));
-          const float wv = w_s[h * CH + j];
-          o[k2].x += wv * x.x;
-          o[k2].y += wv * x.y;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int k2 = 0; k2 < PAIRS; ++k2) {
-    const int t = threadIdx.x + k2 * kNW * 32;
-    if (t < G * D / 2) {
-      const int h = t / (D / 2), d = 2 * (t % (D / 2));
-      const float inv = inv_s[h];
-      *reinterpret_cast<__nv_bfloat162*>(p.out + (static_cast<size_t>(b) * p.Hq + g * G + h) * D + d) =
-          __floats2bfloat162_rn(o[k2].x * inv, o[k2].y * inv);
-    }
-  }
+  merge_splits<D, G, kNW * 32, CH>(p, b, g, r.nsplit, ELT == 3 ? p.v_scale[p.per_head ? g : 0] : 1.f,
+                                   reinterpret_cast<float*>(ring));
 }
 
 template <int D, int ELT, int G>
@@ -616,7 +466,6 @@ cudaError_t launch_decode_g(const DecodeParams& p, int G, cudaStream_t s) {
 
 template <int D>
 cudaError_t launch_decode_d(const DecodeParams& p, int elt, int G, cudaStream_t s) {
-  if (elt == 1) return launch_decode_g<D, 1>(p, G, s);
   if (elt == 2) return launch_decode_g<D, 2>(p, G, s);
   if (elt == 3) return launch_decode_g<D, 3>(p, G, s);
   return cudaErrorInvalidValue;
