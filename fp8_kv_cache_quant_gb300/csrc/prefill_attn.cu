@@ -7,22 +7,27 @@
 // paragraph "Two-level accumulation"); head_dim 256 puts the most pressure on that
 // scheme (section "大 Head Dimension 的限制").
 //
-// CTA = (128-query tile, query head h, sequence b); 10 warps:
-//   warps 0-3  softmax warpgroup: quantise the Q tile to e4m3 into shared memory (bf16
-//              layers copy it); then per key tile, thread i owns query row i (TMEM lane
-//              i): load S from TMEM, scale, mask (causal, sliding window), online softmax
-//              (running max m, unrounded sum l), write P8 = e4m3(p * 448) (bf16 layers:
-//              P rounded to bf16) into shared memory, publish the tile's alpha.
-//   warps 4-7  correction warpgroup: promote the tile's P.V partial from TMEM into the
+// CTA = (128-query tile, query head h, sequence b); 14 warps (10 on bf16 layers):
+//   warps 0-7  softmax: quantise the Q tile to e4m3 into shared memory (bf16 layers copy
+//              it); then per key tile thread i of warp w owns query row 32 (w % 4) + lane
+//              (TMEM lane i) and half of the tile's columns (w / 4): load them from TMEM,
+//              scale, mask (causal, sliding window), the row maximum through a half-row
+//              exchange in shared memory, online softmax (running max m, unrounded sum l
+//              per half), write P8 = e4m3(p * 448) (bf16 layers: P rounded to bf16) into
+//              shared memory, publish the tile's alpha.  Two softmax warps per SM quarter
+//              hide each other's TMEM and barrier latency.  (bf16 layers: warps 0-3,
+//              whole rows.)
+//   next 4     correction warpgroup: promote the tile's P.V partial from TMEM into the
 //              FP32 accumulator O = O * alpha + O_tile (every tile, every N tiles, or
 //              never); epilogue O * v_s / (448 * l) -> bf16.
-//   warp 8     TMA: each 16-token block of K and V is one box [16][row bytes] of the
+//   next       TMA: each 16-token block of K and V is one box [16][row bytes] of the
 //              paged pool (4-D tensor map: row bytes, slot-in-block, KV head, block).
-//   warp 9     allocates TMEM, issues S = Q8 K8^T and O_tile = P8 V8 with tcgen05.mma
+//   last       allocates TMEM, issues S = Q8 K8^T and O_tile = P8 V8 with tcgen05.mma
 //              (kind::f8f6f4 for e4m3, kind::f16 for bf16; FP32 accumulation in TMEM),
 //              commits to mbarriers.
-// Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns: S [0, 128 * SBUF),
-// O_tile [TM_OT, TM_OT + DN), O [TM_OA, TM_OA + D); for head_dim 256 the P.V product runs
+// Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns: S [0, 128),
+// O_tile [TM_OT, TM_OT + OTB * DN) (two buffers up to head_dim 128, so that the P.V of
+// tile t overlaps the promotion of tile t-1), O [TM_OA, TM_OA + D); for head_dim 256 the P.V product runs
 // as two N = 128 halves through one O_tile.
 // Every wait is bounded in time; a timeout records FKV_FAULT_TIMEOUT, lets the CTA's
 // copies and MMAs drain and returns.
@@ -63,12 +68,21 @@ struct PrefillCfg {
   static constexpr int PB = BN * ES;                // bytes of one P row
   static constexpr int PTILE = BM * PB;             // bytes of one P tile
   static constexpr int KSTEP = 32 / ES;             // keys (P columns) of one P.V k-step (32 bytes)
-  static constexpr int SBUF = D <= 128 ? 2 : 1;     // S buffers in TMEM
+  static constexpr int SBUF = 1;                    // S buffers in TMEM
+  static constexpr int OTB = D <= 128 ? 2 : 1;      // O_tile buffers in TMEM
   // unrolling of the softmax / correction chunk loops: full for head_dim <= 128 (the
   // softmax is the critical path there), none for 256 (code size of four warp roles)
   static constexpr int UNR = D <= 128 ? 4 : 1;
   static constexpr bool ONE_LOAD = D <= 128;        // S row loaded once into registers
-  static constexpr int TM_OT = 128 * SBUF, TM_OA = TM_OT + DN;
+  // softmax warps per S row: two on e4m3 layers (each half of the row's columns, so that
+  // every SM quarter has two softmax warps to switch between); one on bf16 layers, whose
+  // 2-byte tiles leave no shared memory for the half-row exchange
+  static constexpr int SPLIT = BF ? 1 : 2;
+  static constexpr int HC = BN / SPLIT;             // columns of a softmax thread
+  static constexpr int HCH = HC / 32;               // its 32-column chunks
+  static constexpr int SW = 4 * SPLIT;              // softmax warps (then 4 correction, TMA, MMA)
+  static constexpr int THREADS = 32 * (SW + 6);
+  static constexpr int TM_OT = 128 * SBUF, TM_OA = TM_OT + OTB * DN;
   static constexpr int TM_COLS = (TM_OA + D) <= 256 ? 256 : 512;
   // shared memory layout (bytes)
   static constexpr int OFF_Q = 0;
@@ -76,9 +90,10 @@ struct PrefillCfg {
   static constexpr int OFF_V = OFF_K + NS * KTILE;
   static constexpr int OFF_P = OFF_V + NS * KTILE;          // two P tiles
   static constexpr int OFF_A = OFF_P + 2 * PTILE;           // alpha [2][128] floats
-  static constexpr int OFF_L = OFF_A + 2 * BM * 4;          // l [128] floats
-  static constexpr int OFF_BAR = OFF_L + BM * 4;
-  static constexpr int NBAR = 17 + 4 * NS;
+  static constexpr int OFF_L = OFF_A + 2 * BM * 4;          // l [SPLIT][128] floats
+  static constexpr int OFF_X = OFF_L + SPLIT * BM * 4;      // half-row maxima [2][SPLIT][128] (SPLIT 2)
+  static constexpr int OFF_BAR = OFF_X + (SPLIT == 2 ? 2 * 2 * BM * 4 : 0);
+  static constexpr int NBAR = 21 + 4 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_QK = BF ? idesc_bf16_f32(128, BN, 0, 0) : idesc_e4m3_f32(128, BN, 0, 0);
@@ -86,6 +101,7 @@ struct PrefillCfg {
   static_assert(TM_OA + D <= 512, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(!ONE_LOAD || BN == 128, "the one-load softmax holds a 128-column S row");
+  static_assert(HC % 32 == 0 && (HCH % 2 == 0 || ONE_LOAD || HCH == 1), "softmax chunks");
 };
 
 // One MMA of the element type: e4m3 (kind::f8f6f4) or bf16 (kind::f16), FP32 accumulation.
@@ -95,10 +111,8 @@ FKV_DEV void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t ides
   else umma_f8(d_tmem, adesc, bdesc, idesc, accumulate);
 }
 
-constexpr int kPrefillThreads = 320;  // softmax WG, correction WG, TMA warp, MMA warp
-
 template <int D, bool BF, bool WIN>
-__global__ void __launch_bounds__(kPrefillThreads, 1)
+__global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
   using C = PrefillCfg<D, BF>;
@@ -116,16 +130,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* s_free = bars + 3;      // [2]
   uint64_t* p_full = bars + 5;      // [2]
   uint64_t* p_free = bars + 7;      // [2]
-  uint64_t* o_full = bars + 9;
-  uint64_t* o_free = bars + 10;
-  uint64_t* l_full = bars + 11;
-  uint64_t* mma_done = bars + 12;
-  uint64_t* a_full = bars + 13;     // [2] alpha of a tile published in slot t % 2
-  uint64_t* a_free = bars + 15;     // [2] ... and read by the correction warpgroup
-  uint64_t* k_full = bars + 17;
+  uint64_t* o_full = bars + 9;      // [2] O_tile of P.V pass n in buffer n % OTB
+  uint64_t* o_free = bars + 11;     // [2]
+  uint64_t* l_full = bars + 13;
+  uint64_t* mma_done = bars + 14;
+  uint64_t* a_full = bars + 15;     // [2] alpha of a tile published in slot t % 2
+  uint64_t* a_free = bars + 17;     // [2] ... and read by the correction warpgroup
+  uint64_t* x_full = bars + 19;     // [2] half-row maxima of tile t in slot t % 2 (SPLIT 2)
+  uint64_t* k_full = bars + 21;
   uint64_t* k_empty = k_full + C::NS;
   uint64_t* v_full = k_empty + C::NS;
   uint64_t* v_empty = v_full + C::NS;
+  float* sX = reinterpret_cast<float*>(smem + C::OFF_X);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_s = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
 
@@ -157,21 +173,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int n_t = (kv_end + C::BN - 1) / C::BN - tb;          // tiles u = 0 .. n_t-1 are tb + u
   const int nblk_seq = (T + 15) >> 4;
 
+  constexpr int NSM = 128 * C::SPLIT;  // softmax threads
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 128);
+    mbar_init(q_full, NSM);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&s_free[i], NSM);
+      mbar_init(&p_full[i], NSM);
       mbar_init(&p_free[i], 1);
+      mbar_init(&x_full[i], NSM);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&a_full[i], 128);
       mbar_init(&a_free[i], 128);
     }
-    mbar_init(o_full, 1);
-    mbar_init(o_free, 128);
-    mbar_init(l_full, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_free[i], 128);
+    }
+    mbar_init(l_full, NSM);
     mbar_init(mma_done, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&k_full[s], 1);
@@ -182,7 +202,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     *abort_s = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == C::SW + 5) {
     tmem_alloc(tmem_slot, C::TM_COLS);
     tmem_relinquish();
     tc_fence_before();
@@ -191,18 +211,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
-    // ============================================================ softmax warpgroup
-    const int i = threadIdx.x;                 // query row within the tile (TMEM lane i)
+  if (warp < C::SW) {
+    // ============================================================ softmax warps
+    // Warp w handles rows 32 (w % 4) .. (TMEM lanes of its SM quarter) and, with SPLIT 2,
+    // the columns [HC hf, HC hf + HC) of every S tile, hf = w / 4.
+    const int hf = warp >> 2;
+    const int i = (warp & 3) * 32 + lane;      // query row within the tile (TMEM lane i)
     const bool row_ok = i < rows;
     const int pos = pos0 + i;                  // its absolute position
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    // ---- prologue: Q row -> e4m3 codes (bf16 values on bf16 layers) in the swizzled Q tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const int c0 = hf * C::HC;                 // first column of this thread's half
+    // ---- prologue: Q row -> e4m3 codes (bf16 values on bf16 layers) in the swizzled Q tile;
+    // the row's 16-byte chunks are shared between the row's SPLIT threads
     {
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D);
       const float iq = BF ? 1.f : __frcp_rn(p.q_scale[p.per_head ? h : 0]);
+      constexpr int QCH = C::DB / 16 / C::SPLIT;  // chunks per thread
 #pragma unroll 4
-      for (int c = 0; c < C::DB / 16; ++c) {
+      for (int cc = 0; cc < QCH; ++cc) {
+        const int c = hf * QCH + cc;
         uint4 out = make_uint4(0u, 0u, 0u, 0u);
         if (row_ok) {
           if constexpr (BF) {
@@ -233,63 +260,69 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                          : p.sm_scale_log2 * p.q_scale[p.per_head ? h : 0] * p.k_scale[p.per_head ? g : 0];
     const int lim_row = (p.causal && row_ok) ? min(T, pos + 1) : T;  // keys [lo_row, lim_row) visible
     const int lo_row = (WIN && row_ok) ? max(0, pos - p.window + 1) : 0;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;              // l: this thread's columns only
     bool ok = true;
     for (int t = 0; t < n_t; ++t) {
       if (abort_warp(abort_s)) { ok = false; break; }
       const int sb = t % C::SBUF;
       if (!wait_warp(&s_full[sb], (t / C::SBUF) & 1)) { ok = false; break; }
       tc_fence_after();
-      const int kbase = (tb + t) * C::BN;
-      const int lim = lim_row - kbase;      // columns [lo, lim) of this tile are visible
+      const int kbase = (tb + t) * C::BN + c0;  // key of this thread's first column
+      const int lim = lim_row - kbase;      // columns [lo, lim) of this thread's half are visible
       // full-attention instantiations fold the lower bound away (it costs the softmax
       // warps dearly when it is a run-time value)
       const int lo = WIN ? lo_row - kbase : -(1 << 30);
-      const bool full = lim >= C::BN && (!WIN || lo <= 0);  // interior tile for this row: nothing masked
-      const uint32_t sc = lane_base + 128 * sb;
-      float vall[C::ONE_LOAD ? 128 : 1];
+      const bool full = lim >= C::HC && (!WIN || lo <= 0);  // nothing masked in this half
+      const uint32_t sc = lane_base + 128 * sb + c0;
+      float vall[C::ONE_LOAD ? C::HC : 1];
       float tmax = -INFINITY;
       if constexpr (C::ONE_LOAD) {
-        // head_dim <= 128: the whole S row in registers, one TMEM wait; S is released at once
+        // head_dim <= 128: the half row in registers, one TMEM wait; S is released at once
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(sc + 32 * c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
+        for (int c = 0; c < C::HCH; ++c) tmem_ld32(sc + 32 * c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&s_free[sb]);
         if (full) {
           float mx = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 128; j += 4) mx = fmax3(mx, fmax3(vall[j], vall[j + 1], vall[j + 2]), vall[j + 3]);
+          for (int j = 0; j < C::HC; j += 4) mx = fmax3(mx, fmax3(vall[j], vall[j + 1], vall[j + 2]), vall[j + 3]);
           tmax = mx * cst;
         } else {
 #pragma unroll
-          for (int j = 0; j < 128; ++j) tmax = fmaxf(tmax, (j < lim && j >= lo) ? vall[j] * cst : -INFINITY);
+          for (int j = 0; j < C::HC; ++j) tmax = fmaxf(tmax, (j < lim && j >= lo) ? vall[j] * cst : -INFINITY);
         }
       } else {
-        // pass 1: row max of the scaled, masked scores (cst > 0, so the raw maximum scales).
+        // pass 1: max of the scaled, masked scores (cst > 0, so the raw maximum scales).
         // The TMEM loads are warp-collective: every lane issues them; only the arithmetic
-        // depends on the row's own mask.  Loops run over 32-column chunks and are not
-        // unrolled at that level, to keep the warp roles' code small.
-        {
-          float mx = -INFINITY;
+        // depends on the row's own mask.
+        float mx = -INFINITY;
   #pragma unroll C::UNR
-          for (int c = 0; c < C::NCH; ++c) {
-            float v[32];
-            tmem_ld32(sc + 32 * c, v);
-            tmem_ld_wait();
-            if (full) {
+        for (int c = 0; c < C::HCH; ++c) {
+          float v[32];
+          tmem_ld32(sc + 32 * c, v);
+          tmem_ld_wait();
+          if (full) {
   #pragma unroll
-              for (int j = 0; j < 32; j += 4) mx = fmax3(mx, fmax3(v[j], v[j + 1], v[j + 2]), v[j + 3]);
-            } else {
+            for (int j = 0; j < 32; j += 4) mx = fmax3(mx, fmax3(v[j], v[j + 1], v[j + 2]), v[j + 3]);
+          } else {
   #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int col = 32 * c + j;
-                tmax = fmaxf(tmax, (col < lim && col >= lo) ? v[j] * cst : -INFINITY);
-              }
+            for (int j = 0; j < 32; ++j) {
+              const int col = 32 * c + j;
+              tmax = fmaxf(tmax, (col < lim && col >= lo) ? v[j] * cst : -INFINITY);
             }
           }
-          if (full) tmax = mx * cst;
         }
+        if (full) tmax = mx * cst;
+      }
+      if constexpr (C::SPLIT == 2) {
+        // the row's maximum: this half's and the other half's (slot t % 2; its previous
+        // use, t - 2, was read by every softmax thread before its arrival for t - 1)
+        float* xs = sX + (t & 1) * 2 * C::BM;
+        xs[hf * C::BM + i] = tmax;
+        mbar_arrive(&x_full[t & 1]);
+        if (!wait_warp(&x_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+        tmax = fmaxf(tmax, xs[(hf ^ 1) * C::BM + i]);
       }
       const float mn = fmaxf(m, tmax);
       const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
@@ -303,7 +336,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       float2 lsum2 = make_float2(0.f, 0.f);
       const float2 cst2 = make_float2(cst, cst), nm2 = make_float2(-msafe, -msafe);
       const float2 k448 = make_float2(448.f, 448.f);
-      auto chunk = [&](const float (&v)[32], int c) {
+      auto chunk = [&](const float (&v)[32], int c) {  // c: chunk of this thread's half
         uint32_t pk[8 * C::ES];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
@@ -331,7 +364,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         // 32 columns = 32 * ES bytes of the P row, in 16-byte pieces
 #pragma unroll
         for (int q = 0; q < 2 * C::ES; ++q) {
-          const int byte = 32 * C::ES * c + 16 * q;
+          const int byte = (c0 + 32 * c) * C::ES + 16 * q;
           const uint32_t lin = static_cast<uint32_t>(i * 128 + (byte % 128));
           *reinterpret_cast<uint4*>(P + (byte / 128) * (C::BM * 128) + swz(lin, 128)) =
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -339,20 +372,23 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       };
       if constexpr (C::ONE_LOAD) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) chunk(*reinterpret_cast<const float(*)[32]>(vall + 32 * c), c);
+        for (int c = 0; c < C::HCH; ++c) chunk(*reinterpret_cast<const float(*)[32]>(vall + 32 * c), c);
+      } else if constexpr (C::HCH == 1) {
+        float va[32];
+        tmem_ld32(sc, va);
+        tmem_ld_wait();
+        chunk(va, 0);
       } else {
-        {
-          float va[32], vb[32];
-          tmem_ld32(sc, va);
+        float va[32], vb[32];
+        tmem_ld32(sc, va);
   #pragma unroll C::UNR
-          for (int c = 0; c < C::NCH; c += 2) {
-            tmem_ld_wait();
-            tmem_ld32(sc + 32 * (c + 1), vb);
-            chunk(va, c);
-            tmem_ld_wait();
-            if (c + 2 < C::NCH) tmem_ld32(sc + 32 * (c + 2), va);
-            chunk(vb, c + 1);
-          }
+        for (int c = 0; c < C::HCH; c += 2) {
+          tmem_ld_wait();
+          tmem_ld32(sc + 32 * (c + 1), vb);
+          chunk(va, c);
+          tmem_ld_wait();
+          if (c + 2 < C::HCH) tmem_ld32(sc + 32 * (c + 2), va);
+          chunk(vb, c + 1);
         }
       }
       const float lsum = lsum2.x + lsum2.y;
@@ -362,10 +398,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       l = l * alpha + lsum;
       m = mn;
-      // alpha slot t%2 is free once the correction warpgroup has read tile t-2's alpha
-      if (t >= 2 && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
-      sAlpha[pb * C::BM + i] = alpha;
-      mbar_arrive(&a_full[pb]);
+      // alpha (the same in both halves) goes out from half 0; its slot t%2 is free once
+      // the correction warpgroup has read tile t-2's alpha
+      if (hf == 0) {
+        if (t >= 2 && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+        sAlpha[pb * C::BM + i] = alpha;
+        mbar_arrive(&a_full[pb]);
+      }
       fence_proxy_async_smem();
       mbar_arrive(&p_full[pb]);
     }
@@ -373,13 +412,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
       *abort_s = 1;
     }
-    sL[i] = l;
+    sL[hf * C::BM + i] = l;
     mbar_arrive(l_full);
-  } else if (warp < 8) {
+  } else if (warp < C::SW + 4) {
     // ============================================================ correction warpgroup
-    const int i = threadIdx.x - 128;           // query row (TMEM lane i)
+    const int i = threadIdx.x - 32 * C::SW;    // query row (TMEM lane i)
     const bool row_ok = i < rows;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - C::SW) * 32) << 16);
     int npv = 0;
     bool ok = true;
     const int pe = p.promote_every;
@@ -391,13 +430,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const float alpha = sAlpha[(t & 1) * C::BM + i];
         mbar_arrive(&a_free[t & 1]);
         for (int hn = 0; hn < C::NH; ++hn) {
-          if (!wait_warp(o_full, npv & 1)) { ok = false; break; }
+          const int ob = npv % C::OTB;
+          if (!wait_warp(&o_full[ob], (npv / C::OTB) & 1)) { ok = false; break; }
           ++npv;
           tc_fence_after();
 #pragma unroll C::UNR
           for (int c = 0; c < C::DN / 32; ++c) {
             float ot[32], oa[32];
-            tmem_ld32(lane_base + C::TM_OT + 32 * c, ot);
+            tmem_ld32(lane_base + C::TM_OT + ob * C::DN + 32 * c, ot);
             if (t > 0) tmem_ld32(lane_base + C::TM_OA + hn * C::DN + 32 * c, oa);
             tmem_ld_wait();
             if (t > 0) {
@@ -411,7 +451,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           }
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(o_free);
+          mbar_arrive(&o_free[ob]);
         }
         if (!ok) break;
       }
@@ -480,7 +520,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
     // ---- epilogue: O * v_s / (448 l) -> bf16 (every lane loads; rows past the chunk do not store)
     if (wait_warp(l_full, 0) && !abort_warp(abort_s)) {
-      const float l = sL[i];
+      float l = sL[i];
+      if constexpr (C::SPLIT == 2) l += sL[C::BM + i];  // the two halves' sums
       const float vs = BF ? 1.f : p.v_scale[p.per_head ? g : 0];
       const float f = (l > 0.f) ? vs / ((BF ? 1.f : 448.f) * l) : 0.f;
       __nv_bfloat16* dst = p.out + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D;
@@ -502,7 +543,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == C::SW + 4) {
     // ============================================================ TMA producer
     const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
     int last_use[C::NS];
@@ -572,7 +613,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
     }
   } else {
-    // ============================================================ MMA issuer (warp 9)
+    // ============================================================ MMA issuer (last warp)
     const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV), sPa = smem_u32(sP);
     int npv = 0;
     // S(t) = Q8 K8^T into S buffer t % SBUF
@@ -636,10 +677,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       if (p.promote_every == 1) {
         for (int hn = 0; hn < C::NH; ++hn) {
-          if (npv > 0 && !wait_warp(o_free, (npv - 1) & 1)) return false;
+          // O_tile buffer npv % OTB is free once the correction promoted pass npv - OTB
+          const int ob = npv % C::OTB;
+          if (npv >= C::OTB && !wait_warp(&o_free[ob], ((npv / C::OTB) - 1) & 1)) return false;
           tc_fence_after();
-          if (lane == 0) issue_pv_pass(st, pb, hn, tmem + C::TM_OT, true);
-          if (lane == 0) umma_commit(o_full);
+          if (lane == 0) issue_pv_pass(st, pb, hn, tmem + C::TM_OT + ob * C::DN, true);
+          if (lane == 0) umma_commit(&o_full[ob]);
           __syncwarp();
           ++npv;
         }
@@ -683,7 +726,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     __syncwarp();
   }
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::SW + 5) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TM_COLS);
   }
@@ -745,7 +788,7 @@ cudaError_t launch_prefill_t(const PrefillParams& p, void* kc, void* vc, cudaStr
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_qtiles, p.Hq, p.B);
-  kern<<<grid, kPrefillThreads, C::SMEM, s>>>(p, tmk, tmv);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(p, tmk, tmv);
   return cudaGetLastError();
 }
 

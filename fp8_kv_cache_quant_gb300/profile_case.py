@@ -32,6 +32,8 @@ def main():
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--prefill", action="store_true",
                     help="run fp8_prefill_attn on the head_dim-256 prefill shape instead (batch 1)")
+    ap.add_argument("--llama", action="store_true",
+                    help="with --prefill: the Llama-3.1-8B head shape (32/8 heads, head_dim 128)")
     ap.add_argument("--seq", type=int, default=8192, help="prefill sequence length")
     a = ap.parse_args()
     if a.prefill:
@@ -67,6 +69,8 @@ def run_prefill(a):
     import synth
 
     w = synth.WORKLOADS[5]
+    if a.llama:
+        w = synth.PrefillWorkload("llama8b-prefill-h32x8-d128", 1, a.seq, 32, 8, 128, seed=1)
     dev = torch.device("cuda:0")
     data = synth.prefill_data(w, device=dev, seq_len=a.seq, batch=1)
     ctx = np.array([a.seq], np.int32)
