@@ -7,7 +7,7 @@
 // paragraph "Two-level accumulation"); head_dim 256 puts the most pressure on that
 // scheme (section "大 Head Dimension 的限制").
 //
-// CTA = (128-query tile, query head h, sequence b); 14 warps (10 on bf16 layers):
+// CTA = (128-query tile, query head h, sequence b); 15 warps (11 on bf16 layers):
 //   warps 0-7  softmax: quantise the Q tile to e4m3 into shared memory (bf16 layers copy
 //              it); then per key tile thread i of warp w owns query row 32 (w % 4) + lane
 //              (TMEM lane i) and half of the tile's columns (w / 4): load them from TMEM,
@@ -19,12 +19,13 @@
 //              whole rows.)
 //   next 4     correction warpgroup: promote the tile's P.V partial from TMEM into the
 //              FP32 accumulator O = O * alpha + O_tile (every tile, every N tiles, or
-//              never); epilogue O * v_s / (448 * l) -> bf16.
+//              never); epilogue O * v_s / l -> bf16 (l sums p * 448 on e4m3 layers).
 //   next       TMA: each 16-token block of K and V is one box [16][row bytes] of the
 //              paged pool (4-D tensor map: row bytes, slot-in-block, KV head, block).
-//   last       allocates TMEM, issues S = Q8 K8^T and O_tile = P8 V8 with tcgen05.mma
-//              (kind::f8f6f4 for e4m3, kind::f16 for bf16; FP32 accumulation in TMEM),
-//              commits to mbarriers.
+//   next       allocates TMEM, issues S = Q8 K8^T with tcgen05.mma (kind::f8f6f4 for e4m3,
+//              kind::f16 for bf16; FP32 accumulation in TMEM), commits to mbarriers.
+//   last       issues O_tile = P8 V8 the same way (an MMA issue holds its thread for about
+//              the product's duration, so the two chains run on two warps).
 // Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns: S [0, 128),
 // O_tile [TM_OT, TM_OT + OTB * DN) (two buffers up to head_dim 128, so that the P.V of
 // tile t overlaps the promotion of tile t-1), O [TM_OA, TM_OA + D); for head_dim 256 the P.V product runs
@@ -39,10 +40,26 @@
 
 namespace fkv {
 
+constexpr float kLog2E4m3Max = 8.807354922057604f;  // log2(448)
+
 FKV_DEV float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
+}
+
+// Maximum of N values as a tree of three-input maxima (depth log3 N, rather than a chain
+// of N / 2 dependent operations).
+template <int N>
+FKV_DEV float max_tree(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else if constexpr (N == 2) {
+    return fmaxf(v[0], v[1]);
+  } else {
+    constexpr int A = (N + 2) / 3, B = (N - A + 1) / 2;
+    return fmax3(max_tree<A>(v), max_tree<B>(v + A), max_tree<N - A - B>(v + A + B));
+  }
 }
 
 template <int D, bool BF>
@@ -80,8 +97,8 @@ struct PrefillCfg {
   static constexpr int SPLIT = BF ? 1 : 2;
   static constexpr int HC = BN / SPLIT;             // columns of a softmax thread
   static constexpr int HCH = HC / 32;               // its 32-column chunks
-  static constexpr int SW = 4 * SPLIT;              // softmax warps (then 4 correction, TMA, MMA)
-  static constexpr int THREADS = 32 * (SW + 6);
+  static constexpr int SW = 4 * SPLIT;              // softmax warps (then 4 correction, TMA, 2 MMA)
+  static constexpr int THREADS = 32 * (SW + 7);
   static constexpr int TM_OT = 128 * SBUF, TM_OA = TM_OT + OTB * DN;
   static constexpr int TM_COLS = (TM_OA + D) <= 256 ? 256 : 512;
   // shared memory layout (bytes)
@@ -173,7 +190,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
   const int n_t = (kv_end + C::BN - 1) / C::BN - tb;          // tiles u = 0 .. n_t-1 are tb + u
   const int nblk_seq = (T + 15) >> 4;
 
-  constexpr int NSM = 128 * C::SPLIT;  // softmax threads
+  // barriers signalled by the softmax or correction warps count warps (one arrival each)
+  constexpr int NSM = C::SW;  // softmax warps
   if (threadIdx.x == 0) {
     mbar_init(q_full, NSM);
     for (int i = 0; i < 2; ++i) {
@@ -184,15 +202,15 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       mbar_init(&x_full[i], NSM);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], 128);
-      mbar_init(&a_free[i], 128);
+      mbar_init(&a_full[i], 4);
+      mbar_init(&a_free[i], 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&o_full[i], 1);
-      mbar_init(&o_free[i], 128);
+      mbar_init(&o_free[i], 4);
     }
     mbar_init(l_full, NSM);
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, 2);  // one commit from each MMA warp
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -254,7 +272,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         *reinterpret_cast<uint4*>(sQ + sub * C::SUB + swz(lin, C::RB)) = out;
       }
       fence_proxy_async_smem();
-      mbar_arrive(q_full);
+      mbar_arrive_warp(q_full);
     }
     const float cst = BF ? p.sm_scale_log2
                          : p.sm_scale_log2 * p.q_scale[p.per_head ? h : 0] * p.k_scale[p.per_head ? g : 0];
@@ -282,12 +300,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         for (int c = 0; c < C::HCH; ++c) tmem_ld32(sc + 32 * c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&s_free[sb]);
+        mbar_arrive_warp(&s_free[sb]);
         if (full) {
-          float mx = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < C::HC; j += 4) mx = fmax3(mx, fmax3(vall[j], vall[j + 1], vall[j + 2]), vall[j + 3]);
-          tmax = mx * cst;
+          tmax = max_tree<C::HC>(vall) * cst;
         } else {
 #pragma unroll
           for (int j = 0; j < C::HC; ++j) tmax = fmaxf(tmax, (j < lim && j >= lo) ? vall[j] * cst : -INFINITY);
@@ -303,8 +318,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
           tmem_ld32(sc + 32 * c, v);
           tmem_ld_wait();
           if (full) {
-  #pragma unroll
-            for (int j = 0; j < 32; j += 4) mx = fmax3(mx, fmax3(v[j], v[j + 1], v[j + 2]), v[j + 3]);
+            mx = fmaxf(mx, max_tree<32>(v));
           } else {
   #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -320,7 +334,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         // use, t - 2, was read by every softmax thread before its arrival for t - 1)
         float* xs = sX + (t & 1) * 2 * C::BM;
         xs[hf * C::BM + i] = tmax;
-        mbar_arrive(&x_full[t & 1]);
+        mbar_arrive_warp(&x_full[t & 1]);
         if (!wait_warp(&x_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
         tmax = fmaxf(tmax, xs[(hf ^ 1) * C::BM + i]);
       }
@@ -334,8 +348,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       // pass 2: p = 2^(s*cst - m), its unrounded sum, and P8 = e4m3(p * 448) into the P tile;
       // the next chunk's TMEM load is in flight while the current one is processed
       float2 lsum2 = make_float2(0.f, 0.f);
-      const float2 cst2 = make_float2(cst, cst), nm2 = make_float2(-msafe, -msafe);
-      const float2 k448 = make_float2(448.f, 448.f);
+      // e4m3 layers fold the factor 448 of P8 into the exponent: p * 448 = 2^(s*cst - m + log2 448),
+      // so l sums p * 448 and the epilogue divides by l alone
+      const float nb = (BF ? 0.f : kLog2E4m3Max) - msafe;
+      const float2 cst2 = make_float2(cst, cst), nm2 = make_float2(nb, nb);
       auto chunk = [&](const float (&v)[32], int c) {  // c: chunk of this thread's half
         uint32_t pk[8 * C::ES];
 #pragma unroll
@@ -356,9 +372,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
             pk[j / 2] = *reinterpret_cast<uint32_t*>(&b0);
             pk[j / 2 + 1] = *reinterpret_cast<uint32_t*>(&b1);
           } else {
-            const float2 y0 = __fmul2_rn(x0, k448), y1 = __fmul2_rn(x1, k448);
-            pk[j / 4] = static_cast<uint32_t>(f32x2_to_e4m3x2(y0.x, y0.y)) |
-                        (static_cast<uint32_t>(f32x2_to_e4m3x2(y1.x, y1.y)) << 16);
+            pk[j / 4] = static_cast<uint32_t>(f32x2_to_e4m3x2(x0.x, x0.y)) |
+                        (static_cast<uint32_t>(f32x2_to_e4m3x2(x1.x, x1.y)) << 16);
           }
         }
         // 32 columns = 32 * ES bytes of the P row, in 16-byte pieces
@@ -394,7 +409,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       const float lsum = lsum2.x + lsum2.y;
       if constexpr (!C::ONE_LOAD) {
         tc_fence_before();
-        mbar_arrive(&s_free[sb]);
+        mbar_arrive_warp(&s_free[sb]);
       }
       l = l * alpha + lsum;
       m = mn;
@@ -403,17 +418,17 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       if (hf == 0) {
         if (t >= 2 && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
         sAlpha[pb * C::BM + i] = alpha;
-        mbar_arrive(&a_full[pb]);
+        mbar_arrive_warp(&a_full[pb]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&p_full[pb]);
+      mbar_arrive_warp(&p_full[pb]);
     }
     if (!ok) {
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
       *abort_s = 1;
     }
     sL[hf * C::BM + i] = l;
-    mbar_arrive(l_full);
+    mbar_arrive_warp(l_full);
   } else if (warp < C::SW + 4) {
     // ============================================================ correction warpgroup
     const int i = threadIdx.x - 32 * C::SW;    // query row (TMEM lane i)
@@ -428,7 +443,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         if (abort_warp(abort_s)) { ok = false; break; }
         if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
         const float alpha = sAlpha[(t & 1) * C::BM + i];
-        mbar_arrive(&a_free[t & 1]);
+        mbar_arrive_warp(&a_free[t & 1]);
         for (int hn = 0; hn < C::NH; ++hn) {
           const int ob = npv % C::OTB;
           if (!wait_warp(&o_full[ob], (npv / C::OTB) & 1)) { ok = false; break; }
@@ -451,7 +466,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
           }
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(&o_free[ob]);
+          mbar_arrive_warp(&o_free[ob]);
         }
         if (!ok) break;
       }
@@ -467,7 +482,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         if (abort_warp(abort_s)) { ok = false; break; }
         if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
         const float alpha = sAlpha[(t & 1) * C::BM + i];
-        mbar_arrive(&a_free[t & 1]);
+        mbar_arrive_warp(&a_free[t & 1]);
         A *= alpha;
         const bool start = pe == 0 ? t == 0 : (t % pe) == 0;
         if (!start) {
@@ -485,7 +500,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
             tmem_st_wait();
           }
           tc_fence_before();
-          mbar_arrive(o_free);
+          mbar_arrive_warp(o_free);
         }
         if (!wait_warp(o_full, t & 1)) { ok = false; break; }
         tc_fence_after();
@@ -510,7 +525,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
           have_o = true;
           A = 1.f;
           tc_fence_before();
-          mbar_arrive(o_free);
+          mbar_arrive_warp(o_free);
         }
       }
     }
@@ -518,12 +533,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
       *abort_s = 1;
     }
-    // ---- epilogue: O * v_s / (448 l) -> bf16 (every lane loads; rows past the chunk do not store)
+    // ---- epilogue: O * v_s / l -> bf16 (every lane loads; rows past the chunk do not store)
     if (wait_warp(l_full, 0) && !abort_warp(abort_s)) {
       float l = sL[i];
       if constexpr (C::SPLIT == 2) l += sL[C::BM + i];  // the two halves' sums
       const float vs = BF ? 1.f : p.v_scale[p.per_head ? g : 0];
-      const float f = (l > 0.f) ? vs / ((BF ? 1.f : 448.f) * l) : 0.f;
+      const float f = (l > 0.f) ? vs / l : 0.f;  // l sums p * 448 on e4m3 layers
       __nv_bfloat16* dst = p.out + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -613,8 +628,18 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       }
     }
   } else {
-    // ============================================================ MMA issuer (last warp)
-    const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV), sPa = smem_u32(sP);
+    // ============================================================ MMA issuers
+    // Warp SW+5 issues S = Q8 K8^T, warp SW+6 O_tile = P8 V8.  A tcgen05.mma issue holds
+    // its thread for about the product's execution time and a commit for tens of cycles, so
+    // one thread issuing both chains (two products, five commits and five waits per tile)
+    // would take longer per tile than the softmax; on two warps the chains overlap.
+    const bool qk_warp = warp == C::SW + 5;
+    // operand descriptors of the tile bases; every operand is one of them advanced by a
+    // compile-time or per-stage byte offset (desc_add)
+    const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 8 * C::RB, C::SWZ);
+    const uint64_t dK = smem_desc(smem_u32(sK), 16, 8 * C::RB, C::SWZ);
+    const uint64_t dV = smem_desc(smem_u32(sV), 8 * C::RB, 8 * C::RB, C::SWZ);
+    const uint64_t dP = smem_desc(smem_u32(sP), 16, 1024, 2);
     int npv = 0;
     // S(t) = Q8 K8^T into S buffer t % SBUF
     auto issue_qk = [&](int t) -> bool {
@@ -628,9 +653,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
           const int byte = kk * 32;
           const uint32_t qoff = (byte / C::RB) * C::SUB + (byte % C::RB);
           const uint32_t koff = (byte / C::RB) * C::KSUB + (byte % C::RB);
-          const uint64_t ad = smem_desc(sQa + qoff, 16, 8 * C::RB, C::SWZ);
-          const uint64_t bd = smem_desc(sKa + st * C::KTILE + koff, 16, 8 * C::RB, C::SWZ);
-          umma<BF>(tmem + 128 * sb, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          umma<BF>(tmem + 128 * sb, desc_add(dQ, qoff), desc_add(dK, st * C::KTILE + koff), C::IDESC_QK,
+                   kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[sb]);
         umma_commit(&k_empty[st]);
@@ -644,12 +668,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
 #pragma unroll
       for (int kk = 0; kk < C::PB / 32; ++kk) {
         const int pbyte = kk * 32;
-        const uint64_t ad = smem_desc(sPa + pb * C::PTILE + (pbyte / 128) * (C::BM * 128) + (pbyte % 128), 16, 1024, 2);
+        const uint64_t ad = desc_add(dP, pb * C::PTILE + (pbyte / 128) * (C::BM * 128) + (pbyte % 128));
 #pragma unroll
         for (int j = 0; j < C::DN / C::EPS; ++j) {
           const int sub = hn * (C::DN / C::EPS) + j;
-          const uint64_t bd = smem_desc(sVa + st * C::KTILE + sub * C::KSUB + kk * C::KSTEP * C::RB, 8 * C::RB,
-                                        8 * C::RB, C::SWZ);
+          const uint64_t bd = desc_add(dV, st * C::KTILE + sub * C::KSUB + kk * C::KSTEP * C::RB);
           umma<BF>(dst + j * C::EPS, ad, bd, C::IDESC_PV, (kk > 0 || !fresh) ? 1u : 0u);
         }
       }
@@ -708,17 +731,25 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       __syncwarp();
       return true;
     };
-    bool ok = wait_warp(q_full, 0) && issue_qk(0);
-    for (int t = 0; ok && t < n_t; ++t) {
-      if (abort_warp(abort_s)) break;
-      if (t + 1 < n_t) ok = issue_qk(t + 1);  // S of the next tile overlaps this tile's softmax
-      if (ok) ok = issue_pv(t);
+    bool ok = true;
+    if (qk_warp) {
+      // S(t+1) is computed while the softmax works on tile t (S is released once loaded)
+      ok = wait_warp(q_full, 0);
+      for (int t = 0; ok && t < n_t; ++t) {
+        if (abort_warp(abort_s)) break;
+        ok = issue_qk(t);
+      }
+    } else {
+      for (int t = 0; ok && t < n_t; ++t) {
+        if (abort_warp(abort_s)) break;
+        ok = issue_pv(t);
+      }
     }
     if (!ok) {
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
       *abort_s = 1;
     }
-    // every MMA issued by this warp completes before TMEM is released
+    // every MMA issued by either warp completes before TMEM is released
     if (lane == 0) {
       umma_commit(mma_done);
       wait_ns(mma_done, 0);

@@ -88,6 +88,11 @@ FKV_DEV uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t 
   return d;
 }
 
+// The descriptor of the operand byte_off bytes further on: the start address field holds
+// address >> 4 in its low 14 bits, so for shared-memory addresses below 256 KB (every
+// offset a multiple of 16) the sum carries into no other field.
+FKV_DEV uint64_t desc_add(uint64_t desc, uint32_t byte_off) { return desc + (byte_off >> 4); }
+
 // Instruction descriptor for kind::f8f6f4 with e4m3 A and B, FP32 accumulation.
 // a_mn / b_mn: operand stored MN-major (1) or K-major (0).
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, int b_mn) {
@@ -130,6 +135,16 @@ FKV_DEV void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// One arrival on behalf of the whole (converged) warp: the warp barrier orders every lane's
+// earlier writes before lane 0's releasing arrive.  A barrier counted in warps takes 32x
+// fewer arrive operations than one counted in threads; each is an update of the same
+// shared-memory word, and hundreds of them per tile delay every other barrier operation
+// of the CTA (the MMA warp's waits and commits among them).
+FKV_DEV void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // ---------------------------------------------------------------- waits
 
 // Pipeline waits of the tensor-core kernels: bounded in wall-clock time (a timeout makes
@@ -137,13 +152,22 @@ FKV_DEV void umma_commit(uint64_t* bar) {
 // rather than spinning.
 constexpr uint64_t kPipeWaitNs = 200000000ull;  // 200 ms per wait
 
-FKV_DEV bool wait_ns(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The timed part of a wait lives out of line: an inlined wait is then one try_wait and a
+// branch.  The MMA and TMA warps pass through many waits per tile, and code that a warp
+// runs once per tile has to be fetched into the instruction cache again every tile (the
+// softmax warps' unrolled loops on the same SM quarter displace it), so their code size
+// is their speed.
+static __device__ __noinline__ bool wait_ns_timed(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
     if (globaltimer_ns() - t0 > kPipeWaitNs) return false;
   }
+}
+
+FKV_DEV bool wait_ns(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_ns_timed(bar, parity);
 }
 
 // Warp-uniform forms: tcgen05.ld / st are warp-collective, so every lane of a warp must
