@@ -560,10 +560,19 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
     }
   } else if (warp == C::SW + 4) {
     // ============================================================ TMA producer
+    // Lane j < NBLK copies the tile's j-th 16-token block (K and V): copies issued from one
+    // thread are serialised, from eight lanes they are in flight together.  The block ids
+    // of tile t+1 are read while tile t's copies are issued.
     const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-    int last_use[C::NS];
+    int k_last[C::NS], v_last[C::NS];  // last use of each stage whose copies were issued
 #pragma unroll
-    for (int s = 0; s < C::NS; ++s) last_use[s] = -1;
+    for (int s = 0; s < C::NS; ++s) k_last[s] = v_last[s] = -1;
+    // blocks past the context read block 0 (their keys are masked)
+    auto block_id = [&](int t) -> int {
+      const int lb = (tb + t) * C::NBLK + lane;
+      return (lane < C::NBLK && t < n_t && lb < nblk_seq) ? trow[lb] : 0;
+    };
+    int id_next = block_id(0);
     for (int t = 0; t < n_t; ++t) {
       int stop = *abort_s;
       if (lane == 0 && (t & 7) == 7 && p.fault && (*reinterpret_cast<volatile int*>(p.fault) & FKV_FAULT_TIMEOUT))
@@ -572,59 +581,50 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         *abort_s = 1;
         break;
       }
-      // NBLK block ids of the tile; blocks past the context read block 0 (their keys are masked)
-      int id = 0;
-      if (lane < C::NBLK) {
-        const int lb = (tb + t) * C::NBLK + lane;
-        if (lb < nblk_seq) {
-          id = trow[lb];
-          if (id < 0 || id >= p.num_blocks) {
-            raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
-            id = 0;
-          }
-        }
+      int id = id_next;
+      if (id < 0 || id >= p.num_blocks) {
+        raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
+        id = 0;
       }
-      int ids[C::NBLK];
-#pragma unroll
-      for (int j = 0; j < C::NBLK; ++j) ids[j] = __shfl_sync(0xffffffffu, id, j);
+      id_next = block_id(t + 1);
       const int st = t % C::NS, use = t / C::NS;
       bool ok = true;
-      if (lane == 0) {
-        if (use > 0) ok = wait_ns(&k_empty[st], (use - 1) & 1);
-        if (ok) {
-          mbar_arrive_expect_tx(&k_full[st], C::KTILE);
-#pragma unroll
-          for (int j = 0; j < C::NBLK; ++j)
-#pragma unroll
-            for (int s = 0; s < C::NSUB; ++s)
-              tma_load_4d(sK + st * C::KTILE + s * C::KSUB + j * 16 * C::RB, &tmk, s * C::RB, 0, g, ids[j],
-                          &k_full[st]);
-          if (use > 0) ok = wait_ns(&v_empty[st], (use - 1) & 1);
-          if (ok) {
-            mbar_arrive_expect_tx(&v_full[st], C::KTILE);
-#pragma unroll
-            for (int j = 0; j < C::NBLK; ++j)
-#pragma unroll
-              for (int s = 0; s < C::NSUB; ++s)
-                tma_load_4d(sV + st * C::KTILE + s * C::KSUB + j * 16 * C::RB, &tmv, s * C::RB, 0, g, ids[j],
-                            &v_full[st]);
-          }
-          last_use[st] = use;
-        }
-        if (!ok) {
-          raise_fault(p.fault, FKV_FAULT_TIMEOUT);
-          *abort_s = 1;
-        }
-      }
+      if (lane == 0 && use > 0) ok = wait_ns(&k_empty[st], (use - 1) & 1);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
+      if (ok) {
+        // the expected byte count is posted before any of the copies can complete
+        if (lane == 0) mbar_arrive_expect_tx(&k_full[st], C::KTILE);
+        __syncwarp();
+        if (lane < C::NBLK) {
+#pragma unroll
+          for (int s = 0; s < C::NSUB; ++s)
+            tma_load_4d(sK + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmk, s * C::RB, 0, g, id, &k_full[st]);
+        }
+        k_last[st] = use;
+        if (lane == 0 && use > 0) ok = wait_ns(&v_empty[st], (use - 1) & 1);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      }
+      if (ok) {
+        if (lane == 0) mbar_arrive_expect_tx(&v_full[st], C::KTILE);
+        __syncwarp();
+        if (lane < C::NBLK) {
+#pragma unroll
+          for (int s = 0; s < C::NSUB; ++s)
+            tma_load_4d(sV + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmv, s * C::RB, 0, g, id, &v_full[st]);
+        }
+        v_last[st] = use;
+      }
+      if (!ok) {
+        if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
+        *abort_s = 1;
+        break;
+      }
     }
     // let every issued copy land before the CTA can exit
     if (lane == 0) {
       for (int s = 0; s < C::NS; ++s) {
-        if (last_use[s] < 0) continue;
-        wait_ns(&k_full[s], last_use[s] & 1);
-        wait_ns(&v_full[s], last_use[s] & 1);
+        if (k_last[s] >= 0) wait_ns(&k_full[s], k_last[s] & 1);
+        if (v_last[s] >= 0) wait_ns(&v_full[s], v_last[s] & 1);
       }
     }
   } else {
