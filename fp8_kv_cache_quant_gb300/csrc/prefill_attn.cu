@@ -110,7 +110,7 @@ struct PrefillCfg {
   static constexpr int OFF_L = OFF_A + 2 * BM * 4;          // l [SPLIT][128] floats
   static constexpr int OFF_X = OFF_L + SPLIT * BM * 4;      // half-row maxima [2][SPLIT][128] (SPLIT 2)
   static constexpr int OFF_BAR = OFF_X + (SPLIT == 2 ? 2 * 2 * BM * 4 : 0);
-  static constexpr int NBAR = 21 + 4 * NS;
+  static constexpr int NBAR = 27 + 4 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_QK = BF ? idesc_bf16_f32(128, BN, 0, 0) : idesc_e4m3_f32(128, BN, 0, 0);
@@ -153,8 +153,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
   uint64_t* mma_done = bars + 14;
   uint64_t* a_full = bars + 15;     // [2] alpha of a tile published in slot t % 2
   uint64_t* a_free = bars + 17;     // [2] ... and read by the correction warpgroup
-  uint64_t* x_full = bars + 19;     // [2] half-row maxima of tile t in slot t % 2 (SPLIT 2)
-  uint64_t* k_full = bars + 21;
+  uint64_t* x_full = bars + 19;     // [4][2] half-row maxima of tile t, slot t % 2, per SM quarter (SPLIT 2)
+  uint64_t* k_full = bars + 27;
   uint64_t* k_empty = k_full + C::NS;
   uint64_t* v_full = k_empty + C::NS;
   uint64_t* v_empty = v_full + C::NS;
@@ -199,8 +199,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       mbar_init(&s_free[i], NSM);
       mbar_init(&p_full[i], NSM);
       mbar_init(&p_free[i], 1);
-      mbar_init(&x_full[i], NSM);
     }
+    for (int i = 0; i < 8; ++i) mbar_init(&x_full[i], 2);  // the two warps of an SM quarter
     for (int i = 0; i < 2; ++i) {
       mbar_init(&a_full[i], 4);
       mbar_init(&a_free[i], 4);
@@ -281,10 +281,17 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
     float m = -INFINITY, l = 0.f;              // l: this thread's columns only
     bool ok = true;
     for (int t = 0; t < n_t; ++t) {
-      if (abort_warp(abort_s)) { ok = false; break; }
+      // another warp's timeout is noticed every 8 tiles (every wait is bounded anyway)
+      if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
       const int sb = t % C::SBUF;
       if (!wait_warp(&s_full[sb], (t / C::SBUF) & 1)) { ok = false; break; }
       tc_fence_after();
+      // the P and alpha slots of tile t (freed by tile t-2's P.V and correction) are
+      // normally free long before they are written: test them now without blocking, and
+      // wait further down only if they were not
+      const int pb = t & 1;
+      const bool p_ready = t < 2 || mbar_test_wait(&p_free[pb], ((t >> 1) - 1) & 1);
+      const bool a_ready = t < 2 || hf != 0 || mbar_test_wait(&a_free[pb], ((t >> 1) - 1) & 1);
       const int kbase = (tb + t) * C::BN + c0;  // key of this thread's first column
       const int lim = lim_row - kbase;      // columns [lo, lim) of this thread's half are visible
       // full-attention instantiations fold the lower bound away (it costs the softmax
@@ -330,20 +337,21 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         if (full) tmax = mx * cst;
       }
       if constexpr (C::SPLIT == 2) {
-        // the row's maximum: this half's and the other half's (slot t % 2; its previous
-        // use, t - 2, was read by every softmax thread before its arrival for t - 1)
+        // the row's maximum: this half's and the other half's, exchanged with the one other
+        // warp of the SM quarter (slot t % 2; its previous use, t - 2, was read by the
+        // partner before its arrival for t - 1)
         float* xs = sX + (t & 1) * 2 * C::BM;
         xs[hf * C::BM + i] = tmax;
-        mbar_arrive_warp(&x_full[t & 1]);
-        if (!wait_warp(&x_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+        uint64_t* xb = &x_full[(warp & 3) * 2 + (t & 1)];
+        mbar_arrive_warp(xb);
+        if (!wait_warp(xb, (t >> 1) & 1)) { ok = false; break; }
         tmax = fmaxf(tmax, xs[(hf ^ 1) * C::BM + i]);
       }
       const float mn = fmaxf(m, tmax);
       const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
       const float msafe = (mn == -INFINITY) ? 0.f : mn;
       // P tile t%2 is free once the P.V of tile t-2 completed
-      const int pb = t & 1;
-      if (t >= 2 && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, p_ready) && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
       uint8_t* P = sP + pb * C::PTILE;
       // pass 2: p = 2^(s*cst - m), its unrounded sum, and P8 = e4m3(p * 448) into the P tile;
       // the next chunk's TMEM load is in flight while the current one is processed
@@ -416,7 +424,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       // alpha (the same in both halves) goes out from half 0; its slot t%2 is free once
       // the correction warpgroup has read tile t-2's alpha
       if (hf == 0) {
-        if (t >= 2 && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, a_ready) && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
         sAlpha[pb * C::BM + i] = alpha;
         mbar_arrive_warp(&a_full[pb]);
       }
@@ -440,7 +448,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
     if (pe == 1) {
       // two-level accumulation every tile: O = O * alpha + O_tile after each P.V
       for (int t = 0; t < n_t; ++t) {
-        if (abort_warp(abort_s)) { ok = false; break; }
+        if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
         if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
         const float alpha = sAlpha[(t & 1) * C::BM + i];
         mbar_arrive_warp(&a_free[t & 1]);
@@ -479,7 +487,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       float A = 1.f;         // product of the alphas since the last promotion
       bool have_o = false;   // O holds promoted groups
       for (int t = 0; t < n_t; ++t) {
-        if (abort_warp(abort_s)) { ok = false; break; }
+        if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
         if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
         const float alpha = sAlpha[(t & 1) * C::BM + i];
         mbar_arrive_warp(&a_free[t & 1]);
@@ -736,12 +744,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       // S(t+1) is computed while the softmax works on tile t (S is released once loaded)
       ok = wait_warp(q_full, 0);
       for (int t = 0; ok && t < n_t; ++t) {
-        if (abort_warp(abort_s)) break;
+        if ((t & 7) == 7 && abort_warp(abort_s)) break;
         ok = issue_qk(t);
       }
     } else {
       for (int t = 0; ok && t < n_t; ++t) {
-        if (abort_warp(abort_s)) break;
+        if ((t & 7) == 7 && abort_warp(abort_s)) break;
         ok = issue_pv(t);
       }
     }
