@@ -47,6 +47,19 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_source_sha(kernel_file: str) -> str:
+    """First 16 hex digits of the sha256 of a kernel's .cu file followed by the shared
+    headers it includes (common.cuh, tc.cuh, decode_common.cuh, kernels.h): a profile
+    summary stays valid only while none of them has changed."""
+    csrc = os.path.join(ROOT, "fp8_kv_cache_quant_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (kernel_file, "common.cuh", "tc.cuh", "decode_common.cuh", "kernels.h"):
+        path = os.path.join(csrc, name)
+        if os.path.exists(path):
+            h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
+
+
 def _traffic_record(kernel_file: str, summary: str):
     """dram bytes per launch from a committed ncu summary, if it was taken on the
     current kernel source (same sha256); else None."""
@@ -54,7 +67,7 @@ def _traffic_record(kernel_file: str, summary: str):
     src = os.path.join(ROOT, "fp8_kv_cache_quant_gb300", "csrc", kernel_file)
     if not (os.path.exists(path) and os.path.exists(src)):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha(kernel_file)
     rec = {}
     for line in open(path):
         if ":" in line:

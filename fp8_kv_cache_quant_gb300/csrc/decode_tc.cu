@@ -138,23 +138,24 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
   // of the prologue (TMEM allocation, block-id staging, the query's quantisation).
   const int n0 = min(C::NS, n_t);  // tiles whose copies go out in the prologue
   if (warp == 8 && lane == 0) {
-    mbar_init(q_full, 128);
+    // barriers signalled by the softmax or correction warps count warps (one arrival each)
+    mbar_init(q_full, 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
       mbar_init(&p_free[i], 1);
       mbar_init(&o_full[i], 1);
-      mbar_init(&o_free[i], 128);
+      mbar_init(&o_free[i], 4);
     }
     mbar_init(mma_done, 1);
     mbar_init(&red_full[0], 4);
     mbar_init(&red_full[1], 4);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], 128);
-      mbar_init(&a_free[i], 128);
+      mbar_init(&a_full[i], 4);
+      mbar_init(&a_free[i], 4);
     }
-    mbar_init(l_full, 128);
+    mbar_init(l_full, 4);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(q_full);
+      mbar_arrive_warp(q_full);
     }
     float cst[G];  // log2(e) * softmax scale * q_s[h] * k_s[g]
 #pragma unroll
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     }
     bool ok = true;
     for (int t = 0; t < n_t; ++t) {
-      if (abort_warp(abort_s)) { ok = false; break; }
+      if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
       const int sb = t & 1;
       if (!wait_warp(&s_full[sb], (t >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       tmem_ld16(lane_base + C::TM_S + sb * C::NP, s16);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&s_free[sb]);
+      mbar_arrive_warp(&s_free[sb]);
       const int key = (bb + 8 * t) * 16 + i;
       const bool valid = key >= klo && key < khi;
       float x[G], wm[G];
@@ -315,8 +316,8 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         if (i == 0) alpha_s[pb * C::NP + h] = alpha;
       }
       fence_proxy_async_smem();
-      mbar_arrive(&p_full[pb]);
-      mbar_arrive(&a_full[pb]);
+      mbar_arrive_warp(&p_full[pb]);
+      mbar_arrive_warp(&a_full[pb]);
     }
     if (!ok) {
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         ml_s[C::NP + h] = (red[h] + red[C::NP + h]) + (red[2 * C::NP + h] + red[3 * C::NP + h]);
       }
     }
-    if (ok) mbar_arrive(l_full);
+    if (ok) mbar_arrive_warp(l_full);
   } else if (warp < 8) {
     // ============================================================ correction warpgroup
     const int i = threadIdx.x - 128;  // TMEM lane i
@@ -362,13 +363,13 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       for (int s2 = 0; s2 < C::NSUB; ++s2) acc[s2][h] = 0.f;
     bool ok = true;
     for (int t = 0; t < n_t; ++t) {
-      if (abort_warp(abort_s)) { ok = false; break; }
+      if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
       const int ob = t & 1;
       if (!wait_warp(&a_full[ob], (t >> 1) & 1)) { ok = false; break; }
       float alpha[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) alpha[h] = alpha_s[ob * C::NP + h];
-      mbar_arrive(&a_free[ob]);
+      mbar_arrive_warp(&a_free[ob]);
       // acc = acc * alpha + O_tile^T(t): the two-level accumulation of tile t
       if (!wait_warp(&o_full[ob], (t >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       for (int s2 = 0; s2 < C::NSUB; ++s2) tmem_ld16(lane_base + C::TM_O + (ob * C::NSUB + s2) * C::NP, o[s2]);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&o_free[ob]);
+      mbar_arrive_warp(&o_free[ob]);
 #pragma unroll
       for (int s2 = 0; s2 < C::NSUB; ++s2)
 #pragma unroll
