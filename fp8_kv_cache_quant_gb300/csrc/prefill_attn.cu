@@ -9,14 +9,14 @@
 //
 // CTA = (128-query tile, query head h, sequence b); 15 warps (11 on bf16 layers):
 //   warps 0-7  softmax: quantise the Q tile to e4m3 into shared memory (bf16 layers copy
-//              it); then per key tile thread i of warp w owns query row 32 (w % 4) + lane
-//              (TMEM lane i) and half of the tile's columns (w / 4): load them from TMEM,
-//              scale, mask (causal, sliding window), the row maximum through a half-row
-//              exchange in shared memory, online softmax (running max m, unrounded sum l
-//              per half), write P8 = e4m3(p * 448) (bf16 layers: P rounded to bf16) into
-//              shared memory, publish the tile's alpha.  Two softmax warps per SM quarter
-//              hide each other's TMEM and barrier latency.  (bf16 layers: warps 0-3,
-//              whole rows.)
+//              it); then per key tile warp w owns 16 query rows of its SM quarter (TMEM
+//              lanes 32 (w % 4) + 16 (w / 4) ..), lanes l and l + 16 each half of a row's
+//              columns (16x32bx2 TMEM loads): scale, mask (causal, sliding window), the row
+//              maximum (one shuffle between the halves), online softmax (running max m,
+//              unrounded sum l per half), write P8 = e4m3(p * 448) (bf16 layers: P rounded
+//              to bf16) into shared memory, publish the tile's alpha.  Two softmax warps
+//              per SM quarter hide each other's TMEM and barrier latency.  (bf16 layers:
+//              warps 0-3, one whole row per lane.)
 //   next 4     correction warpgroup: promote the tile's P.V partial from TMEM into the
 //              FP32 accumulator O = O * alpha + O_tile (every tile, every N tiles, or
 //              never); epilogue O * v_s / l -> bf16 (l sums p * 448 on e4m3 layers).
@@ -108,9 +108,8 @@ struct PrefillCfg {
   static constexpr int OFF_P = OFF_V + NS * KTILE;          // two P tiles
   static constexpr int OFF_A = OFF_P + 2 * PTILE;           // alpha [2][128] floats
   static constexpr int OFF_L = OFF_A + 2 * BM * 4;          // l [SPLIT][128] floats
-  static constexpr int OFF_X = OFF_L + SPLIT * BM * 4;      // half-row maxima [2][SPLIT][128] (SPLIT 2)
-  static constexpr int OFF_BAR = OFF_X + (SPLIT == 2 ? 2 * 2 * BM * 4 : 0);
-  static constexpr int NBAR = 27 + 4 * NS;
+  static constexpr int OFF_BAR = OFF_L + SPLIT * BM * 4;
+  static constexpr int NBAR = 19 + 4 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_QK = BF ? idesc_bf16_f32(128, BN, 0, 0) : idesc_e4m3_f32(128, BN, 0, 0);
@@ -153,12 +152,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
   uint64_t* mma_done = bars + 14;
   uint64_t* a_full = bars + 15;     // [2] alpha of a tile published in slot t % 2
   uint64_t* a_free = bars + 17;     // [2] ... and read by the correction warpgroup
-  uint64_t* x_full = bars + 19;     // [4][2] half-row maxima of tile t, slot t % 2, per SM quarter (SPLIT 2)
-  uint64_t* k_full = bars + 27;
+  uint64_t* k_full = bars + 19;
   uint64_t* k_empty = k_full + C::NS;
   uint64_t* v_full = k_empty + C::NS;
   uint64_t* v_empty = v_full + C::NS;
-  float* sX = reinterpret_cast<float*>(smem + C::OFF_X);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_s = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
 
@@ -200,9 +197,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       mbar_init(&p_full[i], NSM);
       mbar_init(&p_free[i], 1);
     }
-    for (int i = 0; i < 8; ++i) mbar_init(&x_full[i], 2);  // the two warps of an SM quarter
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], 4);
+      mbar_init(&a_full[i], NSM);
       mbar_init(&a_free[i], 4);
     }
     for (int i = 0; i < 2; ++i) {
@@ -231,13 +227,16 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
 
   if (warp < C::SW) {
     // ============================================================ softmax warps
-    // Warp w handles rows 32 (w % 4) .. (TMEM lanes of its SM quarter) and, with SPLIT 2,
-    // the columns [HC hf, HC hf + HC) of every S tile, hf = w / 4.
-    const int hf = warp >> 2;
-    const int i = (warp & 3) * 32 + lane;      // query row within the tile (TMEM lane i)
+    // SPLIT 1: warp w holds the 32 rows of its SM quarter (TMEM lanes 32 (w % 4) ..), one per
+    // lane, all columns.  SPLIT 2: warp w holds 16 of them, 32 (w % 4) + 16 (w / 4) + (lane % 16),
+    // lanes l and l + 16 each half of the row's columns (the 16x32bx2 TMEM load shape), so that
+    // the row maximum is one shuffle away.
+    const int hf = C::SPLIT == 2 ? lane >> 4 : 0;  // column half
+    const int rb = C::SPLIT == 2 ? (warp & 3) * 32 + (warp >> 2) * 16 : (warp & 3) * 32;  // first TMEM lane
+    const int i = rb + (C::SPLIT == 2 ? (lane & 15) : lane);  // query row within the tile (TMEM lane i)
     const bool row_ok = i < rows;
     const int pos = pos0 + i;                  // its absolute position
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(rb) << 16);
     const int c0 = hf * C::HC;                 // first column of this thread's half
     // ---- prologue: Q row -> e4m3 codes (bf16 values on bf16 layers) in the swizzled Q tile;
     // the row's 16-byte chunks are shared between the row's SPLIT threads
@@ -291,20 +290,26 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       // wait further down only if they were not
       const int pb = t & 1;
       const bool p_ready = t < 2 || mbar_test_wait(&p_free[pb], ((t >> 1) - 1) & 1);
-      const bool a_ready = t < 2 || hf != 0 || mbar_test_wait(&a_free[pb], ((t >> 1) - 1) & 1);
+      const bool a_ready = t < 2 || mbar_test_wait(&a_free[pb], ((t >> 1) - 1) & 1);
       const int kbase = (tb + t) * C::BN + c0;  // key of this thread's first column
       const int lim = lim_row - kbase;      // columns [lo, lim) of this thread's half are visible
       // full-attention instantiations fold the lower bound away (it costs the softmax
       // warps dearly when it is a run-time value)
       const int lo = WIN ? lo_row - kbase : -(1 << 30);
       const bool full = lim >= C::HC && (!WIN || lo <= 0);  // nothing masked in this half
-      const uint32_t sc = lane_base + 128 * sb + c0;
+      // chunk c (32 columns) of this thread's columns: its own 32 columns of the row from
+      // [c0 + 32 c, ...), where the 16x32bx2 shape adds c0 = HC for the upper lanes itself
+      const uint32_t sc = lane_base + 128 * sb;
+      auto ld_s = [&](int c, float (&v)[32]) {
+        if constexpr (C::SPLIT == 2) tmem_ld32_16x2<C::HC>(sc + 32 * c, v);
+        else tmem_ld32(sc + 32 * c, v);
+      };
       float vall[C::ONE_LOAD ? C::HC : 1];
       float tmax = -INFINITY;
       if constexpr (C::ONE_LOAD) {
         // head_dim <= 128: the half row in registers, one TMEM wait; S is released at once
 #pragma unroll
-        for (int c = 0; c < C::HCH; ++c) tmem_ld32(sc + 32 * c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
+        for (int c = 0; c < C::HCH; ++c) ld_s(c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive_warp(&s_free[sb]);
@@ -322,7 +327,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
   #pragma unroll C::UNR
         for (int c = 0; c < C::HCH; ++c) {
           float v[32];
-          tmem_ld32(sc + 32 * c, v);
+          ld_s(c, v);
           tmem_ld_wait();
           if (full) {
             mx = fmaxf(mx, max_tree<32>(v));
@@ -336,17 +341,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         }
         if (full) tmax = mx * cst;
       }
-      if constexpr (C::SPLIT == 2) {
-        // the row's maximum: this half's and the other half's, exchanged with the one other
-        // warp of the SM quarter (slot t % 2; its previous use, t - 2, was read by the
-        // partner before its arrival for t - 1)
-        float* xs = sX + (t & 1) * 2 * C::BM;
-        xs[hf * C::BM + i] = tmax;
-        uint64_t* xb = &x_full[(warp & 3) * 2 + (t & 1)];
-        mbar_arrive_warp(xb);
-        if (!wait_warp(xb, (t >> 1) & 1)) { ok = false; break; }
-        tmax = fmaxf(tmax, xs[(hf ^ 1) * C::BM + i]);
-      }
+      // the row's maximum: this half's and the other half's (lane l ^ 16)
+      if constexpr (C::SPLIT == 2) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
       const float mn = fmaxf(m, tmax);
       const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
       const float msafe = (mn == -INFINITY) ? 0.f : mn;
@@ -398,19 +394,19 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         for (int c = 0; c < C::HCH; ++c) chunk(*reinterpret_cast<const float(*)[32]>(vall + 32 * c), c);
       } else if constexpr (C::HCH == 1) {
         float va[32];
-        tmem_ld32(sc, va);
+        ld_s(0, va);
         tmem_ld_wait();
         chunk(va, 0);
       } else {
         float va[32], vb[32];
-        tmem_ld32(sc, va);
+        ld_s(0, va);
   #pragma unroll C::UNR
         for (int c = 0; c < C::HCH; c += 2) {
           tmem_ld_wait();
-          tmem_ld32(sc + 32 * (c + 1), vb);
+          ld_s(c + 1, vb);
           chunk(va, c);
           tmem_ld_wait();
-          if (c + 2 < C::HCH) tmem_ld32(sc + 32 * (c + 2), va);
+          if (c + 2 < C::HCH) ld_s(c + 2, va);
           chunk(vb, c + 1);
         }
       }
@@ -421,13 +417,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       }
       l = l * alpha + lsum;
       m = mn;
-      // alpha (the same in both halves) goes out from half 0; its slot t%2 is free once
-      // the correction warpgroup has read tile t-2's alpha
-      if (hf == 0) {
-        if (!__all_sync(0xffffffffu, a_ready) && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
-        sAlpha[pb * C::BM + i] = alpha;
-        mbar_arrive_warp(&a_full[pb]);
-      }
+      // alpha (the same in both halves) is written by half 0; its slot t%2 is free once the
+      // correction warpgroup has read tile t-2's alpha
+      if (!__all_sync(0xffffffffu, a_ready) && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+      if (hf == 0) sAlpha[pb * C::BM + i] = alpha;
+      mbar_arrive_warp(&a_full[pb]);
       fence_proxy_async_smem();
       mbar_arrive_warp(&p_full[pb]);
     }
