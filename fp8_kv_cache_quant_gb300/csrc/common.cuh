@@ -68,10 +68,9 @@ FKV_DEV void fence_mbar_init() {
 }
 
 FKV_DEV void mbar_arrive(uint64_t* bar) {
-  asm volatile(
-      "{\n\t.reg .b64 st;\n\t"
-      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
-      : "memory");
+  // the returned state is not needed: the sink operand lets the arrive retire without
+  // a result to wait for
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 FKV_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {

@@ -7,7 +7,8 @@
 // paragraph "Two-level accumulation"); head_dim 256 puts the most pressure on that
 // scheme (section "大 Head Dimension 的限制").
 //
-// CTA = (128-query tile, query head h, sequence b); 15 warps (11 on bf16 layers):
+// CTA = (128-query tile, query head h, sequence b); 16 warps (12 on bf16 layers; one fewer
+// at head_dim 256):
 //   warps 0-7  softmax: quantise the Q tile to e4m3 into shared memory (bf16 layers copy
 //              it); then per key tile warp w owns 16 query rows of its SM quarter (TMEM
 //              lanes 32 (w % 4) + 16 (w / 4) ..), lanes l and l + 16 each half of a row's
@@ -20,12 +21,14 @@
 //   next 4     correction warpgroup: promote the tile's P.V partial from TMEM into the
 //              FP32 accumulator O = O * alpha + O_tile (every tile, every N tiles, or
 //              never); epilogue O * v_s / l -> bf16 (l sums p * 448 on e4m3 layers).
-//   next       TMA: each 16-token block of K and V is one box [16][row bytes] of the
-//              paged pool (4-D tensor map: row bytes, slot-in-block, KV head, block).
+//   next       TMA, K tiles: each 16-token block is one box [16][row bytes] of the paged
+//              pool (4-D tensor map: row bytes, slot-in-block, KV head, block).
 //   next       allocates TMEM, issues S = Q8 K8^T with tcgen05.mma (kind::f8f6f4 for e4m3,
 //              kind::f16 for bf16; FP32 accumulation in TMEM), commits to mbarriers.
-//   last       issues O_tile = P8 V8 the same way (an MMA issue holds its thread for about
+//   next       issues O_tile = P8 V8 the same way (an MMA issue holds its thread for about
 //              the product's duration, so the two chains run on two warps).
+//   last       TMA, V tiles (a warp's copies go out one after another, so K and V have a
+//              warp each up to head_dim 128; at 256 the K warp copies both).
 // Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns: S [0, 128),
 // O_tile [TM_OT, TM_OT + OTB * DN) (two buffers up to head_dim 128, so that the P.V of
 // tile t overlaps the promotion of tile t-1), O [TM_OA, TM_OA + D); for head_dim 256 the P.V product runs
@@ -97,8 +100,11 @@ struct PrefillCfg {
   static constexpr int SPLIT = BF ? 1 : 2;
   static constexpr int HC = BN / SPLIT;             // columns of a softmax thread
   static constexpr int HCH = HC / 32;               // its 32-column chunks
-  static constexpr int SW = 4 * SPLIT;              // softmax warps (then 4 correction, TMA, 2 MMA)
-  static constexpr int THREADS = 32 * (SW + 7);
+  static constexpr int SW = 4 * SPLIT;              // softmax warps (then 4 correction, K copies, 2 MMA, V copies)
+  // TMA warps: K and V apart up to head_dim 128; at head_dim 256 (two boxes per block, two
+  // stages) one warp copying both measured faster
+  static constexpr int KVW = D <= 128 ? 2 : 1;
+  static constexpr int THREADS = 32 * (SW + 6 + KVW);
   static constexpr int TM_OT = 128 * SBUF, TM_OA = TM_OT + OTB * DN;
   static constexpr int TM_COLS = (TM_OA + D) <= 256 ? 256 : 512;
   // shared memory layout (bytes)
@@ -560,15 +566,19 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
         }
       }
     }
-  } else if (warp == C::SW + 4) {
-    // ============================================================ TMA producer
-    // Lane j < NBLK copies the tile's j-th 16-token block (K and V): copies issued from one
-    // thread are serialised, from eight lanes they are in flight together.  The block ids
-    // of tile t+1 are read while tile t's copies are issued.
+  } else if (warp == C::SW + 4 || warp == C::SW + 7) {
+    // ============================================================ TMA producers
+    // Up to head_dim 128 warp SW+4 copies the K tiles and warp SW+7 the V tiles: a warp's
+    // copies go out one after another (about 100 cycles per 2 KiB box), so two warps halve
+    // the time a tile's sixteen copies take.  At head_dim 256 warp SW+4 copies both.  Lane
+    // j < NBLK copies the tile's j-th 16-token block; the block ids of tile t+1 are read
+    // while tile t's copies are issued.
+    const int kind0 = warp == C::SW + 7 ? 1 : 0;  // 0: K, 1: V
+    constexpr int KINDS = C::KVW == 2 ? 1 : 2;    // kinds this warp copies
     const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-    int k_last[C::NS], v_last[C::NS];  // last use of each stage whose copies were issued
+    int last[2][C::NS];  // last use of each stage whose copies were issued
 #pragma unroll
-    for (int s = 0; s < C::NS; ++s) k_last[s] = v_last[s] = -1;
+    for (int s = 0; s < C::NS; ++s) last[0][s] = last[1][s] = -1;
     // blocks past the context read block 0 (their keys are masked)
     auto block_id = [&](int t) -> int {
       const int lb = (tb + t) * C::NBLK + lane;
@@ -591,30 +601,23 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       id_next = block_id(t + 1);
       const int st = t % C::NS, use = t / C::NS;
       bool ok = true;
-      if (lane == 0 && use > 0) ok = wait_ns(&k_empty[st], (use - 1) & 1);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (ok) {
-        // the expected byte count is posted before any of the copies can complete
-        if (lane == 0) mbar_arrive_expect_tx(&k_full[st], C::KTILE);
-        __syncwarp();
-        if (lane < C::NBLK) {
 #pragma unroll
-          for (int s = 0; s < C::NSUB; ++s)
-            tma_load_4d(sK + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmk, s * C::RB, 0, g, id, &k_full[st]);
-        }
-        k_last[st] = use;
-        if (lane == 0 && use > 0) ok = wait_ns(&v_empty[st], (use - 1) & 1);
+      for (int kk = 0; kk < KINDS; ++kk) {
+        const int kind = kind0 + kk;
+        uint64_t* full = kind ? v_full : k_full;
+        if (lane == 0 && use > 0) ok = wait_ns(kind ? &v_empty[st] : &k_empty[st], (use - 1) & 1);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      }
-      if (ok) {
-        if (lane == 0) mbar_arrive_expect_tx(&v_full[st], C::KTILE);
+        if (!ok) break;
+        // the expected byte count is posted before any of the copies can complete
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], C::KTILE);
         __syncwarp();
         if (lane < C::NBLK) {
+          uint8_t* dst = (kind ? sV : sK) + st * C::KTILE + lane * 16 * C::RB;
 #pragma unroll
           for (int s = 0; s < C::NSUB; ++s)
-            tma_load_4d(sV + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmv, s * C::RB, 0, g, id, &v_full[st]);
+            tma_load_4d(dst + s * C::KSUB, kind ? &tmv : &tmk, s * C::RB, 0, g, id, &full[st]);
         }
-        v_last[st] = use;
+        last[kind][st] = use;
       }
       if (!ok) {
         if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
@@ -625,11 +628,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
     // let every issued copy land before the CTA can exit
     if (lane == 0) {
       for (int s = 0; s < C::NS; ++s) {
-        if (k_last[s] >= 0) wait_ns(&k_full[s], k_last[s] & 1);
-        if (v_last[s] >= 0) wait_ns(&v_full[s], v_last[s] & 1);
+        if (last[0][s] >= 0) wait_ns(&k_full[s], last[0][s] & 1);
+        if (last[1][s] >= 0) wait_ns(&v_full[s], last[1][s] & 1);
       }
     }
-  } else {
+  } else if (warp < C::SW + 7) {
     // ============================================================ MMA issuers
     // Warp SW+5 issues S = Q8 K8^T, warp SW+6 O_tile = P8 V8.  A tcgen05.mma issue holds
     // its thread for about the product's execution time and a commit for tens of cycles, so
