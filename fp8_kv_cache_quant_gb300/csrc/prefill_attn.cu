@@ -31,8 +31,10 @@
 //              warp each up to head_dim 128; at 256 the K warp copies both).
 // Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns: S [0, 128),
 // O_tile [TM_OT, TM_OT + OTB * DN) (two buffers up to head_dim 128, so that the P.V of
-// tile t overlaps the promotion of tile t-1), O [TM_OA, TM_OA + D); for head_dim 256 the P.V product runs
-// as two N = 128 halves through one O_tile.
+// tile t overlaps the promotion of tile t-1), O [TM_OA, TM_OA + D); for head_dim 256 the
+// P.V product runs as two N = 128 halves through one O_tile.  Windowed e4m3 instantiations
+// up to head_dim 128 instead keep two S buffers and one O_tile, write P8 back into TMEM
+// over the S columns each thread has read, and take it from there as the A operand of P.V.
 // Every wait is bounded in time; a timeout records FKV_FAULT_TIMEOUT, lets the CTA's
 // copies and MMAs drain and returns.
 #include <mutex>
@@ -65,7 +67,7 @@ FKV_DEV float max_tree(const float* v) {
   }
 }
 
-template <int D, bool BF>
+template <int D, bool BF, bool WIN>
 struct PrefillCfg {
   static constexpr int ES = BF ? 2 : 1;             // bytes per element (bf16 / e4m3)
   // 128 queries per CTA; 128 keys per tile, or 64 for bf16 head_dim 256, whose 128-key
@@ -88,8 +90,14 @@ struct PrefillCfg {
   static constexpr int PB = BN * ES;                // bytes of one P row
   static constexpr int PTILE = BM * PB;             // bytes of one P tile
   static constexpr int KSTEP = 32 / ES;             // keys (P columns) of one P.V k-step (32 bytes)
-  static constexpr int SBUF = 1;                    // S buffers in TMEM
-  static constexpr int OTB = D <= 128 ? 2 : 1;      // O_tile buffers in TMEM
+  // Windowed e4m3 up to head_dim 128: each thread writes its P8 back into TMEM over the S
+  // columns it has read, and P.V takes P8 from there as its A operand (two S buffers, one
+  // O_tile).  Otherwise P goes through shared memory (one S buffer, O_tile double-buffered
+  // up to head_dim 128).  Both fill the 512 TMEM columns; with full attention the second
+  // O_tile, which lets a P.V run while the previous tile is promoted, measured faster.
+  static constexpr bool TS = !BF && D <= 128 && WIN;
+  static constexpr int SBUF = TS ? 2 : 1;           // S buffers in TMEM
+  static constexpr int OTB = (!TS && D <= 128) ? 2 : 1;  // O_tile buffers in TMEM
   // unrolling of the softmax / correction chunk loops: full for head_dim <= 128 (the
   // softmax is the critical path there), none for 256 (code size of four warp roles)
   static constexpr int UNR = D <= 128 ? 4 : 1;
@@ -124,6 +132,7 @@ struct PrefillCfg {
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(!ONE_LOAD || BN == 128, "the one-load softmax holds a 128-column S row");
   static_assert(HC % 32 == 0 && (HCH % 2 == 0 || ONE_LOAD || HCH == 1), "softmax chunks");
+  static_assert(!TS || (SPLIT == 2 && ONE_LOAD && HC == 64), "P8 in TMEM: 64 columns (16 words) per thread");
 };
 
 // One MMA of the element type: e4m3 (kind::f8f6f4) or bf16 (kind::f16), FP32 accumulation.
@@ -134,10 +143,10 @@ FKV_DEV void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t ides
 }
 
 template <int D, bool BF, bool WIN>
-__global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
+__global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
-  using C = PrefillCfg<D, BF>;
+  using C = PrefillCfg<D, BF, WIN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::OFF_Q;
@@ -199,7 +208,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
     mbar_init(q_full, NSM);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], NSM);
+      mbar_init(&s_free[i], C::TS ? 1 : NSM);  // TS: released by the P.V that read P8 from it
       mbar_init(&p_full[i], NSM);
       mbar_init(&p_free[i], 1);
     }
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       // normally free long before they are written: test them now without blocking, and
       // wait further down only if they were not
       const int pb = t & 1;
-      const bool p_ready = t < 2 || mbar_test_wait(&p_free[pb], ((t >> 1) - 1) & 1);
+      const bool p_ready = C::TS || t < 2 || mbar_test_wait(&p_free[pb], ((t >> 1) - 1) & 1);
       const bool a_ready = t < 2 || mbar_test_wait(&a_free[pb], ((t >> 1) - 1) & 1);
       const int kbase = (tb + t) * C::BN + c0;  // key of this thread's first column
       const int lim = lim_row - kbase;      // columns [lo, lim) of this thread's half are visible
@@ -317,8 +326,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < C::HCH; ++c) ld_s(c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive_warp(&s_free[sb]);
+        if constexpr (!C::TS) {  // (TS: S is freed by the P.V that reads P8 from it)
+          tc_fence_before();
+          mbar_arrive_warp(&s_free[sb]);
+        }
         if (full) {
           tmax = max_tree<C::HC>(vall) * cst;
         } else {
@@ -353,7 +364,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
       const float msafe = (mn == -INFINITY) ? 0.f : mn;
       // P tile t%2 is free once the P.V of tile t-2 completed
-      if (!__all_sync(0xffffffffu, p_ready) && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+      if (!C::TS && !__all_sync(0xffffffffu, p_ready) && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
       uint8_t* P = sP + pb * C::PTILE;
       // pass 2: p = 2^(s*cst - m), its unrounded sum, and P8 = e4m3(p * 448) into the P tile;
       // the next chunk's TMEM load is in flight while the current one is processed
@@ -362,6 +373,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       // so l sums p * 448 and the epilogue divides by l alone
       const float nb = (BF ? 0.f : kLog2E4m3Max) - msafe;
       const float2 cst2 = make_float2(cst, cst), nm2 = make_float2(nb, nb);
+      uint32_t ptm[C::TS ? 2 * C::HCH * 4 : 1];  // TS: this thread's P8 words (four keys each)
       auto chunk = [&](const float (&v)[32], int c) {  // c: chunk of this thread's half
         uint32_t pk[8 * C::ES];
 #pragma unroll
@@ -386,18 +398,29 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
                         (static_cast<uint32_t>(f32x2_to_e4m3x2(x1.x, x1.y)) << 16);
           }
         }
-        // 32 columns = 32 * ES bytes of the P row, in 16-byte pieces
+        if constexpr (C::TS) {
 #pragma unroll
-        for (int q = 0; q < 2 * C::ES; ++q) {
-          const int byte = (c0 + 32 * c) * C::ES + 16 * q;
-          const uint32_t lin = static_cast<uint32_t>(i * 128 + (byte % 128));
-          *reinterpret_cast<uint4*>(P + (byte / 128) * (C::BM * 128) + swz(lin, 128)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 8; ++q) ptm[8 * c + q] = pk[q];
+        } else {
+          // 32 columns = 32 * ES bytes of the P row, in 16-byte pieces
+#pragma unroll
+          for (int q = 0; q < 2 * C::ES; ++q) {
+            const int byte = (c0 + 32 * c) * C::ES + 16 * q;
+            const uint32_t lin = static_cast<uint32_t>(i * 128 + (byte % 128));
+            *reinterpret_cast<uint4*>(P + (byte / 128) * (C::BM * 128) + swz(lin, 128)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
         }
       };
       if constexpr (C::ONE_LOAD) {
 #pragma unroll
         for (int c = 0; c < C::HCH; ++c) chunk(*reinterpret_cast<const float(*)[32]>(vall + 32 * c), c);
+        if constexpr (C::TS) {
+          // P8 over the first 16 of this thread's S columns (already read): keys 4w .. 4w+3
+          // of its half in column c0 + w of S buffer sb
+          tmem_st16_16x2<C::HC>(sc, ptm);
+          tmem_st_wait();
+        }
       } else if constexpr (C::HCH == 1) {
         float va[32];
         ld_s(0, va);
@@ -428,7 +451,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       if (!__all_sync(0xffffffffu, a_ready) && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
       if (hf == 0) sAlpha[pb * C::BM + i] = alpha;
       mbar_arrive_warp(&a_full[pb]);
-      fence_proxy_async_smem();
+      if constexpr (C::TS) tc_fence_before();
+      else fence_proxy_async_smem();
       mbar_arrive_warp(&p_full[pb]);
     }
     if (!ok) {
@@ -674,11 +698,17 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       for (int kk = 0; kk < C::PB / 32; ++kk) {
         const int pbyte = kk * 32;
         const uint64_t ad = desc_add(dP, pb * C::PTILE + (pbyte / 128) * (C::BM * 128) + (pbyte % 128));
+        // TS: keys 32 kk .. of P8 sit in S buffer pb, half h = 32 kk / HC at column HC h, four
+        // keys per column
+        const uint32_t a_tm =
+            tmem + 128 * pb + C::HC * ((32 * kk) / C::HC) + ((32 * kk) % C::HC) / 4;
 #pragma unroll
         for (int j = 0; j < C::DN / C::EPS; ++j) {
           const int sub = hn * (C::DN / C::EPS) + j;
           const uint64_t bd = desc_add(dV, st * C::KTILE + sub * C::KSUB + kk * C::KSTEP * C::RB);
-          umma<BF>(dst + j * C::EPS, ad, bd, C::IDESC_PV, (kk > 0 || !fresh) ? 1u : 0u);
+          const uint32_t acc = (kk > 0 || !fresh) ? 1u : 0u;
+          if constexpr (C::TS) umma_f8_tmem_a(dst + j * C::EPS, a_tm, bd, C::IDESC_PV, acc);
+          else umma<BF>(dst + j * C::EPS, ad, bd, C::IDESC_PV, acc);
         }
       }
     };
@@ -731,7 +761,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF>::THREADS, 1)
       }
       if (lane == 0) {
         umma_commit(&v_empty[st]);
-        umma_commit(&p_free[pb]);
+        umma_commit(C::TS ? &s_free[pb] : &p_free[pb]);  // TS: P8 lived in S buffer pb
       }
       __syncwarp();
       return true;
@@ -815,7 +845,7 @@ namespace {
 
 template <int D, bool BF, bool WIN>
 cudaError_t launch_prefill_t(const PrefillParams& p, void* kc, void* vc, cudaStream_t s) {
-  using C = PrefillCfg<D, BF>;
+  using C = PrefillCfg<D, BF, WIN>;
   CUtensorMap tmk, tmv;
   if (!make_pool_map(&tmk, kc, C::DB, p.Hkv, p.num_blocks, C::RB) ||
       !make_pool_map(&tmv, vc, C::DB, p.Hkv, p.num_blocks, C::RB))
