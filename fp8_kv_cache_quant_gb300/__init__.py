@@ -32,6 +32,7 @@ EXPORTS = (
     "fkv_status_string", "fkv_version", "kv_quant_cache", "fp8_decode_attn_workspace_size",
     "fp8_decode_attn_num_splits", "fp8_decode_attn", "fkv_prefill_block_n", "fp8_prefill_attn",
     "fp8_decode_attn_noalloc", "fp8_decode_attn_split_blocks", "fkv_decode_block_n", "kv_quant_cache_clips",
+    "fp8_decode_step",
 )
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
@@ -82,6 +83,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.fp8_decode_attn.argtypes = [c_vp, c_i32, c_i32, _LayerCache, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
                                     ctypes.c_int, c_f, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_i32, c_vp,
                                     c_vp]
+    lib.fp8_decode_step.restype = ctypes.c_int
+    lib.fp8_decode_step.argtypes = [c_vp, c_vp] + lib.fp8_decode_attn.argtypes
     lib.fp8_decode_attn_noalloc.restype = ctypes.c_int
     lib.fp8_decode_attn_noalloc.argtypes = [c_vp, c_i32, c_i32, _LayerCache, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
                                             ctypes.c_int, c_f, c_i32, c_i32, c_vp, c_i32, c_vp, c_i32, c_vp, c_vp]
@@ -234,6 +237,29 @@ def fp8_decode_attn(q, cache: LayerCache, block_table, context_lens, q_scale=Non
                              _stream(stream))
     del keep
     _check("fp8_decode_attn", st)
+    return out
+
+
+def fp8_decode_step(k_new, v_new, q, cache: LayerCache, block_table, context_lens, q_scale=None, k_scale=None,
+                    v_scale=None, gran=SCALE_PER_TENSOR, softmax_scale=0.0, window=0, layer=0, skip_layer_mask=None,
+                    out=None, workspace=None, num_splits=0, fault=None, stream=None):
+    """kv_quant_cache of the current token (k_new, v_new: bf16 [batch][num_kv_heads][head_dim], written at
+    position context_lens[b] - 1) and fp8_decode_attn in one launch (e4m3 layers)."""
+    lib = load_library()
+    B, Hq, D = q.shape
+    max_blocks = int(block_table.shape[1])
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, cache, max_blocks, window, num_splits, q.device)
+    mp, nl, keep = _mask_arg(skip_layer_mask)
+    st = lib.fp8_decode_step(_ptr(k_new), _ptr(v_new), _ptr(q), B, Hq, cache.c(), _ptr(block_table), max_blocks,
+                             _ptr(context_lens), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), int(gran),
+                             float(softmax_scale), int(window), int(layer), mp, nl, _ptr(out), _ptr(workspace),
+                             int(workspace.numel() * workspace.element_size()), int(num_splits), _ptr(fault),
+                             _stream(stream))
+    del keep
+    _check("fp8_decode_step", st)
     return out
 
 

@@ -119,6 +119,83 @@ fkv_status cache_write(const void* k, const void* v, const int64_t* slot_mapping
                                               reinterpret_cast<cudaStream_t>(stream), current_num_sms(), clips));
 }
 
+// fp8_decode_attn, and with k_new / v_new given fp8_decode_step (the current token written
+// into the pools by the same launch).
+fkv_status decode_impl(const void* k_new, const void* v_new, const void* q, int32_t batch, int32_t num_q_heads,
+                       fkv_layer_cache cache, const int32_t* block_table, int32_t max_blocks,
+                       const int32_t* context_lens, const float* q_scale, const float* k_scale,
+                       const float* v_scale, fkv_scale_gran gran, float softmax_scale, int32_t window,
+                       int32_t layer, const uint8_t* skip_layer_mask, int32_t num_layers, void* out,
+                       void* workspace, size_t workspace_bytes, int32_t num_splits, int32_t* fault,
+                       fkv_stream_t stream) {
+  const bool step = k_new != nullptr || v_new != nullptr;
+  if (batch < 0 || num_q_heads <= 0 || max_blocks <= 0 || window < 0 || num_splits < 0)
+    return FKV_INVALID_ARG;
+  if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
+  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0 || !valid_format(cache)) return FKV_INVALID_ARG;
+  if (num_q_heads % cache.num_kv_heads != 0) return FKV_INVALID_ARG;
+  if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
+  const int G = num_q_heads / cache.num_kv_heads;
+  if (!supported_group(G, cache.head_dim)) return FKV_UNSUPPORTED;
+  if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
+  if (!(softmax_scale >= 0.f) || std::isinf(softmax_scale)) return FKV_INVALID_ARG;
+  if (batch > 65535 || cache.num_kv_heads > 65535) return FKV_UNSUPPORTED;
+  fkv_status st = FKV_OK;
+  const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
+  if (st != FKV_OK) return st;
+  const int elt = layer_elt(bf16, cache);
+  // the fused write exists for e4m3 pools (the tensor-core decode)
+  if (step && !fkv::decode_uses_tensor_cores(cache.head_dim, elt)) return FKV_UNSUPPORTED;
+  if (batch == 0) return FKV_OK;
+  if (step && (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16))) return FKV_INVALID_ARG;
+  if (!q || !out || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || !workspace)
+    return FKV_INVALID_ARG;
+  if (!bf16 && (!q_scale || !k_scale || !v_scale)) return FKV_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(cache.k_cache, 16) || !aligned(cache.v_cache, 16) ||
+      !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+    return FKV_INVALID_ARG;
+  DecodePlan plan;
+  if (!plan_decode(batch, num_q_heads, cache.num_kv_heads, cache.head_dim, max_blocks, window, num_splits, &plan))
+    return FKV_UNSUPPORTED;
+  if (workspace_bytes < plan.o_bytes + plan.lse_bytes + plan.cnt_bytes) return FKV_INVALID_ARG;
+
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_cache = static_cast<const uint8_t*>(cache.k_cache);
+  p.v_cache = static_cast<const uint8_t*>(cache.v_cache);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.per_head = gran == FKV_SCALE_PER_HEAD;
+  p.B = batch;
+  p.Hq = num_q_heads;
+  p.Hkv = cache.num_kv_heads;
+  p.num_blocks = cache.num_blocks;
+  p.max_blocks = max_blocks;
+  const float tau = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache.head_dim));
+  p.sm_scale_log2 = tau * 1.4426950408889634f;
+  p.window = window;
+  p.bps = plan.bps;
+  p.max_splits = plan.max_splits;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.o_bytes);
+  p.done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plan.o_bytes + plan.lse_bytes);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.fault = fault;
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  // split-completion counters start at zero on every call
+  if (cudaMemsetAsync(p.done, 0, static_cast<size_t>(batch) * cache.num_kv_heads * sizeof(int32_t),
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FKV_CUDA_ERROR;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fkv::decode_uses_tensor_cores(cache.head_dim, elt)) return from_cuda(fkv::launch_decode_tc(p, cache.head_dim, G, s));
+  return from_cuda(fkv::launch_decode(p, cache.head_dim, elt, G, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -133,7 +210,7 @@ const char* fkv_status_string(fkv_status status) {
   return "unknown status";
 }
 
-int32_t fkv_version(void) { return 101; }
+int32_t fkv_version(void) { return 102; }
 
 
 fkv_status kv_quant_cache(const void* k, const void* v, const int64_t* slot_mapping, int32_t n_tokens,
@@ -191,66 +268,22 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads, fk
                            const uint8_t* skip_layer_mask, int32_t num_layers, void* out, void* workspace,
                            size_t workspace_bytes, int32_t num_splits, int32_t* fault,
                            fkv_stream_t stream) {
-  if (batch < 0 || num_q_heads <= 0 || max_blocks <= 0 || window < 0 || num_splits < 0)
-    return FKV_INVALID_ARG;
-  if (cache.block_size != 16) return cache.block_size > 0 ? FKV_UNSUPPORTED : FKV_INVALID_ARG;
-  if (cache.num_blocks <= 0 || cache.num_kv_heads <= 0 || !valid_format(cache)) return FKV_INVALID_ARG;
-  if (num_q_heads % cache.num_kv_heads != 0) return FKV_INVALID_ARG;
-  if (!supported_head_dim(cache.head_dim)) return FKV_UNSUPPORTED;
-  const int G = num_q_heads / cache.num_kv_heads;
-  if (!supported_group(G, cache.head_dim)) return FKV_UNSUPPORTED;
-  if (gran != FKV_SCALE_PER_TENSOR && gran != FKV_SCALE_PER_HEAD) return FKV_INVALID_ARG;
-  if (!(softmax_scale >= 0.f) || std::isinf(softmax_scale)) return FKV_INVALID_ARG;
-  if (batch > 65535 || cache.num_kv_heads > 65535) return FKV_UNSUPPORTED;
-  fkv_status st = FKV_OK;
-  const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
-  if (st != FKV_OK) return st;
-  if (batch == 0) return FKV_OK;
-  if (!q || !out || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || !workspace)
-    return FKV_INVALID_ARG;
-  if (!bf16 && (!q_scale || !k_scale || !v_scale)) return FKV_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(cache.k_cache, 16) || !aligned(cache.v_cache, 16) ||
-      !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(context_lens, 4))
-    return FKV_INVALID_ARG;
-  DecodePlan plan;
-  if (!plan_decode(batch, num_q_heads, cache.num_kv_heads, cache.head_dim, max_blocks, window, num_splits, &plan))
-    return FKV_UNSUPPORTED;
-  if (workspace_bytes < plan.o_bytes + plan.lse_bytes + plan.cnt_bytes) return FKV_INVALID_ARG;
+  return decode_impl(nullptr, nullptr, q, batch, num_q_heads, cache, block_table, max_blocks, context_lens, q_scale,
+                     k_scale, v_scale, gran, softmax_scale, window, layer, skip_layer_mask, num_layers, out, workspace,
+                     workspace_bytes, num_splits, fault, stream);
+}
 
-  DecodeParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k_cache = static_cast<const uint8_t*>(cache.k_cache);
-  p.v_cache = static_cast<const uint8_t*>(cache.v_cache);
-  p.block_table = block_table;
-  p.context_lens = context_lens;
-  p.q_scale = q_scale;
-  p.k_scale = k_scale;
-  p.v_scale = v_scale;
-  p.per_head = gran == FKV_SCALE_PER_HEAD;
-  p.B = batch;
-  p.Hq = num_q_heads;
-  p.Hkv = cache.num_kv_heads;
-  p.num_blocks = cache.num_blocks;
-  p.max_blocks = max_blocks;
-  const float tau = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache.head_dim));
-  p.sm_scale_log2 = tau * 1.4426950408889634f;
-  p.window = window;
-  p.bps = plan.bps;
-  p.max_splits = plan.max_splits;
-  p.o_part = static_cast<float*>(workspace);
-  p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.o_bytes);
-  p.done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plan.o_bytes + plan.lse_bytes);
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.fault = fault;
-  // split-completion counters start at zero on every call
-  if (cudaMemsetAsync(p.done, 0, static_cast<size_t>(batch) * cache.num_kv_heads * sizeof(int32_t),
-                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FKV_CUDA_ERROR;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int elt = layer_elt(bf16, cache);
-  if (fkv::decode_uses_tensor_cores(cache.head_dim, elt)) return from_cuda(fkv::launch_decode_tc(p, cache.head_dim, G, s));
-  return from_cuda(fkv::launch_decode(p, cache.head_dim, elt, G, s));
+fkv_status fp8_decode_step(const void* k_new, const void* v_new, const void* q, int32_t batch,
+                           int32_t num_q_heads, fkv_layer_cache cache, const int32_t* block_table,
+                           int32_t max_blocks, const int32_t* context_lens, const float* q_scale,
+                           const float* k_scale, const float* v_scale, fkv_scale_gran gran,
+                           float softmax_scale, int32_t window, int32_t layer, const uint8_t* skip_layer_mask,
+                           int32_t num_layers, void* out, void* workspace, size_t workspace_bytes,
+                           int32_t num_splits, int32_t* fault, fkv_stream_t stream) {
+  if (!k_new || !v_new) return FKV_INVALID_ARG;
+  return decode_impl(k_new, v_new, q, batch, num_q_heads, cache, block_table, max_blocks, context_lens, q_scale,
+                     k_scale, v_scale, gran, softmax_scale, window, layer, skip_layer_mask, num_layers, out, workspace,
+                     workspace_bytes, num_splits, fault, stream);
 }
 
 int32_t fkv_prefill_block_n(int32_t head_dim) { return supported_head_dim(head_dim) ? 128 : 0; }

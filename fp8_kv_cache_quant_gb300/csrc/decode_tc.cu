@@ -80,6 +80,39 @@ struct DecodeTcCfg {
 
 constexpr int kDecodeTcThreads = 320;  // softmax warpgroup, correction warpgroup, TMA warp, MMA warp
 
+// The current token's K and V row of KV head g, written into the e4m3 pools at position
+// T - 1 exactly as kv_quant_cache writes them: e4m3(fl32(x * fl32(1 / s))), round to
+// nearest even, saturating.  One warp; lane j < 2 D / 8 takes 8 elements of K (j < D / 8)
+// or V.  The fence orders the writes before the TMA copies that read the block back.
+template <int D>
+__device__ void write_current_token(const DecodeParams& p, int b, int g, int T, int lane) {
+  const int pos = T - 1;
+  const int id = p.block_table[static_cast<size_t>(b) * p.max_blocks + (pos >> 4)];
+  if (id < 0 || id >= p.num_blocks) return;  // reported by the block-id checks of the split
+  const size_t row = ((static_cast<size_t>(id) * p.Hkv + g) * 16 + (pos & 15)) * D;  // byte offset
+  const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D;
+  constexpr int CH = D / 8;
+  for (int j = lane; j < 2 * CH; j += 32) {
+    const bool is_v = j >= CH;
+    const int c = is_v ? j - CH : j;
+    const uint4 x = reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + src)[c];
+    const float inv = __frcp_rn((is_v ? p.v_scale : p.k_scale)[p.per_head ? g : 0]);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 f0 = bf16x2_to_f2(w[2 * k]), f1 = bf16x2_to_f2(w[2 * k + 1]);
+      o[k] = static_cast<uint32_t>(f32x2_to_e4m3x2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv))) |
+             (static_cast<uint32_t>(f32x2_to_e4m3x2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv))) << 16);
+    }
+    // the pools are the caller's writable device memory; the params carry them as const
+    // because the plain decode only reads them
+    uint8_t* dst = const_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + row + 8 * c;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
+  }
+  fence_proxy_async_global();
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1)
     decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
@@ -165,6 +198,9 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     *abort_s = 0;
     fence_mbar_init();
   }
+  // fp8_decode_step: the split holding position T - 1 (the last) writes the current token
+  // into the pools before its first copy of that block
+  if (warp == 8 && p.k_new != nullptr && sigma == r.nsplit - 1) write_current_token<D>(p, b, g, T, lane);
   if (warp == 8) {
     __syncwarp();
     const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks + bb;

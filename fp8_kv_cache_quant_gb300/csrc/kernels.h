@@ -28,6 +28,10 @@ struct DecodeParams {
   int32_t* done;        // [B][Hkv] splits finished (zeroed before the launch)
   __nv_bfloat16* out;   // [B][Hq][D]
   int32_t* fault;
+  // the current token's K and V, bf16 [B][Hkv][D], quantised into the (e4m3) pools at
+  // position T - 1 by the launch itself (fp8_decode_step); null: the pools are complete
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
 };
 
 struct PrefillParams {
@@ -59,8 +63,8 @@ cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* s
 // elt: the pool's element type, 1 e4m3, 2 bf16, 3 e5m2
 cudaError_t launch_decode(const DecodeParams& p, int D, int elt, int G, cudaStream_t s);
 
-// e4m3 layers (elt 1) with head_dim 128 / 256 decode on the tensor cores (FP8 P, 128-key
-// tiles); the others on the CUDA cores (P exact).
+// e4m3 layers (elt 1, head_dim 64 / 128 / 256) decode on the tensor cores (FP8 P, 128-key
+// tiles); bf16 and e5m2 layers on the CUDA cores (P exact).
 bool decode_uses_tensor_cores(int D, int elt);
 cudaError_t launch_decode_tc(const DecodeParams& p, int D, int G, cudaStream_t s);
 

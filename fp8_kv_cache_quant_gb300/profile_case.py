@@ -30,6 +30,8 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--bf16", action="store_true", help="bf16 pool (the skip-layer path) instead of e4m3")
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--step", action="store_true",
+                    help="decode through fp8_decode_step (the current token's cache write in the same launch)")
     ap.add_argument("--prefill", action="store_true",
                     help="run fp8_prefill_attn on the head_dim-256 prefill shape instead (batch 1)")
     ap.add_argument("--llama", action="store_true",
@@ -48,15 +50,22 @@ def main():
     cache = f.LayerCache.empty(nb, w.num_kv_heads, w.head_dim, bf16=a.bf16, device=dev)
     slots = torch.from_numpy(synth.slot_mapping(table, ctx)).to(dev)
     f.kv_quant_cache(data.k, data.v, slots, cache, data.k_scale, data.v_scale, gran, layer=0, skip_layer_mask=mask)
+    last = torch.from_numpy(np.cumsum(ctx) - 1).to(dev)
+    k_new, v_new = data.k[last].contiguous(), data.v[last].contiguous()  # each sequence's current token
     del data.k, data.v
     table_d = torch.from_numpy(table).to(dev)
     ctx_d = torch.from_numpy(ctx).to(dev)
     out = torch.empty_like(data.q)
     ws = f.decode_workspace(w.batch, w.num_q_heads, cache, table.shape[1], w.layer_window(a.layer), a.splits, dev)
     for _ in range(a.iters):
-        f.fp8_decode_attn(data.q, cache, table_d, ctx_d, data.q_scale, data.k_scale, data.v_scale, gran,
-                          window=w.layer_window(a.layer), layer=0, skip_layer_mask=mask, out=out, workspace=ws,
-                          num_splits=a.splits)
+        if a.step:
+            f.fp8_decode_step(k_new, v_new, data.q, cache, table_d, ctx_d, data.q_scale, data.k_scale, data.v_scale,
+                              gran, window=w.layer_window(a.layer), layer=0, skip_layer_mask=mask, out=out,
+                              workspace=ws, num_splits=a.splits)
+        else:
+            f.fp8_decode_attn(data.q, cache, table_d, ctx_d, data.q_scale, data.k_scale, data.v_scale, gran,
+                              window=w.layer_window(a.layer), layer=0, skip_layer_mask=mask, out=out, workspace=ws,
+                              num_splits=a.splits)
     torch.cuda.synchronize()
     print("profile_case done", w.name, "layer", a.layer, "bf16" if a.bf16 else "e4m3")
 

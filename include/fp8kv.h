@@ -182,14 +182,13 @@ int32_t fkv_decode_block_n(int32_t head_dim, int32_t layer_kind);
  * (sequence, KV head) last merges the splits through their log-sum-exp in FP32 — the
  * two-level accumulation of the blog's "Two-level accumulation" paragraph, so a 100k+
  * key contraction is summed in true FP32.
- * e4m3 layers with head_dim 128 or 256 run on the tensor cores, FP8 QK and Score*V as in
- * the blog's FP8 attention: S^T = K8 Q8^T and O^T = V8^T P8^T per 128-key tile with
+ * e4m3 layers (head_dim 64, 128 or 256) run on the tensor cores, FP8 QK and Score*V as
+ * in the blog's FP8 attention: S^T = K8 Q8^T and O^T = V8^T P8^T per 128-key tile with
  * P8 = e4m3(p * 448) relative to the split's running maximum, the denominator summing
- * the unrounded p, and each tile's partial promoted into FP32 registers.  Other e4m3
- * layers (head_dim 64) run on the CUDA cores with P exact.  Skip layers read a bf16
- * pool, quantise nothing and keep P exact; e5m2 layers (cache.kv_format) dequantise
- * their codes with the scales and attend with the bf16 query and exact P on the CUDA
- * cores.  fkv_decode_block_n tells which applies.
+ * the unrounded p, and each tile's partial promoted into FP32 registers.  Skip layers
+ * read a bf16 pool, quantise nothing and keep P exact; e5m2 layers (cache.kv_format)
+ * dequantise their codes with the scales and attend with the bf16 query and exact P on
+ * the CUDA cores.  fkv_decode_block_n tells which applies.
  *
  *   q             device bf16 [batch][num_q_heads][head_dim]
  *   block_table   device int32 [batch][max_blocks]
@@ -210,6 +209,35 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads,
                            const int32_t* context_lens, const float* q_scale, const float* k_scale,
                            const float* v_scale, fkv_scale_gran gran, float softmax_scale,
                            int32_t window, int32_t layer, const uint8_t* skip_layer_mask,
+                           int32_t num_layers, void* out, void* workspace, size_t workspace_bytes,
+                           int32_t num_splits, int32_t* fault, fkv_stream_t stream);
+
+/*
+ * fp8_decode_step — the current token's cache write and fp8_decode_attn in one launch.
+ *
+ * A decode step of one layer writes the new token's K and V into the paged cache and
+ * then attends over the whole context, the new token included (the blog's cache write
+ * reshape_and_cache_flash followed by the decode attention).  For every sequence b with
+ * T_b = context_lens[b] >= 1, the rows k_new[b][g][:] and v_new[b][g][:] of every KV
+ * head g are quantised into the pools at position T_b - 1 (block
+ * block_table[b][(T_b - 1) / 16], slot (T_b - 1) % 16) exactly as kv_quant_cache writes
+ * them: e4m3(fl32(x * fl32(1 / s))) with the same k_scale / v_scale and gran; then the
+ * attention is that of fp8_decode_attn with the same arguments.  The write is done by
+ * the CTA whose context split holds position T_b - 1, before its copies read that block,
+ * so the result equals kv_quant_cache followed by fp8_decode_attn, pool bytes and output
+ * bit for bit, with one launch instead of two.
+ *
+ *   k_new, v_new  device bf16 [batch][num_kv_heads][head_dim], 16-byte aligned
+ *   all other arguments as for fp8_decode_attn
+ * Only e4m3 layers (the tensor-core decode): a skip layer or an e5m2 pool returns
+ * FKV_UNSUPPORTED (write with kv_quant_cache and call fp8_decode_attn instead).  A block
+ * id out of range is reported as for fp8_decode_attn and its row is not written.
+ */
+fkv_status fp8_decode_step(const void* k_new, const void* v_new, const void* q, int32_t batch,
+                           int32_t num_q_heads, fkv_layer_cache cache, const int32_t* block_table,
+                           int32_t max_blocks, const int32_t* context_lens, const float* q_scale,
+                           const float* k_scale, const float* v_scale, fkv_scale_gran gran,
+                           float softmax_scale, int32_t window, int32_t layer, const uint8_t* skip_layer_mask,
                            int32_t num_layers, void* out, void* workspace, size_t workspace_bytes,
                            int32_t num_splits, int32_t* fault, fkv_stream_t stream);
 

@@ -137,6 +137,33 @@ def test_decode_validation(lib):
     assert call(batch=0) == f.OK
 
 
+def test_decode_step_validation(lib):
+    """fp8_decode_step: both new rows required and 16-byte aligned; e4m3 pools only."""
+    import ctypes
+    d = lib.fp8_decode_step
+    p = 1 << 12
+    skip = (ctypes.c_uint8 * 1)(1)
+
+    def call(**kw):
+        a = dict(kn=p, vn=p, q=p, batch=2, hq=8, cache=_cache(), table=p, max_blocks=4, ctx=p, qs=p, ks=p, vs=p,
+                 gran=0, sm=0.0, window=0, layer=0, mask=None, nl=0, out=p, ws=p, wsb=1 << 30, splits=0,
+                 fault=None, stream=None)
+        a.update(kw)
+        return d(a["kn"], a["vn"], a["q"], a["batch"], a["hq"], a["cache"], a["table"], a["max_blocks"], a["ctx"],
+                 a["qs"], a["ks"], a["vs"], a["gran"], a["sm"], a["window"], a["layer"], a["mask"], a["nl"],
+                 a["out"], a["ws"], a["wsb"], a["splits"], a["fault"], a["stream"])
+
+    assert call(kn=None) == f.INVALID_ARG
+    assert call(vn=None) == f.INVALID_ARG
+    assert call(kn=p + 8) == f.INVALID_ARG                                   # 16-byte alignment
+    assert call(batch=0, mask=ctypes.cast(skip, ctypes.c_void_p), nl=1) == f.UNSUPPORTED  # bf16 skip layer
+    assert call(batch=0, cache=_cache(fmt=1)) == f.UNSUPPORTED               # e5m2 pool
+    assert call(hq=7) == f.INVALID_ARG                                       # as fp8_decode_attn
+    assert call(batch=0) == f.OK
+    for D in (64, 128, 256):
+        assert call(batch=0, hq=4, cache=_cache(D=D)) == f.OK                # every e4m3 head_dim
+
+
 def test_prefill_validation(lib):
     pre = lib.fp8_prefill_attn
     p = 1 << 12

@@ -1,0 +1,136 @@
+"""fp8_decode_step on the GPU: the current token's cache write fused into the decode launch
+must equal kv_quant_cache of that token followed by fp8_decode_attn — pool bytes and
+output bit for bit.  The separate calls are pinned to the oracle by test_gpu_cache and
+test_gpu_decode; equality carries that over.  Cases cover every head_dim, per-tensor and
+per-head scales, windows, forced split counts, an empty sequence, and consecutive steps
+whose current token opens a new pool block."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from helpers import to_dev
+
+f = pytest.importorskip("fp8_kv_cache_quant_gb300")
+pytestmark = pytest.mark.gpu
+
+
+def _scales(gran, q, k, v):
+    if gran:
+        return synth.amax_scales(q, 1), synth.amax_scales(k, 1), synth.amax_scales(v, 1)
+    return torch.tensor([0.5]), torch.tensor([1.0]), torch.tensor([0.25])
+
+
+def _run_both(ctx, table, nb, q, k, v, qs, ks, vs, gran, window, splits, cache_a, cache_b):
+    """One decode step on two copies of a layer: (A) kv_quant_cache of the current token
+    then fp8_decode_attn, (B) fp8_decode_step.  k / v hold every position of every
+    sequence (sequence-major); the current token of sequence b is position ctx[b] - 1."""
+    B = len(ctx)
+    Hkv, D = k.shape[1], k.shape[2]
+    cu = np.concatenate([[0], np.cumsum(ctx)])
+    k_new = torch.zeros((B, Hkv, D), dtype=torch.bfloat16)
+    v_new = torch.zeros((B, Hkv, D), dtype=torch.bfloat16)
+    slots = np.full(B, -1, np.int64)
+    all_slots = synth.slot_mapping(table, ctx)
+    for b in range(B):
+        if ctx[b] > 0:
+            k_new[b] = k[cu[b + 1] - 1]
+            v_new[b] = v[cu[b + 1] - 1]
+            slots[b] = all_slots[cu[b + 1] - 1]
+    args = (to_dev(table), to_dev(ctx), to_dev(qs), to_dev(ks), to_dev(vs), gran)
+    f.kv_quant_cache(k_new.cuda(), v_new.cuda(), to_dev(slots), cache_a, to_dev(ks), to_dev(vs), gran)
+    out_a = f.fp8_decode_attn(q.cuda(), cache_a, *args, window=window, num_splits=splits)
+    out_b = f.fp8_decode_step(k_new.cuda(), v_new.cuda(), q.cuda(), cache_b, *args, window=window,
+                              num_splits=splits)
+    torch.cuda.synchronize()
+    return out_a, out_b
+
+
+def _layer_before_step(ctx, table, nb, k, v, ks, vs, gran):
+    """Two identical pools holding every position except each sequence's current token
+    (stale bytes elsewhere are NaN codes, 0xFF)."""
+    Hkv, D = k.shape[1], k.shape[2]
+    cu = np.concatenate([[0], np.cumsum(ctx)])
+    slots = synth.slot_mapping(table, ctx).copy()
+    for b in range(len(ctx)):
+        if ctx[b] > 0:
+            slots[cu[b + 1] - 1] = -1
+    a = f.LayerCache.empty(nb, Hkv, D)
+    a.k_cache.view(torch.uint8).fill_(0xFF)
+    a.v_cache.view(torch.uint8).fill_(0xFF)
+    if len(slots):
+        f.kv_quant_cache(k.cuda(), v.cuda(), to_dev(slots), a, to_dev(ks), to_dev(vs), gran)
+    b_ = f.LayerCache.empty(nb, Hkv, D)
+    b_.k_cache.copy_(a.k_cache)
+    b_.v_cache.copy_(a.v_cache)
+    return a, b_
+
+
+@pytest.mark.parametrize("D,G,gran,window,splits", [
+    (128, 4, 1, 0, 0), (64, 8, 0, 0, 3), (256, 2, 1, 0, 0), (128, 16, 0, 50, 0), (64, 4, 1, 40, 2),
+    (128, 1, 0, 0, 1), (256, 8, 0, 33, 0),
+])
+def test_decode_step_equals_write_then_decode(D, G, gran, window, splits):
+    rng = np.random.default_rng(D * 5 + G + window + splits)
+    Hkv = 2
+    Hq = Hkv * G
+    ctx = np.array([1, 15, 16, 17, 300, 1000, 0, 129], np.int32)
+    table, nb = synth.block_table(ctx, seed=19, extra_blocks=2)
+    n = int(ctx.sum())
+    q = torch.from_numpy(rng.standard_normal((len(ctx), Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy((rng.standard_normal((n, Hkv, D)) * 3.0).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((n, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    qs, ks, vs = _scales(gran, q, k, v)
+    cache_a, cache_b = _layer_before_step(ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran)
+    out_a, out_b = _run_both(ctx, table, nb, q, k, v, qs, ks, vs, gran, window, splits, cache_a, cache_b)
+    assert torch.equal(cache_a.k_cache, cache_b.k_cache), "K pool differs"
+    assert torch.equal(cache_a.v_cache, cache_b.v_cache), "V pool differs"
+    assert torch.equal(out_a, out_b), "output differs"
+    assert torch.all(out_b[6] == 0), "a sequence without keys gets a zero row"
+
+
+def test_decode_step_consecutive_steps_across_a_block_boundary():
+    """Three steps of a growing context through fp8_decode_step on one pool, against the
+    separate calls on another: the current token moves from slot 14 to slot 0 of a new
+    block (and in the long sequence past a split boundary)."""
+    rng = np.random.default_rng(7)
+    D, G, Hkv = 128, 4, 2
+    Hq = Hkv * G
+    final = np.array([17, 33, 3, 1666], np.int32)
+    table, nb = synth.block_table(final, seed=23, extra_blocks=1)
+    n = int(final.sum())
+    k = torch.from_numpy((rng.standard_normal((n, Hkv, D)) * 2.0).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((n, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    ks, vs = synth.amax_scales(k, 1), synth.amax_scales(v, 1)
+    qs = torch.full((Hq,), 0.05)
+    cuf = np.concatenate([[0], np.cumsum(final)])
+    start = final - 3  # the first step's context lengths (sequence 2 starts empty)
+
+    def prefix(x, ctx):  # positions [0, ctx[b]) of every sequence, sequence-major
+        return torch.cat([x[cuf[b]:cuf[b] + ctx[b]] for b in range(len(final))])
+
+    cache_a, cache_b = _layer_before_step(start, table, nb, prefix(k, start), prefix(v, start), ks.numpy(),
+                                          vs.numpy(), 1)
+    for step in range(3):
+        ctx = (start + step).astype(np.int32)
+        kc, vc = prefix(k, ctx), prefix(v, ctx)
+        q = torch.from_numpy(rng.standard_normal((len(final), Hq, D)).astype(np.float32)).to(torch.bfloat16)
+        out_a, out_b = _run_both(ctx, table, nb, q, kc, vc, qs, ks, vs, 1, 0, 0, cache_a, cache_b)
+        assert torch.equal(cache_a.k_cache, cache_b.k_cache), f"K pool differs at step {step}"
+        assert torch.equal(cache_a.v_cache, cache_b.v_cache), f"V pool differs at step {step}"
+        assert torch.equal(out_a, out_b), f"output differs at step {step}"
+
+
+def test_decode_step_rejects_non_e4m3_layers():
+    D, Hkv, G = 128, 2, 4
+    ctx = np.array([5], np.int32)
+    table, nb = synth.block_table(ctx, seed=3)
+    q = torch.zeros((1, Hkv * G, D), dtype=torch.bfloat16).cuda()
+    kn = torch.zeros((1, Hkv, D), dtype=torch.bfloat16).cuda()
+    bf16_pool = f.LayerCache.empty(nb, Hkv, D, bf16=True)
+    with pytest.raises(f.FkvError):
+        f.fp8_decode_step(kn, kn, q, bf16_pool, to_dev(table), to_dev(ctx), skip_layer_mask=[1])
+    e5 = f.LayerCache.empty(nb, Hkv, D, kv_format=f.KV_E5M2)
+    one = torch.ones(1).cuda()
+    with pytest.raises(f.FkvError):
+        f.fp8_decode_step(kn, kn, q, e5, to_dev(table), to_dev(ctx), one, one, one)
