@@ -53,7 +53,8 @@ struct DecodePlan {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Split-K plan.  Blocks per split (bps) are multiples of 8 (whole 128-key tiles of the
-// tensor-core decode) up to 128, with at most 1024 splits per sequence.  A requested
+// tensor-core decode) up to kMaxSplitBlocks (256), with at most 1024 splits per sequence.
+// Equal estimates go to the longer splits (fewer CTAs, fewer prologues and merges).  A requested
 // num_splits sets bps = ceil(blocks / num_splits), rounded up.  Otherwise bps minimises
 // the estimated time waves * bps, where a wave is one CTA on every resident slot
 // (3 per SM) and the grid has B * Hkv * ceil(blocks / bps) CTAs: the longest split
@@ -70,7 +71,7 @@ bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_bloc
     const long long units = static_cast<long long>(std::max(B, 1)) * Hkv;
     const long long slots = static_cast<long long>(current_num_sms()) * 3;
     long long best = -1, best_cost = 0;
-    for (long long c = 8; c <= 128; c += 8) {
+    for (long long c = 8; c <= fkv::kMaxSplitBlocks; c += 8) {
       const long long ctas = units * ((nblk_max + c - 1) / c);
       const long long cost = (ctas + slots - 1) / slots * std::min(c, nblk_max);
       if (best < 0 || cost < best_cost || (cost == best_cost && c > best)) {
@@ -80,11 +81,11 @@ bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_bloc
     }
     bps = best;
   }
-  bps = std::min<long long>(bps, 128);
+  bps = std::min<long long>(bps, fkv::kMaxSplitBlocks);
   bps = std::max<long long>(bps, (nblk_max + 1023) / 1024);
   bps = std::max<long long>(bps, 1);
   bps = (bps + 7) / 8 * 8;
-  if (bps > 128) return false;  // context too long for 1024 splits of 128 blocks
+  if (bps > fkv::kMaxSplitBlocks) return false;  // context too long for 1024 splits of 256 blocks
   plan->bps = static_cast<int>(bps);
   plan->max_splits = static_cast<int>((nblk_max + bps - 1) / bps);
   const size_t rows = static_cast<size_t>(B) * Hq * plan->max_splits;

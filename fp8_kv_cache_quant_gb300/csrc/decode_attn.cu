@@ -32,7 +32,7 @@ namespace fkv {
 
 constexpr int kNW = 4;           // warps per CTA; every warp prefetches and consumes its own tiles
 constexpr int kNBUF = 2;         // tile buffers per warp (one in use, one in flight)
-constexpr int kMaxBps = 128;     // blocks per split, upper bound (table ids staged in smem)
+constexpr int kMaxBps = kMaxSplitBlocks;  // blocks per split, upper bound (table ids staged in smem)
 
 // ELT: the pool's element type — 2 bf16, 3 e5m2 (the codes widened to FP32 with the K/V
 // scales applied; the query unquantised and P exact, as on bf16 layers).

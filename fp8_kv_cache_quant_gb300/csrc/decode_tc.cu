@@ -51,7 +51,7 @@ struct DecodeTcCfg {
   static constexpr int KTILE = BN * D;         // bytes of a K or V tile
   static constexpr int MPV = D < 128 ? D : 128;  // M of one P.V product (head_dim rows)
   static constexpr int NS = D == 64 ? 4 : 2;   // K / V stages (small CTAs: 3 per SM up to head_dim 128)
-  static constexpr int MAX_BPS = 128;          // blocks per split (their ids staged in shared memory)
+  static constexpr int MAX_BPS = kMaxSplitBlocks;          // blocks per split (their ids staged in shared memory)
   static constexpr int QSUB = NP * RB;         // bytes of one column block of the Q8 tile
   static constexpr int PTILE = NP * BN;        // bytes of one P8^T tile
   static constexpr int TM_S = 0;               // S^T buffers: TMEM columns [0, 2 * NP)

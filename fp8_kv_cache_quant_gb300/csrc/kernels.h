@@ -8,6 +8,9 @@
 
 namespace fkv {
 
+// Pool blocks per decode split, at most: each split's block ids are staged in shared memory.
+constexpr int kMaxSplitBlocks = 256;
+
 struct DecodeParams {
   const __nv_bfloat16* q;      // [B][Hq][D]
   const uint8_t* k_cache;      // pool bytes

@@ -49,11 +49,11 @@ def test_split_planning(lib):
     assert ws >= 8 * 32 * n * (128 + 1) * 4
     # a requested split count is honoured when whole 8-block tiles allow it
     assert f.fp8_decode_attn_num_splits(1, 32, 8, 128, 256, 0, 4) == 4
-    assert f.fp8_decode_attn_num_splits(1, 32, 8, 128, 256, 0, 1) == 2   # at most 128 blocks per split
+    assert f.fp8_decode_attn_num_splits(1, 32, 8, 128, 512, 0, 1) == 2   # at most 256 blocks per split
     assert f.fp8_decode_attn_split_blocks(1, 32, 8, 128, 100, 0, 3) == 40  # ceil(100 / 3) = 34 -> 40
     assert f.fp8_decode_attn_num_splits(1, 32, 8, 128, 100, 0, 12) == 7   # 9 blocks -> 16: 7 splits
     for auto in (f.fp8_decode_attn_split_blocks(8, 32, 8, 128, 1536), f.fp8_decode_attn_split_blocks(1, 64, 8, 128, 8192)):
-        assert auto % 8 == 0 and 8 <= auto <= 128
+        assert auto % 8 == 0 and 8 <= auto <= 256
     # which decodes round P (tensor cores, 128-key tiles) and which keep it exact
     assert f.fkv_decode_block_n(128) == 128 and f.fkv_decode_block_n(256) == 128 and f.fkv_decode_block_n(64) == 128
     assert f.fkv_decode_block_n(128, True) == 0 and f.fkv_decode_block_n(64, True) == 0
