@@ -49,16 +49,25 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source without its comments, trailing blanks and empty lines."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_sha(kernel_file: str) -> str:
-    """First 16 hex digits of the sha256 of a kernel's .cu file followed by the shared
-    headers it includes (common.cuh, tc.cuh, decode_common.cuh, kernels.h): a profile
-    summary stays valid only while none of them has changed."""
+    """First 16 hex digits of the sha256 of the code (comments removed) of a kernel's .cu
+    file followed by the shared headers it includes (common.cuh, tc.cuh,
+    decode_common.cuh, kernels.h): a profile summary stays valid only while none of them
+    has changed."""
     csrc = os.path.join(ROOT, "fp8_kv_cache_quant_gb300", "csrc")
     h = hashlib.sha256()
     for name in (kernel_file, "common.cuh", "tc.cuh", "decode_common.cuh", "kernels.h"):
         path = os.path.join(csrc, name)
         if os.path.exists(path):
-            h.update(open(path, "rb").read())
+            h.update(_code_only(open(path, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

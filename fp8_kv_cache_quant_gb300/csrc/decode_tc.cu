@@ -25,10 +25,13 @@
 //   warps 4-7  correction: thread i owns head_dim row i (and 128 + i): each tile's
 //              O_tile^T is promoted into FP32 registers, acc = acc * alpha + O_tile, off
 //              the softmax warps' critical path; then the split's output.
-//   warp 8     TMA: each 16-token block of K and V is one box [16][128 bytes] of the
-//              paged pool (4-D tensor map), 8 blocks per tile.
-//   warp 9     allocates TMEM, issues the MMAs (S^T one tile ahead of P.V), commits to
-//              mbarriers.
+//   warp 8     K copies: each 16-token block is one box [16][row bytes] of the paged pool
+//              (4-D tensor map), 8 blocks per tile issued from 8 lanes; in the prologue
+//              also the first tiles' V copies, and (fp8_decode_step) the current token's
+//              K and V written into the pools by the split that holds it.
+//   warp 9     allocates TMEM; polls the pipeline's barriers and issues whichever is ready
+//              of a V tile's copies (8 lanes), an S^T product (one tile ahead) and a P.V
+//              product, committing to mbarriers.
 // The split writes (o / l, log2-sum-exp) per head; the CTA that finishes the last split
 // of (b, g) merges all of them in FP32.  Every wait is bounded in time; a timeout records
 // FKV_FAULT_TIMEOUT, lets the CTA's copies and MMAs drain and returns.

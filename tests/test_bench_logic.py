@@ -117,3 +117,13 @@ def test_max_over_two_gloo_ranks():
     for p in procs:
         p.join(timeout=60)
     assert res == {0: 2.5, 1: 2.5}
+
+
+def test_profile_hash_covers_code_not_comments():
+    """A committed profile's DRAM figure is trusted while the kernel code is unchanged:
+    comments and blank lines do not change the hash, code does."""
+    a = "int x = 1;  // one\n/* a block\n   comment */\n\nint y;\n"
+    b = "int x = 1;\nint y;   // a reason\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only("int x = 2;") != bench._code_only("int x = 1;")
+    assert len(bench.kernel_source_sha("decode_tc.cu")) == 16
