@@ -64,6 +64,20 @@ def test_split_planning(lib):
     assert f.fp8_decode_attn_workspace_size(1, 8, 2, 96, 10) == 0      # unsupported head_dim
 
 
+def test_split_plan_of_the_benchmark_layer():
+    """The automatic plan on the Llama-shaped benchmark layer (8 sequences, up to 1,447
+    blocks, 8 KV heads) for a 152-SM GB300 (the count used when no device is visible):
+    waves x blocks per split is 208 for both 14 splits of 104 blocks (two waves of 896
+    CTAs on 456 slots) and 7 splits of 208 (one wave of 448); the tie goes to the longer
+    splits, which measured 65.6 against 68.5 us per layer."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the plan depends on the visible GPU's SM count")
+    assert f.fp8_decode_attn_split_blocks(8, 32, 8, 128, 1447) == 208
+    assert f.fp8_decode_attn_num_splits(8, 32, 8, 128, 1447) == 7
+    assert f.fp8_decode_attn_split_blocks(8, 32, 8, 128, 1447, 0, 14) == 104   # a requested count still holds
+
+
 def _cache(D=128, bs=16, nb=4, H=2, k=1 << 20, v=1 << 21, fmt=0):
     return f._LayerCache(k, v, nb, bs, H, D, fmt)
 
