@@ -2,7 +2,8 @@
  * fp8kv — FP8 (e4m3) KV-cache quantisation and FP8 attention for GB300 (sm_103a).
  *
  * C ABI of libfp8kv.so.  Every tensor argument is a plain device pointer owned by the
- * caller; the library allocates nothing, keeps no global state, and enqueues its
+ * caller; the library allocates nothing, keeps no state between calls (the one fixed
+ * device array is the scratch of fp8_decode_attn_noalloc, below), and enqueues its
  * kernels on the given stream without synchronising.  Host pointers are marked "host".
  *
  * The operations restate the vLLM blog "FP8 KV-Cache and Attention quantization in
