@@ -276,6 +276,24 @@ def _time_graph(g, stream, steps, warmup, barrier):
     return e0.elapsed_time(e1) / steps
 
 
+def _step_distribution(g, stream, steps):
+    """Per-replay times of a graph (an event pair around every replay, after the timed
+    run): p10 / p50 / p90 in ms.  The events between replays add a little to each step,
+    so these are for the spread; the headline uses the one event pair of _time_graph."""
+    import numpy as np
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(steps):
+            g.replay()
+            ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    t = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)])
+    p10, p50, p90 = np.percentile(t, [10, 50, 90])
+    return {"steps": steps, "p10_ms": float(p10), "p50_ms": float(p50), "p90_ms": float(p90)}
+
+
 def _fp8_dense_peak():
     """FP8 dense tensor peak: the measured bf16 GEMM peak times the nominal fp8/bf16 ratio 2."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -626,6 +644,7 @@ def run_ours(args):
     ms_dec = max_over_ranks(_time_graph(g_dec, stream, args.steps, args.warmup, barrier))
     ms_e2e = max_over_ranks(_time_graph(g_e2e, stream, args.steps, args.warmup, barrier))
     ms_sep = max_over_ranks(_time_graph(g_sep, stream, args.steps, args.warmup, barrier)) if g_sep else None
+    spread = _step_distribution(g_fp8, stream, args.steps)
     clocks.stop()
 
     step_bytes = fp8.step_bytes()
@@ -690,6 +709,7 @@ def run_ours(args):
                        "l2": f"no flush: each step reads {step_bytes / 1e9:.2f} GB (> 129 MB L2)",
                        "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
             "us_per_step": ms_fp8 * 1e3,
+            "step_ms_spread": spread,
             "pct_of_hbm_peak": value / peak,
             "roofline": {"bound": "hbm", "kernel": dec_kernel,
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
