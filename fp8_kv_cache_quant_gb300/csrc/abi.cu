@@ -120,15 +120,22 @@ fkv_status cache_write(const void* k, const void* v, const int64_t* slot_mapping
                                               reinterpret_cast<cudaStream_t>(stream), current_num_sms(), clips));
 }
 
+}  // namespace
+
+namespace fkv {
+
 // fp8_decode_attn, and with k_new / v_new given fp8_decode_step (the current token written
-// into the pools by the same launch).
-fkv_status decode_impl(const void* k_new, const void* v_new, const void* q, int32_t batch, int32_t num_q_heads,
-                       fkv_layer_cache cache, const int32_t* block_table, int32_t max_blocks,
-                       const int32_t* context_lens, const float* q_scale, const float* k_scale,
-                       const float* v_scale, fkv_scale_gran gran, float softmax_scale, int32_t window,
-                       int32_t layer, const uint8_t* skip_layer_mask, int32_t num_layers, void* out,
-                       void* workspace, size_t workspace_bytes, int32_t num_splits, int32_t* fault,
-                       fkv_stream_t stream) {
+// into the pools by the same launch).  With `scratch` non-null the workspace arguments are
+// ignored: after every argument check and the split-K plan, scratch(need, ...) supplies the
+// workspace (fp8_decode_attn_noalloc), so both entry points return the same status for
+// the same arguments.
+fkv_status decode_entry(const void* k_new, const void* v_new, const void* q, int32_t batch, int32_t num_q_heads,
+                        fkv_layer_cache cache, const int32_t* block_table, int32_t max_blocks,
+                        const int32_t* context_lens, const float* q_scale, const float* k_scale,
+                        const float* v_scale, fkv_scale_gran gran, float softmax_scale, int32_t window,
+                        int32_t layer, const uint8_t* skip_layer_mask, int32_t num_layers, void* out,
+                        void* workspace, size_t workspace_bytes, ScratchProvider scratch, int32_t num_splits,
+                        int32_t* fault, fkv_stream_t stream) {
   const bool step = k_new != nullptr || v_new != nullptr;
   if (batch < 0 || num_q_heads <= 0 || max_blocks <= 0 || window < 0 || num_splits < 0)
     return FKV_INVALID_ARG;
@@ -149,16 +156,21 @@ fkv_status decode_impl(const void* k_new, const void* v_new, const void* q, int3
   if (step && !fkv::decode_uses_tensor_cores(cache.head_dim, elt)) return FKV_UNSUPPORTED;
   if (batch == 0) return FKV_OK;
   if (step && (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16))) return FKV_INVALID_ARG;
-  if (!q || !out || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || !workspace)
+  if (!q || !out || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || (!workspace && !scratch))
     return FKV_INVALID_ARG;
   if (!bf16 && (!q_scale || !k_scale || !v_scale)) return FKV_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(cache.k_cache, 16) || !aligned(cache.v_cache, 16) ||
-      !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+      !aligned(block_table, 4) || !aligned(context_lens, 4))
     return FKV_INVALID_ARG;
   DecodePlan plan;
   if (!plan_decode(batch, num_q_heads, cache.num_kv_heads, cache.head_dim, max_blocks, window, num_splits, &plan))
     return FKV_UNSUPPORTED;
-  if (workspace_bytes < plan.o_bytes + plan.lse_bytes + plan.cnt_bytes) return FKV_INVALID_ARG;
+  const size_t need = plan.o_bytes + plan.lse_bytes + plan.cnt_bytes;
+  if (scratch) {
+    const fkv_status sst = scratch(need, &workspace, &workspace_bytes);
+    if (sst != FKV_OK) return sst;
+  }
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return FKV_INVALID_ARG;
 
   DecodeParams p;
   std::memset(&p, 0, sizeof(p));
@@ -197,7 +209,9 @@ fkv_status decode_impl(const void* k_new, const void* v_new, const void* q, int3
   return from_cuda(fkv::launch_decode(p, cache.head_dim, elt, G, s));
 }
 
-}  // namespace
+}  // namespace fkv
+
+using fkv::decode_entry;
 
 extern "C" {
 
@@ -269,9 +283,9 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads, fk
                            const uint8_t* skip_layer_mask, int32_t num_layers, void* out, void* workspace,
                            size_t workspace_bytes, int32_t num_splits, int32_t* fault,
                            fkv_stream_t stream) {
-  return decode_impl(nullptr, nullptr, q, batch, num_q_heads, cache, block_table, max_blocks, context_lens, q_scale,
-                     k_scale, v_scale, gran, softmax_scale, window, layer, skip_layer_mask, num_layers, out, workspace,
-                     workspace_bytes, num_splits, fault, stream);
+  return decode_entry(nullptr, nullptr, q, batch, num_q_heads, cache, block_table, max_blocks, context_lens, q_scale,
+                      k_scale, v_scale, gran, softmax_scale, window, layer, skip_layer_mask, num_layers, out, workspace,
+                      workspace_bytes, nullptr, num_splits, fault, stream);
 }
 
 fkv_status fp8_decode_step(const void* k_new, const void* v_new, const void* q, int32_t batch,
@@ -282,9 +296,9 @@ fkv_status fp8_decode_step(const void* k_new, const void* v_new, const void* q, 
                            int32_t num_layers, void* out, void* workspace, size_t workspace_bytes,
                            int32_t num_splits, int32_t* fault, fkv_stream_t stream) {
   if (!k_new || !v_new) return FKV_INVALID_ARG;
-  return decode_impl(k_new, v_new, q, batch, num_q_heads, cache, block_table, max_blocks, context_lens, q_scale,
-                     k_scale, v_scale, gran, softmax_scale, window, layer, skip_layer_mask, num_layers, out, workspace,
-                     workspace_bytes, num_splits, fault, stream);
+  return decode_entry(k_new, v_new, q, batch, num_q_heads, cache, block_table, max_blocks, context_lens, q_scale,
+                      k_scale, v_scale, gran, softmax_scale, window, layer, skip_layer_mask, num_layers, out, workspace,
+                      workspace_bytes, nullptr, num_splits, fault, stream);
 }
 
 int32_t fkv_prefill_block_n(int32_t head_dim) { return supported_head_dim(head_dim) ? 128 : 0; }

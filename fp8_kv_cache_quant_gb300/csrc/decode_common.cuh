@@ -8,15 +8,20 @@ namespace fkv {
 
 // Keys [lo, T) of sequence b, as blocks [blk_begin, blk_end), in nsplit splits of p.bps
 // blocks.  A context longer than the block table can address is clamped (and reported).
+// `clamped` marks a context length outside [0, max_blocks * 16]: the fused cache write of
+// fp8_decode_step then writes nothing (position T - 1 of the clamped range is a cached
+// token of the caller's, not the current one).
 struct SeqRange {
   int T, lo, blk_begin, blk_end, nsplit;
+  bool clamped;
 };
 
 FKV_DEV SeqRange seq_range(const DecodeParams& p, int b, bool report) {
   SeqRange r;
   int T = p.context_lens[b];
   const int cap = p.max_blocks * 16;
-  if (T < 0 || T > cap) {
+  r.clamped = T < 0 || T > cap;
+  if (r.clamped) {
     if (report) raise_fault(p.fault, FKV_FAULT_CONTEXT);
     T = T < 0 ? 0 : cap;
   }

@@ -9,40 +9,90 @@
 // library, and allocates nothing itself.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
+#include "kernels.h"
 
 namespace {
 
-// Scratch for the split partials (o / l and log-sum-exp of every split).  Every call on
-// a device reuses the same bytes; each call writes every partial it later reads, so no
-// part of it has to start at zero.
+// Scratch for the split partials (o / l and log-sum-exp of every split) and the
+// split-completion counters.  Every call on a device reuses the same bytes: the counters
+// are cleared by each call before its launch, and each split writes every partial that
+// the merge later reads, so nothing else has to start at zero.
 static __device__ __align__(256) unsigned char g_decode_scratch[FKV_NOALLOC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+// The array's device address belongs to the context the module was loaded into: the
+// primary context of a device until a device reset destroys it, or a context the caller
+// created and made current.  The address is therefore cached per context, keyed by the
+// driver's context id (unique for the life of the process, never reused after a reset),
+// and looked up with cudaGetSymbolAddress, with that context current, the first time a
+// context calls.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device.  The name of the array is
-// only a host-side stand-in; the address is looked up once per device, with that device
-// current, and cached.
-fkv_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
+struct Cached {
+  unsigned long long ctx_id;
+  void* addr;
+};
+constexpr int kMaxContexts = 64;
+std::mutex g_mu;
+Cached g_cache[kMaxContexts];
+int g_cached = 0;
+CtxGetCurrentFn g_get_current = nullptr;
+CtxGetIdFn g_get_id = nullptr;
+bool g_driver_looked_up = false;
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return reinterpret_cast<Fn>(ptr);
+}
+
+// Id of the current context, or false when the driver cannot tell (no context current).
+bool current_ctx_id(unsigned long long* id) {
+  CUcontext ctx = nullptr;
+  if (!g_get_current || !g_get_id || g_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return g_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Supplies fp8_decode_attn's workspace from the fixed array (a ScratchProvider): sizes
+// beyond the array are FKV_INVALID_ARG.
+fkv_status noalloc_scratch(size_t need, void** ws, size_t* bytes) {
+  if (need > static_cast<size_t>(FKV_NOALLOC_WORKSPACE_BYTES)) return FKV_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_driver_looked_up) {
+    g_get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    g_get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    g_driver_looked_up = true;
+  }
+  unsigned long long id = 0;
+  bool have_id = current_ctx_id(&id);
+  if (have_id) {
+    for (int i = 0; i < g_cached; ++i)
+      if (g_cache[i].ctx_id == id) {
+        *ws = g_cache[i].addr;
+        *bytes = FKV_NOALLOC_WORKSPACE_BYTES;
+        return FKV_OK;
+      }
+  }
+  // first call in this context: the lookup also makes the runtime's primary context
+  // current when none was (the module is loaded into it)
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
     cudaGetLastError();
     return FKV_CUDA_ERROR;
   }
-  if (dev < 0 || dev >= kMaxDevices) return FKV_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return FKV_CUDA_ERROR;
-    }
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  if (!have_id) have_id = current_ctx_id(&id);
+  if (have_id && g_cached < kMaxContexts) g_cache[g_cached++] = Cached{id, p};
+  *ws = p;
+  *bytes = FKV_NOALLOC_WORKSPACE_BYTES;
   return FKV_OK;
 }
 
@@ -54,21 +104,7 @@ extern "C" fkv_status fp8_decode_attn_noalloc(
     const float* v_scale, fkv_scale_gran gran, float softmax_scale, int32_t window, int32_t layer,
     const uint8_t* skip_layer_mask, int32_t num_layers, void* out, int32_t num_splits, int32_t* fault,
     fkv_stream_t stream) {
-  if (batch < 0 || num_q_heads <= 0 || cache.num_kv_heads <= 0 || max_blocks <= 0) return FKV_INVALID_ARG;
-  if (batch == 0) return FKV_OK;
-  const size_t need = fp8_decode_attn_workspace_size(batch, num_q_heads, cache.num_kv_heads, cache.head_dim,
-                                                     max_blocks, window, num_splits);
-  if (need == 0) {
-    // sizes the split-K plan rejects: let the regular entry point report why
-    return fp8_decode_attn(q, batch, num_q_heads, cache, block_table, max_blocks, context_lens, q_scale, k_scale,
-                           v_scale, gran, softmax_scale, window, layer, skip_layer_mask, num_layers, out, nullptr,
-                           0, num_splits, fault, stream);
-  }
-  if (need > static_cast<size_t>(FKV_NOALLOC_WORKSPACE_BYTES)) return FKV_INVALID_ARG;  // beyond the fixed scratch
-  void* ws = nullptr;
-  const fkv_status st = scratch_address(&ws);
-  if (st != FKV_OK) return st;
-  return fp8_decode_attn(q, batch, num_q_heads, cache, block_table, max_blocks, context_lens, q_scale, k_scale,
-                         v_scale, gran, softmax_scale, window, layer, skip_layer_mask, num_layers, out, ws,
-                         static_cast<size_t>(FKV_NOALLOC_WORKSPACE_BYTES), num_splits, fault, stream);
+  return fkv::decode_entry(nullptr, nullptr, q, batch, num_q_heads, cache, block_table, max_blocks, context_lens,
+                           q_scale, k_scale, v_scale, gran, softmax_scale, window, layer, skip_layer_mask,
+                           num_layers, out, nullptr, 0, noalloc_scratch, num_splits, fault, stream);
 }

@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     fence_mbar_init();
   }
   // fp8_decode_step: the split holding position T - 1 (the last) writes the current token
-  // into the pools before its first copy of that block
-  if (warp == 8 && p.k_new != nullptr && sigma == r.nsplit - 1) write_current_token<D>(p, b, g, T, lane);
+  // into the pools before its first copy of that block (not when the context was clamped)
+  if (warp == 8 && p.k_new != nullptr && sigma == r.nsplit - 1 && !r.clamped) write_current_token<D>(p, b, g, T, lane);
   if (warp == 8) {
     __syncwarp();
     const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks + bb;

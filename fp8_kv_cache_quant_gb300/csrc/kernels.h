@@ -71,4 +71,19 @@ cudaError_t launch_decode(const DecodeParams& p, int D, int elt, int G, cudaStre
 bool decode_uses_tensor_cores(int D, int elt);
 cudaError_t launch_decode_tc(const DecodeParams& p, int D, int G, cudaStream_t s);
 
+// Supplies the decode's workspace of `need` bytes when the caller passes none: sets *ws
+// (256-byte aligned) and *bytes, or returns the status the entry point then returns.
+using ScratchProvider = fkv_status (*)(size_t need, void** ws, size_t* bytes);
+
+// The whole of fp8_decode_attn (k_new = v_new = NULL) and fp8_decode_step: argument
+// checks, the split-K plan, then the launch.  With scratch non-null the workspace comes
+// from it, after every check (fp8_decode_attn_noalloc).
+fkv_status decode_entry(const void* k_new, const void* v_new, const void* q, int32_t batch, int32_t num_q_heads,
+                        fkv_layer_cache cache, const int32_t* block_table, int32_t max_blocks,
+                        const int32_t* context_lens, const float* q_scale, const float* k_scale,
+                        const float* v_scale, fkv_scale_gran gran, float softmax_scale, int32_t window,
+                        int32_t layer, const uint8_t* skip_layer_mask, int32_t num_layers, void* out,
+                        void* workspace, size_t workspace_bytes, ScratchProvider scratch, int32_t num_splits,
+                        int32_t* fault, fkv_stream_t stream);
+
 }  // namespace fkv

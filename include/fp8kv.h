@@ -68,7 +68,10 @@ typedef enum {
 #define FKV_FAULT_BLOCK_ID 1 /* block table entry outside [0, num_blocks): block 0 read instead */
 #define FKV_FAULT_SLOT 2     /* cache-write slot >= num_blocks * block_size: token skipped      */
 #define FKV_FAULT_CONTEXT 4  /* context length < 0 or > max_blocks * block_size: clamped      */
-#define FKV_FAULT_TIMEOUT 8  /* an in-kernel pipeline wait exceeded 1 s: work abandoned        */
+#define FKV_FAULT_TIMEOUT 8  /* an in-kernel wait ran out of time (200 ms per pipeline wait in the
+                                tensor-core kernels, 1 s elsewhere): the CTA's remaining work is
+                                abandoned after its copies and products drain; its partial
+                                results are undefined                                             */
 #define FKV_FAULT_QLEN 16    /* prefill: query length > context length: sequence skipped     */
 
 /* FP8 format of a layer's pools (fkv_layer_cache.kv_format). */
@@ -232,7 +235,8 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads,
  *   all other arguments as for fp8_decode_attn
  * Only e4m3 layers (the tensor-core decode): a skip layer or an e5m2 pool returns
  * FKV_UNSUPPORTED (write with kv_quant_cache and call fp8_decode_attn instead).  A block
- * id out of range is reported as for fp8_decode_attn and its row is not written.
+ * id out of range is reported as for fp8_decode_attn and its row is not written; so is a
+ * context length outside [0, max_blocks * 16] (FKV_FAULT_CONTEXT): no pool byte changes.
  */
 fkv_status fp8_decode_step(const void* k_new, const void* v_new, const void* q, int32_t batch,
                            int32_t num_q_heads, fkv_layer_cache cache, const int32_t* block_table,
@@ -258,9 +262,12 @@ fkv_status fp8_decode_step(const void* k_new, const void* v_new, const void* q, 
  *
  *   - Returns FKV_INVALID_ARG when fp8_decode_attn_workspace_size(...) for these sizes
  *     exceeds FKV_NOALLOC_WORKSPACE_BYTES (use fp8_decode_attn with a caller workspace
- *     for such sizes), and every error fp8_decode_attn returns.
- *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ *     for such sizes), and otherwise exactly the status fp8_decode_attn returns for the
+ *     same arguments (the same checks run first, in the same order).
+ *   - The first call in a CUDA context (the device's primary context, or a context the
+ *     caller made current) looks up the array's device address in that context and
+ *     caches it for that context; make that first call before any stream capture.  A
+ *     device reset or a new context gets its own lookup on its first call.
  *   - All calls share the one array: calls whose kernels overlap on the GPU (other
  *     streams, other host threads) race on it and produce wrong results.  Calls in one
  *     stream are ordered and safe; each call writes every scratch byte it later reads.

@@ -199,3 +199,46 @@ def test_prefill_validation(lib):
     assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, None, p, p, 0, 0.0, 1, 0, 1, 0, None, 0, p, None,
                None) == f.INVALID_ARG
     assert pre(p, p, 0, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 0, 0, 0, None, 0, p, None, None) == f.OK
+
+
+def test_noalloc_returns_the_workspace_entry_points_status(lib):
+    """fp8_decode_attn_noalloc runs fp8_decode_attn's checks first, in the same order, so
+    both return the same status for the same arguments; the fixed scratch is asked for
+    only after them (beyond it: FKV_INVALID_ARG)."""
+    p = 1 << 12
+
+    def args(**kw):
+        a = dict(q=p, batch=2, hq=8, cache=_cache(), table=p, max_blocks=4, ctx=p, qs=p, ks=p, vs=p, gran=0,
+                 sm=0.0, window=0, layer=0, mask=None, nl=0, out=p, splits=0, fault=None, stream=None)
+        a.update(kw)
+        return a
+
+    def ws(a):
+        return lib.fp8_decode_attn(a["q"], a["batch"], a["hq"], a["cache"], a["table"], a["max_blocks"], a["ctx"],
+                                   a["qs"], a["ks"], a["vs"], a["gran"], a["sm"], a["window"], a["layer"], a["mask"],
+                                   a["nl"], a["out"], p, 1 << 40, a["splits"], a["fault"], a["stream"])
+
+    def noalloc(a):
+        return lib.fp8_decode_attn_noalloc(a["q"], a["batch"], a["hq"], a["cache"], a["table"], a["max_blocks"],
+                                           a["ctx"], a["qs"], a["ks"], a["vs"], a["gran"], a["sm"], a["window"],
+                                           a["layer"], a["mask"], a["nl"], a["out"], a["splits"], a["fault"],
+                                           a["stream"])
+
+    variants = [
+        dict(hq=7), dict(hq=64), dict(cache=_cache(D=80)), dict(cache=_cache(bs=32)), dict(batch=-1),
+        dict(window=-3), dict(sm=float("nan")), dict(q=None), dict(qs=None), dict(out=p + 8),
+        dict(layer=3, mask=ctypes.cast((ctypes.c_uint8 * 1)(0), ctypes.c_void_p), nl=1),
+        # bad head_dim together with batch 0: the checks come before the empty-batch shortcut
+        dict(batch=0, cache=_cache(D=96)), dict(batch=0, hq=7),
+        # a context too long for 1024 splits of 256 blocks: the plan rejects it (unsupported)
+        dict(max_blocks=300_000), dict(batch=0),
+    ]
+    for kw in variants:
+        a = args(**kw)
+        assert noalloc(a) == ws(a), kw
+    assert noalloc(args(max_blocks=300_000)) == f.UNSUPPORTED
+    assert noalloc(args(batch=0)) == f.OK
+    # sizes whose workspace exceeds the fixed scratch
+    big = args(batch=512, hq=32, cache=_cache(nb=100, H=8), max_blocks=8192, splits=64)
+    assert f.fp8_decode_attn_workspace_size(512, 32, 8, 128, 8192, 0, 64) > f.NOALLOC_WORKSPACE_BYTES
+    assert noalloc(big) == f.INVALID_ARG

@@ -134,3 +134,33 @@ def test_decode_step_rejects_non_e4m3_layers():
     one = torch.ones(1).cuda()
     with pytest.raises(f.FkvError):
         f.fp8_decode_step(kn, kn, q, e5, to_dev(table), to_dev(ctx), one, one, one)
+
+
+def test_decode_step_oversized_context_writes_nothing():
+    """A context length beyond what the block table can address is clamped and reported
+    (FKV_FAULT_CONTEXT); the fused write must then leave every pool byte as it was,
+    since position T - 1 of the clamped range is one of the caller's cached tokens."""
+    rng = np.random.default_rng(17)
+    ctx = np.array([40, 20], np.int32)
+    table, nb = synth.block_table(ctx, seed=2)
+    Hkv, D, Hq = 2, 128, 8
+    n = int(ctx.sum())
+    k = torch.from_numpy(rng.standard_normal((n, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((n, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    q = torch.from_numpy(rng.standard_normal((2, Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    one = torch.ones(1)
+    cache = f.LayerCache.empty(nb, Hkv, D)
+    cache.k_cache.zero_()
+    cache.v_cache.zero_()
+    f.kv_quant_cache(k.cuda(), v.cuda(), to_dev(synth.slot_mapping(table, ctx)), cache, to_dev(one), to_dev(one), 0)
+    k_before, v_before = cache.k_cache.clone(), cache.v_cache.clone()
+    k_new = torch.full((2, Hkv, D), 3.0, dtype=torch.bfloat16)
+    v_new = torch.full((2, Hkv, D), -3.0, dtype=torch.bfloat16)
+    fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+    long_ctx = np.array([10_000, -5], np.int32)   # beyond the table's 3 blocks; negative
+    o = f.fp8_decode_step(k_new.cuda(), v_new.cuda(), q.cuda(), cache, to_dev(table), to_dev(long_ctx),
+                          to_dev(one), to_dev(one), to_dev(one), 0, fault=fault)
+    torch.cuda.synchronize()
+    assert int(fault.item()) & f.FAULT_CONTEXT
+    assert torch.isfinite(o.float()).all()
+    assert torch.equal(cache.k_cache, k_before) and torch.equal(cache.v_cache, v_before)
