@@ -65,6 +65,29 @@ def softmax_attend(qv, K, V, tau):
     return w @ V, w
 
 
+def p_rounding_bound(qv, K, V, tau):
+    """Element-wise bound on how far an attention that rounds P to e4m3 can sit from the
+    exact softmax result, for one query vector over dequantised K, V [T][D].
+
+    The FP8 Score*V product (vLLM blog, 引言; "Kernel 与 vLLM 改进", Two-level
+    accumulation) multiplies V by P8 = e4m3(p * 448) with p = e^(s - m') taken against a
+    running maximum m' <= M = max_j s_j, and divides by 448 again; the denominator sums
+    the unrounded p (R10, R11).  e4m3 has 3 mantissa bits, so a code >= 2^-6 (normal)
+    is within 2^-4 relatively of p * 448, a subnormal code (spacing 2^-9) within 2^-10
+    absolutely, and p * 448 <= 448 never saturates.  Rescaled to the global maximum
+    (factor e^(m' - M) <= 1), every rounded weight satisfies
+        |p^_j - p_j| <= max(2^-4 p_j, 2^-10 / 448),   p_j = e^(s_j - M),
+    hence, with l = sum_j p_j and o the exact output,
+        |o^_d - o_d| <= B_d = sum_j max(2^-4 p_j, 2^-10 / 448) |v_jd| / l.
+    Returns (o, B), both float64 [D]; the bound holds for every split and tile plan."""
+    s = (np.asarray(K, np.float64) @ np.asarray(qv, np.float64)) * tau
+    p = np.exp(s - np.max(s))
+    l = np.sum(p)
+    Va = np.abs(np.asarray(V, np.float64))
+    eps = np.maximum(2.0 ** -4 * p, 2.0 ** -10 / 448.0)
+    return (p @ V) / l, (eps @ Va) / l
+
+
 def split_decode(qv, K, V, T, lo, tau, *, split_blocks, block_n, p_quant, block_size=16):
     """One query over keys lo .. T-1 (dequantised K, V [T - lo][D]) as a split-K decode
     (R23): splits of ``split_blocks`` blocks from block lo // block_size, each walked in
@@ -93,7 +116,8 @@ def split_decode(qv, K, V, T, lo, tau, *, split_blocks, block_n, p_quant, block_
 
 def decode_attention(q, k_pool, v_pool, block_table, context_lens, q_scale, k_scale, v_scale, *,
                      fp8: bool = True, softmax_scale: float = 0.0, window: int = 0, block_size: int = 16,
-                     p_quant: bool = False, split_blocks: int = 0, block_n: int = 128, fmt: str = "e4m3"):
+                     p_quant: bool = False, split_blocks: int = 0, block_n: int = 128, fmt: str = "e4m3",
+                     p_bound: bool = False):
     """Paged decode attention, one query per sequence.
 
     q: float64 [B][Hq][D] (bf16 values).  k_pool / v_pool: uint8 e4m3 codes
@@ -102,7 +126,8 @@ def decode_attention(q, k_pool, v_pool, block_table, context_lens, q_scale, k_sc
     Returns float64 [B][Hq][D]; a sequence with no key gives a zero row.
     ``split_blocks`` > 0 computes it as the split-K decode of R23 (``p_quant`` rounds P,
     on e4m3 layers only); 0 is the plain softmax.  ``fmt`` "e5m2" reads e5m2 pools with
-    the bf16 query and exact P (R25).
+    the bf16 query and exact P (R25).  ``p_bound`` returns (plain softmax result, the
+    element-wise bound of ``p_rounding_bound``), both [B][Hq][D].
     """
     q = np.asarray(q, dtype=np.float64)
     B, Hq, D = q.shape
@@ -110,6 +135,7 @@ def decode_attention(q, k_pool, v_pool, block_table, context_lens, q_scale, k_sc
     G = Hq // Hkv
     tau = softmax_scale if softmax_scale > 0 else 1.0 / math.sqrt(D)
     out = np.zeros((B, Hq, D), dtype=np.float64)
+    bound = np.zeros((B, Hq, D), dtype=np.float64)
     for b in range(B):
         T = int(context_lens[b])
         lo = max(0, T - window) if window > 0 else 0
@@ -125,22 +151,26 @@ def decode_attention(q, k_pool, v_pool, block_table, context_lens, q_scale, k_sc
                     qv = e4m3.decode(e4m3.quantize(q[b, h], qs)) * qs
                 else:
                     qv = q[b, h]
-                if split_blocks > 0:
+                if p_bound:
+                    out[b, h], bound[b, h] = p_rounding_bound(qv, K, V, tau)
+                elif split_blocks > 0:
                     out[b, h] = split_decode(qv, K, V, T, lo, tau, split_blocks=split_blocks, block_n=block_n,
                                              p_quant=p_quant and fp8 and fmt == "e4m3", block_size=block_size)
                 else:
                     out[b, h], _ = softmax_attend(qv, K, V, tau)
-    return out
+    return (out, bound) if p_bound else out
 
 
 def decode_attention_contiguous(q_b, k_seq, v_seq, q_scale, k_scale, v_scale, *, fp8=True,
                                 softmax_scale=0.0, window=0, heads=None, p_quant=False, split_blocks=0,
-                                block_n=128):
+                                block_n=128, p_bound=False):
     """Decode attention of ONE sequence from its contiguous bf16 K/V ([T][Hkv][D],
     float64 values): the oracle quantises K/V itself with the same rule as the cache
     write, then attends (as the split-K decode of R23 when ``split_blocks`` > 0).  Used
     at full workload sizes on sampled sequences/heads.
-    Returns {h: float64[D]} for the requested query heads (default: all)."""
+    Returns {h: float64[D]} for the requested query heads (default: all); with
+    ``p_bound`` {h: (o, B)}: the exact softmax result and the bound of
+    ``p_rounding_bound`` on an attention that rounds P to e4m3."""
     Hq, D = q_b.shape
     T, Hkv, _ = k_seq.shape
     G = Hq // Hkv
@@ -162,14 +192,16 @@ def decode_attention_contiguous(q_b, k_seq, v_seq, q_scale, k_scale, v_scale, *,
             cache = {g: (K, V)}
         K, V = cache[g]
         if T - lo <= 0:
-            res[h] = np.zeros(D)
+            res[h] = (np.zeros(D), np.zeros(D)) if p_bound else np.zeros(D)
             continue
         if fp8:
             qs = head_scale(q_scale, h)
             qv = e4m3.decode(e4m3.quantize(q_b[h], qs)) * qs
         else:
             qv = q_b[h]
-        if split_blocks > 0:
+        if p_bound:
+            res[h] = p_rounding_bound(qv, K, V, tau)
+        elif split_blocks > 0:
             res[h] = split_decode(qv, K, V, T, lo, tau, split_blocks=split_blocks, block_n=block_n,
                                   p_quant=p_quant and fp8)
         else:

@@ -68,3 +68,58 @@ def oracle_pools(oracle_kvcache, ctx, table, num_blocks, k, v, ks, vs, bf16_laye
     oracle_kvcache.cache_write(synth.bf16_to_f64(k), synth.bf16_to_f64(v), slots, kp, vp,
                                np.asarray(ks, np.float32), np.asarray(vs, np.float32), skip=bf16_layer, fmt=fmt)
     return kp, vp
+
+
+# The tensor-core decode of e4m3 layers and the prefill round P per tile of this many keys
+# (fp8kv.h: fkv_decode_block_n, fkv_prefill_block_n); the tests pass these to the oracle
+# and check that the library agrees.
+DECODE_BLOCK_N = 128
+PREFILL_BLOCK_N = 128
+
+
+def decode_split_blocks(max_blocks, window, num_splits):
+    """Blocks per context split of fp8_decode_attn for a requested split count, restated
+    from the rule include/fp8kv.h documents: n = max_blocks, or with a window W at most
+    ceil(W / 16) + 1 blocks; ceil(n / num_splits), at most 256 and at least
+    ceil(n / 1024), rounded up to a multiple of 8."""
+    assert num_splits > 0
+    n = max_blocks if window <= 0 else min(max_blocks, -(-window // 16) + 1)
+    bps = min(-(-n // num_splits), 256)
+    bps = max(bps, -(-n // 1024), 1)
+    return -(-bps // 8) * 8
+
+
+def auto_split_blocks(batch, num_kv_heads, max_blocks, window, num_sms):
+    """The automatic plan (num_splits 0) restated from include/fp8kv.h: the multiple of 8
+    up to 256 minimising waves * blocks per split, waves counted on 3 resident CTAs per
+    SM, ties to the larger count."""
+    n = max_blocks if window <= 0 else min(max_blocks, -(-window // 16) + 1)
+    units, slots = max(batch, 1) * num_kv_heads, 3 * num_sms
+    best = None
+    for c in range(8, 257, 8):
+        ctas = units * -(-n // c)
+        cost = -(-ctas // slots) * min(c, n)
+        if best is None or cost < best[1] or (cost == best[1] and c > best[0]):
+            best = (c, cost)
+    bps = max(best[0], -(-n // 1024))
+    return -(-bps // 8) * 8
+
+
+def assert_within_p_bound(gpu, exact, bound, what=""):
+    """The tensor-core decode against the plain softmax definition (P exact, reading R9 of
+    the exact result): its output may differ by the rounding of P to e4m3, at most the
+    oracle's p_rounding_bound B per element, plus the kernel's own arithmetic — the
+    bf16 rounding of the output (2^-9 relative) and FP32 scores and sums (relative errors
+    below 1e-4 of the weights) — covered by the factor 1 + 2^-6 on B and 2^-8 |o|.
+    Returns (rel-L2 distance, largest |gpu - exact| / B)."""
+    gpu = np.asarray(gpu, np.float64)
+    exact = np.asarray(exact, np.float64)
+    bound = np.asarray(bound, np.float64)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite GPU output"
+    err = np.abs(gpu - exact)
+    tol = bound * (1 + 2.0 ** -6) + 2.0 ** -8 * np.abs(exact)
+    worst = int(np.argmax(err - tol))
+    assert np.all(err <= tol), (f"{what}: |gpu - exact| {err.flat[worst]:.3e} above {tol.flat[worst]:.3e} "
+                                f"(bound {bound.flat[worst]:.3e}) at {np.unravel_index(worst, err.shape)}")
+    ratio = float(np.max(err / np.where(bound > 0, bound, np.inf))) if err.size else 0.0
+    return rel_l2(gpu, exact), ratio

@@ -1,12 +1,20 @@
 """fp8_decode_attn (split-K paged decode + FP32 merge) on the GPU against the oracle.
 
 Tolerance: max-abs 2e-2 and relative L2 1e-2 of the oracle's float64 FP8-emulated
-result.  Where the library rounds P (the tensor-core decode: fkv_decode_block_n > 0),
-the oracle walks the same splits and tiles with P rounded (reading R23); elsewhere P is
-exact and the oracle is the plain softmax.  Small cases cover every head_dim, several GQA group sizes, both scale
-granularities, the bf16 skip-layer path, windows, ragged and empty contexts and forced
-split counts; the full-size workloads are checked on sampled sequences and heads in the
-launch configuration the benchmark times.
+result.  Where the library rounds P (the tensor-core decode of e4m3 layers), the oracle
+walks the same splits and tiles with P rounded (reading R23); elsewhere P is exact and
+the oracle is the plain softmax.  The split size the oracle walks is never asked of the
+library: every test fixes the split count and derives the blocks per split from the rule
+the header documents (restated in helpers.decode_split_blocks), and asserts that the
+library reports the same; the automatic plan is checked on the benchmark's layer with a
+split size derived by hand for a 152-SM GB300.  Every e4m3 result is also compared with
+the plain softmax definition (P exact), within the element-wise bound that e4m3 rounding
+of P allows (oracle.attention.p_rounding_bound); the distances are recorded as test
+properties (rel_l2_vs_exact, worst_err_over_bound).
+Small cases cover every head_dim, several GQA group sizes, both scale granularities, the
+bf16 skip-layer path, windows, ragged and empty contexts and forced split counts; the
+full-size workloads are checked on sampled sequences and heads with the split plan the
+benchmark runs on a 152-SM GB300.
 """
 import math
 
@@ -15,7 +23,8 @@ import pytest
 import torch
 
 import synth
-from helpers import assert_close, build_layer, oracle_pools, to_dev
+from helpers import (DECODE_BLOCK_N, assert_close, assert_within_p_bound, auto_split_blocks, build_layer,
+                     decode_split_blocks, oracle_pools, to_dev)
 from oracle import attention, e4m3, kvcache
 
 f = pytest.importorskip("fp8_kv_cache_quant_gb300")
@@ -23,12 +32,17 @@ pytestmark = pytest.mark.gpu
 
 
 def _oracle_mode(D, bf16_layer, batch, Hq, Hkv, max_blocks, window, num_splits):
-    """Keyword arguments of the oracle's decode matching the library's kernel choice."""
-    bn = f.fkv_decode_block_n(D, bf16_layer)
-    if bn == 0:
+    """Keyword arguments of the oracle's decode for the kernel the layer runs.  bf16 layers:
+    P exact, the plain softmax.  e4m3 layers: P rounded per 128-key tile of each split
+    (R23), with the blocks per split of the documented rule for this split count."""
+    if bf16_layer:
+        assert f.fkv_decode_block_n(D, True) == 0
         return {}
-    bps = f.fp8_decode_attn_split_blocks(batch, Hq, Hkv, D, max_blocks, window, num_splits)
-    return dict(p_quant=True, split_blocks=bps, block_n=bn)
+    assert num_splits > 0, "e4m3 parity cases fix their split count"
+    assert f.fkv_decode_block_n(D) == DECODE_BLOCK_N
+    bps = decode_split_blocks(max_blocks, window, num_splits)
+    assert f.fp8_decode_attn_split_blocks(batch, Hq, Hkv, D, max_blocks, window, num_splits) == bps
+    return dict(p_quant=True, split_blocks=bps, block_n=DECODE_BLOCK_N)
 
 
 def _inputs(rng, ctx, Hq, Hkv, D, scale_k=3.0):
@@ -40,24 +54,25 @@ def _inputs(rng, ctx, Hq, Hkv, D, scale_k=3.0):
 
 
 CASES = [
-    # D, G, bf16 layer, gran, window, num_splits
-    (128, 4, False, 0, 0, 0),
+    # D, G, bf16 layer, gran, window, num_splits (0: automatic, bf16 layers only)
+    (128, 4, False, 0, 0, 4),
     (128, 4, False, 1, 0, 3),
-    (64, 8, False, 1, 0, 0),
+    (64, 8, False, 1, 0, 2),
     (64, 8, True, 0, 128, 0),
     (128, 8, False, 0, 0, 1),
-    (256, 1, False, 1, 0, 0),
+    (256, 1, False, 1, 0, 6),
     (256, 8, True, 0, 0, 2),
-    (128, 16, False, 1, 50, 0),
+    (128, 16, False, 1, 50, 1),
     (64, 2, False, 0, 0, 5),
     (128, 1, True, 0, 0, 0),
     (64, 16, True, 1, 0, 0),
     (256, 4, False, 0, 33, 1),
+    (64, 4, False, 1, 0, 8),
 ]
 
 
 @pytest.mark.parametrize("D,G,bf16_layer,gran,window,splits", CASES)
-def test_decode_small_parity(D, G, bf16_layer, gran, window, splits):
+def test_decode_small_parity(D, G, bf16_layer, gran, window, splits, record_property):
     rng = np.random.default_rng(D * 7 + G * 3 + window + splits)
     Hkv = 2
     Hq = Hkv * G
@@ -79,7 +94,14 @@ def test_decode_small_parity(D, G, bf16_layer, gran, window, splits):
                                      fp8=not bf16_layer, window=window, **mode)
     got = out.float().cpu().numpy()
     assert np.all(got[6] == 0), "empty context must give a zero row"
-    assert_close(got, ref, what=f"D={D} G={G} bf16={bf16_layer} gran={gran} W={window} splits={splits}")
+    what = f"D={D} G={G} bf16={bf16_layer} gran={gran} W={window} splits={splits}"
+    assert_close(got, ref, what=what)
+    if not bf16_layer:
+        exact, bound = attention.decode_attention(synth.bf16_to_f64(q), kp, vp, table, ctx, qs.numpy(), ks.numpy(),
+                                                  vs.numpy(), window=window, p_bound=True)
+        r, worst = assert_within_p_bound(got, exact, bound, what=what + " vs exact softmax")
+        record_property("rel_l2_vs_exact", r)
+        record_property("worst_err_over_bound", worst)
 
 
 @pytest.mark.parametrize("D,G,gran,window,splits", [
@@ -121,9 +143,10 @@ def test_decode_odd_kv_head_counts(Hkv, G, D):
     q, k, v = _inputs(rng, ctx, Hq, Hkv, D)
     qs, ks, vs = synth.amax_scales(q, 1), synth.amax_scales(k, 1), synth.amax_scales(v, 1)
     cache = build_layer(f, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), 1, False, sentinel=0xFF)
-    out = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(qs), to_dev(ks), to_dev(vs), 1)
+    out = f.fp8_decode_attn(q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(qs), to_dev(ks), to_dev(vs), 1,
+                            num_splits=3)
     kp, vp = oracle_pools(kvcache, ctx, table, nb, k, v, ks.numpy(), vs.numpy(), False)
-    mode = _oracle_mode(D, False, len(ctx), Hq, Hkv, table.shape[1], 0, 0)
+    mode = _oracle_mode(D, False, len(ctx), Hq, Hkv, table.shape[1], 0, 3)
     ref = attention.decode_attention(synth.bf16_to_f64(q), kp, vp, table, ctx, qs.numpy(), ks.numpy(), vs.numpy(),
                                      **mode)
     assert_close(out.float().cpu().numpy(), ref, what=f"Hkv={Hkv} G={G} D={D}")
@@ -145,10 +168,17 @@ def test_split_count_invariance_and_permutation(D):
     assert np.all(np.isfinite(outs[1]))
     if f.fkv_decode_block_n(D) > 0:
         # P rounded per split and tile: each split count against the oracle walking the
-        # same splits (their P codes differ by design)
+        # same splits (their P codes differ by design); the automatic plan's split size is
+        # the documented rule evaluated for this device's SM count
         kp, vp = oracle_pools(kvcache, ctx, table, nb, k, v, one, one, False)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
         for s, o in outs.items():
-            mode = _oracle_mode(D, False, len(ctx), Hq, Hkv, table.shape[1], 0, s)
+            if s > 0:
+                mode = _oracle_mode(D, False, len(ctx), Hq, Hkv, table.shape[1], 0, s)
+            else:
+                bps = auto_split_blocks(len(ctx), Hkv, table.shape[1], 0, sms)
+                assert f.fp8_decode_attn_split_blocks(len(ctx), Hq, Hkv, D, table.shape[1]) == bps
+                mode = dict(p_quant=True, split_blocks=bps, block_n=DECODE_BLOCK_N)
             ref = attention.decode_attention(synth.bf16_to_f64(q), kp, vp, table, ctx, one, one, one, **mode)
             assert_close(o, ref, what=f"num_splits={s}")
     else:
@@ -166,22 +196,48 @@ def test_split_count_invariance_and_permutation(D):
     assert np.array_equal(o2, outs[7])
 
 
-def _decode_layer_check(w, layer, ctx, table, nb, seqs, heads, num_splits=0):
+# Split counts of the full-size workloads: the automatic plan of a 152-SM GB300 (456
+# resident CTAs, 3 per SM), derived by hand from the documented rule (waves x blocks per
+# split minimal, ties to the longer split), passed explicitly so that the tests do not
+# depend on the SM count of the device they run on:
+#   1: 8 units (1 sequence x 8 KV heads), 256 blocks: 8 blocks per split -> 32 splits,
+#      256 CTAs, one wave of cost 8 (any longer split costs more) -> num_splits 32;
+#   2: 64 units, 1,447 blocks: 208 -> 7 splits, 448 CTAs, one wave, cost 208 (104 would
+#      take two waves, cost 208 too; the tie goes to 208) -> num_splits 7 (ceil(1447 / 7)
+#      = 207 -> 208);
+#   3: full layers 64 units, 1,774 blocks: 256 -> 7 splits, 448 CTAs, cost 256 (224 needs
+#      8 splits, 512 CTAs, two waves) -> 7 (ceil(1774 / 7) = 254 -> 256); window-128
+#      layers span at most 9 blocks: 8 -> 2 splits -> 2;
+#   4: 8 units, 8,192 blocks: 144 -> 57 splits, 456 CTAs, exactly one wave (136 needs 61
+#      splits, 488 CTAs) -> 57 (ceil(8192 / 57) = 144).
+WORKLOAD_SPLITS = {1: {0: 32}, 2: {0: 7}, 3: {0: 7, 128: 2}, 4: {0: 57}}
+
+
+def _decode_layer_check(w, layer, ctx, table, nb, seqs, heads, num_splits=None, exact=None, auto_bps=None):
     """Build one full-size layer through the C ABI and compare sampled (b, h) with the
-    oracle computed from the contiguous bf16 inputs."""
+    oracle computed from the contiguous bf16 inputs.  num_splits None: the workload's
+    split count (WORKLOAD_SPLITS); 0: the automatic plan, whose blocks per split the
+    caller gives as ``auto_bps``.  With a list ``exact`` (e4m3 layers) the plain softmax
+    results and their P-rounding bounds of the same (b, h) are appended to it."""
     data = synth.decode_layer(w, layer, ctx, device="cuda")
     bf16_layer = bool(w.skip_mask()[layer])
     gran = f.SCALE_PER_HEAD if w.scale_mode == "amax" else f.SCALE_PER_TENSOR
     cache = build_layer(f, ctx, table, nb, data.k, data.v, data.k_scale.cpu().numpy(), data.v_scale.cpu().numpy(),
                         gran, bf16_layer)
     window = w.layer_window(layer)
+    wid = next(i for i, x in synth.WORKLOADS.items() if x is w)
+    if num_splits is None:
+        num_splits = WORKLOAD_SPLITS[wid][window]
     out = f.fp8_decode_attn(data.q, cache, to_dev(table), to_dev(ctx), data.q_scale, data.k_scale, data.v_scale,
                             gran, window=window, layer=layer, skip_layer_mask=w.skip_mask(),
                             num_splits=num_splits).float().cpu().numpy()
     cu = np.concatenate([[0], np.cumsum(ctx)])
     qs, ks, vs = (x.cpu().numpy() for x in (data.q_scale, data.k_scale, data.v_scale))
-    mode = _oracle_mode(w.head_dim, bf16_layer, w.batch, w.num_q_heads, w.num_kv_heads, table.shape[1], window,
-                        num_splits)
+    if num_splits > 0:
+        mode = _oracle_mode(w.head_dim, bf16_layer, w.batch, w.num_q_heads, w.num_kv_heads, table.shape[1], window,
+                            num_splits)
+    else:  # the automatic plan, whose split size the caller derived
+        mode = dict(p_quant=True, split_blocks=auto_bps, block_n=DECODE_BLOCK_N)
     got, ref = [], []
     G = w.group
     for b in seqs:
@@ -196,46 +252,91 @@ def _decode_layer_check(w, layer, ctx, table, nb, seqs, heads, num_splits=0):
             res = attention.decode_attention_contiguous(
                 qb, kb, vb, sel(qs, slice(g * G, (g + 1) * G)), sel(ks, slice(g, g + 1)), sel(vs, slice(g, g + 1)),
                 fp8=not bf16_layer, window=window, heads=[h - g * G for h in hs], **mode)
+            if exact is not None and not bf16_layer:
+                pb = attention.decode_attention_contiguous(
+                    qb, kb, vb, sel(qs, slice(g * G, (g + 1) * G)), sel(ks, slice(g, g + 1)),
+                    sel(vs, slice(g, g + 1)), window=window, heads=[h - g * G for h in hs], p_bound=True)
+                exact.extend(pb[h - g * G] for h in hs)
             for h in hs:
                 got.append(out[b, h])
                 ref.append(res[h - g * G])
     return np.array(got), np.array(ref), data, out
 
 
-def test_workload1_full():
-    w = synth.WORKLOADS[1]
+def _exact_check(got, exact, what, record_property):
+    o = np.array([e[0] for e in exact])
+    bnd = np.array([e[1] for e in exact])
+    r, worst = assert_within_p_bound(got, o, bnd, what=what + " vs exact softmax")
+    record_property("rel_l2_vs_exact", r)
+    record_property("worst_err_over_bound", worst)
+
+
+def _workload(wid):
+    w = synth.WORKLOADS[wid]
     ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
     table, nb = synth.block_table(ctx, seed=w.seed)
-    got, ref, _, _ = _decode_layer_check(w, 0, ctx, table, nb, range(w.batch), range(w.num_q_heads))
+    return w, ctx, table, nb
+
+
+def test_workload_split_counts_give_the_152_sm_plan():
+    """The explicit split counts of the workload tests reproduce the automatic plan a
+    152-SM GB300 runs (the documented rule, restated in the helpers)."""
+    for wid, by_window in WORKLOAD_SPLITS.items():
+        w, ctx, table, nb = _workload(wid)
+        for window, ns in by_window.items():
+            assert (decode_split_blocks(table.shape[1], window, ns) ==
+                    auto_split_blocks(w.batch, w.num_kv_heads, table.shape[1], window, 152)), (wid, window)
+
+
+def test_workload1_full(record_property):
+    w, ctx, table, nb = _workload(1)
+    exact = []
+    got, ref, _, _ = _decode_layer_check(w, 0, ctx, table, nb, range(w.batch), range(w.num_q_heads), exact=exact)
     assert_close(got, ref, what="workload 1")
+    _exact_check(got, exact, "workload 1", record_property)
 
 
 @pytest.mark.parametrize("layer", [0, 31])
-def test_workload2_sampled(layer):
-    w = synth.WORKLOADS[2]
-    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
-    table, nb = synth.block_table(ctx, seed=w.seed)
-    got, ref, _, _ = _decode_layer_check(w, layer, ctx, table, nb, range(w.batch), [0, 5, 13, 22, 31])
+def test_workload2_sampled(layer, record_property):
+    w, ctx, table, nb = _workload(2)
+    exact = []
+    got, ref, _, _ = _decode_layer_check(w, layer, ctx, table, nb, range(w.batch), [0, 5, 13, 22, 31], exact=exact)
     assert_close(got, ref, what=f"workload 2 layer {layer}")
+    _exact_check(got, exact, f"workload 2 layer {layer}", record_property)
+
+
+def test_workload2_automatic_plan_on_152_sms():
+    """The benchmark's launch configuration itself (num_splits 0) on a 152-SM GB300: the
+    plan must be the hand-derived 208 blocks per split (7 splits), and the output must
+    match the oracle walking those splits."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the hand-derived plan is for a 152-SM GB300")
+    w, ctx, table, nb = _workload(2)
+    assert f.fp8_decode_attn_split_blocks(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, table.shape[1]) == 208
+    assert f.fp8_decode_attn_num_splits(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, table.shape[1]) == 7
+    got, ref, _, _ = _decode_layer_check(w, 5, ctx, table, nb, range(w.batch), [2, 17, 30], num_splits=0,
+                                         auto_bps=208)
+    assert_close(got, ref, what="workload 2 automatic plan")
 
 
 @pytest.mark.parametrize("layer", [0, 1])
-def test_workload3_sampled(layer):
-    w = synth.WORKLOADS[3]
-    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
-    table, nb = synth.block_table(ctx, seed=w.seed)
-    got, ref, _, _ = _decode_layer_check(w, layer, ctx, table, nb, range(w.batch), [0, 9, 33, 63])
+def test_workload3_sampled(layer, record_property):
+    w, ctx, table, nb = _workload(3)
+    exact = []
+    got, ref, _, _ = _decode_layer_check(w, layer, ctx, table, nb, range(w.batch), [0, 9, 33, 63], exact=exact)
     assert_close(got, ref, what=f"workload 3 layer {layer}")
+    if exact:
+        _exact_check(got, exact, f"workload 3 layer {layer}", record_property)
 
 
-def test_workload4_needle_decode():
+def test_workload4_needle_decode(record_property):
     """128k-key contraction: parity on every head, and each KV group's defining head
     returns the needle's (dequantised) value row."""
-    w = synth.WORKLOADS[4]
-    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
-    table, nb = synth.block_table(ctx, seed=w.seed)
-    got, ref, data, out = _decode_layer_check(w, 0, ctx, table, nb, [0], list(range(w.num_q_heads)))
+    w, ctx, table, nb = _workload(4)
+    exact = []
+    got, ref, data, out = _decode_layer_check(w, 0, ctx, table, nb, [0], list(range(w.num_q_heads)), exact=exact)
     assert_close(got, ref, what="workload 4 decode")
+    _exact_check(got, exact, "workload 4 decode", record_property)
     vs = float(data.v_scale.cpu()[0])
     for g in range(w.num_kv_heads):
         vrow = e4m3.decode(e4m3.quantize(synth.bf16_to_f64(data.v[data.needle_pos, g]), vs)) * vs

@@ -12,11 +12,18 @@ import pytest
 import torch
 
 import synth
-from helpers import assert_close, build_layer, to_dev
+from helpers import PREFILL_BLOCK_N, assert_close, build_layer, to_dev
 from oracle import attention
 
 f = pytest.importorskip("fp8_kv_cache_quant_gb300")
 pytestmark = pytest.mark.gpu
+
+
+def _block_n(D):
+    """The prefill's documented tile of 128 keys (fp8kv.h, fkv_prefill_block_n), checked
+    against the library rather than asked of it."""
+    assert f.fkv_prefill_block_n(D) == PREFILL_BLOCK_N
+    return PREFILL_BLOCK_N
 
 
 def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0, promote_every=1, bf16=False, window=0):
@@ -45,7 +52,7 @@ def _run(D, Hq, Hkv, T_list, Lq_list, gran, causal, seed, scale_k=2.0, promote_e
     kl = [synth.bf16_to_f64(k[cs[b]:cs[b + 1]]) for b in range(len(ctx))]
     vl = [synth.bf16_to_f64(v[cs[b]:cs[b + 1]]) for b in range(len(ctx))]
     ref = attention.prefill_attention(synth.bf16_to_f64(q), cu, kl, vl, qs.numpy(), ks.numpy(), vs.numpy(),
-                                      block_n=f.fkv_prefill_block_n(D), causal=causal, fp8=not bf16, window=window)
+                                      block_n=_block_n(D), causal=causal, fp8=not bf16, window=window)
     return out.float().cpu().numpy(), ref
 
 
@@ -175,7 +182,7 @@ def test_workload5_prefill_d256_sampled():
     q_full = np.full((int(cu[-1]), w.num_q_heads, w.head_dim), 0.0)
     q_full[rows] = qh
     ref = attention.prefill_attention(q_full, cu, kl, vl, data.q_scale.cpu().numpy(), data.k_scale.cpu().numpy(),
-                                      data.v_scale.cpu().numpy(), block_n=f.fkv_prefill_block_n(w.head_dim),
+                                      data.v_scale.cpu().numpy(), block_n=_block_n(w.head_dim),
                                       rows=rows)
     _check_promote_variants(outs, ref[rows], "workload 5 prefill")
 
@@ -193,7 +200,7 @@ def test_workload4_prefill_chunk_sampled():
     L = w.prefill_chunk
     cu = np.array([0, L], np.int32)
     rows = _sample_rows(cu, 10, np.random.default_rng(4))
-    heads = [0, 13, 40, 63]
+    heads = list(range(0, 64, 4)) + [13, 63]   # two or more query heads of every KV head
     full = {}
     for pe in (1, 4, 0):
         full[pe] = f.fp8_prefill_attn(qp, to_dev(cu), L, cache, to_dev(table), to_dev(ctx), data.q_scale,
@@ -210,7 +217,7 @@ def test_workload4_prefill_chunk_sampled():
         hs = [h for h in heads if h // G == g]
         q_full = np.zeros((L, len(hs), w.head_dim))
         q_full[rows] = synth.bf16_to_f64(qp[torch.as_tensor(rows, device="cuda")][:, hs])
-        r = attention.prefill_attention(q_full, cu, kb, vb, one, one, one, block_n=f.fkv_prefill_block_n(w.head_dim),
+        r = attention.prefill_attention(q_full, cu, kb, vb, one, one, one, block_n=_block_n(w.head_dim),
                                         rows=rows)
         for j, h in enumerate(hs):
             for pe in full:

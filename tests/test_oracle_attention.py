@@ -466,3 +466,52 @@ def test_e5m2_decode_matches_loops_and_sdpa():
                 torch.tensor(q[b, h], dtype=torch.float64)[None, None], torch.tensor(Kd, dtype=torch.float64)[None],
                 torch.tensor(Vd, dtype=torch.float64)[None], scale=tau)[0, 0]
             np.testing.assert_allclose(got[b, h], sd.numpy(), rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- P-rounding error bound
+
+def test_p_rounding_bound_exact_part_is_sdpa():
+    rng = np.random.default_rng(40)
+    D, T = 16, 90
+    qv, K, V = _dequant(rng.standard_normal((T, D)) * 2, rng.standard_normal((T, D)), rng.standard_normal(D),
+                        np.float32(0.5), np.float32(0.75), np.float32(0.25))
+    tau = 1 / math.sqrt(D)
+    o, B = attention.p_rounding_bound(qv, K, V, tau)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(qv)[None, None], torch.from_numpy(K)[None], torch.from_numpy(V)[None], scale=tau)[0, 0]
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-13)
+    assert np.all(B > 0)
+
+
+@pytest.mark.parametrize("spread", [0.5, 3.0, 12.0])
+@pytest.mark.parametrize("T,window,split_blocks,block_n", [
+    (150, 0, 4, 32), (300, 70, 2, 16), (257, 0, 16, 128), (700, 0, 8, 128), (1000, 333, 1, 16)])
+def test_split_decode_fp8p_within_the_p_rounding_bound(spread, T, window, split_blocks, block_n):
+    """Every split and tile plan of the FP8-P decode stays within the bound: the score
+    spreads reach p far below e4m3's normal range (subnormal codes and codes rounded to 0)."""
+    rng = np.random.default_rng(int(spread * 10) + T + window + split_blocks)
+    D = 8
+    lo = max(0, T - window) if window else 0
+    qv, K, V = _dequant(rng.standard_normal((T, D)) * spread, rng.standard_normal((T, D)),
+                        rng.standard_normal(D) * 2, np.float32(0.5), np.float32(1.0), np.float32(0.25))
+    tau = 1 / math.sqrt(D)
+    got = attention.split_decode(qv, K[lo:], V[lo:], T, lo, tau, split_blocks=split_blocks, block_n=block_n,
+                                 p_quant=True, block_size=16)
+    o, B = attention.p_rounding_bound(qv, K[lo:], V[lo:], tau)
+    assert np.all(np.abs(got - o) <= B * (1 + 1e-9))
+
+
+def test_p_rounding_bound_is_reached_by_its_two_terms():
+    """Two-key cases at the edges of the bound.  (a) p * 448 next to 4.25, a tie of e4m3
+    between 4.0 and 4.5: the rounding error is 1/17 of p, 16/17 of the bound's 2^-4 p.
+    (b) p * 448 just below 2^-10, half the smallest subnormal: the code is 0 and the
+    error is the whole p, just below the bound's 2^-10 / 448."""
+    tau = 1.0
+    for p_target, lo_ratio in ((4.25 / 448.0, 0.93), (0.99 * 2.0 ** -10 / 448.0, 0.98)):
+        K = np.array([[0.0], [math.log(p_target)]])
+        qv = np.array([1.0])
+        V = np.array([[0.0, 0.0], [1.0, 1.0]])
+        got = attention.split_decode(qv, K, V, 2, 0, tau, split_blocks=1, block_n=16, p_quant=True, block_size=16)
+        o, B = attention.p_rounding_bound(qv, K, V, tau)
+        ratio = np.abs(got - o) / B
+        assert np.all(ratio <= 1.0) and np.all(ratio >= lo_ratio), ratio
