@@ -4,8 +4,8 @@
 One step = one decode step of every layer of the workload: for each layer the new
 token's K/V are written into the paged cache (e4m3 with per-KV-head scales) and the
 decode attention reads the whole cached context (split-K + FP32 merge), both in one
-launch (fp8_decode_step) on e4m3 layers, as kv_quant_cache then fp8_decode_attn on bf16
-layers.
+launch (fp8_decode_step) — on bf16 layers too, so that the FP8 and BF16 steps have the
+same launch structure.
 Inputs are seeded synthetic tensors shaped like the pages' Llama-3.1-8B decode under
 load (32 layers, 32/8 heads, head_dim 128, batch 8, contexts U[16384, 24576]); the
 cache (10.5 GB per step) is far larger than L2, so no flush is needed between steps.
@@ -181,8 +181,8 @@ class DecodeState:
         else:
             self.mask = w.skip_mask()
         self.bf16 = [bool(x) for x in self.mask]
-        # e4m3 layers write the current token and decode in one launch (fp8_decode_step)
-        self.fusable = [not b and f.fkv_decode_block_n(w.head_dim) > 0 for b in self.bf16]
+        # every layer writes the current token and decodes in one launch (fp8_decode_step)
+        self.fusable = [True for _ in self.bf16]
         self.gran = f.SCALE_PER_HEAD if w.scale_mode == "amax" else f.SCALE_PER_TENSOR
         self.table_d = torch.from_numpy(self.table).to(device)
         self.ctx_d = torch.from_numpy(self.ctx).to(device)
@@ -292,6 +292,75 @@ def _step_distribution(g, stream, steps):
     t = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)])
     p10, p50, p90 = np.percentile(t, [10, 50, 90])
     return {"steps": steps, "p10_ms": float(p10), "p50_ms": float(p50), "p90_ms": float(p90)}
+
+
+def _time_replays(g, stream, n, flush=None):
+    """Each of n replays of a graph timed alone by an event pair on the launching stream;
+    ``flush`` (a buffer larger than the 129 MB L2) is overwritten before every replay,
+    outside the pair, so that no replay finds the previous one's data in L2.  Returns
+    the per-replay times in ms."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            if flush is not None:
+                flush.zero_()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def _pcts(ts):
+    import numpy as np
+    p10, p50, p90 = np.percentile(np.asarray(ts), [10, 50, 90])
+    return {"p10": float(p10) * 1e3, "p50": float(p50) * 1e3, "p90": float(p90) * 1e3}
+
+
+def _layer_kernels(f, st):
+    """Which decode kernel each layer of a DecodeState runs, counted."""
+    w = st.w
+    names = {}
+    for l, bf in enumerate(st.bf16):
+        if not bf and f.fkv_decode_block_n(w.head_dim) > 0:
+            k = f"decode_tc_kernel<{w.head_dim},{w.group}> (current-token write fused)"
+        else:
+            k = f"decode_split_kernel<{w.head_dim},{'bf16' if bf else 'e5m2'},{w.group}> (current-token write fused)"
+        names[k] = names.get(k, 0) + 1
+    return {k: f"{v} of {w.num_layers} layers" for k, v in names.items()}
+
+
+def per_config(f, device, replays, peak, workloads=(1, 3, 4)):
+    """The other decode workloads, each as one step of all its layers (current-token cache
+    write + decode per layer, as the headline step), with an e4m3 cache and with the same
+    kernels on a bf16 cache: per-replay times with an L2 flush before each replay (the
+    single-layer 4096-key workload reads 8.4 MB, which L2 would otherwise hold), the
+    algorithmic bytes of the step, GB/s and the fraction of the measured HBM peak."""
+    import torch
+    import synth
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    out = {}
+    for wid in workloads:
+        w = synth.WORKLOADS[wid]
+        entry = {"workload": w.name}
+        for variant, kw in (("fp8", {}), ("bf16", {"all_bf16": True})):
+            st = DecodeState(f, w, device, **kw)
+            g = _graph(st.step, stream)
+            _time_replays(g, stream, 3, flush)
+            ts = _time_replays(g, stream, replays, flush)
+            us = _pcts(ts)
+            nbytes = st.step_bytes()
+            gbs = nbytes / (us["p50"] * 1e-6) / 1e9
+            entry[variant] = {"us_per_step": us, "replays": replays, "algorithmic_bytes": nbytes, "GBps": gbs,
+                              "frac": gbs / peak, "kernels": _layer_kernels(f, st),
+                              "launches_per_step": st.launches_per_step()}
+            del g, st
+            torch.cuda.empty_cache()
+        entry["fp8_over_bf16_step_time"] = entry["fp8"]["us_per_step"]["p50"] / entry["bf16"]["us_per_step"]["p50"]
+        out[str(wid)] = entry
+    return out
 
 
 def _fp8_dense_peak():
@@ -404,7 +473,11 @@ def dist_max(dist, world, x, device):
 SWEEP_T = (256, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 125000)
 
 
-def itl_sweep(f, device, steps, warmup, lengths=SWEEP_T):
+ITL_SHORT_T = (1024, 4096, 16384, 65536, 125000)
+TTFT_SHORT_L = (2048, 8192, 16384, 32768, 65536, 125000)
+
+
+def itl_sweep(f, device, steps, warmup, lengths=SWEEP_T, shapes=("llama8b", "gptoss20b-hybrid")):
     """The ITL-slope proxy: per-step decode time of all layers at batch 1 versus the cached
     context T, for an e4m3 cache and for a bf16 cache, with least-squares lines (the blog's
     ITL = slope * input_len + intercept) and the break-even context.  Shapes: the
@@ -415,22 +488,25 @@ def itl_sweep(f, device, steps, warmup, lengths=SWEEP_T):
     import torch
     import synth
     out = {}
-    shapes = {"llama8b": (synth.WORKLOADS[2], [("fp8", {}), ("bf16", {"all_bf16": True})]),
-              "gptoss20b-hybrid": (synth.WORKLOADS[3], [("fp8-skip-sw", {}), ("fp8", {"no_skip": True}),
-                                                        ("bf16", {"all_bf16": True})])}
+    all_shapes = {"llama8b": (synth.WORKLOADS[2], [("fp8", {}), ("bf16", {"all_bf16": True})]),
+                  "gptoss20b-hybrid": (synth.WORKLOADS[3], [("fp8-skip-sw", {}), ("fp8", {"no_skip": True}),
+                                                            ("bf16", {"all_bf16": True})])}
     stream = torch.cuda.Stream(device)
-    for name, (base, variants) in shapes.items():
+    # short contexts fit in L2 (32 layers x 1024 keys of e4m3 = 67 MB): flush before each replay
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    for name in shapes:
+        base, variants = all_shapes[name]
         res = {v: [] for v, _ in variants}
         for T in lengths:
             w = dataclasses.replace(base, batch=1, ctx_lo=T, ctx_hi=T, name=f"{base.name}-b1-t{T}")
             for v, kw in variants:
                 st = DecodeState(f, w, device, **kw)
                 g = _graph(st.step, stream)
-                ms = _time_graph(g, stream, steps, warmup, lambda: None)
-                res[v].append(ms * 1e3)
+                _time_replays(g, stream, warmup, flush)
+                res[v].append(_pcts(_time_replays(g, stream, steps, flush))["p50"])
                 del g, st
                 torch.cuda.empty_cache()
-        entry = {"T": list(lengths), "us_per_step": res}
+        entry = {"T": list(lengths), "us_per_step": res, "timing": "median of per-replay times, L2 flushed"}
         fits = {v: linear_fit(list(lengths), ys) for v, ys in res.items()}
         entry["slope_us_per_1k_tokens"] = {v: fi[0] * 1e3 for v, fi in fits.items()}
         entry["intercept_us"] = {v: fi[1] for v, fi in fits.items()}
@@ -452,7 +528,7 @@ def quadratic_fit(xs, ys):
     return float(a) / 1e6, float(b) / 1e3, float(c)
 
 
-def ttft_sweep(f, device, steps, warmup, lengths=SWEEP_T):
+def ttft_sweep(f, device, steps, warmup, lengths=SWEEP_T, shape_names=("llama8b", "hd256")):
     """The TTFT proxy: one layer's prefill of a single prompt of L tokens (cache write of
     its K/V + causal attention over it) versus L, fitted with TTFT = a L^2 + b L + c, for
     an e4m3 cache (two-level accumulation, and without promotion) and a bf16 cache.
@@ -469,6 +545,7 @@ def ttft_sweep(f, device, steps, warmup, lengths=SWEEP_T):
         "llama8b": synth.PrefillWorkload("llama8b-prefill-h32x8-d128", 1, Lmax, 32, 8, 128, seed=1),
         "hd256": dataclasses.replace(synth.WORKLOADS[5], batch=1, seq_len=Lmax, name="prefill-h8x1-d256"),
     }
+    shapes = {k: v for k, v in shapes.items() if k in shape_names}
     variants = [("fp8", 1, False), ("fp8-no-promote", 0, False), ("bf16", 1, True)]
     stream = torch.cuda.Stream(device)
     out = {}
@@ -517,28 +594,48 @@ def ttft_sweep(f, device, steps, warmup, lengths=SWEEP_T):
 
 def oracle_sample(workload_id: int, keys: int, heads: int):
     """Time the oracle on one sequence of layer 0: its cache write (quantise K/V) and its
-    decode attention for ``heads`` query heads over ``keys`` cached keys.  Returns
-    (seconds, algorithmic bytes of that sample)."""
+    decode attention for ``heads`` query heads (heads / G KV heads) over ``keys`` cached
+    keys, with the workload's scale recipe (1.0, or amax/448 per head).  Returns
+    (seconds, algorithmic bytes of that sample: the e4m3 K/V it reads)."""
     import numpy as np
     import synth
-    from oracle import attention, e4m3
+    from oracle import attention
     w = synth.WORKLOADS[workload_id]
     G = w.group
     nkv = max(1, heads // G)
-    q = synth.bf16_to_f64(synth.randn_bf16((heads, w.head_dim), w.seed, 0, "q"))
-    k = synth.bf16_to_f64(synth.randn_bf16((keys, nkv, w.head_dim), w.seed, 0, "k"))
-    v = synth.bf16_to_f64(synth.randn_bf16((keys, nkv, w.head_dim), w.seed, 0, "v"))
-    s = np.ones(1, np.float32) * np.float32(0.01)
+    q = synth.randn_bf16((heads, w.head_dim), w.seed, 0, "q")
+    k = synth.randn_bf16((keys, nkv, w.head_dim), w.seed, 0, "k")
+    v = synth.randn_bf16((keys, nkv, w.head_dim), w.seed, 0, "v")
+    if w.scale_mode == "amax":
+        qs, ks, vs = (synth.amax_scales(x, 1).numpy() for x in (q, k, v))
+    else:
+        qs = ks = vs = np.ones(1, np.float32)
+    qf, kf, vf = synth.bf16_to_f64(q), synth.bf16_to_f64(k), synth.bf16_to_f64(v)
     t0 = time.perf_counter()
-    attention.decode_attention_contiguous(q, k, v, s, s, s, fp8=True)
+    attention.decode_attention_contiguous(qf, kf, vf, qs, ks, vs, fp8=True)
     dt = time.perf_counter() - t0
     return dt, 2 * nkv * w.head_dim * keys
 
 
-def _cpu_baseline_subprocess(workload_id: int, keys: int, heads: int):
+def oracle_sample_shape(workload_id: int):
+    """The bounded sample both CPU legs time, one per step: layer 0, sequence 0 of the
+    workload (its whole context), KV head 0 and its G query heads.  Returns (keys, heads,
+    description)."""
+    import synth
+    w = synth.WORKLOADS[workload_id]
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    keys = int(ctx[0])
+    return keys, w.group, (f"layer 0, sequence 0 of {w.batch}: {keys} cached keys of KV head 0 x its {w.group} "
+                           f"query heads: e4m3 cache quantisation + decode attention in float64 NumPy")
+
+
+def _cpu_baseline_subprocess(workload_id: int, repeats: int):
+    """The oracle sample timed ``repeats`` times in a fresh single-threaded process (no
+    CUDA context).  Returns (seconds, bytes) summed over the repeats, or None."""
+    keys, heads, _ = oracle_sample_shape(workload_id)
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
-    code = (f"import bench, json; dt, b = bench.oracle_sample({workload_id}, {keys}, {heads}); "
-            f"print(json.dumps({{'s': dt, 'bytes': b}}))")
+    code = (f"import bench, json; r = [bench.oracle_sample({workload_id}, {keys}, {heads}) for _ in range({repeats})]; "
+            f"print(json.dumps({{'s': sum(x[0] for x in r), 'bytes': sum(x[1] for x in r)}}))")
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         return None
@@ -546,35 +643,54 @@ def _cpu_baseline_subprocess(workload_id: int, keys: int, heads: int):
     return d["s"], d["bytes"]
 
 
+def _host_cores():
+    return {"host_cpu_count": os.cpu_count(), "blas_threads": 1,
+            "threads_note": "the oracle runs single-threaded (OPENBLAS/OMP/MKL_NUM_THREADS=1)"}
+
+
+def workload_config(w, ctx, world, step_bytes=None):
+    """The ``config`` object of both arms' JSON lines for a decode workload."""
+    cfg = {"workload": w.name, "layers": w.num_layers, "batch": w.batch, "q_heads": w.num_q_heads,
+           "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "context": [int(x) for x in ctx], "block_size": 16,
+           "kv_cache_dtype": "e4m3", "scales": "per-KV-head amax/448" if w.scale_mode == "amax" else "per-tensor 1.0",
+           "l2": "no flush: each step reads {:.2f} GB (> 129 MB L2)".format(
+               (step_bytes if step_bytes is not None else _step_bytes_host(w, ctx)) / 1e9),
+           "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"}
+    return cfg
+
+
+def _step_bytes_host(w, ctx):
+    bf = [bool(x) for x in w.skip_mask()]
+    return sum(x["decode"] + x["write"] for x in decode_bytes(w, ctx, bf))
+
+
 # ----------------------------------------------------------------------------- arms
 
 def run_reference(args):
-    """The reference arm: the CPU oracle as it stands, one bounded sample per step."""
+    """The reference arm: the CPU oracle as it stands, one bounded sample per step (the
+    same sample as the benchmark line's cpu_baseline)."""
     import synth
     rank, world, _ = _env_rank()
     if rank != 0:
         return 0
     w = synth.WORKLOADS[args.workload]
-    heads = w.group
-    budget = 90.0 / max(1, args.steps + args.warmup)
-    probe_keys = 2048
-    dt, _ = oracle_sample(args.workload, probe_keys, heads)
-    keys = int(max(512, min(w.ctx_hi, budget / max(dt, 1e-6) * probe_keys)))
+    keys, heads, sample = oracle_sample_shape(args.workload)
     for _ in range(args.warmup):
         oracle_sample(args.workload, keys, heads)
     tot_s, tot_b = 0.0, 0
     for _ in range(args.steps):
-        s, b = oracle_sample(args.workload, keys, heads)
-        tot_s += s
+        s_, b = oracle_sample(args.workload, keys, heads)
+        tot_s += s_
         tot_b += b
     value = tot_b / tot_s / 1e9
-    sample = f"1 sequence x {keys} keys x {heads} query heads (one KV head) of layer 0, per step"
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "config": workload_config(w, ctx, args.gpus),
+        "cpu_baseline": dict({"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                              "sample": sample + " (one sample per step)"}, **_host_cores()),
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -665,20 +781,30 @@ def run_ours(args):
     # the same step with a bf16 cache (all layers), for the FP8-vs-BF16 per-token cost
     bf16_info = None
     if not args.no_bf16:
-        del g_fp8, g_dec, g_e2e, g_sep
         bf = DecodeState(f, w, device, all_bf16=True)
         g_bf = _graph(bf.step, stream)
         ms_bf = max_over_ranks(_time_graph(g_bf, stream, args.steps, args.warmup, barrier))
         bf_bytes = bf.step_bytes()
         kv_fp8 = sum(x["kv"] for x in fp8.bytes)
         kv_bf = sum(x["kv"] for x in bf.bytes)
+        g_bf_sep = _graph(lambda: bf.step(fused=False), stream)
+        ms_bf_sep = max_over_ranks(_time_graph(g_bf_sep, stream, args.steps, args.warmup, barrier))
         bf16_info = {"ms_per_step": ms_bf, "GBps": bf_bytes / (ms_bf * 1e-3) / 1e9,
-                     # both steps with the cache write as its own launch; then the fused fp8 step
-                     "fp8_over_bf16_step_time": ms_sep / ms_bf,
-                     "fp8_fused_over_bf16_step_time": ms_fp8 / ms_bf,
-                     "fp8_unfused_ms_per_step": ms_sep,
+                     # both steps fused (one launch per layer: cache write + decode)
+                     "fp8_over_bf16_step_time": ms_fp8 / ms_bf,
+                     # both steps with the cache write as its own launch
+                     "fp8_over_bf16_step_time_unfused": ms_sep / ms_bf_sep,
+                     "fp8_unfused_ms_per_step": ms_sep, "bf16_unfused_ms_per_step": ms_bf_sep,
                      "kv_bytes_fp8": kv_fp8, "kv_bytes_bf16": kv_bf}
+        del g_bf_sep
 
+    fp8_ctx, fp8_launches = fp8.ctx, fp8.launches_per_step()
+    del fp8, g_fp8, g_dec, g_e2e, g_sep
+    if not args.no_bf16:
+        del bf, g_bf
+    torch.cuda.empty_cache()
+    clocks_x = ClockSampler(local)   # clocks of the remaining measurements
+    clocks_x.start()
     prefill = None
     if not args.no_prefill:
         torch.cuda.synchronize()
@@ -686,28 +812,36 @@ def run_ours(args):
                    time_prefill(f, 4, device, iters=min(args.steps, 10), warmup=3, promote_every=(1, 4, 0)))
         torch.cuda.synchronize()
 
+    # the other decode workloads, the ITL-slope proxy and the TTFT fit (short forms of
+    # --sweep / --ttft), each on this GPU in the same run
+    others = None
+    if not args.no_per_config:
+        others = per_config(f, device, replays=max(20, min(args.steps, 100)), peak=peak)
+    itl = None
+    if not args.no_itl:
+        itl = itl_sweep(f, device, steps=max(10, min(args.steps, 30)), warmup=3, lengths=ITL_SHORT_T,
+                        shapes=("llama8b",))
+    ttft = None
+    if not args.no_ttft:
+        ttft = ttft_sweep(f, device, steps=3, warmup=2, lengths=TTFT_SHORT_L)
+    clocks_x.stop()
+
     cpu = None
     if rank == 0 and not args.no_cpu:
-        keys = int(sum(int(t) for t in fp8.ctx))
-        r = _cpu_baseline_subprocess(args.workload, keys, w.num_q_heads)
+        repeats = 20
+        r = _cpu_baseline_subprocess(args.workload, repeats)
         if r is not None:
             s, b = r
-            cpu = {"value": b / s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                   "sample": f"layer 0 of {w.num_layers}, {keys} cached keys (the batch's total context) x all "
-                             f"{w.num_q_heads} query heads: cache quantisation + decode attention, {s:.1f} s "
-                             f"single-threaded NumPy"}
+            _, _, sample = oracle_sample_shape(args.workload)
+            cpu = dict({"value": b / s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                        "sample": f"{sample}, timed {repeats} times ({s:.1f} s)"}, **_host_cores())
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_fp8, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "layers": w.num_layers, "batch": w.batch, "q_heads": w.num_q_heads,
-                       "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                       "context": [int(x) for x in fp8.ctx], "block_size": 16, "kv_cache_dtype": "e4m3",
-                       "scales": "per-KV-head amax/448" if w.scale_mode == "amax" else "per-tensor 1.0",
-                       "l2": f"no flush: each step reads {step_bytes / 1e9:.2f} GB (> 129 MB L2)",
-                       "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
+            "config": workload_config(w, fp8_ctx, world),
             "us_per_step": ms_fp8 * 1e3,
             "step_ms_spread": spread,
             "pct_of_hbm_peak": value / peak,
@@ -717,10 +851,14 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": dec_bytes, "launch_ms": dec_launch_ms},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": ms_e2e},
-            "gpu_launches": fp8.launches_per_step() * args.steps,
+            "gpu_launches": fp8_launches * args.steps,
             "clocks": clocks.summary(),
+            "clocks_other_measurements": clocks_x.summary(),
             "bf16": bf16_info,
             "prefill": prefill,
+            "per_config": others,
+            "itl_slope": itl,
+            "ttft_fit": ttft,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -739,6 +877,9 @@ def main():
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the other decode workloads")
+    ap.add_argument("--no-itl", action="store_true", help="skip the short ITL-slope sweep")
+    ap.add_argument("--no-ttft", action="store_true", help="skip the short TTFT fit")
     ap.add_argument("--sweep", action="store_true", help="ITL-slope sweep instead of the benchmark line")
     ap.add_argument("--ttft", action="store_true", help="TTFT quadratic-fit sweep instead of the benchmark line")
     args = ap.parse_args()

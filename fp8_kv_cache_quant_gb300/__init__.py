@@ -32,7 +32,7 @@ EXPORTS = (
     "fkv_status_string", "fkv_version", "kv_quant_cache", "fp8_decode_attn_workspace_size",
     "fp8_decode_attn_num_splits", "fp8_decode_attn", "fkv_prefill_block_n", "fp8_prefill_attn",
     "fp8_decode_attn_noalloc", "fp8_decode_attn_split_blocks", "fkv_decode_block_n", "kv_quant_cache_clips",
-    "fp8_decode_step",
+    "fp8_decode_step", "fkv_set_decode_wait_limit_ns",
 )
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
@@ -65,6 +65,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.fkv_status_string.restype = ctypes.c_char_p
     lib.fkv_status_string.argtypes = [ctypes.c_int]
     lib.fkv_version.restype = c_i32
+    lib.fkv_set_decode_wait_limit_ns.restype = None
+    lib.fkv_set_decode_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.kv_quant_cache.restype = ctypes.c_int
     lib.kv_quant_cache.argtypes = [c_vp, c_vp, c_vp, c_i32, _LayerCache, c_vp, c_vp, ctypes.c_int, c_i32, c_vp,
                                    c_i32, c_vp, c_vp]

@@ -1,5 +1,6 @@
 // The C ABI of libfp8kv.so: argument validation, launch planning and dispatch.
 // Nothing here allocates memory or keeps state between calls.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -97,6 +98,11 @@ bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_bloc
 
 fkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FKV_OK : FKV_CUDA_ERROR; }
 
+// Bound of the tensor-core decode's pipeline waits set by fkv_set_decode_wait_limit_ns;
+// 0 = the default (kPipeWaitNs).
+std::atomic<unsigned long long> g_decode_wait_ns{0};
+constexpr unsigned long long kDefaultPipeWaitNs = 200000000ull;  // 200 ms, as kPipeWaitNs in tc.cuh
+
 fkv_status cache_write(const void* k, const void* v, const int64_t* slot_mapping, int32_t n_tokens,
                        fkv_layer_cache cache, const float* k_scale, const float* v_scale, fkv_scale_gran gran,
                        int32_t layer, const uint8_t* skip_layer_mask, int32_t num_layers, int32_t* fault,
@@ -152,8 +158,6 @@ fkv_status decode_entry(const void* k_new, const void* v_new, const void* q, int
   const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
   if (st != FKV_OK) return st;
   const int elt = layer_elt(bf16, cache);
-  // the fused write exists for e4m3 pools (the tensor-core decode)
-  if (step && !fkv::decode_uses_tensor_cores(cache.head_dim, elt)) return FKV_UNSUPPORTED;
   if (batch == 0) return FKV_OK;
   if (step && (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16))) return FKV_INVALID_ARG;
   if (!q || !out || !block_table || !context_lens || !cache.k_cache || !cache.v_cache || (!workspace && !scratch))
@@ -200,6 +204,8 @@ fkv_status decode_entry(const void* k_new, const void* v_new, const void* q, int
   p.fault = fault;
   p.k_new = static_cast<const __nv_bfloat16*>(k_new);
   p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  const unsigned long long wait_ns = g_decode_wait_ns.load(std::memory_order_relaxed);
+  p.pipe_wait_ns = wait_ns != 0 ? wait_ns : kDefaultPipeWaitNs;
   // split-completion counters start at zero on every call
   if (cudaMemsetAsync(p.done, 0, static_cast<size_t>(batch) * cache.num_kv_heads * sizeof(int32_t),
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -225,7 +231,9 @@ const char* fkv_status_string(fkv_status status) {
   return "unknown status";
 }
 
-int32_t fkv_version(void) { return 102; }
+int32_t fkv_version(void) { return 103; }
+
+void fkv_set_decode_wait_limit_ns(unsigned long long ns) { g_decode_wait_ns.store(ns, std::memory_order_relaxed); }
 
 
 fkv_status kv_quant_cache(const void* k, const void* v, const int64_t* slot_mapping, int32_t n_tokens,

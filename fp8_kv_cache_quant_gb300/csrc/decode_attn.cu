@@ -96,6 +96,44 @@ FKV_DEV void to_f2(const uint32_t* w, float2* out) {
   }
 }
 
+// fp8_decode_step on a bf16 (skip) or e5m2 layer: the current token's K and V rows of KV
+// head g written into the pools at position T - 1 exactly as kv_quant_cache writes them
+// (bf16: a copy; e5m2: e5m2(fl32(x * fl32(1 / s))), round to nearest even, saturating).
+// Threads j < 2 D / 8 of the CTA take 8 elements of K (j < D / 8) or V each; each writer
+// fences its stores against the async proxy, and the CTA barrier that follows orders
+// them before the bulk copies that read the block back.
+template <int D, int ELT>
+__device__ void write_current_token_cc(const DecodeParams& p, int b, int g, int T) {
+  const int pos = T - 1;
+  const int id = p.block_table[static_cast<size_t>(b) * p.max_blocks + (pos >> 4)];
+  if (id < 0 || id >= p.num_blocks) return;  // reported by the block-id checks of the split
+  constexpr int CH = D / 8;
+  const int j = threadIdx.x;
+  if (j >= 2 * CH) return;
+  const bool is_v = j >= CH;
+  const int c = is_v ? j - CH : j;
+  const size_t elem = ((static_cast<size_t>(id) * p.Hkv + g) * 16 + (pos & 15)) * D + 8 * c;
+  const uint4 x = reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + (static_cast<size_t>(b) * p.Hkv + g) * D)[c];
+  // the pools are the caller's writable device memory; the params carry them as const
+  // because the plain decode only reads them
+  uint8_t* pool = const_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache);
+  if constexpr (ELT == 2) {
+    *reinterpret_cast<uint4*>(pool + 2 * elem) = x;
+  } else {
+    const float inv = __frcp_rn((is_v ? p.v_scale : p.k_scale)[p.per_head ? g : 0]);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 f0 = bf16x2_to_f2(w[2 * k]), f1 = bf16x2_to_f2(w[2 * k + 1]);
+      o[k] = static_cast<uint32_t>(f32x2_to_e5m2x2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv))) |
+             (static_cast<uint32_t>(f32x2_to_e5m2x2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv))) << 16);
+    }
+    *reinterpret_cast<uint2*>(pool + elem) = make_uint2(o[0], o[1]);
+  }
+  fence_proxy_async_global();
+}
+
 template <int D, int ELT, int G>
 __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
     decode_split_kernel(const DecodeParams p) {
@@ -137,6 +175,9 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
       ids_s[i] = id;
     }
   }
+  // fp8_decode_step: the split holding position T - 1 (the last) writes the current token
+  // into the pools before any copy of that block is issued (not when the context was clamped)
+  if (p.k_new != nullptr && sigma == r.nsplit - 1 && !r.clamped) write_current_token_cc<D, ELT>(p, b, g, r.T);
   __syncthreads();
 
   // ---------------------------------------------------------------- per-warp pipeline

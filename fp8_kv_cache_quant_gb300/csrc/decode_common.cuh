@@ -39,26 +39,39 @@ FKV_DEV SeqRange seq_range(const DecodeParams& p, int b, bool report) {
 // and o_s its normalised output, o = v_s * sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
 // M = max_s lse_s, written as bf16.  Every thread of the CTA calls it (it synchronises);
 // `scratch` holds at least 2 * G + G * CH floats of shared memory.
+// The partials come from L2; a load whose value the next instruction needs holds the
+// warp for the whole round trip, so the log-sum-exps are read by a warp per head with
+// the lanes striding over the splits, and each output pair's split partials are loaded
+// eight at a time before they are summed (in split order).
 template <int D, int G, int NT, int CH>
 FKV_DEV void merge_splits(const DecodeParams& p, int b, int g, int ns, float vs, float* scratch) {
   float* ms_s = scratch;       // [G] max of lse
   float* inv_s = ms_s + G;     // [G] v_s / sum of weights
   float* w_s = inv_s + G;      // [G][CH] weights of a chunk of splits
+  constexpr int NWARP = NT / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t row_base = (static_cast<size_t>(b) * p.Hq + g * G) * p.max_splits;
-  for (int t = threadIdx.x; t < G; t += NT) {
-    const size_t row0 = row_base + static_cast<size_t>(t) * p.max_splits;
+  for (int h = warp; h < G; h += NWARP) {
+    const float* lse = p.lse_part + row_base + static_cast<size_t>(h) * p.max_splits;
     float M = -INFINITY;
-    for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(p.lse_part + row0 + s2));
+    for (int s2 = lane; s2 < ns; s2 += 32) M = fmaxf(M, __ldcg(lse + s2));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float W = 0.f;
     if (M != -INFINITY)
-      for (int s2 = 0; s2 < ns; ++s2) {
-        const float lv = __ldcg(p.lse_part + row0 + s2);
+      for (int s2 = lane; s2 < ns; s2 += 32) {
+        const float lv = __ldcg(lse + s2);
         W += (lv == -INFINITY) ? 0.f : ex2(lv - M);
       }
-    ms_s[t] = M;
-    inv_s[t] = (W > 0.f) ? vs / W : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    if (lane == 0) {
+      ms_s[h] = M;
+      inv_s[h] = (W > 0.f) ? vs / W : 0.f;
+    }
   }
   constexpr int PAIRS = (G * D / 2 + NT - 1) / NT;  // output pairs per thread
+  constexpr int U = 8;                               // split partials loaded before use
   float2 o[PAIRS];
 #pragma unroll
   for (int k2 = 0; k2 < PAIRS; ++k2) o[k2] = make_float2(0.f, 0.f);
@@ -77,9 +90,22 @@ FKV_DEV void merge_splits(const DecodeParams& p, int b, int g, int ns, float vs,
       if (t < G * D / 2) {
         const int h = t / (D / 2), d = 2 * (t % (D / 2));
         const float* src = p.o_part + (row_base + static_cast<size_t>(h) * p.max_splits + c0) * D + d;
-        for (int j = 0; j < nc; ++j) {
+        const float* wh = w_s + h * CH;
+        int j = 0;
+        for (; j + U <= nc; j += U) {
+          float2 x[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) x[u] = __ldcg(reinterpret_cast<const float2*>(src + static_cast<size_t>(j + u) * D));
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const float wv = wh[j + u];
+            o[k2].x += wv * x[u].x;
+            o[k2].y += wv * x[u].y;
+          }
+        }
+        for (; j < nc; ++j) {
           const float2 x = __ldcg(reinterpret_cast<const float2*>(src + static_cast<size_t>(j) * D));
-          const float wv = w_s[h * CH + j];
+          const float wv = wh[j];
           o[k2].x += wv * x.x;
           o[k2].y += wv * x.y;
         }

@@ -33,8 +33,9 @@
 //              of a V tile's copies (8 lanes), an S^T product (one tile ahead) and a P.V
 //              product, committing to mbarriers.
 // The split writes (o / l, log2-sum-exp) per head; the CTA that finishes the last split
-// of (b, g) merges all of them in FP32.  Every wait is bounded in time; a timeout records
-// FKV_FAULT_TIMEOUT, lets the CTA's copies and MMAs drain and returns.
+// of (b, g) merges all of them in FP32.  Every wait is bounded in time (the pipeline's by
+// p.pipe_wait_ns); a timeout records FKV_FAULT_TIMEOUT, lets the CTA's copies and MMAs
+// drain (those waits keep the fixed bound kPipeWaitNs) and returns.
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "kernels.h"
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     for (int t = 0; t < n_t; ++t) {
       if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
       const int sb = t & 1;
-      if (!wait_warp(&s_full[sb], (t >> 1) & 1)) { ok = false; break; }
+      if (!wait_warp(&s_full[sb], (t >> 1) & 1, p.pipe_wait_ns)) { ok = false; break; }
       tc_fence_after();
       float s16[16];
       tmem_ld16(lane_base + C::TM_S + sb * C::NP, s16);
@@ -336,12 +337,12 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         for (int h = 0; h < G; ++h) red[warp * C::NP + h] = wm[h];
         mbar_arrive(&red_full[t & 1]);
       }
-      if (!wait_warp(&red_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+      if (!wait_warp(&red_full[t & 1], (t >> 1) & 1, p.pipe_wait_ns)) { ok = false; break; }
       const int pb = t & 1;
       // P8^T tile t % 2 is free once the P.V of tile t-2 completed; alpha slot t % 2 once
       // the correction warpgroup read tile t-2's alpha
-      if (t >= 2 && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
-      if (t >= 2 && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+      if (t >= 2 && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1, p.pipe_wait_ns)) { ok = false; break; }
+      if (t >= 2 && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1, p.pipe_wait_ns)) { ok = false; break; }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float tmax = fmaxf(fmaxf(red[h], red[C::NP + h]), fmaxf(red[2 * C::NP + h], red[3 * C::NP + h]));
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       for (int h = 0; h < G; ++h) red[warp * C::NP + h] = lsum[h];
       mbar_arrive(&red_full[n_t & 1]);
     }
-    if (ok && !wait_warp(&red_full[n_t & 1], (n_t >> 1) & 1)) {
+    if (ok && !wait_warp(&red_full[n_t & 1], (n_t >> 1) & 1, p.pipe_wait_ns)) {
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
       *abort_s = 1;
       ok = false;
@@ -404,13 +405,13 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     for (int t = 0; t < n_t; ++t) {
       if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
       const int ob = t & 1;
-      if (!wait_warp(&a_full[ob], (t >> 1) & 1)) { ok = false; break; }
+      if (!wait_warp(&a_full[ob], (t >> 1) & 1, p.pipe_wait_ns)) { ok = false; break; }
       float alpha[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) alpha[h] = alpha_s[ob * C::NP + h];
       mbar_arrive_warp(&a_free[ob]);
       // acc = acc * alpha + O_tile^T(t): the two-level accumulation of tile t
-      if (!wait_warp(&o_full[ob], (t >> 1) & 1)) { ok = false; break; }
+      if (!wait_warp(&o_full[ob], (t >> 1) & 1, p.pipe_wait_ns)) { ok = false; break; }
       tc_fence_after();
       float o[C::NSUB][16];
 #pragma unroll
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       *abort_s = 1;
     }
     // ---- this split's result: o = acc / (448 l) and lse = m + log2(l) per head
-    if (ok && wait_warp(l_full, 0)) {
+    if (ok && wait_warp(l_full, 0, p.pipe_wait_ns)) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float L = ml_s[C::NP + h];
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     for (int t = n0; t < n_t; ++t) {
       if (abort_warp(abort_s)) break;
       const int st = t % C::NS, use = t / C::NS;
-      if (use > 0 && !wait_warp(&k_empty[st], (use - 1) & 1)) {
+      if (use > 0 && !wait_warp(&k_empty[st], (use - 1) & 1, p.pipe_wait_ns)) {
         if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
         *abort_s = 1;
         break;
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     int v_last[C::NS];
 #pragma unroll
     for (int s = 0; s < C::NS; ++s) v_last[s] = s < n0 ? 0 : -1;
-    bool ok = wait_warp(q_full, 0);
+    bool ok = wait_warp(q_full, 0, p.pipe_wait_ns);
     uint64_t t_progress = globaltimer_ns();
     while (ok && tp < n_t) {
       if (abort_warp(abort_s)) break;
@@ -577,7 +578,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       }
       if (events != 0) {
         t_progress = globaltimer_ns();
-      } else if (globaltimer_ns() - t_progress > kPipeWaitNs) {
+      } else if (globaltimer_ns() - t_progress > p.pipe_wait_ns) {
         ok = false;
       } else {
         __nanosleep(32);  // leave the issue slots to the softmax warp sharing this SM quarter

@@ -35,6 +35,9 @@ struct DecodeParams {
   // position T - 1 by the launch itself (fp8_decode_step); null: the pools are complete
   const __nv_bfloat16* k_new;
   const __nv_bfloat16* v_new;
+  // wall-clock bound of the tensor-core decode's pipeline waits (ns); the waits that let
+  // issued copies and products drain before the CTA exits keep their own bound
+  uint64_t pipe_wait_ns;
 };
 
 struct PrefillParams {

@@ -187,24 +187,27 @@ constexpr uint64_t kPipeWaitNs = 200000000ull;  // 200 ms per wait
 // branch.  The MMA and TMA warps pass through many waits per tile, and code that a warp
 // runs once per tile has to be fetched into the instruction cache again every tile (the
 // softmax warps' unrolled loops on the same SM quarter displace it), so their code size
-// is their speed.
-static __device__ __noinline__ bool wait_ns_timed(uint64_t* bar, uint32_t parity) {
+// is their speed.  A bound below the 1 ms suspend hint polls without suspending, so that
+// it can run out within its own length.
+static __device__ __noinline__ bool wait_ns_timed(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
-    if (globaltimer_ns() - t0 > kPipeWaitNs) return false;
+    if (limit_ns >= 1000000u ? mbar_try_wait_hint(bar, parity, 1000000u) : mbar_test_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
-FKV_DEV bool wait_ns(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_ns_timed(bar, parity);
+// mbarrier.try_wait may itself suspend the thread until the phase completes (for a
+// system-dependent time), so a bound below the suspend hint tests without waiting.
+FKV_DEV bool wait_ns(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kPipeWaitNs) {
+  if (limit_ns >= 1000000u ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity)) return true;
+  return wait_ns_timed(bar, parity, limit_ns);
 }
 
 // Warp-uniform forms: tcgen05.ld / st are warp-collective, so every lane of a warp must
 // take the same branch around them.
-FKV_DEV bool wait_warp(uint64_t* bar, uint32_t parity) {
-  const bool ok = wait_ns(bar, parity);
+FKV_DEV bool wait_warp(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kPipeWaitNs) {
+  const bool ok = wait_ns(bar, parity, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 FKV_DEV bool abort_warp(volatile int* flag) { return __any_sync(0xffffffffu, *flag != 0); }

@@ -2,9 +2,10 @@
  * fp8kv — FP8 (e4m3) KV-cache quantisation and FP8 attention for GB300 (sm_103a).
  *
  * C ABI of libfp8kv.so.  Every tensor argument is a plain device pointer owned by the
- * caller; the library allocates nothing, keeps no state between calls (the one fixed
- * device array is the scratch of fp8_decode_attn_noalloc, below), and enqueues its
- * kernels on the given stream without synchronising.  Host pointers are marked "host".
+ * caller; the library allocates nothing, keeps no state between calls (the exceptions:
+ * the one fixed device array that is the scratch of fp8_decode_attn_noalloc, and the wait
+ * bound of the test hook fkv_set_decode_wait_limit_ns), and enqueues its kernels on the
+ * given stream without synchronising.  Host pointers are marked "host".
  *
  * The operations restate the vLLM blog "FP8 KV-Cache and Attention quantization in
  * vLLM" (2026-04-22):
@@ -101,6 +102,20 @@ const char* fkv_status_string(fkv_status status);
 int32_t fkv_version(void);
 
 /*
+ * fkv_set_decode_wait_limit_ns — test hook for the timeout path of the tensor-core decode.
+ *
+ * Sets, for fp8_decode_attn / fp8_decode_step / fp8_decode_attn_noalloc launches on e4m3
+ * layers made after the call (process-wide), the wall-clock bound of each in-kernel
+ * pipeline wait; 0 restores the default of 200 ms.  A bound shorter than the pipeline's
+ * own latency makes the first unsatisfied wait run out, so that FKV_FAULT_TIMEOUT and the
+ * recovery that follows can be exercised without a stalled GPU: the CTA stops, lets
+ * every copy and product it issued complete (those waits keep the 200 ms bound), frees
+ * its tensor memory and returns; the output of such a launch is undefined (the split
+ * merge reads whatever the workspace held).  Not for production use.
+ */
+void fkv_set_decode_wait_limit_ns(unsigned long long ns);
+
+/*
  * kv_quant_cache — write new tokens' K and V into one layer of the paged cache.
  *
  * The blog's cache write (`reshape_and_cache_flash`, section "Kernel 与 vLLM 改进",
@@ -160,7 +175,13 @@ int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t n
 /*
  * Pool blocks per context split of fp8_decode_attn for these sizes (a multiple of 8):
  * split s of a sequence covers blocks [lo / 16 + s * n, lo / 16 + (s + 1) * n).  0 for
- * invalid sizes.
+ * invalid sizes.  With n_blk = max_blocks (window 0) or min(max_blocks, ceil(window / 16)
+ * + 1), a requested num_splits > 0 gives ceil(n_blk / num_splits) blocks, at most 256 and
+ * at least ceil(n_blk / 1024), rounded up to a multiple of 8 (a multiple of 8 above 256
+ * means the context is too long: 0).  num_splits 0 picks, among the multiples of 8 up
+ * to 256, the count c minimising waves(c) * min(c, n_blk), where waves(c) =
+ * ceil(batch * num_kv_heads * ceil(n_blk / c) / (3 * SMs of the current device)); ties
+ * go to the larger c.
  */
 int32_t fp8_decode_attn_split_blocks(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                      int32_t head_dim, int32_t max_blocks, int32_t window,
@@ -223,20 +244,20 @@ fkv_status fp8_decode_attn(const void* q, int32_t batch, int32_t num_q_heads,
  * then attends over the whole context, the new token included (the blog's cache write
  * reshape_and_cache_flash followed by the decode attention).  For every sequence b with
  * T_b = context_lens[b] >= 1, the rows k_new[b][g][:] and v_new[b][g][:] of every KV
- * head g are quantised into the pools at position T_b - 1 (block
+ * head g are written into the pools at position T_b - 1 (block
  * block_table[b][(T_b - 1) / 16], slot (T_b - 1) % 16) exactly as kv_quant_cache writes
- * them: e4m3(fl32(x * fl32(1 / s))) with the same k_scale / v_scale and gran; then the
- * attention is that of fp8_decode_attn with the same arguments.  The write is done by
- * the CTA whose context split holds position T_b - 1, before its copies read that block,
- * so the result equals kv_quant_cache followed by fp8_decode_attn, pool bytes and output
- * bit for bit, with one launch instead of two.
+ * them — e4m3(fl32(x * fl32(1 / s))) with the same k_scale / v_scale and gran, e5m2 likewise
+ * on e5m2 pools, an exact copy on a skip layer's bf16 pools — then the attention is that
+ * of fp8_decode_attn with the same arguments.  The write is done by the CTA whose context
+ * split holds position T_b - 1, before its copies read that block, so the result equals
+ * kv_quant_cache followed by fp8_decode_attn, pool bytes and output bit for bit, with one
+ * launch instead of two.
  *
  *   k_new, v_new  device bf16 [batch][num_kv_heads][head_dim], 16-byte aligned
  *   all other arguments as for fp8_decode_attn
- * Only e4m3 layers (the tensor-core decode): a skip layer or an e5m2 pool returns
- * FKV_UNSUPPORTED (write with kv_quant_cache and call fp8_decode_attn instead).  A block
- * id out of range is reported as for fp8_decode_attn and its row is not written; so is a
- * context length outside [0, max_blocks * 16] (FKV_FAULT_CONTEXT): no pool byte changes.
+ * A block id out of range is reported as for fp8_decode_attn and its row is not written;
+ * so is a context length outside [0, max_blocks * 16] (FKV_FAULT_CONTEXT): no pool byte
+ * changes.
  */
 fkv_status fp8_decode_step(const void* k_new, const void* v_new, const void* q, int32_t batch,
                            int32_t num_q_heads, fkv_layer_cache cache, const int32_t* block_table,

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def _declared():
     text = open(os.path.join(ROOT, "include", "fp8kv.h")).read()
-    return set(re.findall(r"^(?:const char\*|fkv_status|size_t|int32_t)\s+(\w+)\(", text, re.M))
+    return set(re.findall(r"^(?:const char\*|fkv_status|size_t|int32_t|void)\s+(\w+)\(", text, re.M))
 
 
 @pytest.fixture(scope="module")

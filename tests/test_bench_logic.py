@@ -127,3 +127,15 @@ def test_profile_hash_covers_code_not_comments():
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only("int x = 2;") != bench._code_only("int x = 1;")
     assert len(bench.kernel_source_sha("decode_tc.cu")) == 16
+
+
+def test_both_arms_describe_the_same_workload_and_sample():
+    """The reference arm and the benchmark line's cpu_baseline time the same oracle sample
+    and print the same config object."""
+    w = synth.WORKLOADS[2]
+    keys, heads, text = bench.oracle_sample_shape(2)
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    assert keys == int(ctx[0]) and heads == w.group and str(keys) in text
+    a = bench.workload_config(w, ctx, 1)
+    b = bench.workload_config(w, ctx, 1, step_bytes=bench._step_bytes_host(w, ctx))
+    assert a == b and a["workload"] == w.name and a["context"] == [int(x) for x in ctx]

@@ -366,3 +366,45 @@ def test_fault_bits_block_id_and_context():
     torch.cuda.synchronize()
     assert int(fault.item()) & f.FAULT_CONTEXT
     assert torch.isfinite(o.float()).all()
+
+
+def test_pipeline_wait_timeout_is_reported_and_the_next_call_is_correct():
+    """The timeout path of the tensor-core decode, exercised without a stalled GPU: the
+    test hook bounds every pipeline wait at 1 ns, so the first wait not already satisfied
+    runs out.  The launch must record FKV_FAULT_TIMEOUT, let its copies and products
+    complete (those waits keep their 200 ms bound) and return; its output, merged from a
+    zeroed workspace, is finite.  The next call, with the default bound, must reproduce a
+    call made before the timeout bit for bit and raise no fault."""
+    lib = f.load_library()
+    rng = np.random.default_rng(55)
+    D, G, Hkv = 128, 4, 2
+    Hq = Hkv * G
+    ctx = np.array([3000, 700], np.int32)
+    table, nb = synth.block_table(ctx, seed=55)
+    q, k, v = _inputs(rng, ctx, Hq, Hkv, D)
+    one = np.ones(1, np.float32)
+    cache = build_layer(f, ctx, table, nb, k, v, one, one, 0, False, sentinel=0xFF)
+    ws = f.decode_workspace(len(ctx), Hq, cache, table.shape[1], num_splits=2)
+    args = (q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(one), to_dev(one), to_dev(one), 0)
+    fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = f.fp8_decode_attn(*args, workspace=ws, num_splits=2, fault=fault)
+    torch.cuda.synchronize()
+    assert int(fault.item()) == 0
+    kp, vp = oracle_pools(kvcache, ctx, table, nb, k, v, one, one, False)
+    mode = _oracle_mode(D, False, len(ctx), Hq, Hkv, table.shape[1], 0, 2)
+    assert_close(ref.float().cpu().numpy(), attention.decode_attention(
+        synth.bf16_to_f64(q), kp, vp, table, ctx, one, one, one, **mode), what="before the timeout")
+    ws.zero_()
+    lib.fkv_set_decode_wait_limit_ns(1)
+    try:
+        out = f.fp8_decode_attn(*args, workspace=ws, num_splits=2, fault=fault)
+        torch.cuda.synchronize()
+    finally:
+        lib.fkv_set_decode_wait_limit_ns(0)
+    assert int(fault.item()) & f.FAULT_TIMEOUT
+    assert torch.isfinite(out.float()).all()
+    fault.zero_()
+    again = f.fp8_decode_attn(*args, workspace=ws, num_splits=2, fault=fault)
+    torch.cuda.synchronize()
+    assert int(fault.item()) == 0
+    assert torch.equal(again.view(torch.int16), ref.view(torch.int16))

@@ -3,7 +3,8 @@ must equal kv_quant_cache of that token followed by fp8_decode_attn — pool byt
 output bit for bit.  The separate calls are pinned to the oracle by test_gpu_cache and
 test_gpu_decode; equality carries that over.  Cases cover every head_dim, per-tensor and
 per-head scales, windows, forced split counts, an empty sequence, and consecutive steps
-whose current token opens a new pool block."""
+whose current token opens a new pool block; the same on bf16 (skip) and e5m2 layers, whose
+CUDA-core decode writes the current token in its launch too."""
 import numpy as np
 import pytest
 import torch
@@ -21,7 +22,17 @@ def _scales(gran, q, k, v):
     return torch.tensor([0.5]), torch.tensor([1.0]), torch.tensor([0.25])
 
 
-def _run_both(ctx, table, nb, q, k, v, qs, ks, vs, gran, window, splits, cache_a, cache_b):
+def _kind_args(kind):
+    """LayerCache.empty / call keywords of a layer kind: e4m3 pools, a skip layer's bf16
+    pools, or e5m2 pools."""
+    if kind == "bf16":
+        return dict(bf16=True), dict(skip_layer_mask=[1])
+    if kind == "e5m2":
+        return dict(kv_format=f.KV_E5M2), {}
+    return {}, {}
+
+
+def _run_both(ctx, table, nb, q, k, v, qs, ks, vs, gran, window, splits, cache_a, cache_b, kind="e4m3"):
     """One decode step on two copies of a layer: (A) kv_quant_cache of the current token
     then fp8_decode_attn, (B) fp8_decode_step.  k / v hold every position of every
     sequence (sequence-major); the current token of sequence b is position ctx[b] - 1."""
@@ -37,16 +48,17 @@ def _run_both(ctx, table, nb, q, k, v, qs, ks, vs, gran, window, splits, cache_a
             k_new[b] = k[cu[b + 1] - 1]
             v_new[b] = v[cu[b + 1] - 1]
             slots[b] = all_slots[cu[b + 1] - 1]
+    _, kw = _kind_args(kind)
     args = (to_dev(table), to_dev(ctx), to_dev(qs), to_dev(ks), to_dev(vs), gran)
-    f.kv_quant_cache(k_new.cuda(), v_new.cuda(), to_dev(slots), cache_a, to_dev(ks), to_dev(vs), gran)
-    out_a = f.fp8_decode_attn(q.cuda(), cache_a, *args, window=window, num_splits=splits)
+    f.kv_quant_cache(k_new.cuda(), v_new.cuda(), to_dev(slots), cache_a, to_dev(ks), to_dev(vs), gran, **kw)
+    out_a = f.fp8_decode_attn(q.cuda(), cache_a, *args, window=window, num_splits=splits, **kw)
     out_b = f.fp8_decode_step(k_new.cuda(), v_new.cuda(), q.cuda(), cache_b, *args, window=window,
-                              num_splits=splits)
+                              num_splits=splits, **kw)
     torch.cuda.synchronize()
     return out_a, out_b
 
 
-def _layer_before_step(ctx, table, nb, k, v, ks, vs, gran):
+def _layer_before_step(ctx, table, nb, k, v, ks, vs, gran, kind="e4m3"):
     """Two identical pools holding every position except each sequence's current token
     (stale bytes elsewhere are NaN codes, 0xFF)."""
     Hkv, D = k.shape[1], k.shape[2]
@@ -55,12 +67,13 @@ def _layer_before_step(ctx, table, nb, k, v, ks, vs, gran):
     for b in range(len(ctx)):
         if ctx[b] > 0:
             slots[cu[b + 1] - 1] = -1
-    a = f.LayerCache.empty(nb, Hkv, D)
+    ck, kw = _kind_args(kind)
+    a = f.LayerCache.empty(nb, Hkv, D, **ck)
     a.k_cache.view(torch.uint8).fill_(0xFF)
     a.v_cache.view(torch.uint8).fill_(0xFF)
     if len(slots):
-        f.kv_quant_cache(k.cuda(), v.cuda(), to_dev(slots), a, to_dev(ks), to_dev(vs), gran)
-    b_ = f.LayerCache.empty(nb, Hkv, D)
+        f.kv_quant_cache(k.cuda(), v.cuda(), to_dev(slots), a, to_dev(ks), to_dev(vs), gran, **kw)
+    b_ = f.LayerCache.empty(nb, Hkv, D, **ck)
     b_.k_cache.copy_(a.k_cache)
     b_.v_cache.copy_(a.v_cache)
     return a, b_
@@ -121,19 +134,36 @@ def test_decode_step_consecutive_steps_across_a_block_boundary():
         assert torch.equal(out_a, out_b), f"output differs at step {step}"
 
 
-def test_decode_step_rejects_non_e4m3_layers():
-    D, Hkv, G = 128, 2, 4
-    ctx = np.array([5], np.int32)
-    table, nb = synth.block_table(ctx, seed=3)
-    q = torch.zeros((1, Hkv * G, D), dtype=torch.bfloat16).cuda()
-    kn = torch.zeros((1, Hkv, D), dtype=torch.bfloat16).cuda()
-    bf16_pool = f.LayerCache.empty(nb, Hkv, D, bf16=True)
-    with pytest.raises(f.FkvError):
-        f.fp8_decode_step(kn, kn, q, bf16_pool, to_dev(table), to_dev(ctx), skip_layer_mask=[1])
-    e5 = f.LayerCache.empty(nb, Hkv, D, kv_format=f.KV_E5M2)
-    one = torch.ones(1).cuda()
-    with pytest.raises(f.FkvError):
-        f.fp8_decode_step(kn, kn, q, e5, to_dev(table), to_dev(ctx), one, one, one)
+@pytest.mark.parametrize("kind,D,G,gran,window,splits", [
+    ("bf16", 128, 4, 0, 0, 0), ("bf16", 64, 8, 0, 128, 0), ("bf16", 256, 2, 0, 0, 3), ("bf16", 64, 16, 0, 0, 2),
+    ("e5m2", 128, 4, 1, 0, 0), ("e5m2", 64, 8, 0, 40, 2), ("e5m2", 256, 1, 1, 0, 0),
+])
+def test_decode_step_on_bf16_and_e5m2_layers(kind, D, G, gran, window, splits):
+    """The CUDA-core decode's fused write: a skip layer's bf16 pools (an exact copy of the
+    current token) and e5m2 pools (e5m2 of x / s) — the same bytes and output as
+    kv_quant_cache then fp8_decode_attn, so a bf16 decode step compares with the e4m3 one
+    launch for launch."""
+    rng = np.random.default_rng(D * 3 + G + window + splits + (kind == "e5m2"))
+    Hkv = 2
+    Hq = Hkv * G
+    ctx = np.array([1, 15, 16, 17, 300, 1000, 0, 129], np.int32)
+    table, nb = synth.block_table(ctx, seed=29, extra_blocks=2)
+    n = int(ctx.sum())
+    q = torch.from_numpy(rng.standard_normal((len(ctx), Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy((rng.standard_normal((n, Hkv, D)) * 3.0).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((n, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    qs, ks, vs = _scales(gran, q, k, v)
+    if kind == "e5m2":
+        ks, vs = ks * 0.01, vs * 0.01   # scaled values far past e4m3's range, inside e5m2's
+    cache_a, cache_b = _layer_before_step(ctx, table, nb, k, v, ks.numpy(), vs.numpy(), gran, kind)
+    out_a, out_b = _run_both(ctx, table, nb, q, k, v, qs, ks, vs, gran, window, splits, cache_a, cache_b, kind)
+    # bit patterns: stale slots hold NaN codes, which never compare equal as values
+    bits = lambda t: t.view(torch.uint8)
+    assert torch.equal(bits(cache_a.k_cache), bits(cache_b.k_cache)), "K pool differs"
+    assert torch.equal(bits(cache_a.v_cache), bits(cache_b.v_cache)), "V pool differs"
+    assert torch.equal(out_a, out_b), "output differs"
+    assert torch.isfinite(out_b.float()).all()
+    assert torch.all(out_b[6] == 0), "a sequence without keys gets a zero row"
 
 
 def test_decode_step_oversized_context_writes_nothing():
