@@ -216,7 +216,7 @@ class DecodeState:
                                                                   lay["window"]))
             del data
         torch.cuda.synchronize()
-        self.ws = torch.empty(max_ws, dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(max_ws, dtype=torch.uint8, device=device)   # split counters start at zero
         self.bytes = decode_bytes(w, self.ctx, self.bf16)
 
     def step(self, decode_only=False, fused=True):

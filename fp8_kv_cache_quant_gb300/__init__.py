@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_PKG, "libfp8kv.so")
 OK, INVALID_ARG, UNSUPPORTED, CUDA_ERROR = 0, 1, 2, 3
 SCALE_PER_TENSOR, SCALE_PER_HEAD = 0, 1
 KV_E4M3, KV_E5M2 = 0, 1
-FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT, FAULT_QLEN = 1, 2, 4, 8, 16
+FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT, FAULT_QLEN, FAULT_WORKSPACE = 1, 2, 4, 8, 16, 32
 
 # Entry points declared by include/fp8kv.h (checked by the tests).
 EXPORTS = (
@@ -216,9 +216,11 @@ def fkv_decode_block_n(head_dim: int, bf16_layer: bool = False, kv_format: int =
 
 
 def decode_workspace(batch, num_q_heads, cache: LayerCache, max_blocks, window=0, num_splits=0, device="cuda"):
+    """A zero-filled decode workspace (the split counters at its start must be zero when a
+    call begins; every call leaves them zero)."""
     n = fp8_decode_attn_workspace_size(batch, num_q_heads, cache.num_kv_heads, cache.head_dim, max_blocks,
                                        window, num_splits)
-    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def fp8_decode_attn(q, cache: LayerCache, block_table, context_lens, q_scale=None, k_scale=None, v_scale=None,

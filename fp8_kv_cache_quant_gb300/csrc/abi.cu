@@ -171,7 +171,8 @@ fkv_status decode_entry(const void* k_new, const void* v_new, const void* q, int
     return FKV_UNSUPPORTED;
   const size_t need = plan.o_bytes + plan.lse_bytes + plan.cnt_bytes;
   if (scratch) {
-    const fkv_status sst = scratch(need, &workspace, &workspace_bytes);
+    const fkv_status sst = scratch(need, plan.cnt_bytes, reinterpret_cast<cudaStream_t>(stream), &workspace,
+                                   &workspace_bytes);
     if (sst != FKV_OK) return sst;
   }
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return FKV_INVALID_ARG;
@@ -197,19 +198,17 @@ fkv_status decode_entry(const void* k_new, const void* v_new, const void* q, int
   p.window = window;
   p.bps = plan.bps;
   p.max_splits = plan.max_splits;
-  p.o_part = static_cast<float*>(workspace);
-  p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.o_bytes);
-  p.done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plan.o_bytes + plan.lse_bytes);
+  // workspace: the split-completion counters first (zero between calls), then the
+  // splits' log-sum-exps and normalised outputs (written before they are read)
+  p.done = static_cast<int32_t*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.cnt_bytes);
+  p.o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.cnt_bytes + plan.lse_bytes);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.fault = fault;
   p.k_new = static_cast<const __nv_bfloat16*>(k_new);
   p.v_new = static_cast<const __nv_bfloat16*>(v_new);
   const unsigned long long wait_ns = g_decode_wait_ns.load(std::memory_order_relaxed);
   p.pipe_wait_ns = wait_ns != 0 ? wait_ns : kDefaultPipeWaitNs;
-  // split-completion counters start at zero on every call
-  if (cudaMemsetAsync(p.done, 0, static_cast<size_t>(batch) * cache.num_kv_heads * sizeof(int32_t),
-                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FKV_CUDA_ERROR;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (fkv::decode_uses_tensor_cores(cache.head_dim, elt)) return from_cuda(fkv::launch_decode_tc(p, cache.head_dim, G, s));
   return from_cuda(fkv::launch_decode(p, cache.head_dim, elt, G, s));

@@ -18,6 +18,17 @@ FKV_DEV void raise_fault(int32_t* fault, int32_t bits) {
   if (fault) atomicOr(fault, bits);
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation
+// may start while the kernel before it in the stream is still running.
+// griddep_launch_dependents lets the next such kernel's CTAs be scheduled (as this grid's
+// CTAs leave the SMs); griddep_wait returns once every earlier grid has completed and its
+// memory writes are visible, and precedes every read or write of global memory that an
+// earlier kernel may produce or consume.  (Both are no-ops for a plain launch.)
+FKV_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+FKV_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- e4m3
 
 // Two float32 values -> two e4m3 codes, round-to-nearest-even, saturating to +-448

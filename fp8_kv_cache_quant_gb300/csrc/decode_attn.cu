@@ -148,6 +148,14 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
 
   const int sigma = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the next kernel in the stream may be scheduled as this grid's CTAs finish; the
+  // barriers need no input and are set up before waiting for the kernels before this one
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNW * kNBUF; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  griddep_wait();
   const SeqRange r = seq_range(p, b, sigma == 0 && g == 0 && threadIdx.x == 0);
   if (sigma >= r.nsplit) {  // uniform over the CTA
     if (sigma == 0) {  // a sequence without keys: zero output rows
@@ -160,10 +168,6 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
   const int nblk = min(p.bps, r.blk_end - blk_first);
   const int ntiles = (nblk + C::TB - 1) / C::TB;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kNW * kNBUF; ++s) mbar_init(&full[s], 1);
-    fence_mbar_init();
-  }
   {
     const int* row = p.block_table + static_cast<size_t>(b) * p.max_blocks + blk_first;
     for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(kNW * 32, DecodeCfg<D, ELT, G>::MIN_CTAS)
   volatile int* last_s = ids_s;  // the block ids are no longer needed
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) *last_s = atomicAdd(&p.done[b * p.Hkv + g], 1) == r.nsplit - 1;
+  if (threadIdx.x == 0) *last_s = count_split_done(p, b * p.Hkv + g, r.nsplit);
   __syncthreads();
   if (!*last_s) return;
   __threadfence();
@@ -487,8 +491,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(p.max_splits, p.Hkv, p.B);
-  kern<<<grid, kNW * 32, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dim3(kNW * 32), smem, s, p);
 }
 
 template <int D, int ELT>

@@ -34,6 +34,19 @@ FKV_DEV SeqRange seq_range(const DecodeParams& p, int b, bool report) {
   return r;
 }
 
+// One split of unit u (a sequence's KV head) is done: count it.  Returns true for the
+// split that completes the unit, whose CTA then merges; that CTA also returns the counter
+// to zero, since every other split has counted, so the workspace's counters are zero
+// again for the next call.  A count already at nsplit or beyond means the counters were
+// not zero when the call began (a workspace not zero-filled before first use).
+FKV_DEV bool count_split_done(const DecodeParams& p, int u, int nsplit) {
+  const int old = atomicAdd(&p.done[u], 1);
+  if (old >= nsplit) raise_fault(p.fault, FKV_FAULT_WORKSPACE);
+  if (old != nsplit - 1) return false;
+  p.done[u] = 0;
+  return true;
+}
+
 // The second, FP32 level of the split-K accumulation, run by the CTA that finished the
 // last split of (sequence b, KV head g): with lse_s the base-2 log-sum-exp of split s
 // and o_s its normalised output, o = v_s * sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
@@ -41,8 +54,8 @@ FKV_DEV SeqRange seq_range(const DecodeParams& p, int b, bool report) {
 // `scratch` holds at least 2 * G + G * CH floats of shared memory.
 // The partials come from L2; a load whose value the next instruction needs holds the
 // warp for the whole round trip, so the log-sum-exps are read by a warp per head with
-// the lanes striding over the splits, and each output pair's split partials are loaded
-// eight at a time before they are summed (in split order).
+// the lanes striding over the splits, and each group of four outputs' split partials are
+// loaded sixteen at a time (16-byte loads) before they are summed (in split order).
 template <int D, int G, int NT, int CH>
 FKV_DEV void merge_splits(const DecodeParams& p, int b, int g, int ns, float vs, float* scratch) {
   float* ms_s = scratch;       // [G] max of lse
@@ -70,11 +83,11 @@ FKV_DEV void merge_splits(const DecodeParams& p, int b, int g, int ns, float vs,
       inv_s[h] = (W > 0.f) ? vs / W : 0.f;
     }
   }
-  constexpr int PAIRS = (G * D / 2 + NT - 1) / NT;  // output pairs per thread
-  constexpr int U = 8;                               // split partials loaded before use
-  float2 o[PAIRS];
+  constexpr int QUADS = (G * D / 4 + NT - 1) / NT;  // groups of 4 outputs per thread
+  constexpr int U = 16;                              // split partials loaded before use
+  float4 o[QUADS];
 #pragma unroll
-  for (int k2 = 0; k2 < PAIRS; ++k2) o[k2] = make_float2(0.f, 0.f);
+  for (int k2 = 0; k2 < QUADS; ++k2) o[k2] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c0 = 0; c0 < ns; c0 += CH) {
     const int nc = min(CH, ns - c0);
     __syncthreads();
@@ -85,41 +98,46 @@ FKV_DEV void merge_splits(const DecodeParams& p, int b, int g, int ns, float vs,
     }
     __syncthreads();
 #pragma unroll
-    for (int k2 = 0; k2 < PAIRS; ++k2) {
+    for (int k2 = 0; k2 < QUADS; ++k2) {
       const int t = threadIdx.x + k2 * NT;
-      if (t < G * D / 2) {
-        const int h = t / (D / 2), d = 2 * (t % (D / 2));
+      if (t < G * D / 4) {
+        const int h = t / (D / 4), d = 4 * (t % (D / 4));
         const float* src = p.o_part + (row_base + static_cast<size_t>(h) * p.max_splits + c0) * D + d;
         const float* wh = w_s + h * CH;
         int j = 0;
         for (; j + U <= nc; j += U) {
-          float2 x[U];
+          float4 x[U];
 #pragma unroll
-          for (int u = 0; u < U; ++u) x[u] = __ldcg(reinterpret_cast<const float2*>(src + static_cast<size_t>(j + u) * D));
+          for (int u = 0; u < U; ++u) x[u] = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(j + u) * D));
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const float wv = wh[j + u];
             o[k2].x += wv * x[u].x;
             o[k2].y += wv * x[u].y;
+            o[k2].z += wv * x[u].z;
+            o[k2].w += wv * x[u].w;
           }
         }
         for (; j < nc; ++j) {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + static_cast<size_t>(j) * D));
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(j) * D));
           const float wv = wh[j];
           o[k2].x += wv * x.x;
           o[k2].y += wv * x.y;
+          o[k2].z += wv * x.z;
+          o[k2].w += wv * x.w;
         }
       }
     }
   }
 #pragma unroll
-  for (int k2 = 0; k2 < PAIRS; ++k2) {
+  for (int k2 = 0; k2 < QUADS; ++k2) {
     const int t = threadIdx.x + k2 * NT;
-    if (t < G * D / 2) {
-      const int h = t / (D / 2), d = 2 * (t % (D / 2));
+    if (t < G * D / 4) {
+      const int h = t / (D / 4), d = 4 * (t % (D / 4));
       const float inv = inv_s[h];
-      *reinterpret_cast<__nv_bfloat162*>(p.out + (static_cast<size_t>(b) * p.Hq + g * G + h) * D + d) =
-          __floats2bfloat162_rn(o[k2].x * inv, o[k2].y * inv);
+      __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(p.out + (static_cast<size_t>(b) * p.Hq + g * G + h) * D + d);
+      dst[0] = __floats2bfloat162_rn(o[k2].x * inv, o[k2].y * inv);
+      dst[1] = __floats2bfloat162_rn(o[k2].z * inv, o[k2].w * inv);
     }
   }
 }

@@ -16,10 +16,10 @@
 
 namespace {
 
-// Scratch for the split partials (o / l and log-sum-exp of every split) and the
-// split-completion counters.  Every call on a device reuses the same bytes: the counters
-// are cleared by each call before its launch, and each split writes every partial that
-// the merge later reads, so nothing else has to start at zero.
+// Scratch for the split-completion counters (at its start) and the split partials (o / l
+// and log-sum-exp of every split).  Every call on a device reuses the same bytes: device
+// arrays start zero-filled, each call returns the counters to zero, and each split writes
+// every partial that the merge later reads.
 static __device__ __align__(256) unsigned char g_decode_scratch[FKV_NOALLOC_WORKSPACE_BYTES];
 
 // The array's device address belongs to the context the module was loaded into: the
@@ -55,6 +55,8 @@ Fn driver_fn(const char* name) {
   return reinterpret_cast<Fn>(ptr);
 }
 
+fkv_status noalloc_address(void** ws, size_t* bytes);
+
 // Id of the current context, or false when the driver cannot tell (no context current).
 bool current_ctx_id(unsigned long long* id) {
   CUcontext ctx = nullptr;
@@ -63,9 +65,20 @@ bool current_ctx_id(unsigned long long* id) {
 }
 
 // Supplies fp8_decode_attn's workspace from the fixed array (a ScratchProvider): sizes
-// beyond the array are FKV_INVALID_ARG.
-fkv_status noalloc_scratch(size_t need, void** ws, size_t* bytes) {
+// beyond the array are FKV_INVALID_ARG.  The split counters at the array's start are
+// cleared on the stream first: an earlier call with fewer (sequence, KV head) units left
+// other scratch where this call's counters lie, and the array cannot be handed to the
+// caller to clear.
+fkv_status noalloc_scratch(size_t need, size_t counter_bytes, cudaStream_t stream, void** ws, size_t* bytes) {
   if (need > static_cast<size_t>(FKV_NOALLOC_WORKSPACE_BYTES)) return FKV_INVALID_ARG;
+  const fkv_status st = noalloc_address(ws, bytes);
+  if (st != FKV_OK) return st;
+  if (cudaMemsetAsync(*ws, 0, counter_bytes, stream) != cudaSuccess) return FKV_CUDA_ERROR;
+  return FKV_OK;
+}
+
+// The array's device address in the current context (looked up on the context's first call).
+fkv_status noalloc_address(void** ws, size_t* bytes) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_driver_looked_up) {
     g_get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");

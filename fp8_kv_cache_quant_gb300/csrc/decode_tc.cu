@@ -155,25 +155,10 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
 
   const int sigma = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const SeqRange r = seq_range(p, b, sigma == 0 && g == 0 && threadIdx.x == 0);
-  if (sigma >= r.nsplit) {  // uniform over the CTA
-    if (sigma == 0) {       // a sequence without keys: zero output rows
-      for (int t = threadIdx.x; t < G * D; t += blockDim.x)
-        p.out[(static_cast<size_t>(b) * p.Hq + g * G + t / D) * D + t % D] = __float2bfloat16(0.f);
-    }
-    return;
-  }
-  // this split: blocks [bb, be), keys [klo, khi), tiles of 8 blocks from block bb
-  const int bb = r.blk_begin + sigma * p.bps;
-  const int be = min(bb + p.bps, r.blk_end);
-  const int klo = max(r.lo, bb * 16), khi = min(r.T, be * 16);
-  const int n_t = (be - bb + 7) / 8;
-  const int T = r.T;
-
-  // The K-producer warp sets up the barriers and, before the CTA-wide barrier, issues the
-  // K and V copies of the first NS tiles, so that the first HBM latency overlaps the rest
-  // of the prologue (TMEM allocation, block-id staging, the query's quantisation).
-  const int n0 = min(C::NS, n_t);  // tiles whose copies go out in the prologue
+  // The next kernel in the stream may be scheduled as this grid's CTAs finish.  The
+  // barriers and the tensor memory need no input, so they are set up before waiting for
+  // the kernels before this one (their writes to the inputs, the pools and the workspace).
+  griddep_launch_dependents();
   if (warp == 8 && lane == 0) {
     // barriers signalled by the softmax or correction warps count warps (one arrival each)
     mbar_init(q_full, 4);
@@ -202,6 +187,36 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     *abort_s = 0;
     fence_mbar_init();
   }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, C::TM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  griddep_wait();
+  const SeqRange r = seq_range(p, b, sigma == 0 && g == 0 && threadIdx.x == 0);
+  if (sigma >= r.nsplit) {  // uniform over the CTA
+    if (sigma == 0) {       // a sequence without keys: zero output rows
+      for (int t = threadIdx.x; t < G * D; t += blockDim.x)
+        p.out[(static_cast<size_t>(b) * p.Hq + g * G + t / D) * D + t % D] = __float2bfloat16(0.f);
+    }
+    __syncthreads();
+    if (warp == 9) {
+      tc_fence_after();
+      tmem_dealloc(*tmem_slot, C::TM_COLS);
+    }
+    return;
+  }
+  // this split: blocks [bb, be), keys [klo, khi), tiles of 8 blocks from block bb
+  const int bb = r.blk_begin + sigma * p.bps;
+  const int be = min(bb + p.bps, r.blk_end);
+  const int klo = max(r.lo, bb * 16), khi = min(r.T, be * 16);
+  const int n_t = (be - bb + 7) / 8;
+  const int T = r.T;
+
+  // Before the CTA-wide barrier the K-producer warp issues the K and V copies of the first
+  // NS tiles, so that the first HBM latency overlaps the rest of the prologue (block-id
+  // staging, the query's quantisation).
+  const int n0 = min(C::NS, n_t);  // tiles whose copies go out in the prologue
   // fp8_decode_step: the split holding position T - 1 (the last) writes the current token
   // into the pools before its first copy of that block (not when the context was clamped)
   if (warp == 8 && p.k_new != nullptr && sigma == r.nsplit - 1 && !r.clamped) write_current_token<D>(p, b, g, T, lane);
@@ -233,11 +248,6 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         }
       }
     }
-  }
-  if (warp == 9) {
-    tmem_alloc(tmem_slot, C::TM_COLS);
-    tmem_relinquish();
-    tc_fence_before();
   }
   // the split's other block ids, checked once (an id out of range reads block 0 and is reported)
   {
@@ -607,7 +617,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
   // ---------------------------------------------------- the last split of (b, g) merges
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) *last_s = atomicAdd(&p.done[b * p.Hkv + g], 1) == r.nsplit - 1;
+  if (threadIdx.x == 0) *last_s = count_split_done(p, b * p.Hkv + g, r.nsplit);
   __syncthreads();
   if (!*last_s) return;
   __threadfence();
@@ -627,8 +637,7 @@ cudaError_t launch_decode_tc_t(const DecodeParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.max_splits, p.Hkv, p.B);
-  kern<<<grid, kDecodeTcThreads, C::SMEM, s>>>(p, tmk, tmv);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dim3(kDecodeTcThreads), C::SMEM, s, p, tmk, tmv);
 }
 
 template <int D>

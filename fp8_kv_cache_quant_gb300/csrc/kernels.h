@@ -61,6 +61,24 @@ struct PrefillParams {
 cudaError_t launch_prefill(const PrefillParams& p, int D, bool bf16_layer, void* k_cache, void* v_cache,
                            cudaStream_t s);
 
+// Launch `kern` with programmatic stream serialisation (the kernel must call griddep_wait
+// before touching global memory that earlier kernels produce or consume).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_kv_quant_cache(const void* k, const void* v, const int64_t* slots, int n_tokens,
                                   const fkv_layer_cache& cache, const float* ks, const float* vs,
                                   int per_head, bool bf16_layer, int32_t* fault, cudaStream_t s,
@@ -75,8 +93,11 @@ bool decode_uses_tensor_cores(int D, int elt);
 cudaError_t launch_decode_tc(const DecodeParams& p, int D, int G, cudaStream_t s);
 
 // Supplies the decode's workspace of `need` bytes when the caller passes none: sets *ws
-// (256-byte aligned) and *bytes, or returns the status the entry point then returns.
-using ScratchProvider = fkv_status (*)(size_t need, void** ws, size_t* bytes);
+// (256-byte aligned) and *bytes, with its first `counter_bytes` (the split counters) zero
+// by the time work enqueued afterwards on `stream` runs, or returns the status the entry
+// point then returns.
+using ScratchProvider = fkv_status (*)(size_t need, size_t counter_bytes, cudaStream_t stream, void** ws,
+                                       size_t* bytes);
 
 // The whole of fp8_decode_attn (k_new = v_new = NULL) and fp8_decode_step: argument
 // checks, the split-K plan, then the launch.  With scratch non-null the workspace comes

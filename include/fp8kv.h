@@ -32,6 +32,11 @@
  *             query scale num_q_heads values.
  *   GQA       query head h reads KV head h / (num_q_heads / num_kv_heads).
  *
+ * Launches.  The decode kernels are launched with programmatic stream serialisation: a
+ * decode kernel may be scheduled while the kernel before it in the stream finishes, and
+ * sets up its barriers and tensor memory then, but reads and writes no global memory
+ * until that kernel has completed, so the stream's ordering is kept.
+ *
  * Errors.  Argument checks run on the host before anything is enqueued and return
  * FKV_INVALID_ARG or FKV_UNSUPPORTED; a failed launch returns FKV_CUDA_ERROR.  Data
  * errors that only the GPU can see (a block id outside [0, num_blocks), a slot outside
@@ -74,6 +79,8 @@ typedef enum {
                                 abandoned after its copies and products drain; its partial
                                 results are undefined                                             */
 #define FKV_FAULT_QLEN 16    /* prefill: query length > context length: sequence skipped     */
+#define FKV_FAULT_WORKSPACE 32 /* decode: a split counter of the workspace was not zero when the
+                                  call began (zero-fill a workspace before its first call)     */
 
 /* FP8 format of a layer's pools (fkv_layer_cache.kv_format). */
 typedef enum {
@@ -222,8 +229,14 @@ int32_t fkv_decode_block_n(int32_t head_dim, int32_t layer_kind);
  *   softmax_scale 0 selects 1/sqrt(head_dim)
  *   window        0 = full attention, else the number of most recent keys attended
  *   out           device bf16 [batch][num_q_heads][head_dim]
- *   workspace     device, >= fp8_decode_attn_workspace_size(...) bytes, 256-byte aligned;
- *                 scratch only (no state is kept across calls)
+ *   workspace     device, >= fp8_decode_attn_workspace_size(...) bytes, 256-byte aligned,
+ *                 zero-filled before its first call.  Its first 4 * batch * num_kv_heads
+ *                 bytes are split-completion counters, which must be zero when a call
+ *                 begins and which every call leaves at zero; the rest is scratch, written
+ *                 before it is read.  A workspace is therefore reused without clearing by
+ *                 calls in one stream with the same or a smaller batch * num_kv_heads
+ *                 (zero it again when that grows).  A counter found non-zero sets
+ *                 FKV_FAULT_WORKSPACE.
  *   num_splits    0 = automatic, else the requested number of context splits (each split
  *                 is then rounded up to whole multiples of 8 blocks, so fewer may result)
  * head_dim in {64, 128, 256}; G = num_q_heads / num_kv_heads in {1, 2, 4, 8, 16} with
@@ -291,7 +304,9 @@ fkv_status fp8_decode_step(const void* k_new, const void* v_new, const void* q, 
  *     device reset or a new context gets its own lookup on its first call.
  *   - All calls share the one array: calls whose kernels overlap on the GPU (other
  *     streams, other host threads) race on it and produce wrong results.  Calls in one
- *     stream are ordered and safe; each call writes every scratch byte it later reads.
+ *     stream are ordered and safe: each call clears its split counters (the array's
+ *     first 4 * batch * num_kv_heads bytes) on the stream before its kernel, and writes
+ *     every other scratch byte before it reads it.
  */
 fkv_status fp8_decode_attn_noalloc(const void* q, int32_t batch, int32_t num_q_heads,
                                    fkv_layer_cache cache, const int32_t* block_table,

@@ -408,3 +408,36 @@ def test_pipeline_wait_timeout_is_reported_and_the_next_call_is_correct():
     torch.cuda.synchronize()
     assert int(fault.item()) == 0
     assert torch.equal(again.view(torch.int16), ref.view(torch.int16))
+
+
+def test_workspace_counters_are_left_zero_and_checked():
+    """The workspace's split counters (its first 4 * batch * num_kv_heads bytes) must be
+    zero when a call begins, and every call leaves them zero: consecutive calls on one
+    workspace, also with another split plan, give the oracle's results.  A counter that
+    is not zero sets FKV_FAULT_WORKSPACE."""
+    rng = np.random.default_rng(66)
+    D, G, Hkv = 128, 4, 2
+    Hq = Hkv * G
+    ctx = np.array([2000, 129, 700], np.int32)
+    table, nb = synth.block_table(ctx, seed=66)
+    q, k, v = _inputs(rng, ctx, Hq, Hkv, D)
+    one = np.ones(1, np.float32)
+    cache = build_layer(f, ctx, table, nb, k, v, one, one, 0, False, sentinel=0xFF)
+    kp, vp = oracle_pools(kvcache, ctx, table, nb, k, v, one, one, False)
+    ws = f.decode_workspace(len(ctx), Hq, cache, table.shape[1], num_splits=1)
+    ws = torch.zeros(max(ws.numel(), f.fp8_decode_attn_workspace_size(len(ctx), Hq, Hkv, D, table.shape[1], 0, 5)),
+                     dtype=torch.uint8, device="cuda")
+    counters = ws[:4 * len(ctx) * Hkv].view(torch.int32)
+    fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+    args = (q.cuda(), cache, to_dev(table), to_dev(ctx), to_dev(one), to_dev(one), to_dev(one), 0)
+    for splits in (5, 2, 5, 1):
+        out = f.fp8_decode_attn(*args, workspace=ws, num_splits=splits, fault=fault)
+        torch.cuda.synchronize()
+        assert int(fault.item()) == 0 and int(counters.abs().sum().item()) == 0
+        mode = _oracle_mode(D, False, len(ctx), Hq, Hkv, table.shape[1], 0, splits)
+        assert_close(out.float().cpu().numpy(), attention.decode_attention(
+            synth.bf16_to_f64(q), kp, vp, table, ctx, one, one, one, **mode), what=f"num_splits={splits}")
+    counters[0] = 1000
+    f.fp8_decode_attn(*args, workspace=ws, num_splits=2, fault=fault)
+    torch.cuda.synchronize()
+    assert int(fault.item()) & f.FAULT_WORKSPACE
