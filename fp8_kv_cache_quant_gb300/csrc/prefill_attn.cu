@@ -38,6 +38,7 @@
 // Every wait is bounded in time; a timeout records FKV_FAULT_TIMEOUT, lets the CTA's
 // copies and MMAs drain and returns.
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -312,6 +313,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       // warps dearly when it is a run-time value)
       const int lo = WIN ? lo_row - kbase : -(1 << 30);
       const bool full = lim >= C::HC && (!WIN || lo <= 0);  // nothing masked in this half
+      // nothing masked in any row of the warp: selects the unmasked code paths, which hold
+      // warp-collective TMEM loads and so must be taken by the whole warp (a masked path
+      // is correct for every row)
+      const bool wfull = __all_sync(0xffffffffu, full);
       // chunk c (32 columns) of this thread's columns: its own 32 columns of the row from
       // [c0 + 32 c, ...), where the 16x32bx2 shape adds c0 = HC for the upper lanes itself
       const uint32_t sc = lane_base + 128 * sb;
@@ -340,15 +345,24 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
         // pass 1: max of the scaled, masked scores (cst > 0, so the raw maximum scales).
         // The TMEM loads are warp-collective: every lane issues them; only the arithmetic
         // depends on the row's own mask.
-        float mx = -INFINITY;
+        // (the mask test is taken once per tile: tested per element, it costs every
+        // element of every tile a compare and a select)
+        if (wfull) {
+          float mx = -INFINITY;
   #pragma unroll C::UNR
-        for (int c = 0; c < C::HCH; ++c) {
-          float v[32];
-          ld_s(c, v);
-          tmem_ld_wait();
-          if (full) {
+          for (int c = 0; c < C::HCH; ++c) {
+            float v[32];
+            ld_s(c, v);
+            tmem_ld_wait();
             mx = fmaxf(mx, max_tree<32>(v));
-          } else {
+          }
+          tmax = mx * cst;
+        } else {
+  #pragma unroll C::UNR
+          for (int c = 0; c < C::HCH; ++c) {
+            float v[32];
+            ld_s(c, v);
+            tmem_ld_wait();
   #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int col = 32 * c + j;
@@ -356,7 +370,6 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
             }
           }
         }
-        if (full) tmax = mx * cst;
       }
       // the row's maximum: this half's and the other half's (lane l ^ 16)
       if constexpr (C::SPLIT == 2) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
@@ -374,14 +387,19 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       const float nb = (BF ? 0.f : kLog2E4m3Max) - msafe;
       const float2 cst2 = make_float2(cst, cst), nm2 = make_float2(nb, nb);
       uint32_t ptm[C::TS ? 2 * C::HCH * 4 : 1];  // TS: this thread's P8 words (four keys each)
-      auto chunk = [&](const float (&v)[32], int c) {  // c: chunk of this thread's half
+      // c: chunk of this thread's half; `masked` says whether to apply the row's mask, which
+      // only tiles not wholly visible need: a compile-time flag on e4m3 layers (the choice is
+      // made once per tile), the run-time test of `full` on bf16 layers (whose registers do
+      // not hold two copies of the loop)
+      auto chunk = [&](const float (&v)[32], int c, auto masked) {
+        constexpr int MASKED = decltype(masked)::value;  // 0 never, 1 always, 2 unless full
         uint32_t pk[8 * C::ES];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           float2 x0 = __ffma2_rn(make_float2(v[j], v[j + 1]), cst2, nm2);
           float2 x1 = __ffma2_rn(make_float2(v[j + 2], v[j + 3]), cst2, nm2);
           x0.x = ex2(x0.x); x0.y = ex2(x0.y); x1.x = ex2(x1.x); x1.y = ex2(x1.y);
-          if (!full) {
+          if (MASKED == 1 || (MASKED == 2 && !full)) {
             const int col = 32 * c + j;
             if (col >= lim || col < lo) x0.x = 0.f;
             if (col + 1 >= lim || col + 1 < lo) x0.y = 0.f;
@@ -412,31 +430,45 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
           }
         }
       };
-      if constexpr (C::ONE_LOAD) {
+      using Unmasked = std::integral_constant<int, 0>;
+      using Masked = std::integral_constant<int, 1>;
+      using MaskedUnlessFull = std::integral_constant<int, 2>;
+      // the whole pass 2 for one masking mode
+      auto pass2 = [&](auto masked) {
+        if constexpr (C::ONE_LOAD) {
 #pragma unroll
-        for (int c = 0; c < C::HCH; ++c) chunk(*reinterpret_cast<const float(*)[32]>(vall + 32 * c), c);
+          for (int c = 0; c < C::HCH; ++c) chunk(*reinterpret_cast<const float(*)[32]>(vall + 32 * c), c, masked);
+        } else if constexpr (C::HCH == 1) {
+          float va[32];
+          ld_s(0, va);
+          tmem_ld_wait();
+          chunk(va, 0, masked);
+        } else {
+          float va[32], vb[32];
+          ld_s(0, va);
+    #pragma unroll C::UNR
+          for (int c = 0; c < C::HCH; c += 2) {
+            tmem_ld_wait();
+            ld_s(c + 1, vb);
+            chunk(va, c, masked);
+            tmem_ld_wait();
+            if (c + 2 < C::HCH) ld_s(c + 2, va);
+            chunk(vb, c + 1, masked);
+          }
+        }
+      };
+      if constexpr (BF) {
+        pass2(MaskedUnlessFull());
+      } else {
+        if (wfull) pass2(Unmasked());
+        else pass2(Masked());
+      }
+      if constexpr (C::ONE_LOAD) {
         if constexpr (C::TS) {
           // P8 over the first 16 of this thread's S columns (already read): keys 4w .. 4w+3
           // of its half in column c0 + w of S buffer sb
           tmem_st16_16x2<C::HC>(sc, ptm);
           tmem_st_wait();
-        }
-      } else if constexpr (C::HCH == 1) {
-        float va[32];
-        ld_s(0, va);
-        tmem_ld_wait();
-        chunk(va, 0);
-      } else {
-        float va[32], vb[32];
-        ld_s(0, va);
-  #pragma unroll C::UNR
-        for (int c = 0; c < C::HCH; c += 2) {
-          tmem_ld_wait();
-          ld_s(c + 1, vb);
-          chunk(va, c);
-          tmem_ld_wait();
-          if (c + 2 < C::HCH) ld_s(c + 2, va);
-          chunk(vb, c + 1);
         }
       }
       const float lsum = lsum2.x + lsum2.y;
