@@ -20,7 +20,9 @@
 //              warps 0-3, one whole row per lane.)
 //   next 4     correction warpgroup: promote the tile's P.V partial from TMEM into the
 //              FP32 accumulator O = O * alpha + O_tile (every tile, every N tiles, or
-//              never); epilogue O * v_s / l -> bf16 (l sums p * 448 on e4m3 layers).
+//              never); epilogue O * v_s / l -> bf16 (l sums p * 448 on e4m3 layers).  For
+//              full-attention e4m3 up to head_dim 128, O is held in these threads'
+//              registers (one row per thread).
 //   next       TMA, K tiles: each 16-token block is one box [16][row bytes] of the paged
 //              pool (4-D tensor map: row bytes, slot-in-block, KV head, block).
 //   next       allocates TMEM, issues S = Q8 K8^T with tcgen05.mma (kind::f8f6f4 for e4m3,
@@ -29,12 +31,19 @@
 //              the product's duration, so the two chains run on two warps).
 //   last       TMA, V tiles (a warp's copies go out one after another, so K and V have a
 //              warp each up to head_dim 128; at 256 the K warp copies both).
-// Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns: S [0, 128),
-// O_tile [TM_OT, TM_OT + OTB * DN) (two buffers up to head_dim 128, so that the P.V of
-// tile t overlaps the promotion of tile t-1), O [TM_OA, TM_OA + D); for head_dim 256 the
-// P.V product runs as two N = 128 halves through one O_tile.  Windowed e4m3 instantiations
-// up to head_dim 128 instead keep two S buffers and one O_tile, write P8 back into TMEM
-// over the S columns each thread has read, and take it from there as the A operand of P.V.
+// Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns, by instantiation:
+//   full-attention e4m3 up to head_dim 128: two S buffers [0, 256), two O_tile buffers
+//     from 256; O in the correction warps' registers (with promote_every 0 the tensor core
+//     accumulates into O_tile buffer 0).  The QK^T of tile t+1 then runs while the softmax
+//     works on tile t, and the P.V of tile t while tile t-1 is promoted.  The registers
+//     come from per-warpgroup budgets (setmaxnreg): softmax 120, correction 232, copy and
+//     MMA warps 40 per thread;
+//   windowed e4m3 up to head_dim 128: two S buffers and one O_tile; each thread writes
+//     its P8 back into TMEM over the S columns it has read, and P.V takes it from there
+//     as its A operand; O in TMEM;
+//   otherwise: one S buffer [0, 128), O_tile (two buffers on bf16 layers up to head_dim
+//     128), O in TMEM; at head_dim 256 the P.V product runs as two N = 128 halves through
+//     one O_tile.
 // Every wait is bounded in time; a timeout records FKV_FAULT_TIMEOUT, lets the CTA's
 // copies and MMAs drain and returns.
 #include <mutex>
@@ -68,6 +77,19 @@ FKV_DEV float max_tree(const float* v) {
   }
 }
 
+// The waits of this kernel take their timed path inline: the warpgroups of the e4m3
+// instantiations up to head_dim 128 run under different register budgets, which one
+// out-of-line function cannot serve (and inline waits measured faster at head_dim 256 too).
+FKV_DEV bool pf_wait(uint64_t* bar, uint32_t parity) { return wait_ns<true>(bar, parity); }
+FKV_DEV bool pf_wait_warp(uint64_t* bar, uint32_t parity) { return wait_warp<true>(bar, parity); }
+
+// An empty statement that "uses and redefines" 32 values: placed after the arithmetic on them,
+// it keeps the compiler from moving that arithmetic below the next TMEM load (which would
+// keep every chunk's loaded values live at once).
+FKV_DEV void pin32(float* v) {
+  asm volatile("" : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31]));
+}
+
 template <int D, bool BF, bool WIN>
 struct PrefillCfg {
   static constexpr int ES = BF ? 2 : 1;             // bytes per element (bf16 / e4m3)
@@ -97,12 +119,16 @@ struct PrefillCfg {
   // up to head_dim 128).  Both fill the 512 TMEM columns; with full attention the second
   // O_tile, which lets a P.V run while the previous tile is promoted, measured faster.
   static constexpr bool TS = !BF && D <= 128 && WIN;
-  static constexpr int SBUF = TS ? 2 : 1;           // S buffers in TMEM
+  // Full-attention e4m3 up to head_dim 128: two S buffers and two O_tile buffers fill the
+  // TMEM, and the FP32 accumulator O lives in the correction warps' registers (which take
+  // registers from the copy / MMA warpgroup through setmaxnreg).
+  static constexpr bool REGO = !BF && D <= 128 && !WIN;
+  static constexpr int SBUF = (TS || REGO) ? 2 : 1;  // S buffers in TMEM
   static constexpr int OTB = (!TS && D <= 128) ? 2 : 1;  // O_tile buffers in TMEM
   // unrolling of the softmax / correction chunk loops: full for head_dim <= 128 (the
   // softmax is the critical path there), none for 256 (code size of four warp roles)
   static constexpr int UNR = D <= 128 ? 4 : 1;
-  static constexpr bool ONE_LOAD = D <= 128;        // S row loaded once into registers
+  static constexpr bool ONE_LOAD = D <= 128 || !BF;  // S row loaded once into registers
   // softmax warps per S row: two on e4m3 layers (each half of the row's columns, so that
   // every SM quarter has two softmax warps to switch between); one on bf16 layers, whose
   // 2-byte tiles leave no shared memory for the half-row exchange
@@ -114,8 +140,15 @@ struct PrefillCfg {
   // stages) one warp copying both measured faster
   static constexpr int KVW = D <= 128 ? 2 : 1;
   static constexpr int THREADS = 32 * (SW + 6 + KVW);
-  static constexpr int TM_OT = 128 * SBUF, TM_OA = TM_OT + OTB * DN;
-  static constexpr int TM_COLS = (TM_OA + D) <= 256 ? 256 : 512;
+  // TMEM columns; with REGO, "O" in TMEM is O_tile buffer 0 (used only when the tensor
+  // core accumulates the whole contraction, promote_every 0)
+  static constexpr int TM_OT = 128 * SBUF, TM_OA = REGO ? TM_OT : TM_OT + OTB * DN;
+  static constexpr int TM_COLS = (TM_OT + OTB * DN + (REGO ? 0 : D)) <= 256 ? 256 : 512;
+  // register budgets per warpgroup with REGO (launch: 128 per thread, 512 threads): softmax
+  // warpgroups 120, the correction warpgroup 232 (144 at head_dim 64), the copy / MMA
+  // warpgroup the rest.  setmaxnreg.dec may only lower and .inc only raise a budget.
+  static constexpr int REG_LAUNCH = 128, REG_SOFT = 120, REG_CORR = D > 64 ? 232 : 144,
+                       REG_MISC = 4 * REG_LAUNCH - 2 * REG_SOFT - REG_CORR;
   // shared memory layout (bytes)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + TILE;
@@ -129,7 +162,14 @@ struct PrefillCfg {
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_QK = BF ? idesc_bf16_f32(128, BN, 0, 0) : idesc_e4m3_f32(128, BN, 0, 0);
   static constexpr uint32_t IDESC_PV = BF ? idesc_bf16_f32(128, EPS, 0, 1) : idesc_e4m3_f32(128, EPS, 0, 1);
-  static_assert(TM_OA + D <= 512, "TMEM budget");
+  static_assert(TM_OA + D <= 512 && TM_OT + OTB * DN <= 512, "TMEM budget");
+  static_assert(!REGO || (THREADS == 512 && 2 * REG_SOFT + REG_CORR + REG_MISC <= 4 * REG_LAUNCH),
+                "register budgets of the warpgroups");
+  static_assert(!REGO || (REG_SOFT <= REG_LAUNCH && REG_MISC <= REG_LAUNCH && REG_CORR >= REG_LAUNCH),
+                "budgets lowered by setmaxnreg.dec and raised by .inc");
+  static_assert(!REGO || (REG_SOFT % 8 == 0 && REG_CORR % 8 == 0 && REG_MISC % 8 == 0 && REG_MISC >= 24 &&
+                          REG_CORR <= 256),
+                "setmaxnreg counts: multiples of 8 in [24, 256]");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(!ONE_LOAD || BN == 128, "the one-load softmax holds a 128-column S row");
   static_assert(HC % 32 == 0 && (HCH % 2 == 0 || ONE_LOAD || HCH == 1), "softmax chunks");
@@ -243,6 +283,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
 
   if (warp < C::SW) {
     // ============================================================ softmax warps
+    if constexpr (C::REGO && C::REG_SOFT < C::REG_LAUNCH) regs_dec<C::REG_SOFT>();
     // SPLIT 1: warp w holds the 32 rows of its SM quarter (TMEM lanes 32 (w % 4) ..), one per
     // lane, all columns.  SPLIT 2: warp w holds 16 of them, 32 (w % 4) + 16 (w / 4) + (lane % 16),
     // lanes l and l + 16 each half of the row's columns (the 16x32bx2 TMEM load shape), so that
@@ -299,7 +340,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       // another warp's timeout is noticed every 8 tiles (every wait is bounded anyway)
       if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
       const int sb = t % C::SBUF;
-      if (!wait_warp(&s_full[sb], (t / C::SBUF) & 1)) { ok = false; break; }
+      if (!pf_wait_warp(&s_full[sb], (t / C::SBUF) & 1)) { ok = false; break; }
       tc_fence_after();
       // the P and alpha slots of tile t (freed by tile t-2's P.V and correction) are
       // normally free long before they are written: test them now without blocking, and
@@ -377,7 +418,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
       const float msafe = (mn == -INFINITY) ? 0.f : mn;
       // P tile t%2 is free once the P.V of tile t-2 completed
-      if (!C::TS && !__all_sync(0xffffffffu, p_ready) && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+      if (!C::TS && !__all_sync(0xffffffffu, p_ready) && !pf_wait_warp(&p_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
       uint8_t* P = sP + pb * C::PTILE;
       // pass 2: p = 2^(s*cst - m), its unrounded sum, and P8 = e4m3(p * 448) into the P tile;
       // the next chunk's TMEM load is in flight while the current one is processed
@@ -480,7 +521,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       m = mn;
       // alpha (the same in both halves) is written by half 0; its slot t%2 is free once the
       // correction warpgroup has read tile t-2's alpha
-      if (!__all_sync(0xffffffffu, a_ready) && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, a_ready) && !pf_wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
       if (hf == 0) sAlpha[pb * C::BM + i] = alpha;
       mbar_arrive_warp(&a_full[pb]);
       if constexpr (C::TS) tc_fence_before();
@@ -495,22 +536,107 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     mbar_arrive_warp(l_full);
   } else if (warp < C::SW + 4) {
     // ============================================================ correction warpgroup
+    if constexpr (C::REGO) regs_inc<C::REG_CORR>();  // O in registers
     const int i = threadIdx.x - 32 * C::SW;    // query row (TMEM lane i)
     const bool row_ok = i < rows;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - C::SW) * 32) << 16);
     int npv = 0;
     bool ok = true;
     const int pe = p.promote_every;
-    if (pe == 1) {
+    // REGO: the FP32 accumulator O of this row in registers (promote_every != 0)
+    float O[C::REGO ? D : 1];
+    if constexpr (C::REGO) {
+#pragma unroll
+      for (int j = 0; j < D; ++j) O[j] = 0.f;
+    }
+    if constexpr (C::REGO) {
+      if (pe == 1) {
+        // two-level accumulation every tile: O = O * alpha + O_tile(t), O_tile in buffer t % 2
+        // (tile 0 assigns O; a select per element instead costs the allocation dearly)
+        auto promote = [&](int t, auto first) -> bool {
+          if (!pf_wait_warp(&a_full[t & 1], (t >> 1) & 1)) return false;
+          const float alpha = sAlpha[(t & 1) * C::BM + i];
+          mbar_arrive_warp(&a_free[t & 1]);
+          const int ob = t & 1;
+          if (!pf_wait_warp(&o_full[ob], (t >> 1) & 1)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float ot[32];
+            tmem_ld32(lane_base + C::TM_OT + ob * C::DN + 32 * c, ot);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if constexpr (decltype(first)::value) O[32 * c + j] = ot[j];
+              else O[32 * c + j] = fmaf(O[32 * c + j], alpha, ot[j]);
+            }
+            pin32(O + 32 * c);
+          }
+          tc_fence_before();
+          mbar_arrive_warp(&o_free[ob]);
+          return true;
+        };
+        ok = n_t == 0 || promote(0, std::true_type());
+        for (int t = 1; ok && t < n_t; ++t) {
+          if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
+          ok = promote(t, std::false_type());
+        }
+      } else {
+        // the running sum in O_tile buffer 0, rescaled in place when a row's maximum moved;
+        // promoted into O every pe tiles (pe >= 2) or never (pe == 0: O stays in TMEM)
+        float A = 1.f;
+        for (int t = 0; t < n_t; ++t) {
+          if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
+          if (!pf_wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+          const float alpha = sAlpha[(t & 1) * C::BM + i];
+          mbar_arrive_warp(&a_free[t & 1]);
+          A *= alpha;
+          const bool start = pe == 0 ? t == 0 : (t % pe) == 0;
+          if (!start) {
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+              for (int c = 0; c < D / 32; ++c) {
+                float x[32];
+                tmem_ld32(lane_base + C::TM_OT + 32 * c, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] *= alpha;
+                tmem_st32(lane_base + C::TM_OT + 32 * c, x);
+              }
+              tmem_st_wait();
+            }
+            tc_fence_before();
+            mbar_arrive_warp(o_free);
+          }
+          if (!pf_wait_warp(o_full, t & 1)) { ok = false; break; }
+          tc_fence_after();
+          const bool last = pe != 0 && ((t + 1) % pe == 0 || t == n_t - 1);
+          if (last) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              float ot[32];
+              tmem_ld32(lane_base + C::TM_OT + 32 * c, ot);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) O[32 * c + j] = fmaf(O[32 * c + j], A, ot[j]);  // O starts at 0
+              pin32(O + 32 * c);
+            }
+            A = 1.f;
+            tc_fence_before();
+            mbar_arrive_warp(o_free);
+          }
+        }
+      }
+    } else if (pe == 1) {
       // two-level accumulation every tile: O = O * alpha + O_tile after each P.V
       for (int t = 0; t < n_t; ++t) {
         if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
-        if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+        if (!pf_wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
         const float alpha = sAlpha[(t & 1) * C::BM + i];
         mbar_arrive_warp(&a_free[t & 1]);
         for (int hn = 0; hn < C::NH; ++hn) {
           const int ob = npv % C::OTB;
-          if (!wait_warp(&o_full[ob], (npv / C::OTB) & 1)) { ok = false; break; }
+          if (!pf_wait_warp(&o_full[ob], (npv / C::OTB) & 1)) { ok = false; break; }
           ++npv;
           tc_fence_after();
 #pragma unroll C::UNR
@@ -544,7 +670,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       bool have_o = false;   // O holds promoted groups
       for (int t = 0; t < n_t; ++t) {
         if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
-        if (!wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+        if (!pf_wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
         const float alpha = sAlpha[(t & 1) * C::BM + i];
         mbar_arrive_warp(&a_free[t & 1]);
         A *= alpha;
@@ -566,7 +692,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
           tc_fence_before();
           mbar_arrive_warp(o_free);
         }
-        if (!wait_warp(o_full, t & 1)) { ok = false; break; }
+        if (!pf_wait_warp(o_full, t & 1)) { ok = false; break; }
         tc_fence_after();
         const bool last = pe != 0 && ((t + 1) % pe == 0 || t == n_t - 1);
         if (last) {
@@ -598,17 +724,14 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       *abort_s = 1;
     }
     // ---- epilogue: O * v_s / l -> bf16 (every lane loads; rows past the chunk do not store)
-    if (wait_warp(l_full, 0) && !abort_warp(abort_s)) {
+    if (pf_wait_warp(l_full, 0) && !abort_warp(abort_s)) {
       float l = sL[i];
       if constexpr (C::SPLIT == 2) l += sL[C::BM + i];  // the two halves' sums
       const float vs = BF ? 1.f : p.v_scale[p.per_head ? g : 0];
       const float f = (l > 0.f) ? vs / l : 0.f;  // l sums p * 448 on e4m3 layers
       __nv_bfloat16* dst = p.out + (static_cast<size_t>(r0 + q0 + i) * p.Hq + h) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float oa[32];
-        tmem_ld32(lane_base + C::TM_OA + 32 * c, oa);
-        tmem_ld_wait();
+      // 32 values of the row, columns 32 c .. 32 c + 31, scaled and stored as bf16
+      auto store32 = [&](int c, const float (&oa)[32]) {
         if (row_ok) {
           uint32_t w[16];
 #pragma unroll
@@ -620,9 +743,34 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) o4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
+      };
+      bool from_regs = false;
+      if constexpr (C::REGO) {
+        if (pe != 0) {
+          from_regs = true;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float oa[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) oa[j] = O[32 * c + j];
+            store32(c, oa);
+          }
+        }
+      }
+      if (!from_regs) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float oa[32];
+          tmem_ld32(lane_base + C::TM_OA + 32 * c, oa);
+          tmem_ld_wait();
+          store32(c, oa);
+        }
       }
     }
-  } else if (warp == C::SW + 4 || warp == C::SW + 7) {
+  } else {
+  // the copy and MMA-issue warpgroup needs few registers
+  if constexpr (C::REGO && C::REG_MISC < C::REG_LAUNCH) regs_dec<C::REG_MISC>();
+  if (warp == C::SW + 4 || warp == C::SW + 7) {
     // ============================================================ TMA producers
     // Up to head_dim 128 warp SW+4 copies the K tiles and warp SW+7 the V tiles: a warp's
     // copies go out one after another (about 100 cycles per 2 KiB box), so two warps halve
@@ -661,7 +809,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       for (int kk = 0; kk < KINDS; ++kk) {
         const int kind = kind0 + kk;
         uint64_t* full = kind ? v_full : k_full;
-        if (lane == 0 && use > 0) ok = wait_ns(kind ? &v_empty[st] : &k_empty[st], (use - 1) & 1);
+        if (lane == 0 && use > 0) ok = pf_wait(kind ? &v_empty[st] : &k_empty[st], (use - 1) & 1);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // the expected byte count is posted before any of the copies can complete
@@ -684,11 +832,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     // let every issued copy land before the CTA can exit
     if (lane == 0) {
       for (int s = 0; s < C::NS; ++s) {
-        if (last[0][s] >= 0) wait_ns(&k_full[s], last[0][s] & 1);
-        if (last[1][s] >= 0) wait_ns(&v_full[s], last[1][s] & 1);
+        if (last[0][s] >= 0) pf_wait(&k_full[s], last[0][s] & 1);
+        if (last[1][s] >= 0) pf_wait(&v_full[s], last[1][s] & 1);
       }
     }
-  } else if (warp < C::SW + 7) {
+  } else {
     // ============================================================ MMA issuers
     // Warp SW+5 issues S = Q8 K8^T, warp SW+6 O_tile = P8 V8.  A tcgen05.mma issue holds
     // its thread for about the product's execution time and a commit for tens of cycles, so
@@ -705,8 +853,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     // S(t) = Q8 K8^T into S buffer t % SBUF
     auto issue_qk = [&](int t) -> bool {
       const int st = t % C::NS, sb = t % C::SBUF;
-      if (!wait_warp(&k_full[st], (t / C::NS) & 1)) return false;
-      if (t >= C::SBUF && !wait_warp(&s_free[sb], ((t / C::SBUF) - 1) & 1)) return false;
+      if (!pf_wait_warp(&k_full[st], (t / C::NS) & 1)) return false;
+      if (t >= C::SBUF && !pf_wait_warp(&s_free[sb], ((t / C::SBUF) - 1) & 1)) return false;
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
@@ -747,8 +895,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     // O_tile = P8(t) V8(t), in NH products of N = DN
     auto issue_pv = [&](int t) -> bool {
       const int st = t % C::NS, pb = t & 1;
-      if (!wait_warp(&p_full[pb], (t >> 1) & 1)) return false;
-      if (!wait_warp(&v_full[st], (t / C::NS) & 1)) return false;
+      if (!pf_wait_warp(&p_full[pb], (t >> 1) & 1)) return false;
+      if (!pf_wait_warp(&v_full[st], (t / C::NS) & 1)) return false;
       // keys past the context may hold stale bytes (NaN codes): zero their V rows, since
       // 0 * NaN would poison the product even though their P is 0
       const int kbase = (tb + t) * C::BN;
@@ -769,7 +917,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
         for (int hn = 0; hn < C::NH; ++hn) {
           // O_tile buffer npv % OTB is free once the correction promoted pass npv - OTB
           const int ob = npv % C::OTB;
-          if (npv >= C::OTB && !wait_warp(&o_free[ob], ((npv / C::OTB) - 1) & 1)) return false;
+          if (npv >= C::OTB && !pf_wait_warp(&o_free[ob], ((npv / C::OTB) - 1) & 1)) return false;
           tc_fence_after();
           if (lane == 0) issue_pv_pass(st, pb, hn, tmem + C::TM_OT + ob * C::DN, true);
           if (lane == 0) umma_commit(&o_full[ob]);
@@ -779,7 +927,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       } else {
         // the running sum (O_tile, or O when never promoted) is ready once the correction
         // warpgroup has promoted or rescaled it for this tile
-        if (t > 0 && !wait_warp(o_free, (t - 1) & 1)) return false;
+        if (t > 0 && !pf_wait_warp(o_free, (t - 1) & 1)) return false;
         tc_fence_after();
         const int pe = p.promote_every;
         const bool fresh = pe == 0 ? t == 0 : (t % pe) == 0;
@@ -801,7 +949,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     bool ok = true;
     if (qk_warp) {
       // S(t+1) is computed while the softmax works on tile t (S is released once loaded)
-      ok = wait_warp(q_full, 0);
+      ok = pf_wait_warp(q_full, 0);
       for (int t = 0; ok && t < n_t; ++t) {
         if ((t & 7) == 7 && abort_warp(abort_s)) break;
         ok = issue_qk(t);
@@ -819,9 +967,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     // every MMA issued by either warp completes before TMEM is released
     if (lane == 0) {
       umma_commit(mma_done);
-      wait_ns(mma_done, 0);
+      pf_wait(mma_done, 0);
     }
     __syncwarp();
+  }
   }
   __syncthreads();
   if (warp == C::SW + 5) {
@@ -885,6 +1034,18 @@ cudaError_t launch_prefill_t(const PrefillParams& p, void* kc, void* vc, cudaStr
   auto kern = prefill_kernel<D, BF, WIN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  if constexpr (C::REGO) {
+    // the warpgroups' register budgets add up to the launch's 128 per thread: a kernel built
+    // with fewer would wait forever in setmaxnreg.inc, so it is never launched
+    static int regs = -1;
+    if (regs < 0) {
+      cudaFuncAttributes a;
+      e = cudaFuncGetAttributes(&a, kern);
+      if (e != cudaSuccess) return e;
+      regs = a.numRegs;
+    }
+    if (regs != C::REG_LAUNCH) return cudaErrorInvalidKernelImage;
+  }
   dim3 grid(p.n_qtiles, p.Hq, p.B);
   kern<<<grid, C::THREADS, C::SMEM, s>>>(p, tmk, tmv);
   return cudaGetLastError();

@@ -22,6 +22,14 @@ FKV_DEV void tmem_relinquish() {
 FKV_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
+// Per-warpgroup register budgets (setmaxnreg): every warp of the warpgroup executes the same
+// instruction.  An increase takes registers that other warpgroups of the CTA have released,
+// so the budgets of all warpgroups must add up to no more than the CTA was launched with.
+template <int N>
+FKV_DEV void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+FKV_DEV void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+
 FKV_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 FKV_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -183,31 +191,38 @@ FKV_DEV void mbar_arrive_warp(uint64_t* bar) {
 // rather than spinning.
 constexpr uint64_t kPipeWaitNs = 200000000ull;  // 200 ms per wait
 
-// The timed part of a wait lives out of line: an inlined wait is then one try_wait and a
-// branch.  The MMA and TMA warps pass through many waits per tile, and code that a warp
-// runs once per tile has to be fetched into the instruction cache again every tile (the
-// softmax warps' unrolled loops on the same SM quarter displace it), so their code size
-// is their speed.  A bound below the 1 ms suspend hint polls without suspending, so that
-// it can run out within its own length.
-static __device__ __noinline__ bool wait_ns_timed(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+// The timed part of a wait.  A bound below the 1 ms suspend hint polls without suspending,
+// so that it can run out within its own length.
+FKV_DEV bool wait_ns_timed_body(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (limit_ns >= 1000000u ? mbar_try_wait_hint(bar, parity, 1000000u) : mbar_test_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
+// The same out of line: an inlined wait is then one try_wait and a branch.  In the decode,
+// whose MMA and TMA warps pass through many waits per tile, code that a warp runs once per
+// tile has to be fetched into the instruction cache again every tile, so their code size
+// is their speed.  (A kernel whose warpgroups run under different register budgets takes
+// the inline form: one out-of-line function cannot serve callers of different budgets.)
+static __device__ __noinline__ bool wait_ns_timed(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return wait_ns_timed_body(bar, parity, limit_ns);
+}
 
 // mbarrier.try_wait may itself suspend the thread until the phase completes (for a
 // system-dependent time), so a bound below the suspend hint tests without waiting.
+template <bool INLINE_SLOW = false>
 FKV_DEV bool wait_ns(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kPipeWaitNs) {
   if (limit_ns >= 1000000u ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity)) return true;
-  return wait_ns_timed(bar, parity, limit_ns);
+  if constexpr (INLINE_SLOW) return wait_ns_timed_body(bar, parity, limit_ns);
+  else return wait_ns_timed(bar, parity, limit_ns);
 }
 
 // Warp-uniform forms: tcgen05.ld / st are warp-collective, so every lane of a warp must
 // take the same branch around them.
+template <bool INLINE_SLOW = false>
 FKV_DEV bool wait_warp(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kPipeWaitNs) {
-  const bool ok = wait_ns(bar, parity, limit_ns);
+  const bool ok = wait_ns<INLINE_SLOW>(bar, parity, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 FKV_DEV bool abort_warp(volatile int* flag) { return __any_sync(0xffffffffu, *flag != 0); }
