@@ -808,7 +808,7 @@ def run_ours(args):
     prefill = None
     if not args.no_prefill:
         torch.cuda.synchronize()
-        prefill = (time_prefill(f, 5, device, iters=min(args.steps, 10), warmup=3, promote_every=(1, 0)) +
+        prefill = (time_prefill(f, 5, device, iters=min(args.steps, 10), warmup=3, promote_every=(1, 4, 0)) +
                    time_prefill(f, 4, device, iters=min(args.steps, 10), warmup=3, promote_every=(1, 4, 0)))
         torch.cuda.synchronize()
 

@@ -8,7 +8,7 @@
 // scheme (section "大 Head Dimension 的限制").
 //
 // CTA = (128-query tile, query head h, sequence b); 16 warps (12 on bf16 layers; one fewer
-// at head_dim 256):
+// on bf16 and windowed layers at head_dim 256):
 //   warps 0-7  softmax: quantise the Q tile to e4m3 into shared memory (bf16 layers copy
 //              it); then per key tile warp w owns 16 query rows of its SM quarter (TMEM
 //              lanes 32 (w % 4) + 16 (w / 4) ..), lanes l and l + 16 each half of a row's
@@ -21,8 +21,8 @@
 //   next 4     correction warpgroup: promote the tile's P.V partial from TMEM into the
 //              FP32 accumulator O = O * alpha + O_tile (every tile, every N tiles, or
 //              never); epilogue O * v_s / l -> bf16 (l sums p * 448 on e4m3 layers).  For
-//              full-attention e4m3 up to head_dim 128, O is held in these threads'
-//              registers (one row per thread).
+//              full-attention e4m3, O is held in these threads' registers (one row per
+//              thread; at head_dim 256 its first 128 columns, the rest in TMEM).
 //   next       TMA, K tiles: each 16-token block is one box [16][row bytes] of the paged
 //              pool (4-D tensor map: row bytes, slot-in-block, KV head, block).
 //   next       allocates TMEM, issues S = Q8 K8^T with tcgen05.mma (kind::f8f6f4 for e4m3,
@@ -30,7 +30,8 @@
 //   next       issues O_tile = P8 V8 the same way (an MMA issue holds its thread for about
 //              the product's duration, so the two chains run on two warps).
 //   last       TMA, V tiles (a warp's copies go out one after another, so K and V have a
-//              warp each up to head_dim 128; at 256 the K warp copies both).
+//              warp each, except bf16 and windowed layers at head_dim 256, where the K
+//              warp copies both).
 // Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns, by instantiation:
 //   full-attention e4m3 up to head_dim 128: two S buffers [0, 256), two O_tile buffers
 //     from 256; O in the correction warps' registers (with promote_every 0 the tensor core
@@ -38,12 +39,17 @@
 //     works on tile t, and the P.V of tile t while tile t-1 is promoted.  The registers
 //     come from per-warpgroup budgets (setmaxnreg): softmax 120, correction 232, copy and
 //     MMA warps 40 per thread;
+//   full-attention e4m3 at head_dim 256: one S buffer [0, 128), two 128-column O_tile
+//     buffers [128, 384) that take the two N = 128 halves of each P.V product, and the
+//     second half of O at [384, 512); the first half of O in registers.  Each half is
+//     promoted while the tensor core works on the other.  With promote_every >= 2 or 0
+//     the running sum spans both O_tile buffers;
 //   windowed e4m3 up to head_dim 128: two S buffers and one O_tile; each thread writes
 //     its P8 back into TMEM over the S columns it has read, and P.V takes it from there
 //     as its A operand; O in TMEM;
-//   otherwise: one S buffer [0, 128), O_tile (two buffers on bf16 layers up to head_dim
-//     128), O in TMEM; at head_dim 256 the P.V product runs as two N = 128 halves through
-//     one O_tile.
+//   otherwise (bf16 layers; windows at head_dim 256): one S buffer [0, 128), O_tile (two
+//     buffers up to head_dim 128), O in TMEM; at head_dim 256 the P.V product runs as two
+//     N = 128 halves through one O_tile.
 // Every wait is bounded in time; a timeout records FKV_FAULT_TIMEOUT, lets the CTA's
 // copies and MMAs drain and returns.
 #include <mutex>
@@ -115,16 +121,14 @@ struct PrefillCfg {
   static constexpr int KSTEP = 32 / ES;             // keys (P columns) of one P.V k-step (32 bytes)
   // Windowed e4m3 up to head_dim 128: each thread writes its P8 back into TMEM over the S
   // columns it has read, and P.V takes P8 from there as its A operand (two S buffers, one
-  // O_tile).  Otherwise P goes through shared memory (one S buffer, O_tile double-buffered
-  // up to head_dim 128).  Both fill the 512 TMEM columns; with full attention the second
-  // O_tile, which lets a P.V run while the previous tile is promoted, measured faster.
+  // O_tile).  Otherwise P goes through shared memory.
   static constexpr bool TS = !BF && D <= 128 && WIN;
-  // Full-attention e4m3 up to head_dim 128: two S buffers and two O_tile buffers fill the
-  // TMEM, and the FP32 accumulator O lives in the correction warps' registers (which take
-  // registers from the copy / MMA warpgroup through setmaxnreg).
-  static constexpr bool REGO = !BF && D <= 128 && !WIN;
-  static constexpr int SBUF = (TS || REGO) ? 2 : 1;  // S buffers in TMEM
-  static constexpr int OTB = (!TS && D <= 128) ? 2 : 1;  // O_tile buffers in TMEM
+  // Full-attention e4m3: the FP32 accumulator O lives in the correction warps' registers
+  // (at head_dim 256 its first half), which take registers from the other warpgroups through
+  // setmaxnreg; the freed TMEM holds two O_tile buffers (and two S buffers up to head_dim 128).
+  static constexpr bool REGO = !BF && !WIN;
+  static constexpr int SBUF = (TS || (REGO && D <= 128)) ? 2 : 1;  // S buffers in TMEM
+  static constexpr int OTB = (!TS && (D <= 128 || REGO)) ? 2 : 1;  // O_tile buffers in TMEM
   // unrolling of the softmax / correction chunk loops: full for head_dim <= 128 (the
   // softmax is the critical path there), none for 256 (code size of four warp roles)
   static constexpr int UNR = D <= 128 ? 4 : 1;
@@ -136,14 +140,16 @@ struct PrefillCfg {
   static constexpr int HC = BN / SPLIT;             // columns of a softmax thread
   static constexpr int HCH = HC / 32;               // its 32-column chunks
   static constexpr int SW = 4 * SPLIT;              // softmax warps (then 4 correction, K copies, 2 MMA, V copies)
-  // TMA warps: K and V apart up to head_dim 128; at head_dim 256 (two boxes per block, two
-  // stages) one warp copying both measured faster
-  static constexpr int KVW = D <= 128 ? 2 : 1;
+  // TMA warps: K and V apart, except on bf16 and windowed layers at head_dim 256, whose
+  // kernels (two boxes per block, two stages) measured faster with one warp copying both
+  static constexpr int KVW = (D <= 128 || REGO) ? 2 : 1;
   static constexpr int THREADS = 32 * (SW + 6 + KVW);
   // TMEM columns; with REGO, "O" in TMEM is O_tile buffer 0 (used only when the tensor
   // core accumulates the whole contraction, promote_every 0)
   static constexpr int TM_OT = 128 * SBUF, TM_OA = REGO ? TM_OT : TM_OT + OTB * DN;
-  static constexpr int TM_COLS = (TM_OT + OTB * DN + (REGO ? 0 : D)) <= 256 ? 256 : 512;
+  // REGO: O columns [0, DR) in registers, [DR, D) (head_dim 256) in TMEM from TM_OH
+  static constexpr int DR = REGO ? DN : 1, TM_OH = TM_OT + OTB * DN;
+  static constexpr int TM_COLS = (TM_OT + OTB * DN + (REGO ? D - DN : D)) <= 256 ? 256 : 512;
   // register budgets per warpgroup with REGO (launch: 128 per thread, 512 threads): softmax
   // warpgroups 120, the correction warpgroup 232 (144 at head_dim 64), the copy / MMA
   // warpgroup the rest.  setmaxnreg.dec may only lower and .inc only raise a budget.
@@ -162,7 +168,7 @@ struct PrefillCfg {
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_QK = BF ? idesc_bf16_f32(128, BN, 0, 0) : idesc_e4m3_f32(128, BN, 0, 0);
   static constexpr uint32_t IDESC_PV = BF ? idesc_bf16_f32(128, EPS, 0, 1) : idesc_e4m3_f32(128, EPS, 0, 1);
-  static_assert(TM_OA + D <= 512 && TM_OT + OTB * DN <= 512, "TMEM budget");
+  static_assert(TM_OA + D <= 512 && TM_OT + OTB * DN <= 512 && (!REGO || TM_OH + D - DN <= 512), "TMEM budget");
   static_assert(!REGO || (THREADS == 512 && 2 * REG_SOFT + REG_CORR + REG_MISC <= 4 * REG_LAUNCH),
                 "register budgets of the warpgroups");
   static_assert(!REGO || (REG_SOFT <= REG_LAUNCH && REG_MISC <= REG_LAUNCH && REG_CORR >= REG_LAUNCH),
@@ -543,37 +549,63 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     int npv = 0;
     bool ok = true;
     const int pe = p.promote_every;
-    // REGO: the FP32 accumulator O of this row in registers (promote_every != 0)
-    float O[C::REGO ? D : 1];
-    if constexpr (C::REGO) {
+    // REGO: the FP32 accumulator O of this row: columns [0, DR) in registers, the rest
+    // (head_dim 256) in TMEM at TM_OH
+    float O[C::DR];
 #pragma unroll
-      for (int j = 0; j < D; ++j) O[j] = 0.f;
-    }
+    for (int j = 0; j < C::DR; ++j) O[j] = 0.f;
+    // the promotion of one O_tile pass into O: hn 0 into the registers, hn 1 into TMEM
+    // (first: O takes the partial itself)
+    auto promote_pass = [&](uint32_t src, int hn, float alpha, auto first) {
+      if (hn == 0) {
+#pragma unroll
+        for (int c = 0; c < C::DN / 32; ++c) {
+          float ot[32];
+          tmem_ld32(src + 32 * c, ot);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if constexpr (decltype(first)::value) O[32 * c + j] = ot[j];
+            else O[32 * c + j] = fmaf(O[32 * c + j], alpha, ot[j]);
+          }
+          pin32(O + 32 * c);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < C::DN / 32; ++c) {
+          float ot[32], oh[32];
+          const uint32_t dst = lane_base + C::TM_OH + (hn - 1) * C::DN + 32 * c;
+          tmem_ld32(src + 32 * c, ot);
+          if constexpr (!decltype(first)::value) tmem_ld32(dst, oh);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if constexpr (decltype(first)::value) oh[j] = ot[j];
+            else oh[j] = fmaf(oh[j], alpha, ot[j]);
+          }
+          tmem_st32(dst, oh);
+        }
+        tmem_st_wait();
+      }
+    };
     if constexpr (C::REGO) {
       if (pe == 1) {
-        // two-level accumulation every tile: O = O * alpha + O_tile(t), O_tile in buffer t % 2
-        // (tile 0 assigns O; a select per element instead costs the allocation dearly)
+        // two-level accumulation every tile: O = O * alpha + O_tile(t); pass hn of tile t is
+        // P.V product NH t + hn, in O_tile buffer (NH t + hn) % 2 (tile 0 assigns O: a
+        // select per element instead costs the register allocation dearly)
         auto promote = [&](int t, auto first) -> bool {
           if (!pf_wait_warp(&a_full[t & 1], (t >> 1) & 1)) return false;
           const float alpha = sAlpha[(t & 1) * C::BM + i];
           mbar_arrive_warp(&a_free[t & 1]);
-          const int ob = t & 1;
-          if (!pf_wait_warp(&o_full[ob], (t >> 1) & 1)) return false;
-          tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float ot[32];
-            tmem_ld32(lane_base + C::TM_OT + ob * C::DN + 32 * c, ot);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if constexpr (decltype(first)::value) O[32 * c + j] = ot[j];
-              else O[32 * c + j] = fmaf(O[32 * c + j], alpha, ot[j]);
-            }
-            pin32(O + 32 * c);
+          for (int hn = 0; hn < C::NH; ++hn) {
+            const int n = C::NH * t + hn, ob = n & 1;
+            if (!pf_wait_warp(&o_full[ob], (n >> 1) & 1)) return false;
+            tc_fence_after();
+            promote_pass(lane_base + C::TM_OT + ob * C::DN, hn, alpha, first);
+            tc_fence_before();
+            mbar_arrive_warp(&o_free[ob]);
           }
-          tc_fence_before();
-          mbar_arrive_warp(&o_free[ob]);
           return true;
         };
         ok = n_t == 0 || promote(0, std::true_type());
@@ -582,9 +614,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
           ok = promote(t, std::false_type());
         }
       } else {
-        // the running sum in O_tile buffer 0, rescaled in place when a row's maximum moved;
-        // promoted into O every pe tiles (pe >= 2) or never (pe == 0: O stays in TMEM)
+        // the running sum over all D columns from TM_OT (O_tile buffer 0, or both buffers at
+        // head_dim 256), rescaled in place when a row's maximum moved; promoted into O
+        // every pe tiles (pe >= 2) or never (pe == 0: O stays in TMEM)
         float A = 1.f;
+        bool first = true;
         for (int t = 0; t < n_t; ++t) {
           if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
           if (!pf_wait_warp(&a_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
@@ -613,14 +647,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
           const bool last = pe != 0 && ((t + 1) % pe == 0 || t == n_t - 1);
           if (last) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              float ot[32];
-              tmem_ld32(lane_base + C::TM_OT + 32 * c, ot);
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) O[32 * c + j] = fmaf(O[32 * c + j], A, ot[j]);  // O starts at 0
-              pin32(O + 32 * c);
+            for (int hn = 0; hn < C::NH; ++hn) {
+              if (first) promote_pass(lane_base + C::TM_OT + hn * C::DN, hn, A, std::true_type());
+              else promote_pass(lane_base + C::TM_OT + hn * C::DN, hn, A, std::false_type());
             }
+            first = false;
             A = 1.f;
             tc_fence_before();
             mbar_arrive_warp(o_free);
@@ -749,10 +780,17 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
         if (pe != 0) {
           from_regs = true;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < C::DR / 32; ++c) {
             float oa[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) oa[j] = O[32 * c + j];
+            store32(c, oa);
+          }
+#pragma unroll 1
+          for (int c = C::DR / 32; c < D / 32; ++c) {
+            float oa[32];
+            tmem_ld32(lane_base + C::TM_OH + 32 * c - C::DR, oa);
+            tmem_ld_wait();
             store32(c, oa);
           }
         }
@@ -772,9 +810,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
   if constexpr (C::REGO && C::REG_MISC < C::REG_LAUNCH) regs_dec<C::REG_MISC>();
   if (warp == C::SW + 4 || warp == C::SW + 7) {
     // ============================================================ TMA producers
-    // Up to head_dim 128 warp SW+4 copies the K tiles and warp SW+7 the V tiles: a warp's
-    // copies go out one after another (about 100 cycles per 2 KiB box), so two warps halve
-    // the time a tile's sixteen copies take.  At head_dim 256 warp SW+4 copies both.  Lane
+    // Warp SW+4 copies the K tiles and warp SW+7 the V tiles: a warp's copies go out one
+    // after another (about 100 cycles per 2 KiB box), so two warps halve the time a tile's
+    // copies take.  On bf16 and windowed layers at head_dim 256 warp SW+4 copies both.  Lane
     // j < NBLK copies the tile's j-th 16-token block; the block ids of tile t+1 are read
     // while tile t's copies are issued.
     const int kind0 = warp == C::SW + 7 ? 1 : 0;  // 0: K, 1: V
@@ -934,7 +972,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
         if (lane == 0) {
 #pragma unroll
           for (int hn = 0; hn < C::NH; ++hn)
-            issue_pv_pass(st, pb, hn, pe == 0 ? tmem + C::TM_OA + hn * C::DN : tmem + C::TM_OT, fresh);
+            issue_pv_pass(st, pb, hn,
+                          pe == 0 ? tmem + C::TM_OA + hn * C::DN : tmem + C::TM_OT + (C::REGO ? hn * C::DN : 0),
+                          fresh);
           umma_commit(o_full);
         }
         __syncwarp();

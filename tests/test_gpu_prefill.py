@@ -70,7 +70,8 @@ def test_prefill_small_parity(D, Hq, Hkv, T_list, Lq_list, gran, causal):
     assert_close(got, ref, what=f"D={D} Hq={Hq} Hkv={Hkv} T={T_list} Lq={Lq_list} causal={causal}")
 
 
-@pytest.mark.parametrize("D,promote_every", [(128, 0), (128, 2), (128, 3), (64, 4), (64, 0), (256, 0)])
+@pytest.mark.parametrize("D,promote_every", [(128, 0), (128, 2), (128, 3), (64, 4), (64, 0), (256, 0), (256, 2),
+                                             (256, 3)])
 def test_prefill_promote_every_variants(D, promote_every):
     """The tensor core accumulating N tiles (or the whole contraction) before promotion
     computes the same attention; the oracle is the same, only rounding differs."""
@@ -160,7 +161,7 @@ def _check_promote_variants(outs, ref, what):
 
 def test_workload5_prefill_d256_sampled():
     """head_dim 256, 4 x 32768 causal, per-head scales: sampled rows of every head, for
-    two-level accumulation every tile (1) and none (0)."""
+    two-level accumulation every tile (1), every 4 tiles (4) and none (0)."""
     w = synth.WORKLOADS[5]
     data = synth.prefill_data(w, device="cuda")
     ctx = np.full(w.batch, w.seq_len, np.int32)
@@ -171,7 +172,7 @@ def test_workload5_prefill_d256_sampled():
     cu = np.arange(w.batch + 1, dtype=np.int32) * w.seq_len
     rows = _sample_rows(cu, 12, np.random.default_rng(5))
     outs = {}
-    for pe in (1, 0):
+    for pe in (1, 4, 0):
         out = f.fp8_prefill_attn(data.q, to_dev(cu), w.seq_len, cache, to_dev(table), to_dev(ctx), data.q_scale,
                                  data.k_scale, data.v_scale, f.SCALE_PER_HEAD, causal=True, promote_every=pe)
         outs[pe] = out.float().cpu().numpy()[rows]
