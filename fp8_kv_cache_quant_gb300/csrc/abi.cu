@@ -329,8 +329,8 @@ fkv_status fp8_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int32_t 
   fkv_status st = FKV_OK;
   const bool bf16 = layer_is_bf16(layer, skip_layer_mask, num_layers, &st);
   if (st != FKV_OK) return st;
-  // head_dim 256 bf16 and windowed layers: TMEM holds one 128-column O_tile
-  if (promote_every >= 2 && cache.head_dim > 128 && (bf16 || window > 0)) return FKV_UNSUPPORTED;
+  // bf16 layers at head_dim 256: TMEM holds one 128-column O_tile
+  if (promote_every >= 2 && cache.head_dim > 128 && bf16) return FKV_UNSUPPORTED;
   if (!bf16 && cache.kv_format == FKV_KV_E5M2) return FKV_UNSUPPORTED;  // e5m2 layers: decode only
   if (batch > 65535 || num_q_heads > 65535) return FKV_UNSUPPORTED;
   if (batch == 0 || max_q_len == 0) return FKV_OK;

@@ -8,7 +8,7 @@
 // scheme (section "大 Head Dimension 的限制").
 //
 // CTA = (128-query tile, query head h, sequence b); 16 warps (12 on bf16 layers; one fewer
-// on bf16 and windowed layers at head_dim 256):
+// on bf16 layers at head_dim 256):
 //   warps 0-7  softmax: quantise the Q tile to e4m3 into shared memory (bf16 layers copy
 //              it); then per key tile warp w owns 16 query rows of its SM quarter (TMEM
 //              lanes 32 (w % 4) + 16 (w / 4) ..), lanes l and l + 16 each half of a row's
@@ -20,9 +20,10 @@
 //              warps 0-3, one whole row per lane.)
 //   next 4     correction warpgroup: promote the tile's P.V partial from TMEM into the
 //              FP32 accumulator O = O * alpha + O_tile (every tile, every N tiles, or
-//              never); epilogue O * v_s / l -> bf16 (l sums p * 448 on e4m3 layers).  For
-//              full-attention e4m3, O is held in these threads' registers (one row per
-//              thread; at head_dim 256 its first 128 columns, the rest in TMEM).
+//              never); epilogue O * v_s / l -> bf16 (l sums p * 448 on e4m3 layers).  On
+//              e4m3 layers (but windowed ones up to head_dim 128) O is held in these
+//              threads' registers (one row per thread; at head_dim 256 its first 128
+//              columns, the rest in TMEM).
 //   next       TMA, K tiles: each 16-token block is one box [16][row bytes] of the paged
 //              pool (4-D tensor map: row bytes, slot-in-block, KV head, block).
 //   next       allocates TMEM, issues S = Q8 K8^T with tcgen05.mma (kind::f8f6f4 for e4m3,
@@ -30,8 +31,8 @@
 //   next       issues O_tile = P8 V8 the same way (an MMA issue holds its thread for about
 //              the product's duration, so the two chains run on two warps).
 //   last       TMA, V tiles (a warp's copies go out one after another, so K and V have a
-//              warp each, except bf16 and windowed layers at head_dim 256, where the K
-//              warp copies both).
+//              warp each, except bf16 layers at head_dim 256, where the K warp copies
+//              both).
 // Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns, by instantiation:
 //   full-attention e4m3 up to head_dim 128: two S buffers [0, 256), two O_tile buffers
 //     from 256; O in the correction warps' registers (with promote_every 0 the tensor core
@@ -39,7 +40,7 @@
 //     works on tile t, and the P.V of tile t while tile t-1 is promoted.  The registers
 //     come from per-warpgroup budgets (setmaxnreg): softmax 120, correction 232, copy and
 //     MMA warps 40 per thread;
-//   full-attention e4m3 at head_dim 256: one S buffer [0, 128), two 128-column O_tile
+//   e4m3 at head_dim 256 (full or windowed): one S buffer [0, 128), two 128-column O_tile
 //     buffers [128, 384) that take the two N = 128 halves of each P.V product, and the
 //     second half of O at [384, 512); the first half of O in registers.  Each half is
 //     promoted while the tensor core works on the other.  With promote_every >= 2 or 0
@@ -47,9 +48,8 @@
 //   windowed e4m3 up to head_dim 128: two S buffers and one O_tile; each thread writes
 //     its P8 back into TMEM over the S columns it has read, and P.V takes it from there
 //     as its A operand; O in TMEM;
-//   otherwise (bf16 layers; windows at head_dim 256): one S buffer [0, 128), O_tile (two
-//     buffers up to head_dim 128), O in TMEM; at head_dim 256 the P.V product runs as two
-//     N = 128 halves through one O_tile.
+//   bf16 layers: one S buffer [0, 128), O_tile (two buffers up to head_dim 128), O in
+//     TMEM; at head_dim 256 the P.V product runs as two N = 128 halves through one O_tile.
 // Every wait is bounded in time; a timeout records FKV_FAULT_TIMEOUT, lets the CTA's
 // copies and MMAs drain and returns.
 #include <mutex>
@@ -123,10 +123,12 @@ struct PrefillCfg {
   // columns it has read, and P.V takes P8 from there as its A operand (two S buffers, one
   // O_tile).  Otherwise P goes through shared memory.
   static constexpr bool TS = !BF && D <= 128 && WIN;
-  // Full-attention e4m3: the FP32 accumulator O lives in the correction warps' registers
-  // (at head_dim 256 its first half), which take registers from the other warpgroups through
-  // setmaxnreg; the freed TMEM holds two O_tile buffers (and two S buffers up to head_dim 128).
-  static constexpr bool REGO = !BF && !WIN;
+  // Full-attention e4m3, and windowed e4m3 at head_dim 256: the FP32 accumulator O lives in
+  // the correction warps' registers (at head_dim 256 its first half), which take registers
+  // from the other warpgroups through setmaxnreg; the freed TMEM holds two O_tile buffers
+  // (and two S buffers up to head_dim 128).  (Windowed up to head_dim 128, TS measured 2 %
+  // faster.)
+  static constexpr bool REGO = !BF && !TS;
   static constexpr int SBUF = (TS || (REGO && D <= 128)) ? 2 : 1;  // S buffers in TMEM
   static constexpr int OTB = (!TS && (D <= 128 || REGO)) ? 2 : 1;  // O_tile buffers in TMEM
   // unrolling of the softmax / correction chunk loops: full for head_dim <= 128 (the
@@ -140,8 +142,8 @@ struct PrefillCfg {
   static constexpr int HC = BN / SPLIT;             // columns of a softmax thread
   static constexpr int HCH = HC / 32;               // its 32-column chunks
   static constexpr int SW = 4 * SPLIT;              // softmax warps (then 4 correction, K copies, 2 MMA, V copies)
-  // TMA warps: K and V apart, except on bf16 and windowed layers at head_dim 256, whose
-  // kernels (two boxes per block, two stages) measured faster with one warp copying both
+  // TMA warps: K and V apart, except on bf16 layers at head_dim 256, whose kernel (two boxes
+  // per block, two stages) measured faster with one warp copying both
   static constexpr int KVW = (D <= 128 || REGO) ? 2 : 1;
   static constexpr int THREADS = 32 * (SW + 6 + KVW);
   // TMEM columns; with REGO, "O" in TMEM is O_tile buffer 0 (used only when the tensor
@@ -812,7 +814,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     // ============================================================ TMA producers
     // Warp SW+4 copies the K tiles and warp SW+7 the V tiles: a warp's copies go out one
     // after another (about 100 cycles per 2 KiB box), so two warps halve the time a tile's
-    // copies take.  On bf16 and windowed layers at head_dim 256 warp SW+4 copies both.  Lane
+    // copies take.  On bf16 layers at head_dim 256 warp SW+4 copies both.  Lane
     // j < NBLK copies the tile's j-th 16-token block; the block ids of tile t+1 are read
     // while tile t's copies are issued.
     const int kind0 = warp == C::SW + 7 ? 1 : 0;  // 0: K, 1: V

@@ -343,7 +343,7 @@ int32_t fkv_prefill_block_n(int32_t head_dim);
  *   promote_every 1: promote each tile's P.V partial into the FP32 accumulator (two-level
  *                 accumulation, the default); N >= 2: let the tensor core accumulate N tiles
  *                 (rescaled in place when a row's maximum moves) before promoting (at
- *                 head_dim 256 on full-attention e4m3 layers only, else FKV_UNSUPPORTED);
+ *                 head_dim 256 on e4m3 layers only, else FKV_UNSUPPORTED);
  *                 0: never promote — the tensor core accumulates
  *                 the whole contraction (the blog's "大 Head Dimension 的限制": accumulate
  *                 every N steps, or disable two-level accumulation); negative: FKV_INVALID_ARG

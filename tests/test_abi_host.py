@@ -188,14 +188,13 @@ def test_prefill_validation(lib):
     assert pre(p, p, 0, 8, 16, _cache(), p, 4, p, None, None, None, 0, 0.0, 1, 0, 1, 0, mask, 1, p, None,
                None) == f.OK
     assert f.fkv_prefill_block_n(128) == 128 and f.fkv_prefill_block_n(100) == 0
-    # promote_every: negative is invalid; N >= 2 at head_dim 256 runs on full-attention e4m3
-    # layers only (bf16 and windowed layers keep one 128-column O_tile there)
+    # promote_every: negative is invalid; N >= 2 at head_dim 256 runs on e4m3 layers only
+    # (bf16 layers keep one 128-column O_tile there)
     assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, 0, -1, 0, None, 0, p, None, None) == f.INVALID_ARG
-    assert pre(p, p, 1, 8, 16, _cache(D=256), p, 4, p, p, p, p, 0, 0.0, 1, 64, 2, 0, None, 0, p, None,
-               None) == f.UNSUPPORTED
     assert pre(p, p, 1, 8, 16, _cache(D=256), p, 4, p, None, None, None, 0, 0.0, 1, 0, 2, 0, mask, 1, p, None,
                None) == f.UNSUPPORTED
     assert pre(p, p, 0, 8, 16, _cache(D=256), p, 4, p, p, p, p, 0, 0.0, 1, 0, 2, 0, None, 0, p, None, None) == f.OK
+    assert pre(p, p, 0, 8, 16, _cache(D=256), p, 4, p, p, p, p, 0, 0.0, 1, 64, 2, 0, None, 0, p, None, None) == f.OK
     # a sliding window is causal: negative is invalid, non-causal is unsupported
     assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 1, -1, 1, 0, None, 0, p, None, None) == f.INVALID_ARG
     assert pre(p, p, 1, 8, 16, _cache(), p, 4, p, p, p, p, 0, 0.0, 0, 64, 1, 0, None, 0, p, None, None) == f.UNSUPPORTED

@@ -104,7 +104,8 @@ def test_prefill_bf16_skip_layer_parity(D, Hq, Hkv, T_list, Lq_list, gran, causa
 
 @pytest.mark.parametrize("D,bf16,window,promote_every", [
     (128, False, 1, 1), (128, False, 100, 1), (128, False, 128, 1), (128, False, 300, 1), (128, False, 5000, 1),
-    (64, False, 257, 1), (256, False, 200, 1), (256, False, 200, 0), (128, False, 300, 0), (64, False, 77, 3),
+    (64, False, 257, 1), (256, False, 200, 1), (256, False, 200, 0), (256, False, 333, 2), (256, False, 1, 1),
+    (128, False, 300, 0), (64, False, 77, 3),
     (128, True, 1, 1), (128, True, 300, 1), (64, True, 129, 1), (128, True, 250, 0),
     (256, True, 1, 1), (256, True, 65, 1), (256, True, 512, 0),
 ])
