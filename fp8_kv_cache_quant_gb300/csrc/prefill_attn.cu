@@ -21,9 +21,8 @@
 //   next 4     correction warpgroup: promote the tile's P.V partial from TMEM into the
 //              FP32 accumulator O = O * alpha + O_tile (every tile, every N tiles, or
 //              never); epilogue O * v_s / l -> bf16 (l sums p * 448 on e4m3 layers).  On
-//              e4m3 layers (but windowed ones up to head_dim 128) O is held in these
-//              threads' registers (one row per thread; at head_dim 256 its first 128
-//              columns, the rest in TMEM).
+//              e4m3 layers O is held in these threads' registers (one row per thread; at
+//              head_dim 256 its first 128 columns, the rest in TMEM).
 //   next       TMA, K tiles: each 16-token block is one box [16][row bytes] of the paged
 //              pool (4-D tensor map: row bytes, slot-in-block, KV head, block).
 //   next       allocates TMEM, issues S = Q8 K8^T with tcgen05.mma (kind::f8f6f4 for e4m3,
@@ -34,20 +33,18 @@
 //              warp each, except bf16 layers at head_dim 256, where the K warp copies
 //              both).
 // Key tiles hold 128 keys (64 for bf16 head_dim 256).  TMEM columns, by instantiation:
-//   full-attention e4m3 up to head_dim 128: two S buffers [0, 256), two O_tile buffers
-//     from 256; O in the correction warps' registers (with promote_every 0 the tensor core
-//     accumulates into O_tile buffer 0).  The QK^T of tile t+1 then runs while the softmax
-//     works on tile t, and the P.V of tile t while tile t-1 is promoted.  The registers
-//     come from per-warpgroup budgets (setmaxnreg): softmax 120, correction 232, copy and
-//     MMA warps 40 per thread;
+//   e4m3 up to head_dim 128: two S buffers [0, 256), two O_tile buffers from 256; O in the
+//     correction warps' registers (with promote_every 0 the tensor core accumulates into
+//     O_tile buffer 0).  The QK^T of tile t+1 then runs while the softmax works on tile t,
+//     and the P.V of tile t while tile t-1 is promoted.  The registers come from
+//     per-warpgroup budgets (setmaxnreg): softmax 120, correction 232, copy and MMA warps
+//     40 per thread.  Windowed layers write P8 back into TMEM over the S columns each
+//     thread has read, and P.V takes it from there as its A operand;
 //   e4m3 at head_dim 256 (full or windowed): one S buffer [0, 128), two 128-column O_tile
 //     buffers [128, 384) that take the two N = 128 halves of each P.V product, and the
 //     second half of O at [384, 512); the first half of O in registers.  Each half is
 //     promoted while the tensor core works on the other.  With promote_every >= 2 or 0
 //     the running sum spans both O_tile buffers;
-//   windowed e4m3 up to head_dim 128: two S buffers and one O_tile; each thread writes
-//     its P8 back into TMEM over the S columns it has read, and P.V takes it from there
-//     as its A operand; O in TMEM;
 //   bf16 layers: one S buffer [0, 128), O_tile (two buffers up to head_dim 128), O in
 //     TMEM; at head_dim 256 the P.V product runs as two N = 128 halves through one O_tile.
 // Every wait is bounded in time; a timeout records FKV_FAULT_TIMEOUT, lets the CTA's
@@ -120,17 +117,16 @@ struct PrefillCfg {
   static constexpr int PTILE = BM * PB;             // bytes of one P tile
   static constexpr int KSTEP = 32 / ES;             // keys (P columns) of one P.V k-step (32 bytes)
   // Windowed e4m3 up to head_dim 128: each thread writes its P8 back into TMEM over the S
-  // columns it has read, and P.V takes P8 from there as its A operand (two S buffers, one
-  // O_tile).  Otherwise P goes through shared memory.
+  // columns it has read, and P.V takes P8 from there as its A operand (measured 3 % faster
+  // there; with full attention, no faster).  Otherwise P goes through shared memory.
   static constexpr bool TS = !BF && D <= 128 && WIN;
-  // Full-attention e4m3, and windowed e4m3 at head_dim 256: the FP32 accumulator O lives in
-  // the correction warps' registers (at head_dim 256 its first half), which take registers
-  // from the other warpgroups through setmaxnreg; the freed TMEM holds two O_tile buffers
-  // (and two S buffers up to head_dim 128).  (Windowed up to head_dim 128, TS measured 2 %
-  // faster.)
-  static constexpr bool REGO = !BF && !TS;
+  // e4m3 layers: the FP32 accumulator O lives in the correction warps' registers (at
+  // head_dim 256 its first half), which take registers from the other warpgroups through
+  // setmaxnreg; the freed TMEM holds two O_tile buffers (and two S buffers up to head_dim
+  // 128, where windowed layers also keep P8 in them).
+  static constexpr bool REGO = !BF;
   static constexpr int SBUF = (TS || (REGO && D <= 128)) ? 2 : 1;  // S buffers in TMEM
-  static constexpr int OTB = (!TS && (D <= 128 || REGO)) ? 2 : 1;  // O_tile buffers in TMEM
+  static constexpr int OTB = (REGO || (!TS && D <= 128)) ? 2 : 1;  // O_tile buffers in TMEM
   // unrolling of the softmax / correction chunk loops: full for head_dim <= 128 (the
   // softmax is the critical path there), none for 256 (code size of four warp roles)
   static constexpr int UNR = D <= 128 ? 4 : 1;
