@@ -45,6 +45,10 @@ bool supported_group(int32_t G, int32_t D) {
   return G * D <= 2048;
 }
 
+// Pool blocks per tile of the tensor-core decode (its P-rounding granularity): 128 keys,
+// 256 at head_dim 64.  The split plan keeps whole tiles for every layer kind.
+int decode_tile_blocks(int32_t D) { return D == 64 ? 16 : 8; }
+
 struct DecodePlan {
   int bps = 0;
   int max_splits = 0;
@@ -53,8 +57,9 @@ struct DecodePlan {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Split-K plan.  Blocks per split (bps) are multiples of 8 (whole 128-key tiles of the
-// tensor-core decode) up to kMaxSplitBlocks (256), with at most 1024 splits per sequence.
+// Split-K plan.  Blocks per split (bps) are multiples of the tensor-core decode's tile (8
+// blocks of 16 keys; 16 at head_dim 64) up to kMaxSplitBlocks (256), with at most 1024
+// splits per sequence.
 // Equal estimates go to the longer splits (fewer CTAs, fewer prologues and merges).  A requested
 // num_splits sets bps = ceil(blocks / num_splits), rounded up.  Otherwise bps minimises
 // the estimated time waves * bps, where a wave is one CTA on every resident slot
@@ -65,6 +70,7 @@ bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_bloc
   if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks <= 0 || window < 0 || num_splits < 0) return false;
   long long nblk_max = max_blocks;
   if (window > 0) nblk_max = std::min<long long>(max_blocks, (window + 15) / 16 + 1);
+  const long long tpb = decode_tile_blocks(D);
   long long bps;
   if (num_splits > 0) {
     bps = (nblk_max + num_splits - 1) / num_splits;
@@ -72,7 +78,7 @@ bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_bloc
     const long long units = static_cast<long long>(std::max(B, 1)) * Hkv;
     const long long slots = static_cast<long long>(current_num_sms()) * 3;
     long long best = -1, best_cost = 0;
-    for (long long c = 8; c <= fkv::kMaxSplitBlocks; c += 8) {
+    for (long long c = tpb; c <= fkv::kMaxSplitBlocks; c += tpb) {
       const long long ctas = units * ((nblk_max + c - 1) / c);
       const long long cost = (ctas + slots - 1) / slots * std::min(c, nblk_max);
       if (best < 0 || cost < best_cost || (cost == best_cost && c > best)) {
@@ -85,7 +91,7 @@ bool plan_decode(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_bloc
   bps = std::min<long long>(bps, fkv::kMaxSplitBlocks);
   bps = std::max<long long>(bps, (nblk_max + 1023) / 1024);
   bps = std::max<long long>(bps, 1);
-  bps = (bps + 7) / 8 * 8;
+  bps = (bps + tpb - 1) / tpb * tpb;
   if (bps > fkv::kMaxSplitBlocks) return false;  // context too long for 1024 splits of 256 blocks
   plan->bps = static_cast<int>(bps);
   plan->max_splits = static_cast<int>((nblk_max + bps - 1) / bps);
@@ -230,7 +236,7 @@ const char* fkv_status_string(fkv_status status) {
   return "unknown status";
 }
 
-int32_t fkv_version(void) { return 104; }
+int32_t fkv_version(void) { return 105; }
 
 void fkv_set_decode_wait_limit_ns(unsigned long long ns) { g_decode_wait_ns.store(ns, std::memory_order_relaxed); }
 
@@ -272,7 +278,7 @@ int32_t fp8_decode_attn_split_blocks(int32_t batch, int32_t num_q_heads, int32_t
 
 int32_t fkv_decode_block_n(int32_t head_dim, int32_t layer_kind) {
   const int elt = layer_kind == 0 ? 1 : layer_kind == 1 ? 2 : layer_kind == 2 ? 3 : 0;
-  return elt != 0 && fkv::decode_uses_tensor_cores(head_dim, elt) ? 128 : 0;
+  return elt != 0 && fkv::decode_uses_tensor_cores(head_dim, elt) ? 16 * decode_tile_blocks(head_dim) : 0;
 }
 
 int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,

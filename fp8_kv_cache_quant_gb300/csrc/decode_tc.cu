@@ -11,14 +11,16 @@
 // query rows.  The products are therefore taken transposed, with the keys and head_dim on
 // the MMA's M side and the G query heads (padded to 16) on N:
 //   S^T [128 keys][16]   = K8 [128 keys][D]   . Q8^T [D][16]        (K, Q8 K-major)
-//   O^T [128 d][16]     += V8^T [128 d][128 keys] . P8^T [128 keys][16]   (V MN-major)
+//   O^T [128 d][16]     += V8^T [128 d][BN keys] . P8^T [BN keys][16]   (V MN-major)
 // so the cache tiles are the A operands exactly as TMA lands them from the pool.
-// head_dim 64 uses 64-byte rows (64-byte swizzle) and an M = 64 P.V product, whose
-// accumulator row r sits in TMEM lane 32 (r / 16) + r % 16.
+// head_dim 64 uses 64-byte rows (64-byte swizzle), tiles of BN = 256 keys (two S^T
+// products of 128 keys; a tile's fixed costs, the softmax's reductions and barriers and
+// the products' latencies, then serve twice the bytes), and an M = 64 P.V product, whose
+// accumulator row r sits in TMEM lane 32 (r / 16) + r % 16.  Other head_dims: BN = 128.
 //
 // CTA = (split, KV head g, sequence b), 10 warps:
-//   warps 0-3  softmax: quantise the G query rows to e4m3 (prologue); per 128-key tile
-//              thread i owns key i (TMEM lane i): S^T row from TMEM, scale, mask,
+//   warps 0-3  softmax: quantise the G query rows to e4m3 (prologue); per tile thread i
+//              owns key i (and 128 + i at head_dim 64; TMEM lane i): S^T row from TMEM, scale, mask,
 //              per-head tile maximum across the 128 keys (shuffles + shared memory),
 //              running max m, p = 2^(s - m), its unrounded sum, P8 = e4m3(p * 448) into
 //              the P^T tile; the tile's alpha = 2^(m_old - m) is published in shared memory.
@@ -26,7 +28,7 @@
 //              O_tile^T is promoted into FP32 registers, acc = acc * alpha + O_tile, off
 //              the softmax warps' critical path; then the split's output.
 //   warp 8     K copies: each 16-token block is one box [16][row bytes] of the paged pool
-//              (4-D tensor map), 8 blocks per tile issued from 8 lanes; in the prologue
+//              (4-D tensor map), a tile's BN / 16 blocks issued from as many lanes; in the prologue
 //              also the first tiles' V copies, and (fp8_decode_step) the current token's
 //              K and V written into the pools by the split that holds it.
 //   warp 9     allocates TMEM; polls the pipeline's barriers and issues whichever is ready
@@ -46,7 +48,9 @@ namespace {
 
 template <int D, int G>
 struct DecodeTcCfg {
-  static constexpr int BN = 128;               // keys per tile (M of S^T)
+  static constexpr int BN = D == 64 ? 256 : 128;  // keys per tile (the P rounding's tile)
+  static constexpr int TPB = BN / 16;             // pool blocks per tile
+  static constexpr int NHALF = BN / 128;          // S^T products (M = 128 keys each) per tile
   static constexpr int NP = 16;                // query heads padded to the MMA's N
   static constexpr int RB = D < 128 ? D : 128; // bytes of one swizzled row
   static constexpr int SWZ = RB == 128 ? 2 : 4;  // descriptor swizzle mode (128 / 64 bytes)
@@ -54,12 +58,17 @@ struct DecodeTcCfg {
   static constexpr int KSUB = BN * RB;         // bytes of one column block of a K / V tile
   static constexpr int KTILE = BN * D;         // bytes of a K or V tile
   static constexpr int MPV = D < 128 ? D : 128;  // M of one P.V product (head_dim rows)
-  static constexpr int NS = D == 64 ? 4 : 2;   // K / V stages (small CTAs: 3 per SM up to head_dim 128)
-  static constexpr int MAX_BPS = kMaxSplitBlocks;          // blocks per split (their ids staged in shared memory)
+  static constexpr int NS = 2;                 // K / V stages (small CTAs: 3 per SM up to head_dim 128)
+  static constexpr int MAX_BPS = kMaxSplitBlocks;          // blocks per split
   static constexpr int QSUB = NP * RB;         // bytes of one column block of the Q8 tile
-  static constexpr int PTILE = NP * BN;        // bytes of one P8^T tile
-  static constexpr int TM_S = 0;               // S^T buffers: TMEM columns [0, 2 * NP)
-  static constexpr int TM_O = 2 * NP;          // O_tile^T buffers: [TM_O, TM_O + 2 * NSUB * NP)
+  static constexpr int PTILE = NP * BN;        // bytes of one P8^T tile: NHALF sub-tiles [NP][128 keys]
+  static constexpr int TM_S = 0;               // S^T buffers: TMEM columns [0, 2 * NHALF * NP)
+  static constexpr int TM_O = 2 * NHALF * NP;  // O_tile^T buffers: [TM_O, TM_O + 2 * NSUB * NP)
+  static constexpr int SLD = (D == 64 && G <= 8) ? 8 : 16;  // S^T columns a softmax thread loads
+  // block ids of the split staged in shared memory once (head_dim 128 and 256); at head_dim
+  // 64, whose three CTAs per SM leave no room for them, each copying lane reads its block's
+  // id one tile ahead of the copy
+  static constexpr bool STAGE_IDS = D != 64;
   static constexpr int TM_COLS = TM_O + 2 * NSUB * NP <= 64 ? 64 : 128;
   // shared memory (bytes; tiles on 1024-byte boundaries for the 128-byte swizzle)
   static constexpr int OFF_K = 0;
@@ -70,8 +79,8 @@ struct DecodeTcCfg {
   static constexpr int OFF_A = OFF_RED + 2 * 4 * NP * 4;  // alpha [2][NP]; then m, l [2][NP]
   static constexpr int OFF_BAR = OFF_A + 4 * NP * 4;
   static constexpr int NBAR = 21 + 4 * NS;
-  static constexpr int OFF_IDS = OFF_BAR + NBAR * 8;     // [MAX_BPS] block ids of the split
-  static constexpr int OFF_MISC = OFF_IDS + MAX_BPS * 4;
+  static constexpr int OFF_IDS = OFF_BAR + NBAR * 8;     // [MAX_BPS] block ids of the split (STAGE_IDS)
+  static constexpr int OFF_MISC = OFF_IDS + (STAGE_IDS ? MAX_BPS * 4 : 0);
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_QK = idesc_e4m3_f32(128, NP, 0, 0);  // K8 and Q8 K-major
   static constexpr uint32_t IDESC_PV = idesc_e4m3_f32(MPV, NP, 1, 0);  // V8 MN-major, P8 K-major
@@ -79,7 +88,11 @@ struct DecodeTcCfg {
   static constexpr int CH = (NS * KTILE / 4 - 2 * G) / G < 256 ? (NS * KTILE / 4 - 2 * G) / G : 256;
   static_assert(G >= 1 && G <= NP, "query heads per KV head");
   static_assert(D == 64 || D == 128 || D == 256, "head_dim");
+  static_assert(MAX_BPS % TPB == 0 && TPB * NS <= 32, "whole tiles per split; the prologue's ids in one warp");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  // three CTAs per SM up to head_dim 128 (G <= 8): each takes SMEM plus 1 KB the hardware
+  // reserves, out of the SM's 228 KB
+  static_assert(D > 128 || G > 8 || 3 * (SMEM + 1024) <= 228 * 1024, "three CTAs per SM");
 };
 
 constexpr int kDecodeTcThreads = 320;  // softmax warpgroup, correction warpgroup, TMA warp, MMA warp
@@ -206,12 +219,23 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     }
     return;
   }
-  // this split: blocks [bb, be), keys [klo, khi), tiles of 8 blocks from block bb
+  // this split: blocks [bb, be), keys [klo, khi), tiles of TPB blocks from block bb
+  constexpr int TPB = C::TPB;
   const int bb = r.blk_begin + sigma * p.bps;
   const int be = min(bb + p.bps, r.blk_end);
   const int klo = max(r.lo, bb * 16), khi = min(r.T, be * 16);
-  const int n_t = (be - bb + 7) / 8;
+  const int n_t = (be - bb + TPB - 1) / TPB;
   const int T = r.T;
+  // block id of block j of the split (an id out of range reads block 0 and is reported)
+  auto split_block_id = [&](int j) -> int {
+    if (j >= be - bb) return 0;
+    int id = p.block_table[static_cast<size_t>(b) * p.max_blocks + bb + j];
+    if (id < 0 || id >= p.num_blocks) {
+      raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
+      id = 0;
+    }
+    return id;
+  };
 
   // Before the CTA-wide barrier the K-producer warp issues the K and V copies of the first
   // NS tiles, so that the first HBM latency overlaps the rest of the prologue (block-id
@@ -222,19 +246,11 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
   if (warp == 8 && p.k_new != nullptr && sigma == r.nsplit - 1 && !r.clamped) write_current_token<D>(p, b, g, T, lane);
   if (warp == 8) {
     __syncwarp();
-    const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks + bb;
-    int id = 0;
-    if (lane < 8 * n0 && lane < be - bb) {  // block `lane` of the split
-      id = trow[lane];
-      if (id < 0 || id >= p.num_blocks) {
-        raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
-        id = 0;
-      }
-      ids_s[lane] = id;
-    }
+    const int id = lane < TPB * n0 ? split_block_id(lane) : 0;  // block `lane` of the split
+    if (C::STAGE_IDS && lane < TPB * n0) ids_s[lane] = id;
     for (int t = 0; t < n0; ++t) {
-      const int nblk = min(8, be - bb - 8 * t);
-      const int idt = __shfl_sync(0xffffffffu, id, 8 * t + (lane & 7));
+      const int nblk = min(TPB, be - bb - TPB * t);
+      const int idt = __shfl_sync(0xffffffffu, id, TPB * t + (lane & (TPB - 1)));
       if (lane == 0) {
         mbar_arrive_expect_tx(&k_full[t], nblk * 16 * D);
         mbar_arrive_expect_tx(&v_full[t], nblk * 16 * D);
@@ -249,17 +265,9 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       }
     }
   }
-  // the split's other block ids, checked once (an id out of range reads block 0 and is reported)
-  {
-    const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks + bb;
-    for (int j = 8 * n0 + threadIdx.x; j < be - bb; j += blockDim.x) {
-      int id = trow[j];
-      if (id < 0 || id >= p.num_blocks) {
-        raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
-        id = 0;
-      }
-      ids_s[j] = id;
-    }
+  if constexpr (C::STAGE_IDS) {
+    // the split's other block ids, checked once
+    for (int j = TPB * n0 + threadIdx.x; j < be - bb; j += blockDim.x) ids_s[j] = split_block_id(j);
   }
   __syncthreads();
   tc_fence_after();
@@ -296,10 +304,11 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
                                   swz(static_cast<uint32_t>(row * C::RB + byte % C::RB), C::RB)) = w4;
       }
       if constexpr (G < C::NP) {
-        for (int x = i; x < 2 * (C::NP - G) * 8; x += 128) {
-          const int tile = x / ((C::NP - G) * 8), rem = x % ((C::NP - G) * 8);
-          *reinterpret_cast<uint4*>(sP + tile * C::PTILE + (G + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+        constexpr int PAD = (C::NP - G) * 8;  // 16-byte chunks of one sub-tile's padding rows
+        for (int x = i; x < 2 * C::NHALF * PAD; x += 128) {
+          const int sub = x / PAD, rem = x % PAD;  // sub-tile (tile * NHALF + half)
+          *reinterpret_cast<uint4*>(sP + (sub / C::NHALF) * C::PTILE + (sub % C::NHALF) * (C::NP * 128) +
+                                    (G + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async_smem();
@@ -321,20 +330,33 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       const int sb = t & 1;
       if (!wait_warp(&s_full[sb], (t >> 1) & 1, p.pipe_wait_ns)) { ok = false; break; }
       tc_fence_after();
-      float s16[16];
-      tmem_ld16(lane_base + C::TM_S + sb * C::NP, s16);
+      constexpr int NH2 = C::NHALF;
+      float sv[NH2][C::SLD];  // key i + 128 hh of the tile: S^T product hh, lane i
+#pragma unroll
+      for (int hh = 0; hh < NH2; ++hh) {
+        const uint32_t col = lane_base + C::TM_S + (sb * NH2 + hh) * C::NP;
+        if constexpr (C::SLD == 8) tmem_ld8(col, sv[hh]);
+        else tmem_ld16(col, sv[hh]);
+      }
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive_warp(&s_free[sb]);
-      const int key = (bb + 8 * t) * 16 + i;
-      const bool valid = key >= klo && key < khi;
-      float x[G], wm[G];
+      bool valid[NH2];
+      float x[NH2][G], wm[G];
+#pragma unroll
+      for (int hh = 0; hh < NH2; ++hh) {
+        const int key = (bb + TPB * t) * 16 + 128 * hh + i;
+        valid[hh] = key >= klo && key < khi;
+      }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        x[h] = valid ? s16[h] * cst[h] : -INFINITY;
-        wm[h] = x[h];
+#pragma unroll
+        for (int hh = 0; hh < NH2; ++hh) x[hh][h] = valid[hh] ? sv[hh][h] * cst[h] : -INFINITY;
+        wm[h] = x[0][h];
+#pragma unroll
+        for (int hh = 1; hh < NH2; ++hh) wm[h] = fmaxf(wm[h], x[hh][h]);
       }
-      // tile maximum of each head over the 128 keys: within the warp, then across the 4
+      // tile maximum of each head over the tile's keys: within the warp, then across the 4
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
@@ -358,11 +380,17 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         const float tmax = fmaxf(fmaxf(red[h], red[C::NP + h]), fmaxf(red[2 * C::NP + h], red[3 * C::NP + h]));
         const float mn = fmaxf(m[h], tmax);
         const float alpha = (m[h] == -INFINITY) ? 0.f : ex2(m[h] - mn);
-        const float pv = valid ? ex2(x[h] - mn) : 0.f;
-        lsum[h] = fmaf(lsum[h], alpha, pv);
+        float psum = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < NH2; ++hh) {
+          const float pv = valid[hh] ? ex2(x[hh][h] - mn) : 0.f;
+          psum = hh == 0 ? pv : psum + pv;
+          const uint16_t code2 = f32x2_to_e4m3x2(pv * 448.f, 0.f);
+          sP[pb * C::PTILE + hh * (C::NP * 128) + swz(static_cast<uint32_t>(h * 128 + i), 128)] =
+              static_cast<uint8_t>(code2 & 0xFF);
+        }
+        lsum[h] = fmaf(lsum[h], alpha, psum);
         m[h] = mn;
-        const uint16_t code2 = f32x2_to_e4m3x2(pv * 448.f, 0.f);
-        sP[pb * C::PTILE + swz(static_cast<uint32_t>(h * 128 + i), 128)] = static_cast<uint8_t>(code2 & 0xFF);
         if (i == 0) alpha_s[pb * C::NP + h] = alpha;
       }
       fence_proxy_async_smem();
@@ -373,7 +401,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
       *abort_s = 1;
     }
-    // ---- the split's l (summed over the 128 key lanes: reduction n_t) and m, published
+    // ---- the split's l (summed over the 128 key threads: reduction n_t) and m, published
     // for the correction warpgroup
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
@@ -464,6 +492,8 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     int last_use[C::NS];
 #pragma unroll
     for (int s = 0; s < C::NS; ++s) last_use[s] = s < n0 ? 0 : -1;  // the prologue's copies
+    // (head_dim 64: block `lane` of tile n0, read ahead)
+    int kid = (!C::STAGE_IDS && lane < TPB) ? split_block_id(TPB * n0 + lane) : 0;
     for (int t = n0; t < n_t; ++t) {
       if (abort_warp(abort_s)) break;
       const int st = t % C::NS, use = t / C::NS;
@@ -472,14 +502,19 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         *abort_s = 1;
         break;
       }
-      const int nblk = min(8, be - bb - 8 * t);
+      const int nblk = min(TPB, be - bb - TPB * t);
+      int id_t = kid;
+      if constexpr (C::STAGE_IDS) {
+        id_t = lane < TPB ? ids_s[TPB * t + lane] : 0;
+      } else {
+        kid = lane < TPB ? split_block_id(TPB * (t + 1) + lane) : 0;  // the next tile's, read meanwhile
+      }
       if (lane == 0) mbar_arrive_expect_tx(&k_full[st], nblk * 16 * D);
       __syncwarp();
       if (lane < nblk) {
 #pragma unroll
         for (int s = 0; s < C::NSUB; ++s)
-          tma_load_4d(sK + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmk, s * C::RB, 0, g, ids_s[8 * t + lane],
-                      &k_full[st]);
+          tma_load_4d(sK + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmk, s * C::RB, 0, g, id_t, &k_full[st]);
       }
       last_use[st] = use;
     }
@@ -498,6 +533,8 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     int v_last[C::NS];
 #pragma unroll
     for (int s = 0; s < C::NS; ++s) v_last[s] = s < n0 ? 0 : -1;
+    // (head_dim 64: block `lane` of tile tv, read ahead)
+    int vid = (!C::STAGE_IDS && lane < TPB) ? split_block_id(TPB * tv + lane) : 0;
     bool ok = wait_warp(q_full, 0, p.pipe_wait_ns);
     uint64_t t_progress = globaltimer_ns();
     while (ok && tp < n_t) {
@@ -510,17 +547,18 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         vgo = tv < n_t && (tv < C::NS || mbar_test_wait(&v_empty[tv % C::NS], ((tv / C::NS) - 1) & 1));
       if (__shfl_sync(0xffffffffu, vgo, 0)) {
         const int st = tv % C::NS;
-        const int nblk = min(8, be - bb - 8 * tv);
+        const int nblk = min(TPB, be - bb - TPB * tv);
         if (lane == 0) mbar_arrive_expect_tx(&v_full[st], nblk * 16 * D);
         __syncwarp();
+        if constexpr (C::STAGE_IDS) vid = lane < TPB ? ids_s[TPB * tv + lane] : 0;
         if (lane < nblk) {
 #pragma unroll
           for (int s = 0; s < C::NSUB; ++s)
-            tma_load_4d(sV + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmv, s * C::RB, 0, g, ids_s[8 * tv + lane],
-                        &v_full[st]);
+            tma_load_4d(sV + st * C::KTILE + s * C::KSUB + lane * 16 * C::RB, &tmv, s * C::RB, 0, g, vid, &v_full[st]);
         }
         v_last[st] = tv / C::NS;
         ++tv;
+        if constexpr (!C::STAGE_IDS) vid = lane < TPB ? split_block_id(TPB * tv + lane) : 0;  // the next tile's
         events |= 1;
       }
       if (lane == 0) {
@@ -529,14 +567,18 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
             (tq < 2 || mbar_test_wait(&s_free[tq & 1], ((tq >> 1) - 1) & 1))) {
           const int st = tq % C::NS, sb = tq & 1;
           tc_fence_after();
+          // one product per 128 keys of the tile (rows 128 hh .. of the K tile)
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk) {
-            const int byte = kk * 32;
-            const uint64_t ad =
-                smem_desc(sKa + st * C::KTILE + (byte / C::RB) * C::KSUB + byte % C::RB, 16, 8 * C::RB, C::SWZ);
-            const uint64_t bd = smem_desc(sQa + (byte / C::RB) * C::QSUB + byte % C::RB, 16, 8 * C::RB, C::SWZ);
-            umma_f8(tmem + C::TM_S + sb * C::NP, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
-          }
+          for (int hh = 0; hh < C::NHALF; ++hh)
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk) {
+              const int byte = kk * 32;
+              const uint64_t ad = smem_desc(sKa + st * C::KTILE + (byte / C::RB) * C::KSUB + hh * 128 * C::RB +
+                                                byte % C::RB,
+                                            16, 8 * C::RB, C::SWZ);
+              const uint64_t bd = smem_desc(sQa + (byte / C::RB) * C::QSUB + byte % C::RB, 16, 8 * C::RB, C::SWZ);
+              umma_f8(tmem + C::TM_S + (sb * C::NHALF + hh) * C::NP, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+            }
           umma_commit(&s_full[sb]);
           umma_commit(&k_empty[st]);
           ++tq;
@@ -553,7 +595,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         const int st = tp % C::NS, pb = tp & 1;
         // keys past the context may hold stale bytes (NaN codes) or were not loaded: zero
         // their V rows, since 0 * NaN would poison the product even though their P is 0
-        const int kbase = (bb + 8 * tp) * 16;
+        const int kbase = (bb + TPB * tp) * 16;
         if (kbase + C::BN > T) {
           const int first = max(T - kbase, 0);
           constexpr int CPR = C::RB / 16;  // 16-byte chunks per row
@@ -576,7 +618,8 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
             for (int kk = 0; kk < C::BN / 32; ++kk) {
               const uint64_t ad = smem_desc(sVa + st * C::KTILE + s * C::KSUB + kk * 32 * C::RB, 8 * C::RB, 8 * C::RB,
                                             C::SWZ);
-              const uint64_t bd = smem_desc(sPa + pb * C::PTILE + kk * 32, 16, 1024, 2);
+              // keys 32 kk ..: sub-tile kk / 4 of P8^T, 32 bytes into its 128-byte rows
+              const uint64_t bd = smem_desc(sPa + pb * C::PTILE + (kk / 4) * (C::NP * 128) + (kk % 4) * 32, 16, 1024, 2);
               umma_f8(tmem + C::TM_O + (pb * C::NSUB + s) * C::NP, ad, bd, C::IDESC_PV, kk > 0 ? 1u : 0u);
             }
           umma_commit(&o_full[pb]);
@@ -628,7 +671,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
 template <int D, int G>
 cudaError_t launch_decode_tc_t(const DecodeParams& p, cudaStream_t s) {
   using C = DecodeTcCfg<D, G>;
-  if (p.bps > C::MAX_BPS || p.bps % 8 != 0) return cudaErrorInvalidValue;  // whole tiles, ids staged in smem
+  if (p.bps > C::MAX_BPS || p.bps % C::TPB != 0) return cudaErrorInvalidValue;  // whole tiles
   CUtensorMap tmk, tmv;
   if (!make_pool_map(&tmk, const_cast<uint8_t*>(p.k_cache), D, p.Hkv, p.num_blocks, C::RB) ||
       !make_pool_map(&tmv, const_cast<uint8_t*>(p.v_cache), D, p.Hkv, p.num_blocks, C::RB))

@@ -180,15 +180,16 @@ int32_t fp8_decode_attn_num_splits(int32_t batch, int32_t num_q_heads, int32_t n
                                    int32_t num_splits);
 
 /*
- * Pool blocks per context split of fp8_decode_attn for these sizes (a multiple of 8):
- * split s of a sequence covers blocks [lo / 16 + s * n, lo / 16 + (s + 1) * n).  0 for
- * invalid sizes.  With n_blk = max_blocks (window 0) or min(max_blocks, ceil(window / 16)
- * + 1), a requested num_splits > 0 gives ceil(n_blk / num_splits) blocks, at most 256 and
- * at least ceil(n_blk / 1024), rounded up to a multiple of 8 (a multiple of 8 above 256
- * means the context is too long: 0).  num_splits 0 picks, among the multiples of 8 up
- * to 256, the count c minimising waves(c) * min(c, n_blk), where waves(c) =
- * ceil(batch * num_kv_heads * ceil(n_blk / c) / (3 * SMs of the current device)); ties
- * go to the larger c.
+ * Pool blocks per context split of fp8_decode_attn for these sizes (a multiple of u,
+ * the blocks of one tensor-core decode tile: u = 16 at head_dim 64, else 8): split s of
+ * a sequence covers blocks [lo / 16 + s * n, lo / 16 + (s + 1) * n).  0 for invalid
+ * sizes.  With n_blk = max_blocks (window 0) or min(max_blocks, ceil(window / 16) + 1), a
+ * requested num_splits > 0 gives ceil(n_blk / num_splits) blocks, at most 256 and at
+ * least ceil(n_blk / 1024), rounded up to a multiple of u (a result above 256 means the
+ * context is too long: 0).  num_splits 0 picks, among the multiples of u up to 256, the
+ * count c minimising waves(c) * min(c, n_blk), where waves(c) = ceil(batch *
+ * num_kv_heads * ceil(n_blk / c) / (3 * SMs of the current device)); ties go to the
+ * larger c.
  */
 int32_t fp8_decode_attn_split_blocks(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                      int32_t head_dim, int32_t max_blocks, int32_t window,
@@ -215,7 +216,8 @@ int32_t fkv_decode_block_n(int32_t head_dim, int32_t layer_kind);
  * two-level accumulation of the blog's "Two-level accumulation" paragraph, so a 100k+
  * key contraction is summed in true FP32.
  * e4m3 layers (head_dim 64, 128 or 256) run on the tensor cores, FP8 QK and Score*V as
- * in the blog's FP8 attention: S^T = K8 Q8^T and O^T = V8^T P8^T per 128-key tile with
+ * in the blog's FP8 attention: S^T = K8 Q8^T and O^T = V8^T P8^T per tile of
+ * fkv_decode_block_n keys (128; 256 at head_dim 64) with
  * P8 = e4m3(p * 448) relative to the split's running maximum, the denominator summing
  * the unrounded p, and each tile's partial promoted into FP32 registers.  Skip layers
  * read a bf16 pool, quantise nothing and keep P exact; e5m2 layers (cache.kv_format)
@@ -238,7 +240,8 @@ int32_t fkv_decode_block_n(int32_t head_dim, int32_t layer_kind);
  *                 (zero it again when that grows).  A counter found non-zero sets
  *                 FKV_FAULT_WORKSPACE.
  *   num_splits    0 = automatic, else the requested number of context splits (each split
- *                 is then rounded up to whole multiples of 8 blocks, so fewer may result)
+ *                 is then rounded up to whole tiles, see fp8_decode_attn_split_blocks, so
+ *                 fewer may result)
  * head_dim in {64, 128, 256}; G = num_q_heads / num_kv_heads in {1, 2, 4, 8, 16} with
  * G * head_dim <= 2048.  A sequence with no key gets a zero row.
  */

@@ -70,39 +70,45 @@ def oracle_pools(oracle_kvcache, ctx, table, num_blocks, k, v, ks, vs, bf16_laye
     return kp, vp
 
 
-# The tensor-core decode of e4m3 layers and the prefill round P per tile of this many keys
-# (fp8kv.h: fkv_decode_block_n, fkv_prefill_block_n); the tests pass these to the oracle
-# and check that the library agrees.
-DECODE_BLOCK_N = 128
+# The prefill rounds P per tile of this many keys (fp8kv.h: fkv_prefill_block_n); the
+# tests pass it to the oracle and check that the library agrees.
 PREFILL_BLOCK_N = 128
 
 
-def decode_split_blocks(max_blocks, window, num_splits):
+def decode_block_n(head_dim):
+    """Keys per tile over which the tensor-core decode of e4m3 layers rounds P, restated
+    from include/fp8kv.h (fkv_decode_block_n): 256 at head_dim 64, else 128."""
+    return 256 if head_dim == 64 else 128
+
+
+def decode_split_blocks(max_blocks, window, num_splits, head_dim=128):
     """Blocks per context split of fp8_decode_attn for a requested split count, restated
     from the rule include/fp8kv.h documents: n = max_blocks, or with a window W at most
     ceil(W / 16) + 1 blocks; ceil(n / num_splits), at most 256 and at least
-    ceil(n / 1024), rounded up to a multiple of 8."""
+    ceil(n / 1024), rounded up to a multiple of u, the blocks of one decode tile."""
     assert num_splits > 0
+    u = decode_block_n(head_dim) // 16
     n = max_blocks if window <= 0 else min(max_blocks, -(-window // 16) + 1)
     bps = min(-(-n // num_splits), 256)
     bps = max(bps, -(-n // 1024), 1)
-    return -(-bps // 8) * 8
+    return -(-bps // u) * u
 
 
-def auto_split_blocks(batch, num_kv_heads, max_blocks, window, num_sms):
-    """The automatic plan (num_splits 0) restated from include/fp8kv.h: the multiple of 8
-    up to 256 minimising waves * blocks per split, waves counted on 3 resident CTAs per
-    SM, ties to the larger count."""
+def auto_split_blocks(batch, num_kv_heads, max_blocks, window, num_sms, head_dim=128):
+    """The automatic plan (num_splits 0) restated from include/fp8kv.h: the multiple of u
+    (the blocks of one decode tile) up to 256 minimising waves * blocks per split, waves
+    counted on 3 resident CTAs per SM, ties to the larger count."""
+    u = decode_block_n(head_dim) // 16
     n = max_blocks if window <= 0 else min(max_blocks, -(-window // 16) + 1)
     units, slots = max(batch, 1) * num_kv_heads, 3 * num_sms
     best = None
-    for c in range(8, 257, 8):
+    for c in range(u, 257, u):
         ctas = units * -(-n // c)
         cost = -(-ctas // slots) * min(c, n)
         if best is None or cost < best[1] or (cost == best[1] and c > best[0]):
             best = (c, cost)
     bps = max(best[0], -(-n // 1024))
-    return -(-bps // 8) * 8
+    return -(-bps // u) * u
 
 
 def assert_within_p_bound(gpu, exact, bound, what=""):

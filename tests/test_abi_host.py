@@ -55,7 +55,7 @@ def test_split_planning(lib):
     for auto in (f.fp8_decode_attn_split_blocks(8, 32, 8, 128, 1536), f.fp8_decode_attn_split_blocks(1, 64, 8, 128, 8192)):
         assert auto % 8 == 0 and 8 <= auto <= 256
     # which decodes round P (tensor cores, 128-key tiles) and which keep it exact
-    assert f.fkv_decode_block_n(128) == 128 and f.fkv_decode_block_n(256) == 128 and f.fkv_decode_block_n(64) == 128
+    assert f.fkv_decode_block_n(128) == 128 and f.fkv_decode_block_n(256) == 128 and f.fkv_decode_block_n(64) == 256
     assert f.fkv_decode_block_n(128, True) == 0 and f.fkv_decode_block_n(64, True) == 0
     # a window bounds the splits by the window's blocks
     assert f.fp8_decode_attn_num_splits(8, 64, 8, 64, 2048, 128, 0) <= 9
@@ -264,6 +264,7 @@ def test_documented_split_rule(lib):
         mb = rng.randint(1, 300_000)
         win = rng.choice([0, 0, 0, 1, 16, 100, 128, 4096])
         ns = rng.choice([0, 0, 1, 2, 3, 7, 57, 1000, 2000])
-        got = f.fp8_decode_attn_split_blocks(B, 4 * Hkv, Hkv, 128, mb, win, ns)
-        want = auto_split_blocks(B, Hkv, mb, win, 152) if ns == 0 else decode_split_blocks(mb, win, ns)
-        assert got == (want if want <= 256 else 0), (B, Hkv, mb, win, ns)
+        D = rng.choice([64, 128, 256])
+        got = f.fp8_decode_attn_split_blocks(B, 4 * Hkv, Hkv, D, mb, win, ns)
+        want = auto_split_blocks(B, Hkv, mb, win, 152, D) if ns == 0 else decode_split_blocks(mb, win, ns, D)
+        assert got == (want if want <= 256 else 0), (B, Hkv, D, mb, win, ns)
