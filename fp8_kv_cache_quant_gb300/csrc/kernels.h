@@ -8,7 +8,8 @@
 
 namespace fkv {
 
-// Pool blocks per decode split, at most: each split's block ids are staged in shared memory.
+// Pool blocks per decode split, at most (the CUDA-core decode and the tensor-core decode at
+// head_dim 128 and 256 stage a split's block ids in shared memory).
 constexpr int kMaxSplitBlocks = 256;
 
 struct DecodeParams {
