@@ -69,6 +69,8 @@ CASES = [
     (64, 16, True, 1, 0, 0),
     (256, 4, False, 0, 33, 1),
     (64, 4, False, 1, 0, 8),
+    (64, 4, False, 0, 77, 1),
+    (64, 8, False, 1, 300, 2),
 ]
 
 
