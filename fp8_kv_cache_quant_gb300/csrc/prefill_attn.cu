@@ -561,10 +561,19 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
           float ot[32];
           tmem_ld32(src + 32 * c, ot);
           tmem_ld_wait();
+          if constexpr (decltype(first)::value) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if constexpr (decltype(first)::value) O[32 * c + j] = ot[j];
-            else O[32 * c + j] = fmaf(O[32 * c + j], alpha, ot[j]);
+            for (int j = 0; j < 32; ++j) O[32 * c + j] = ot[j];
+          } else {
+            // packed: two fused multiply-adds per instruction, the same rounding as fmaf
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float2 r = __ffma2_rn(make_float2(O[32 * c + j], O[32 * c + j + 1]), a2,
+                                          make_float2(ot[j], ot[j + 1]));
+              O[32 * c + j] = r.x;
+              O[32 * c + j + 1] = r.y;
+            }
           }
           pin32(O + 32 * c);
         }
@@ -576,10 +585,17 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
           tmem_ld32(src + 32 * c, ot);
           if constexpr (!decltype(first)::value) tmem_ld32(dst, oh);
           tmem_ld_wait();
+          if constexpr (decltype(first)::value) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if constexpr (decltype(first)::value) oh[j] = ot[j];
-            else oh[j] = fmaf(oh[j], alpha, ot[j]);
+            for (int j = 0; j < 32; ++j) oh[j] = ot[j];
+          } else {
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float2 r = __ffma2_rn(make_float2(oh[j], oh[j + 1]), a2, make_float2(ot[j], ot[j + 1]));
+              oh[j] = r.x;
+              oh[j + 1] = r.y;
+            }
           }
           tmem_st32(dst, oh);
         }
