@@ -372,6 +372,44 @@ def _fp8_dense_peak():
     return 2.0 * 1900.0, "fallback 1.9 PFLOP/s bf16 x 2"
 
 
+def time_cache_write(f, device, peak, replays=20):
+    """kv_quant_cache at fill size: the 131,072-token context of the needle workload (8 KV
+    heads, head_dim 128, per-tensor scales) written into a shuffled e4m3 pool, timed per
+    call with CUDA events, L2 flushed between calls.  Algorithmic bytes: the bf16 K and V
+    read, the e4m3 codes written, the int64 slots read."""
+    import numpy as np
+    import torch
+    import synth
+    w = synth.WORKLOADS[4]
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    data = synth.decode_layer(w, 0, ctx, device=device)
+    cache = f.LayerCache.empty(nb, w.num_kv_heads, w.head_dim, device=device)
+    slots = torch.from_numpy(synth.slot_mapping(table, ctx)).to(device)
+    n = int(slots.numel())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    call = lambda: f.kv_quant_cache(data.k, data.v, slots, cache, data.k_scale, data.v_scale, f.SCALE_PER_TENSOR)
+    for _ in range(3):
+        call()
+    ts = []
+    for _ in range(replays):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    pc = _pcts(ts)
+    by = n * w.num_kv_heads * w.head_dim * 2 * (2 + 1) + n * 8
+    gbs = by / (pc["p50"] * 1e-6) / 1e9
+    del data, cache, slots, flush
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}-fill", "kernel": "kv_quant_cache_kernel", "tokens": n,
+            "us_p10_p50_p90": [pc["p10"], pc["p50"], pc["p90"]], "algorithmic_bytes": by,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak}}
+
+
 def time_prefill(f, workload_id, device, iters, warmup, promote_every=(1,)):
     """Time fp8_prefill_attn on a prefill workload: the head_dim-256 causal batch (5) or the
     4096-query chunk over the 131072-key cache (4).  Algorithmic FLOPs = 4 * D * unmasked
@@ -812,6 +850,10 @@ def run_ours(args):
                    time_prefill(f, 4, device, iters=min(args.steps, 10), warmup=3, promote_every=(1, 4, 0)))
         torch.cuda.synchronize()
 
+    cache_write = None
+    if not args.no_prefill:
+        cache_write = time_cache_write(f, device, peak)
+
     # the other decode workloads, the ITL-slope proxy and the TTFT fit (short forms of
     # --sweep / --ttft), each on this GPU in the same run
     others = None
@@ -856,6 +898,7 @@ def run_ours(args):
             "clocks_other_measurements": clocks_x.summary(),
             "bf16": bf16_info,
             "prefill": prefill,
+            "cache_write": cache_write,
             "per_config": others,
             "itl_slope": itl,
             "ttft_fit": ttft,
