@@ -1,6 +1,7 @@
 """Run one workload layer's kernels a few times, eagerly, for ncu captures.
 
     python -m fp8_kv_cache_quant_gb300.profile_case --workload 2 --layer 0 --iters 3 [--bf16]
+    python -m fp8_kv_cache_quant_gb300.profile_case --workload 4 --fill --iters 3
 
 Builds one layer of a decode workload (seeded synthetic inputs, pool filled by
 kv_quant_cache) and launches fp8_decode_attn ``iters`` times.  The layer's cache is
@@ -37,9 +38,13 @@ def main():
     ap.add_argument("--llama", action="store_true",
                     help="with --prefill: the Llama-3.1-8B head shape (32/8 heads, head_dim 128)")
     ap.add_argument("--seq", type=int, default=8192, help="prefill sequence length")
+    ap.add_argument("--fill", action="store_true",
+                    help="run kv_quant_cache over the workload's whole context (one layer's fill) instead")
     a = ap.parse_args()
     if a.prefill:
         return run_prefill(a)
+    if a.fill:
+        return run_fill(a)
     w = synth.WORKLOADS[a.workload]
     dev = torch.device("cuda:0")
     ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
@@ -68,6 +73,26 @@ def main():
                               num_splits=a.splits)
     torch.cuda.synchronize()
     print("profile_case done", w.name, "layer", a.layer, "bf16" if a.bf16 else "e4m3")
+
+
+def run_fill(a):
+    import torch
+
+    import fp8_kv_cache_quant_gb300 as f
+    import synth
+
+    w = synth.WORKLOADS[a.workload]
+    dev = torch.device("cuda:0")
+    ctx = synth.context_lengths(w.batch, w.ctx_lo, w.ctx_hi, w.seed)
+    table, nb = synth.block_table(ctx, seed=w.seed)
+    data = synth.decode_layer(w, a.layer, ctx, device=dev)
+    gran = f.SCALE_PER_HEAD if w.scale_mode == "amax" else f.SCALE_PER_TENSOR
+    cache = f.LayerCache.empty(nb, w.num_kv_heads, w.head_dim, device=dev)
+    slots = torch.from_numpy(synth.slot_mapping(table, ctx)).to(dev)
+    for _ in range(a.iters):
+        f.kv_quant_cache(data.k, data.v, slots, cache, data.k_scale, data.v_scale, gran)
+    torch.cuda.synchronize()
+    print("profile_case done fill", w.name, int(slots.numel()), "tokens")
 
 
 def run_prefill(a):
