@@ -57,17 +57,30 @@ def _code_only(text: str) -> str:
     return "\n".join(ln for ln in lines if ln)
 
 
+def _local_includes(csrc: str, name: str, seen=None) -> set:
+    """The files of csrc/ that `name` includes, directly or through one another."""
+    import re
+    seen = set() if seen is None else seen
+    path = os.path.join(csrc, name)
+    if name in seen or not os.path.exists(path):
+        return seen
+    seen.add(name)
+    for inc in re.findall(r'^\s*#include\s+"([^"/]+)"', open(path, encoding="utf-8").read(), flags=re.M):
+        _local_includes(csrc, inc, seen)
+    return seen
+
+
 def kernel_source_sha(kernel_file: str) -> str:
     """First 16 hex digits of the sha256 of the code (comments removed) of a kernel's .cu
-    file followed by the shared headers it includes (common.cuh, tc.cuh,
-    decode_common.cuh, kernels.h): a profile summary stays valid only while none of them
-    has changed."""
+    file followed by those of the shared headers common.cuh, tc.cuh, decode_common.cuh and
+    kernels.h (in that order) that it includes: a profile summary stays valid only while
+    none of them has changed."""
     csrc = os.path.join(ROOT, "fp8_kv_cache_quant_gb300", "csrc")
+    used = _local_includes(csrc, kernel_file)
     h = hashlib.sha256()
     for name in (kernel_file, "common.cuh", "tc.cuh", "decode_common.cuh", "kernels.h"):
-        path = os.path.join(csrc, name)
-        if os.path.exists(path):
-            h.update(_code_only(open(path, encoding="utf-8").read()).encode())
+        if name in used:
+            h.update(_code_only(open(os.path.join(csrc, name), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

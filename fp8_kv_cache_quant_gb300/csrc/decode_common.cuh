@@ -53,11 +53,66 @@ FKV_DEV bool count_split_done(const DecodeParams& p, int u, int nsplit) {
 // M = max_s lse_s, written as bf16.  Every thread of the CTA calls it (it synchronises);
 // `scratch` holds at least 2 * G + G * CH floats of shared memory.
 // The partials come from L2; a load whose value the next instruction needs holds the
-// warp for the whole round trip, so the log-sum-exps are read by a warp per head with
-// the lanes striding over the splits, and each group of four outputs' split partials are
-// loaded sixteen at a time (16-byte loads) before they are summed (in split order).
+// warp for the whole round trip.  With at most eight splits and one group of four
+// outputs per thread, each thread issues all its loads (its head's log-sum-exps and its
+// outputs' partials) at once and merges alone: one round trip.  Otherwise the
+// log-sum-exps are read by a warp per head with the lanes striding over the splits, and
+// each group of four outputs' split partials are loaded sixteen at a time (16-byte
+// loads) before they are summed.  Both sum the outputs in split order and the weights
+// in the same pairwise order, so they give the same bits.
 template <int D, int G, int NT, int CH>
 FKV_DEV void merge_splits(const DecodeParams& p, int b, int g, int ns, float vs, float* scratch) {
+  constexpr int QUADS = (G * D / 4 + NT - 1) / NT;  // groups of 4 outputs per thread
+  constexpr int UF = 8;  // splits merged in one round trip (every load issued at once)
+  static_assert(UF == 8, "the pairwise weight sum below is written for eight splits");
+  if (ns <= UF && QUADS == 1) {
+    // few splits: each thread loads its four outputs of every split and its head's
+    // log-sum-exps together, then merges them itself
+    const int t = threadIdx.x;
+    if (t < G * D / 4) {
+      const int h = t / (D / 4), d = 4 * (t % (D / 4));
+      const size_t row = (static_cast<size_t>(b) * p.Hq + g * G + h) * p.max_splits;
+      const float* src = p.o_part + row * D + d;
+      float4 x[UF];
+      float lv[UF];
+#pragma unroll
+      for (int u = 0; u < UF; ++u) {
+        if (u < ns) {
+          x[u] = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(u) * D));
+          lv[u] = __ldcg(p.lse_part + row + u);
+        }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < UF; ++u)
+        if (u < ns) M = fmaxf(M, lv[u]);
+      float w[UF];
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < UF; ++u) w[u] = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int u = 0; u < UF; ++u) {
+          if (u < ns) {
+            const float wv = (lv[u] == -INFINITY) ? 0.f : ex2(lv[u] - M);
+            w[u] = wv;
+            o.x += wv * x[u].x;
+            o.y += wv * x[u].y;
+            o.z += wv * x[u].z;
+            o.w += wv * x[u].w;
+          }
+        }
+      }
+      // the weights summed pairwise in the order of a warp's butterfly over eight lanes,
+      // as the general path below sums them
+      const float W = ((w[0] + w[4]) + (w[2] + w[6])) + ((w[1] + w[5]) + (w[3] + w[7]));
+      const float inv = (W > 0.f) ? vs / W : 0.f;
+      __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(p.out + (static_cast<size_t>(b) * p.Hq + g * G + h) * D + d);
+      dst[0] = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+      dst[1] = __floats2bfloat162_rn(o.z * inv, o.w * inv);
+    }
+    return;
+  }
   float* ms_s = scratch;       // [G] max of lse
   float* inv_s = ms_s + G;     // [G] v_s / sum of weights
   float* w_s = inv_s + G;      // [G][CH] weights of a chunk of splits
@@ -83,7 +138,6 @@ FKV_DEV void merge_splits(const DecodeParams& p, int b, int g, int ns, float vs,
       inv_s[h] = (W > 0.f) ? vs / W : 0.f;
     }
   }
-  constexpr int QUADS = (G * D / 4 + NT - 1) / NT;  // groups of 4 outputs per thread
   constexpr int U = 16;                              // split partials loaded before use
   float4 o[QUADS];
 #pragma unroll

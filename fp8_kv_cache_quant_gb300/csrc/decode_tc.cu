@@ -205,7 +205,14 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     tmem_relinquish();
     tc_fence_before();
   }
+  constexpr int TPB = C::TPB;
   griddep_wait();
+  // Without a window a split's blocks start at sigma * bps whatever the context length,
+  // so the producer warp reads its first tiles' table entries alongside the length
+  // (entries past the sequence's blocks are read but not used).
+  int id_spec = 0;
+  if (warp == 8 && p.window <= 0 && lane < TPB * C::NS && sigma * p.bps + lane < p.max_blocks)
+    id_spec = p.block_table[static_cast<size_t>(b) * p.max_blocks + sigma * p.bps + lane];
   const SeqRange r = seq_range(p, b, sigma == 0 && g == 0 && threadIdx.x == 0);
   if (sigma >= r.nsplit) {  // uniform over the CTA
     if (sigma == 0) {       // a sequence without keys: zero output rows
@@ -220,21 +227,22 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
     return;
   }
   // this split: blocks [bb, be), keys [klo, khi), tiles of TPB blocks from block bb
-  constexpr int TPB = C::TPB;
   const int bb = r.blk_begin + sigma * p.bps;
   const int be = min(bb + p.bps, r.blk_end);
   const int klo = max(r.lo, bb * 16), khi = min(r.T, be * 16);
   const int n_t = (be - bb + TPB - 1) / TPB;
   const int T = r.T;
   // block id of block j of the split (an id out of range reads block 0 and is reported)
-  auto split_block_id = [&](int j) -> int {
-    if (j >= be - bb) return 0;
-    int id = p.block_table[static_cast<size_t>(b) * p.max_blocks + bb + j];
+  auto checked_block_id = [&](int id) -> int {
     if (id < 0 || id >= p.num_blocks) {
       raise_fault(p.fault, FKV_FAULT_BLOCK_ID);
       id = 0;
     }
     return id;
+  };
+  auto split_block_id = [&](int j) -> int {
+    if (j >= be - bb) return 0;
+    return checked_block_id(p.block_table[static_cast<size_t>(b) * p.max_blocks + bb + j]);
   };
 
   // Before the CTA-wide barrier the K-producer warp issues the K and V copies of the first
@@ -246,7 +254,9 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
   if (warp == 8 && p.k_new != nullptr && sigma == r.nsplit - 1 && !r.clamped) write_current_token<D>(p, b, g, T, lane);
   if (warp == 8) {
     __syncwarp();
-    const int id = lane < TPB * n0 ? split_block_id(lane) : 0;  // block `lane` of the split
+    int id = 0;  // block `lane` of the split
+    if (lane < TPB * n0)
+      id = p.window > 0 ? split_block_id(lane) : (lane < be - bb ? checked_block_id(id_spec) : 0);
     if (C::STAGE_IDS && lane < TPB * n0) ids_s[lane] = id;
     for (int t = 0; t < n0; ++t) {
       const int nblk = min(TPB, be - bb - TPB * t);

@@ -129,6 +129,20 @@ def test_profile_hash_covers_code_not_comments():
     assert len(bench.kernel_source_sha("decode_tc.cu")) == 16
 
 
+def test_profile_hash_covers_the_headers_a_kernel_includes():
+    """The hash of a kernel's source takes in the shared headers it includes, directly or
+    through another header, and no other: the decode's shared merge code is part of the
+    decode kernels' hashes, not of the prefill's or the cache write's."""
+    import os
+    csrc = os.path.join(bench.ROOT, "fp8_kv_cache_quant_gb300", "csrc")
+    tc = bench._local_includes(csrc, "decode_tc.cu")
+    assert {"decode_tc.cu", "common.cuh", "tc.cuh", "decode_common.cuh", "kernels.h"} <= tc
+    assert "decode_common.cuh" in bench._local_includes(csrc, "decode_attn.cu")
+    assert "decode_common.cuh" not in bench._local_includes(csrc, "prefill_attn.cu")
+    assert "tc.cuh" not in bench._local_includes(csrc, "kv_quant_cache.cu")
+    assert bench.kernel_source_sha("prefill_attn.cu") != bench.kernel_source_sha("decode_tc.cu")
+
+
 def test_both_arms_describe_the_same_workload_and_sample():
     """The reference arm and the benchmark line's cpu_baseline time the same oracle sample
     and print the same config object."""
