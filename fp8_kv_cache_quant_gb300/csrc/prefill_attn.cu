@@ -131,6 +131,10 @@ struct PrefillCfg {
   // softmax is the critical path there), none for 256 (code size of four warp roles)
   static constexpr int UNR = D <= 128 ? 4 : 1;
   static constexpr bool ONE_LOAD = D <= 128 || !BF;  // S row loaded once into registers
+  // e4m3 layers up to head_dim 128 mask a partly visible tile by setting its hidden scores
+  // to -inf in registers (one code path for every tile); head_dim 256 keeps a masked copy
+  // of the exponent pass, which measured slightly faster there
+  static constexpr bool PREMASK = !BF && D <= 128;
   // softmax warps per S row: two on e4m3 layers (each half of the row's columns, so that
   // every SM quarter has two softmax warps to switch between); one on bf16 layers, whose
   // 2-byte tiles leave no shared memory for the half-row exchange
@@ -346,6 +350,20 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       const int sb = t % C::SBUF;
       if (!pf_wait_warp(&s_full[sb], (t / C::SBUF) & 1)) { ok = false; break; }
       tc_fence_after();
+      // chunk c (32 columns) of this thread's columns: its own 32 columns of the row from
+      // [c0 + 32 c, ...), where the 16x32bx2 shape adds c0 = HC for the upper lanes itself
+      const uint32_t sc = lane_base + 128 * sb;
+      auto ld_s = [&](int c, float (&v)[32]) {
+        if constexpr (C::SPLIT == 2) tmem_ld32_16x2<C::HC>(sc + 32 * c, v);
+        else tmem_ld32(sc + 32 * c, v);
+      };
+      // head_dim <= 128: the half row's loads go out first; the tile's bookkeeping below
+      // runs while they are in flight
+      float vall[C::ONE_LOAD ? C::HC : 1];
+      if constexpr (C::ONE_LOAD) {
+#pragma unroll
+        for (int c = 0; c < C::HCH; ++c) ld_s(c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
+      }
       // the P and alpha slots of tile t (freed by tile t-2's P.V and correction) are
       // normally free long before they are written: test them now without blocking, and
       // wait further down only if they were not
@@ -362,25 +380,27 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       // warp-collective TMEM loads and so must be taken by the whole warp (a masked path
       // is correct for every row)
       const bool wfull = __all_sync(0xffffffffu, full);
-      // chunk c (32 columns) of this thread's columns: its own 32 columns of the row from
-      // [c0 + 32 c, ...), where the 16x32bx2 shape adds c0 = HC for the upper lanes itself
-      const uint32_t sc = lane_base + 128 * sb;
-      auto ld_s = [&](int c, float (&v)[32]) {
-        if constexpr (C::SPLIT == 2) tmem_ld32_16x2<C::HC>(sc + 32 * c, v);
-        else tmem_ld32(sc + 32 * c, v);
-      };
-      float vall[C::ONE_LOAD ? C::HC : 1];
       float tmax = -INFINITY;
       if constexpr (C::ONE_LOAD) {
-        // head_dim <= 128: the half row in registers, one TMEM wait; S is released at once
-#pragma unroll
-        for (int c = 0; c < C::HCH; ++c) ld_s(c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
+        // the half row in registers, one TMEM wait; S is released at once
         tmem_ld_wait();
         if constexpr (!C::TS) {  // (TS: S is freed by the P.V that reads P8 from it)
           tc_fence_before();
           mbar_arrive_warp(&s_free[sb]);
         }
-        if (full) {
+        if constexpr (C::PREMASK) {
+          // a warp with a partly visible row: the hidden scores of its rows become -inf
+          // here, so that one unmasked code path serves every tile (2^(-inf) = 0 is their
+          // p, the zero the mask asks for; cst > 0, so the maximum of the visible raw
+          // scores scales to the maximum of the scaled ones).  The branch is taken by the
+          // whole warp: a per-thread branch here cost the full tiles about 4 %.
+          if (!wfull) {
+#pragma unroll
+            for (int j = 0; j < C::HC; ++j)
+              if (j >= lim || j < lo) vall[j] = -INFINITY;
+          }
+          tmax = max_tree<C::HC>(vall) * cst;
+        } else if (full) {
           tmax = max_tree<C::HC>(vall) * cst;
         } else {
 #pragma unroll
@@ -433,7 +453,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       const float2 cst2 = make_float2(cst, cst), nm2 = make_float2(nb, nb);
       uint32_t ptm[C::TS ? 2 * C::HCH * 4 : 1];  // TS: this thread's P8 words (four keys each)
       // c: chunk of this thread's half; `masked` says whether to apply the row's mask, which
-      // only tiles not wholly visible need: a compile-time flag on e4m3 layers (the choice is
+      // only tiles not wholly visible need: never on e4m3 layers up to head_dim 128 (the
+      // hidden scores are -inf already), a compile-time flag at head_dim 256 (the choice is
       // made once per tile), the run-time test of `full` on bf16 layers (whose registers do
       // not hold two copies of the loop)
       auto chunk = [&](const float (&v)[32], int c, auto masked) {
@@ -504,6 +525,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       };
       if constexpr (BF) {
         pass2(MaskedUnlessFull());
+      } else if constexpr (C::PREMASK) {
+        pass2(Unmasked());  // hidden scores are -inf already
       } else {
         if (wfull) pass2(Unmasked());
         else pass2(Masked());
@@ -556,26 +579,34 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     // (first: O takes the partial itself)
     auto promote_pass = [&](uint32_t src, int hn, float alpha, auto first) {
       if (hn == 0) {
+        // two 32-column loads per TMEM wait (one at head_dim 64, whose correction warps
+        // run under a smaller register budget)
+        constexpr int PAIR = (D >= 128 && (C::DN / 32) % 2 == 0) ? 2 : 1;
 #pragma unroll
-        for (int c = 0; c < C::DN / 32; ++c) {
-          float ot[32];
-          tmem_ld32(src + 32 * c, ot);
+        for (int c2 = 0; c2 < C::DN / 32; c2 += PAIR) {
+          float ot[PAIR][32];
+#pragma unroll
+          for (int u = 0; u < PAIR; ++u) tmem_ld32(src + 32 * (c2 + u), ot[u]);
           tmem_ld_wait();
-          if constexpr (decltype(first)::value) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) O[32 * c + j] = ot[j];
-          } else {
-            // packed: two fused multiply-adds per instruction, the same rounding as fmaf
-            const float2 a2 = make_float2(alpha, alpha);
+          for (int u = 0; u < PAIR; ++u) {
+            const int c = c2 + u;
+            if constexpr (decltype(first)::value) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float2 r = __ffma2_rn(make_float2(O[32 * c + j], O[32 * c + j + 1]), a2,
-                                          make_float2(ot[j], ot[j + 1]));
-              O[32 * c + j] = r.x;
-              O[32 * c + j + 1] = r.y;
+              for (int j = 0; j < 32; ++j) O[32 * c + j] = ot[u][j];
+            } else {
+              // packed: two fused multiply-adds per instruction, the same rounding as fmaf
+              const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                const float2 r = __ffma2_rn(make_float2(O[32 * c + j], O[32 * c + j + 1]), a2,
+                                            make_float2(ot[u][j], ot[u][j + 1]));
+                O[32 * c + j] = r.x;
+                O[32 * c + j + 1] = r.y;
+              }
             }
+            pin32(O + 32 * c);
           }
-          pin32(O + 32 * c);
         }
       } else {
 #pragma unroll 1
