@@ -130,6 +130,14 @@ __device__ void write_current_token(const DecodeParams& p, int b, int g, int T, 
   fence_proxy_async_global();
 }
 
+// Maximum of a value over the 32 lanes of a warp, in one warp-wide reduction (every lane
+// takes part and receives the result).
+FKV_DEV float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1)
     decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
@@ -366,11 +374,10 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
 #pragma unroll
         for (int hh = 1; hh < NH2; ++hh) wm[h] = fmaxf(wm[h], x[hh][h]);
       }
-      // tile maximum of each head over the tile's keys: within the warp, then across the 4
+      // tile maximum of each head over the tile's keys: within the warp (one warp-wide
+      // reduction per head), then across the 4
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int h = 0; h < G; ++h) wm[h] = fmaxf(wm[h], __shfl_xor_sync(0xffffffffu, wm[h], off));
+      for (int h = 0; h < G; ++h) wm[h] = warp_max(wm[h]);
       // reduction t uses slot t % 2 (its previous use, t - 2, was read by every warp
       // before that warp's arrival for t - 1)
       float* red = red_s + (t & 1) * 4 * C::NP;
@@ -385,6 +392,7 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
       // the correction warpgroup read tile t-2's alpha
       if (t >= 2 && !wait_warp(&p_free[pb], ((t >> 1) - 1) & 1, p.pipe_wait_ns)) { ok = false; break; }
       if (t >= 2 && !wait_warp(&a_free[pb], ((t >> 1) - 1) & 1, p.pipe_wait_ns)) { ok = false; break; }
+      float pvs[NH2][G];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float tmax = fmaxf(fmaxf(red[h], red[C::NP + h]), fmaxf(red[2 * C::NP + h], red[3 * C::NP + h]));
@@ -395,13 +403,22 @@ __global__ void __launch_bounds__(kDecodeTcThreads, (D <= 128 && G <= 8) ? 3 : 1
         for (int hh = 0; hh < NH2; ++hh) {
           const float pv = valid[hh] ? ex2(x[hh][h] - mn) : 0.f;
           psum = hh == 0 ? pv : psum + pv;
-          const uint16_t code2 = f32x2_to_e4m3x2(pv * 448.f, 0.f);
-          sP[pb * C::PTILE + hh * (C::NP * 128) + swz(static_cast<uint32_t>(h * 128 + i), 128)] =
-              static_cast<uint8_t>(code2 & 0xFF);
+          pvs[hh][h] = pv * 448.f;
         }
         lsum[h] = fmaf(lsum[h], alpha, psum);
         m[h] = mn;
         if (i == 0) alpha_s[pb * C::NP + h] = alpha;
+      }
+      // P8 codes, two heads per conversion
+#pragma unroll
+      for (int hh = 0; hh < NH2; ++hh) {
+#pragma unroll
+        for (int h = 0; h < G; h += 2) {
+          const uint16_t code2 = f32x2_to_e4m3x2(pvs[hh][h], h + 1 < G ? pvs[hh][h + 1] : 0.f);
+          uint8_t* row = sP + pb * C::PTILE + hh * (C::NP * 128);
+          row[swz(static_cast<uint32_t>(h * 128 + i), 128)] = static_cast<uint8_t>(code2 & 0xFF);
+          if (h + 1 < G) row[swz(static_cast<uint32_t>((h + 1) * 128 + i), 128)] = static_cast<uint8_t>(code2 >> 8);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive_warp(&p_full[pb]);
