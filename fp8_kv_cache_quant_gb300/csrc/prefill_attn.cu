@@ -135,6 +135,10 @@ struct PrefillCfg {
   // to -inf in registers (one code path for every tile); head_dim 256 keeps a masked copy
   // of the exponent pass, which measured slightly faster there
   static constexpr bool PREMASK = !BF && D <= 128;
+  // the softmax tests its P and alpha slots without blocking as soon as S arrives (and
+  // waits later only if they were not free); full attention at head_dim 256 measured
+  // faster waiting for them only where they are written
+  static constexpr bool PRETEST = D <= 128 || WIN;
   // softmax warps per S row: two on e4m3 layers (each half of the row's columns, so that
   // every SM quarter has two softmax warps to switch between); one on bf16 layers, whose
   // 2-byte tiles leave no shared memory for the half-row exchange
@@ -368,8 +372,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       // normally free long before they are written: test them now without blocking, and
       // wait further down only if they were not
       const int pb = t & 1;
-      const bool p_ready = C::TS || t < 2 || mbar_test_wait(&p_free[pb], ((t >> 1) - 1) & 1);
-      const bool a_ready = t < 2 || mbar_test_wait(&a_free[pb], ((t >> 1) - 1) & 1);
+      const bool p_ready = C::TS || t < 2 || (C::PRETEST && mbar_test_wait(&p_free[pb], ((t >> 1) - 1) & 1));
+      const bool a_ready = t < 2 || (C::PRETEST && mbar_test_wait(&a_free[pb], ((t >> 1) - 1) & 1));
       const int kbase = (tb + t) * C::BN + c0;  // key of this thread's first column
       const int lim = lim_row - kbase;      // columns [lo, lim) of this thread's half are visible
       // full-attention instantiations fold the lower bound away (it costs the softmax
