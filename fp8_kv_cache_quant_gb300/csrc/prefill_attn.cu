@@ -139,6 +139,10 @@ struct PrefillCfg {
   // waits later only if they were not free); full attention at head_dim 256 measured
   // faster waiting for them only where they are written
   static constexpr bool PRETEST = D <= 128 || WIN;
+  // full attention at head_dim 256 waits for S(t+1) and issues its loads right after
+  // publishing P8(t), ahead of tile t's alpha (measured 0.5 % faster there; up to head_dim
+  // 128 the same order was slower)
+  static constexpr bool PIPE = D == 256 && !BF && !WIN;
   // softmax warps per S row: two on e4m3 layers (each half of the row's columns, so that
   // every SM quarter has two softmax warps to switch between); one on bf16 layers, whose
   // 2-byte tiles leave no shared memory for the half-row exchange
@@ -348,12 +352,29 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     const int lo_row = (WIN && row_ok) ? max(0, pos - p.window + 1) : 0;
     float m = -INFINITY, l = 0.f;              // l: this thread's columns only
     bool ok = true;
-    for (int t = 0; t < n_t; ++t) {
+    // the half row of S in registers (one-load softmax)
+    float vall[C::ONE_LOAD ? C::HC : 1];
+    // PIPE: wait for S(t) and issue the loads of this thread's half row
+    auto load_s_row = [&](int t) -> bool {
+      const int sb = t % C::SBUF;
+      if (!pf_wait_warp(&s_full[sb], (t / C::SBUF) & 1)) return false;
+      tc_fence_after();
+      if constexpr (C::PIPE) {
+        const uint32_t sc = lane_base + 128 * sb;
+#pragma unroll
+        for (int c = 0; c < C::HCH; ++c) tmem_ld32_16x2<C::HC>(sc + 32 * c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
+      }
+      return true;
+    };
+    if constexpr (C::PIPE) ok = n_t == 0 || load_s_row(0);
+    for (int t = 0; ok && t < n_t; ++t) {
       // another warp's timeout is noticed every 8 tiles (every wait is bounded anyway)
       if ((t & 7) == 7 && abort_warp(abort_s)) { ok = false; break; }
       const int sb = t % C::SBUF;
-      if (!pf_wait_warp(&s_full[sb], (t / C::SBUF) & 1)) { ok = false; break; }
-      tc_fence_after();
+      if constexpr (!C::PIPE) {
+        if (!pf_wait_warp(&s_full[sb], (t / C::SBUF) & 1)) { ok = false; break; }
+        tc_fence_after();
+      }
       // chunk c (32 columns) of this thread's columns: its own 32 columns of the row from
       // [c0 + 32 c, ...), where the 16x32bx2 shape adds c0 = HC for the upper lanes itself
       const uint32_t sc = lane_base + 128 * sb;
@@ -363,8 +384,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       };
       // head_dim <= 128: the half row's loads go out first; the tile's bookkeeping below
       // runs while they are in flight
-      float vall[C::ONE_LOAD ? C::HC : 1];
-      if constexpr (C::ONE_LOAD) {
+      if constexpr (C::ONE_LOAD && !C::PIPE) {
 #pragma unroll
         for (int c = 0; c < C::HCH; ++c) ld_s(c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
       }
@@ -543,6 +563,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
           tmem_st_wait();
         }
       }
+      if constexpr (C::PIPE) {
+        fence_proxy_async_smem();
+        mbar_arrive_warp(&p_full[pb]);
+        if (t + 1 < n_t && !load_s_row(t + 1)) { ok = false; break; }
+      }
       const float lsum = lsum2.x + lsum2.y;
       if constexpr (!C::ONE_LOAD) {
         tc_fence_before();
@@ -555,10 +580,13 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
       if (!__all_sync(0xffffffffu, a_ready) && !pf_wait_warp(&a_free[pb], ((t >> 1) - 1) & 1)) { ok = false; break; }
       if (hf == 0) sAlpha[pb * C::BM + i] = alpha;
       mbar_arrive_warp(&a_full[pb]);
-      if constexpr (C::TS) tc_fence_before();
-      else fence_proxy_async_smem();
-      mbar_arrive_warp(&p_full[pb]);
+      if constexpr (!C::PIPE) {
+        if constexpr (C::TS) tc_fence_before();
+        else fence_proxy_async_smem();
+        mbar_arrive_warp(&p_full[pb]);
+      }
     }
+    if constexpr (C::PIPE) tmem_ld_wait();  // no load left in flight on an early exit
     if (!ok) {
       if (lane == 0) raise_fault(p.fault, FKV_FAULT_TIMEOUT);
       *abort_s = 1;
