@@ -354,7 +354,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
     bool ok = true;
     // the half row of S in registers (one-load softmax)
     float vall[C::ONE_LOAD ? C::HC : 1];
-    // PIPE: wait for S(t) and issue the loads of this thread's half row
+    // PIPE: wait for S(t) and issue the loads of this thread's half row (called before the
+    // loop for tile 0 and at the end of tile t-1 for tile t)
     auto load_s_row = [&](int t) -> bool {
       const int sb = t % C::SBUF;
       if (!pf_wait_warp(&s_full[sb], (t / C::SBUF) & 1)) return false;
@@ -382,8 +383,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, BF, WIN>::THREADS, 1)
         if constexpr (C::SPLIT == 2) tmem_ld32_16x2<C::HC>(sc + 32 * c, v);
         else tmem_ld32(sc + 32 * c, v);
       };
-      // head_dim <= 128: the half row's loads go out first; the tile's bookkeeping below
-      // runs while they are in flight
+      // one-load softmax: the half row's loads go out first (with PIPE they went out at the
+      // end of the previous tile); the tile's bookkeeping below runs while they are in flight
       if constexpr (C::ONE_LOAD && !C::PIPE) {
 #pragma unroll
         for (int c = 0; c < C::HCH; ++c) ld_s(c, *reinterpret_cast<float(*)[32]>(vall + 32 * c));
